@@ -1,0 +1,333 @@
+"""Benchmark of the complex chunkwise SSD forward (libssdc) on GB300.
+
+One step = one forward pass of the whole scan (chunk-state kernel, state pass,
+chunk-scan kernel) over the single-layer production workload (B=2, T=2048,
+H=16, D=N=64 complex, Q=64), inputs resident in HBM. Metric: token-heads/s
+(B*T*H per step). L2 is flushed (a 512 MiB write) before every timed step and
+each step is timed on its stream with CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own independent batch (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from state_space_sequence_complex_gb300 import inputs  # noqa: E402
+
+METRIC = "complex-SSD fwd token·heads/s at Q=64"
+UNIT = "token·heads/s"
+FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--precision", choices=["auto", "tf32", "fp32"], default="auto")
+    ap.add_argument("--workload", choices=["layer"], default="layer")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes_per_unit(w) -> float:
+    # x, B_t, C_t read and y written (complex64 = 8 B each element), dt read,
+    # final state written once per sequence.
+    return 16 * w.D + 16 * w.N + 4 + 8 * w.N * w.D / w.T
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_oracle_baseline(w, inp, max_seconds=12.0, max_reps=20):
+    """Time the CPU oracle, as it stands, on the full workload, repeated."""
+    from oracle import naive_scan_inputs
+    from oracle.ssd_oracle import default_threads
+    cores = default_threads()
+    reps, t_total = 0, 0.0
+    while reps < max_reps and t_total < max_seconds:
+        t0 = time.perf_counter()
+        naive_scan_inputs(inp, threads=cores)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    units = w.token_heads * reps
+    return {"value": units / t_total, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"full workload ({w.name}) x {reps} passes, {t_total:.1f} s"}
+
+
+def reference_arm(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import naive_scan_inputs
+    from oracle.ssd_oracle import default_threads
+    inp = inputs.generate(w)
+    cores = default_threads()
+    # each step is one full pass of the workload on the host cores
+    for _ in range(args.warmup):
+        naive_scan_inputs(inp, threads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        naive_scan_inputs(inp, threads=cores)
+        times.append(time.perf_counter() - t0)
+    ms = 1000.0 * sum(times) / len(times)
+    value = w.token_heads / (ms / 1000.0)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
+                   "chunk_size": w.Q, "seed": w.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"full workload per step ({w.name})"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = inputs.LAYER
+    if args.impl == "reference":
+        reference_arm(args, w)
+        return
+    import torch
+    from state_space_sequence_complex_gb300 import build, ssdc
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if dist.is_nccl_available() else "gloo")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    ssdc.load()
+
+    # each rank processes its own independently seeded batch (weak scaling)
+    inp = inputs.generate(w, layer=rank)
+    host = {k: torch.from_numpy(np.ascontiguousarray(v)) for k, v in inp.arrays().items()}
+    d_in = {k: v.to(dev) for k, v in host.items()}
+    Bn, T, H, N, D = inp.dims
+
+    precision = args.precision
+    if precision == "auto":
+        precision = "tf32" if ssdc.ssd_complex_fwd_supported(ssdc.dims(Bn, T, H, N, D, "tf32"), w.Q) == 0 else "fp32"
+    f = ssdc.Forward(Bn, T, H, N, D, w.Q, precision, device=dev)
+    stream = torch.cuda.current_stream()
+    order = ["x_re", "x_im", "A_re", "A_im", "B_re", "B_im", "C_re", "C_im", "dt"]
+    call = lambda: f(*[d_in[k] for k in order])
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for i in range(max(args.warmup, 3)):
+        flush.fill_(float(i))
+        call()
+    torch.cuda.synchronize()
+    st = f.status()
+    if st != ssdc.SSDC_OK:
+        raise SystemExit(f"device status after warm-up: {ssdc.strerror(st)}")
+
+    # ---- timed region: device-resident inputs ----
+    ssdc.timing_enable(True)
+    names = None
+    per_kernel = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.1)
+    launches_per_step = 0
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+        per_kernel.append(ssdc.timing_read())
+        launches_per_step = ssdc.last_launch_count()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ssdc.timing_enable(False)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    st = f.status()
+    if st != ssdc.SSDC_OK:
+        raise SystemExit(f"device status after timed steps: {ssdc.strerror(st)}")
+
+    # ---- end to end through the C ABI with host buffers ----
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    y_host = [torch.empty(f.y_re.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    s_host = [torch.empty(f.fs_re.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    h2d = sum(v.numel() * 4 for v in pinned.values())
+    d2h = 2 * (f.y_re.numel() + f.fs_re.numel()) * 4
+
+    def e2e_step():
+        for k2 in order:
+            d_in[k2].copy_(pinned[k2], non_blocking=True)
+        call()
+        y_host[0].copy_(f.y_re, non_blocking=True)
+        y_host[1].copy_(f.y_im, non_blocking=True)
+        s_host[0].copy_(f.fs_re, non_blocking=True)
+        s_host[1].copy_(f.fs_im, non_blocking=True)
+
+    for i in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(e2e_steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for k in range(e2e_steps):
+        flush.fill_(float(k))
+        e2e_ev[k][0].record(stream)
+        e2e_step()
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+
+    units = w.token_heads * world
+    value = units / (ms / 1000.0)
+    e2e_value = units / (e2e_ms / 1000.0)
+
+    # dominant kernel: the launch with the largest mean device time
+    nk = min(len(p) for p in per_kernel)
+    kmeans = [sum(p[i] for p in per_kernel) / len(per_kernel) for i in range(nk)]
+    names = (["chunk_state", "state_pass", "chunk_scan"] if nk == 3 else [f"launch{i}" for i in range(nk)])
+    top = int(np.argmax(kmeans))
+    peak, peak_kind = peaks()
+    bytes_per_launch = algorithmic_bytes_per_unit(w) * w.token_heads
+    achieved = bytes_per_launch / (kmeans[top] / 1000.0) / 1e9
+    step_achieved = bytes_per_launch / (ms / 1000.0) / 1e9 / 1.0
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = run_oracle_baseline(w, inp)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
+                   "chunk_size": w.Q, "seed": w.seed, "precision": precision,
+                   "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"weak: {world} independent batch(es), no collective"},
+        "roofline": {"bound": "hbm", "kernel": names[top], "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "kernel_ms": {n: m for n, m in zip(names, kmeans)},
+                     "step_frac": step_achieved / peak},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * ssdc.h -- C ABI of libssdc.so: forward pass of the complex-valued chunkwise
+ * SSD scan (the core scan of a Mamba-3 block) on one GB300 (sm_103a).
+ *
+ * The operation (page "Extending -- SSM variants & Triton kernels", Path A,
+ * Step 1, the naive O(T) scan and the discretisation it calls; landing page
+ * "03 Chunkwise SSD" for the chunked decomposition):
+ *
+ *   A_bar[b,t,h] = exp(softplus(dt[b,t,h]) * A[h])            (complex)
+ *   s_t = A_bar_t * s_{t-1} + B_t (outer) x_t,   s_{-1} = 0     s: (N, D)
+ *   y_t = sum_n C_t[n] * s_t[n, :]
+ *
+ * computed chunk by chunk with chunk size Q (the pages' chunk_size):
+ *   Acs     inclusive in-chunk cumulative sum of softplus(dt) * A
+ *   L[l,s]  = exp(Acs[l] - Acs[s]) for l >= s, else 0
+ *   Y_diag  = (C B^T o L) X
+ *   S_loc   = B^T (dec o X),  dec[s] = exp(Acs[Q-1] - Acs[s])
+ *   S_in[c+1] = exp(Acs_c[Q-1]) S_in[c] + S_loc[c],  S_in[0] = 0
+ *   y       = Y_diag + (C o exp(Acs)) S_in[c]
+ *
+ * Re(y), the real output the pages' chunkwise function returns, is the real
+ * plane of y: no separate buffer is written for it.
+ *
+ * Layout. Every complex array is PLANAR: two separate float32 device arrays
+ * (real plane, imaginary plane), each dense row-major over the shape given:
+ *   x      (B, T, H, D)        A (H)          dt (B, T, H)  (real)
+ *   B_t    (B, T, H, N)        C_t (B, T, H, N)
+ *   y      (B, T, H, D)        final_state (B, H, N, D)
+ * All pointers are device pointers, 16-byte aligned. Outputs must not
+ * overlap inputs or each other.
+ *
+ * Ownership. The caller owns every buffer; the library keeps no pointer after
+ * a call returns. Work is enqueued on `stream` and runs asynchronously: inputs
+ * must stay unchanged, and outputs unread, until the stream reaches that point.
+ *
+ * Errors. Every entry point returns an int status: 0 (SSDC_OK) or a negative
+ * SSDC_ERR_* code. Argument errors are detected on the host before anything
+ * is enqueued; nothing aborts, throws or falls back to another path. Errors
+ * detected on the device (a bounded wait that gave up) are recorded in the
+ * workspace and reported by ssd_complex_status().
+ *
+ * Precision. SSDC_PREC_TF32 runs the chunk contractions on the tcgen05 tensor
+ * cores with TF32 operands and fp32 accumulation; SSDC_PREC_FP32 runs every
+ * step in exact fp32 on the SIMT cores (the checking variant). The state pass
+ * between chunks is fp32 in both.
+ */
+#ifndef SSDC_H
+#define SSDC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSDC_OK 0
+#define SSDC_ERR_INVALID (-1)     /* null pointer, size <= 0, bad precision, overlap */
+#define SSDC_ERR_UNSUPPORTED (-2) /* Q, N or D outside the supported set */
+#define SSDC_ERR_ALIGN (-3)       /* a pointer not 16-byte aligned */
+#define SSDC_ERR_WORKSPACE (-4)   /* workspace null, misaligned or too small */
+#define SSDC_ERR_CUDA (-5)        /* a CUDA call or launch failed */
+#define SSDC_ERR_TIMEOUT (-6)     /* a bounded device wait gave up */
+#define SSDC_ERR_DEVICE (-7)      /* the current device is not sm_103 */
+
+#define SSDC_PREC_TF32 0
+#define SSDC_PREC_FP32 1
+
+/* Problem sizes: batch B, sequence length T, heads H, complex state size N,
+ * complex head dimension D; precision is SSDC_PREC_TF32 or SSDC_PREC_FP32. */
+typedef struct {
+    int64_t B, T, H, N, D;
+    int32_t precision;
+} ssdc_dims;
+
+/* A planar complex input / output: real plane and imaginary plane. */
+typedef struct {
+    const float *re, *im;
+} ssdc_cin;
+typedef struct {
+    float *re, *im;
+} ssdc_cout;
+
+/*
+ * Supported sizes.
+ *   SSDC_PREC_FP32: chunk_size in {16, 32, 64, 128, 256};
+ *                   N and D multiples of 8 in [8, 64].
+ *   SSDC_PREC_TF32: chunk_size in {32, 64, 128, 256}; N = D = 64.
+ * T need not be a multiple of chunk_size: the last chunk is partial.
+ */
+int ssd_complex_fwd_supported(ssdc_dims dims, int chunk_size);
+
+/* Bytes of device workspace ssd_complex_fwd_ws needs for these sizes (0 on
+ * invalid or unsupported sizes). It holds the per-chunk states, the per-chunk
+ * decays and a device status word. */
+size_t ssd_complex_fwd_workspace_bytes(ssdc_dims dims, int chunk_size);
+
+/*
+ * Forward pass with a caller-provided workspace (device memory, 256-byte
+ * aligned, at least ssd_complex_fwd_workspace_bytes() bytes). The workspace's
+ * contents need no initialisation; the call resets its status word. Calls
+ * that share one workspace must be ordered on the stream.
+ *
+ *   x, A, B_t, C_t, dt   inputs (see Layout)
+ *   dims, chunk_size     sizes, precision and the chunk length Q
+ *   y                    output (B,T,H,D) complex; y.re is Re(y)
+ *   final_state          output (B,H,N,D) complex, the state after t = T-1
+ *   stream               CUDA stream (0 = legacy default stream)
+ */
+int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
+                       const float *dt, ssdc_dims dims, int chunk_size,
+                       ssdc_cout y, ssdc_cout final_state, void *workspace,
+                       size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Forward pass that allocates its workspace on `stream` (cudaMallocAsync /
+ * cudaFreeAsync, stream-ordered). A device-side error cannot be queried after
+ * it returns; use the _ws form with ssd_complex_status() to read one.
+ */
+int ssd_complex_fwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
+                    const float *dt, ssdc_dims dims, int chunk_size, ssdc_cout y,
+                    ssdc_cout final_state, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns the device status recorded in
+ * `workspace` by the last call that used it (SSDC_OK or SSDC_ERR_TIMEOUT), or
+ * SSDC_ERR_CUDA if the stream reports an error. */
+int ssd_complex_status(void *workspace, cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *ssd_complex_strerror(int status);
+
+/* Number of kernel launches the last successful forward call enqueued on its
+ * stream (from the calling thread). */
+int ssd_complex_last_launch_count(void);
+
+/*
+ * Per-kernel timing (instrumentation for benchmarks). While enabled, every
+ * forward call records a CUDA event on its stream before its first launch and
+ * after each launch. ssd_complex_timing_read() waits for the last call's
+ * events and writes the device time of each of its launches, in
+ * milliseconds, to ms[0 .. min(n, launches)); it returns the launch count or
+ * a negative status. Process-wide state: do not use from several threads.
+ */
+int ssd_complex_timing_enable(int enable);
+int ssd_complex_timing_read(float *ms, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSDC_H */

@@ -1,0 +1,257 @@
+// Host side of the C ABI declared in include/ssdc.h: argument checks,
+// workspace carving and the launch sequence
+//   chunk-state kernel -> state pass -> chunk-scan kernel
+// on the caller's stream. No allocation happens in ssd_complex_fwd_ws.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/ssdc.h"
+#include "ssdc_kernels.h"
+
+namespace {
+
+thread_local int g_last_launches = 0;
+
+// Instrumentation events (see ssd_complex_timing_enable).
+constexpr int kMaxTimed = 8;
+bool g_timing = false;
+int g_timed_launches = 0;
+cudaEvent_t g_events[kMaxTimed + 1] = {};
+bool g_events_made = false;
+
+int record_event(int i, cudaStream_t stream) {
+    if (!g_timing) return SSDC_OK;
+    if (i > kMaxTimed) return SSDC_ERR_INVALID;
+    return cudaEventRecord(g_events[i], stream) == cudaSuccess ? SSDC_OK : SSDC_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_attr_done[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+int check_sizes(const ssdc_dims& d, int Q) {
+    if (d.B <= 0 || d.T <= 0 || d.H <= 0 || d.N <= 0 || d.D <= 0 || Q <= 0) return SSDC_ERR_INVALID;
+    if (d.precision != SSDC_PREC_TF32 && d.precision != SSDC_PREC_FP32) return SSDC_ERR_INVALID;
+    if (d.B > 65535 || d.H > 65535 || d.B * d.H > 65535) return SSDC_ERR_UNSUPPORTED;
+    const int64_t nc = ssdc::ceil_div64(d.T, Q);
+    if (nc * 4 > INT32_MAX) return SSDC_ERR_UNSUPPORTED;
+    // every plane must be indexable
+    const int64_t big = d.B * d.T * d.H * (d.N > d.D ? d.N : d.D);
+    if (big <= 0 || big > (int64_t(1) << 40)) return SSDC_ERR_UNSUPPORTED;
+    if (d.precision == SSDC_PREC_FP32) {
+        if (!is_pow2_in(Q, 16, 256)) return SSDC_ERR_UNSUPPORTED;
+        if (d.N % 8 || d.D % 8 || d.N > 64 || d.D > 64) return SSDC_ERR_UNSUPPORTED;
+    } else {
+        if (!ssdc::tc_supported((int)d.N, (int)d.D, Q)) return SSDC_ERR_UNSUPPORTED;
+    }
+    return SSDC_OK;
+}
+
+size_t ws_bytes_for(const ssdc_dims& d, int Q) {
+    const int64_t nc = ssdc::ceil_div64(d.T, Q);
+    const int64_t chunks = d.B * d.H * nc;
+    size_t s = (size_t)chunks * 2 * d.N * d.D * sizeof(float);
+    s = (s + 255) & ~size_t(255);
+    size_t a = (size_t)chunks * 2 * sizeof(float);
+    a = (a + 255) & ~size_t(255);
+    return s + a + 256;
+}
+
+ssdc::Workspace carve(void* ws, const ssdc_dims& d, int Q) {
+    // [status word, padded to 256 B][S][a]
+    const int64_t nc = ssdc::ceil_div64(d.T, Q);
+    const int64_t chunks = d.B * d.H * nc;
+    size_t s = (size_t)chunks * 2 * d.N * d.D * sizeof(float);
+    s = (s + 255) & ~size_t(255);
+    char* base = static_cast<char*>(ws);
+    ssdc::Workspace w;
+    w.status = reinterpret_cast<int*>(base);
+    w.S = reinterpret_cast<float*>(base + 256);
+    w.a = reinterpret_cast<float*>(base + 256 + s);
+    return w;
+}
+
+int setup_device_attrs() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SSDC_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SSDC_ERR_CUDA;
+    if (g_attr_done[dev].load(std::memory_order_acquire)) return SSDC_OK;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return SSDC_ERR_CUDA;
+    if (major != 10 || minor != 3) return SSDC_ERR_DEVICE;
+    if (cudaFuncSetAttribute(ssdc::ssdc_simt_chunk_state, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssdc::simt_state_smem()) != cudaSuccess)
+        return SSDC_ERR_CUDA;
+    if (cudaFuncSetAttribute(ssdc::ssdc_simt_chunk_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssdc::simt_scan_smem()) != cudaSuccess)
+        return SSDC_ERR_CUDA;
+    g_attr_done[dev].store(1, std::memory_order_release);
+    return SSDC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_complex_fwd_supported(ssdc_dims dims, int chunk_size) { return check_sizes(dims, chunk_size); }
+
+size_t ssd_complex_fwd_workspace_bytes(ssdc_dims dims, int chunk_size) {
+    if (check_sizes(dims, chunk_size) != SSDC_OK) return 0;
+    return ws_bytes_for(dims, chunk_size);
+}
+
+int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt,
+                       ssdc_dims dims, int chunk_size, ssdc_cout y, ssdc_cout final_state,
+                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    int rc = check_sizes(dims, chunk_size);
+    if (rc != SSDC_OK) return rc;
+    const void* ptrs[] = {x.re, x.im, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt,
+                          y.re, y.im, final_state.re, final_state.im};
+    for (const void* q : ptrs)
+        if (q == nullptr) return SSDC_ERR_INVALID;
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return SSDC_ERR_ALIGN;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return SSDC_ERR_WORKSPACE;
+    if (ws_bytes < ws_bytes_for(dims, chunk_size)) return SSDC_ERR_WORKSPACE;
+
+    // outputs must not overlap inputs, the workspace or each other
+    const int64_t BTH = dims.B * dims.T * dims.H;
+    auto rng = [](const void* p, int64_t n) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{lo, lo + (uintptr_t)n * sizeof(float)};
+    };
+    const Range in[] = {rng(x.re, BTH * dims.D), rng(x.im, BTH * dims.D), rng(A.re, dims.H),
+                        rng(A.im, dims.H), rng(B_t.re, BTH * dims.N), rng(B_t.im, BTH * dims.N),
+                        rng(C_t.re, BTH * dims.N), rng(C_t.im, BTH * dims.N), rng(dt, BTH),
+                        Range{reinterpret_cast<uintptr_t>(workspace),
+                              reinterpret_cast<uintptr_t>(workspace) + ws_bytes}};
+    const int64_t fsn = dims.B * dims.H * dims.N * dims.D;
+    const Range out[] = {rng(y.re, BTH * dims.D), rng(y.im, BTH * dims.D), rng(final_state.re, fsn),
+                         rng(final_state.im, fsn)};
+    for (const Range& o : out)
+        for (const Range& i : in)
+            if (overlaps(o, i)) return SSDC_ERR_INVALID;
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(out[i], out[j])) return SSDC_ERR_INVALID;
+
+    rc = setup_device_attrs();
+    if (rc != SSDC_OK) return rc;
+
+    ssdc::Problem p;
+    p.x_re = x.re; p.x_im = x.im; p.A_re = A.re; p.A_im = A.im;
+    p.B_re = B_t.re; p.B_im = B_t.im; p.C_re = C_t.re; p.C_im = C_t.im; p.dt = dt;
+    p.y_re = y.re; p.y_im = y.im; p.fs_re = final_state.re; p.fs_im = final_state.im;
+    p.T = dims.T; p.B = (int)dims.B; p.H = (int)dims.H; p.N = (int)dims.N; p.D = (int)dims.D;
+    p.Q = chunk_size;
+    p.nc = ssdc::ceil_div64(dims.T, chunk_size);
+    ssdc::Workspace w = carve(workspace, dims, chunk_size);
+
+    (void)cudaGetLastError();  // clear a stale error from unrelated work
+    int launches = 0;
+    if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
+    const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
+                         (unsigned)(p.B * p.H));
+    if (dims.precision == SSDC_PREC_FP32) {
+        const dim3 sgrid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
+        ssdc::ssdc_simt_chunk_state<<<sgrid, 256, ssdc::simt_state_smem(), stream>>>(p, w);
+        record_event(++launches, stream);
+        ssdc::ssdc_state_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(p, w);
+        record_event(++launches, stream);
+        const int lblocks = (p.Q + 63) / 64;
+        const dim3 cgrid((unsigned)(p.nc * lblocks), (unsigned)p.H, (unsigned)p.B);
+        ssdc::ssdc_simt_chunk_scan<<<cgrid, 256, ssdc::simt_scan_smem(), stream>>>(p, w);
+        record_event(++launches, stream);
+    } else {
+        int n = ssdc::tc_launch_chunk_state(p, w, stream);
+        if (n < 0) return n;
+        launches += n;
+        record_event(launches, stream);
+        ssdc::ssdc_state_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(p, w);
+        record_event(++launches, stream);
+        n = ssdc::tc_launch_chunk_scan(p, w, stream);
+        if (n < 0) return n;
+        launches += n;
+        record_event(launches, stream);
+    }
+    if (cudaGetLastError() != cudaSuccess) return SSDC_ERR_CUDA;
+    g_last_launches = launches;
+    if (g_timing) g_timed_launches = launches;
+    return SSDC_OK;
+}
+
+int ssd_complex_fwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt,
+                    ssdc_dims dims, int chunk_size, ssdc_cout y, ssdc_cout final_state,
+                    cudaStream_t stream) {
+    int rc = check_sizes(dims, chunk_size);
+    if (rc != SSDC_OK) return rc;
+    const size_t bytes = ws_bytes_for(dims, chunk_size);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) return SSDC_ERR_CUDA;
+    rc = ssd_complex_fwd_ws(x, A, B_t, C_t, dt, dims, chunk_size, y, final_state, ws, bytes, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == SSDC_OK) rc = SSDC_ERR_CUDA;
+    return rc;
+}
+
+int ssd_complex_status(void* workspace, cudaStream_t stream) {
+    if (workspace == nullptr) return SSDC_ERR_INVALID;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SSDC_ERR_CUDA;
+    int status = SSDC_ERR_CUDA;
+    if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SSDC_ERR_CUDA;
+    return status;
+}
+
+const char* ssd_complex_strerror(int status) {
+    switch (status) {
+        case SSDC_OK: return "ok";
+        case SSDC_ERR_INVALID: return "invalid argument (null pointer, size <= 0, bad precision or overlapping buffers)";
+        case SSDC_ERR_UNSUPPORTED: return "unsupported size (chunk_size, N or D outside the supported set)";
+        case SSDC_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case SSDC_ERR_WORKSPACE: return "workspace null, not 256-byte aligned or too small";
+        case SSDC_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case SSDC_ERR_TIMEOUT: return "a bounded device wait gave up";
+        case SSDC_ERR_DEVICE: return "current device is not a compute capability 10.3 GPU";
+        default: return "unknown status";
+    }
+}
+
+int ssd_complex_last_launch_count(void) { return g_last_launches; }
+
+int ssd_complex_timing_enable(int enable) {
+    if (enable && !g_events_made) {
+        for (int i = 0; i <= kMaxTimed; ++i)
+            if (cudaEventCreate(&g_events[i]) != cudaSuccess) return SSDC_ERR_CUDA;
+        g_events_made = true;
+    }
+    g_timing = enable != 0;
+    g_timed_launches = 0;
+    return SSDC_OK;
+}
+
+int ssd_complex_timing_read(float* ms, int n) {
+    if (ms == nullptr || n < 0) return SSDC_ERR_INVALID;
+    const int k = g_timed_launches;
+    if (k == 0) return 0;
+    if (cudaEventSynchronize(g_events[k]) != cudaSuccess) return SSDC_ERR_CUDA;
+    for (int i = 0; i < k && i < n; ++i)
+        if (cudaEventElapsedTime(&ms[i], g_events[i], g_events[i + 1]) != cudaSuccess) return SSDC_ERR_CUDA;
+    return k;
+}
+
+}  // extern "C"

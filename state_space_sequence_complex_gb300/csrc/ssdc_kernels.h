@@ -1,0 +1,37 @@
+// Internal declarations shared by the host entry points and the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "ssdc_common.cuh"
+
+namespace ssdc {
+
+// Sizes and device pointers of one forward call (planar complex planes).
+struct Problem {
+    const float *x_re, *x_im, *A_re, *A_im, *B_re, *B_im, *C_re, *C_im, *dt;
+    float *y_re, *y_im, *fs_re, *fs_im;
+    int64_t T;
+    int B, H, N, D, Q;
+    int64_t nc;  // chunks per sequence, ceil(T / Q)
+};
+
+// SIMT (exact fp32) kernels.
+__global__ void ssdc_simt_chunk_state(Problem p, Workspace ws);
+__global__ void ssdc_simt_chunk_scan(Problem p, Workspace ws);
+size_t simt_state_smem();
+size_t simt_scan_smem();
+
+// Inter-chunk state pass (fp32, both precisions).
+__global__ void ssdc_state_pass(Problem p, Workspace ws);
+constexpr int kPassThreads = 256;
+
+// tcgen05 / TMA kernels (TF32 tensor cores). Returns the number of launches
+// enqueued, or a negative SSDC_ERR_* code.
+int tc_launch_chunk_state(const Problem& p, const Workspace& ws, cudaStream_t stream);
+int tc_launch_chunk_scan(const Problem& p, const Workspace& ws, cudaStream_t stream);
+bool tc_supported(int N, int D, int Q);
+
+}  // namespace ssdc

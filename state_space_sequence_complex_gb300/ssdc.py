@@ -1,0 +1,204 @@
+"""Thin ctypes binding of libssdc.so (include/ssdc.h): argument marshalling only.
+
+Every step of the scan runs in the library's CUDA kernels. PyTorch supplies
+device memory and the current stream. There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libssdc.so")
+
+SSDC_OK = 0
+SSDC_ERR_INVALID = -1
+SSDC_ERR_UNSUPPORTED = -2
+SSDC_ERR_ALIGN = -3
+SSDC_ERR_WORKSPACE = -4
+SSDC_ERR_CUDA = -5
+SSDC_ERR_TIMEOUT = -6
+SSDC_ERR_DEVICE = -7
+
+PREC = {"tf32": 0, "fp32": 1}
+
+# Every symbol include/ssdc.h declares.
+EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_complex_fwd_ws",
+           "ssd_complex_fwd", "ssd_complex_status", "ssd_complex_strerror",
+           "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read")
+
+
+class ssdc_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("D", ctypes.c_int64), ("precision", ctypes.c_int32)]
+
+
+class ssdc_cin(ctypes.Structure):
+    _fields_ = [("re", ctypes.c_void_p), ("im", ctypes.c_void_p)]
+
+
+class ssdc_cout(ctypes.Structure):
+    _fields_ = [("re", ctypes.c_void_p), ("im", ctypes.c_void_p)]
+
+
+class SSDCError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Open libssdc.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.ssd_complex_fwd_supported.argtypes = [ssdc_dims, ctypes.c_int]
+    lib.ssd_complex_fwd_supported.restype = ctypes.c_int
+    lib.ssd_complex_fwd_workspace_bytes.argtypes = [ssdc_dims, ctypes.c_int]
+    lib.ssd_complex_fwd_workspace_bytes.restype = sz
+    common = [ssdc_cin, ssdc_cin, ssdc_cin, ssdc_cin, vp, ssdc_dims, ctypes.c_int, ssdc_cout, ssdc_cout]
+    lib.ssd_complex_fwd_ws.argtypes = common + [vp, sz, vp]
+    lib.ssd_complex_fwd_ws.restype = ctypes.c_int
+    lib.ssd_complex_fwd.argtypes = common + [vp]
+    lib.ssd_complex_fwd.restype = ctypes.c_int
+    lib.ssd_complex_status.argtypes = [vp, vp]
+    lib.ssd_complex_status.restype = ctypes.c_int
+    lib.ssd_complex_strerror.argtypes = [ctypes.c_int]
+    lib.ssd_complex_strerror.restype = ctypes.c_char_p
+    lib.ssd_complex_last_launch_count.argtypes = []
+    lib.ssd_complex_last_launch_count.restype = ctypes.c_int
+    lib.ssd_complex_timing_enable.argtypes = [ctypes.c_int]
+    lib.ssd_complex_timing_enable.restype = ctypes.c_int
+    lib.ssd_complex_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int]
+    lib.ssd_complex_timing_read.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    return load().ssd_complex_strerror(int(status)).decode()
+
+
+def dims(Bn, T, H, N, D, precision="tf32") -> ssdc_dims:
+    return ssdc_dims(int(Bn), int(T), int(H), int(N), int(D), PREC[precision] if isinstance(precision, str) else int(precision))
+
+
+def ssd_complex_fwd_supported(d: ssdc_dims, chunk_size: int) -> int:
+    return load().ssd_complex_fwd_supported(d, int(chunk_size))
+
+
+def ssd_complex_fwd_workspace_bytes(d: ssdc_dims, chunk_size: int) -> int:
+    return int(load().ssd_complex_fwd_workspace_bytes(d, int(chunk_size)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cin(re, im):
+    return ssdc_cin(re.data_ptr(), im.data_ptr())
+
+
+def _cout(re, im):
+    return ssdc_cout(re.data_ptr(), im.data_ptr())
+
+
+def ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
+                       precision="tf32", y_re, y_im, fs_re, fs_im, workspace, stream=None,
+                       check=True) -> int:
+    """Call ``ssd_complex_fwd_ws`` on torch CUDA tensors (planar float32).
+
+    ``workspace`` is a uint8 CUDA tensor of at least the queried size;
+    ``stream`` a ``torch.cuda.Stream`` (default: the current stream).
+    Returns the status (raises on a non-zero one unless ``check`` is False).
+    """
+    import torch
+
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    d = dims(Bn, T, H, N, D, precision)
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_fwd_ws(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt), d,
+        int(chunk_size), _cout(y_re, y_im), _cout(fs_re, fs_im), _ptr(workspace),
+        int(workspace.numel()), ctypes.c_void_p(s.cuda_stream))
+    if check and rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_fwd_ws")
+    return rc
+
+
+def ssd_complex_status(workspace, stream=None) -> int:
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return load().ssd_complex_status(_ptr(workspace), ctypes.c_void_p(s.cuda_stream))
+
+
+def last_launch_count() -> int:
+    return load().ssd_complex_last_launch_count()
+
+
+def timing_enable(on: bool = True) -> None:
+    rc = load().ssd_complex_timing_enable(1 if on else 0)
+    if rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_timing_enable")
+
+
+def timing_read(n: int = 8) -> list[float]:
+    """Per-launch device times (ms) of the last instrumented forward call."""
+    buf = (ctypes.c_float * n)()
+    k = load().ssd_complex_timing_read(buf, n)
+    if k < 0:
+        raise SSDCError(k, "ssd_complex_timing_read")
+    return [float(buf[i]) for i in range(min(k, n))]
+
+
+class Forward:
+    """Holds the outputs and the workspace of one problem size, so repeated
+    calls allocate nothing. ``__call__`` takes the planar inputs as CUDA
+    tensors and returns ``(y_re, y_im, final_state_re, final_state_im)``;
+    ``y_re`` is Re(y)."""
+
+    def __init__(self, Bn, T, H, N, D, chunk_size, precision="tf32", device="cuda"):
+        import torch
+
+        self.shape = (Bn, T, H, N, D)
+        self.chunk_size = int(chunk_size)
+        self.precision = precision
+        d = dims(Bn, T, H, N, D, precision)
+        rc = ssd_complex_fwd_supported(d, chunk_size)
+        if rc != SSDC_OK:
+            raise SSDCError(rc, "ssd_complex_fwd_supported")
+        nbytes = ssd_complex_fwd_workspace_bytes(d, chunk_size)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.y_re = torch.empty((Bn, T, H, D), **f32)
+        self.y_im = torch.empty((Bn, T, H, D), **f32)
+        self.fs_re = torch.empty((Bn, H, N, D), **f32)
+        self.fs_im = torch.empty((Bn, H, N, D), **f32)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, stream=None):
+        ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, self.chunk_size,
+                           precision=self.precision, y_re=self.y_re, y_im=self.y_im,
+                           fs_re=self.fs_re, fs_im=self.fs_im, workspace=self.workspace,
+                           stream=stream)
+        return self.y_re, self.y_im, self.fs_re, self.fs_im
+
+    def status(self, stream=None) -> int:
+        return ssd_complex_status(self.workspace, stream)
+
+
+def ssd_complex_fwd(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, precision="tf32"):
+    """One forward call on torch CUDA tensors; returns (y_re, y_im, fs_re, fs_im)."""
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    f = Forward(Bn, T, H, N, D, chunk_size, precision, device=x_re.device)
+    return f(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt)

@@ -1,0 +1,141 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before anything reaches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_sequence_complex_gb300 import ssdc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssdc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from state_space_sequence_complex_gb300 import build
+    build.build()
+    return ssdc.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_complex_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(ssdc.EXPORTS) == names
+
+
+def test_strerror(lib):
+    for code in range(0, -8, -1):
+        s = ssdc.strerror(code)
+        assert s and s != "unknown status"
+    assert ssdc.strerror(-99) == "unknown status"
+
+
+def test_supported_sets(lib):
+    ok = ssdc.ssd_complex_fwd_supported
+    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == 0
+    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "fp32"), 64) == 0
+    assert ok(ssdc.dims(1, 128, 2, 8, 8, "fp32"), 16) == 0
+    assert ok(ssdc.dims(1, 128, 2, 8, 8, "tf32"), 16) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 48) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 512) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 72, 64, "fp32"), 64) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 12, 64, "fp32"), 64) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(0, 128, 2, 64, 64, "fp32"), 64) == ssdc.SSDC_ERR_INVALID
+    assert ok(ssdc.dims(1, -1, 2, 64, 64, "fp32"), 64) == ssdc.SSDC_ERR_INVALID
+    assert ok(ssdc.dims(1, 128, 2, 64, 64, 7), 64) == ssdc.SSDC_ERR_INVALID
+    assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 0) == ssdc.SSDC_ERR_INVALID
+
+
+def test_workspace_bytes(lib):
+    d = ssdc.dims(2, 2048, 16, 64, 64, "tf32")
+    nb = ssdc.ssd_complex_fwd_workspace_bytes(d, 64)
+    chunks = 2 * 16 * 32
+    assert nb >= chunks * 2 * 64 * 64 * 4 + chunks * 8 + 4
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 48) == 0
+    # uneven T rounds the chunk count up
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(1, 65, 1, 64, 64, "fp32"), 64) > \
+        ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(1, 64, 1, 64, 64, "fp32"), 64)
+
+
+def _call(lib, ptrs, d, Q=64, ws=None, ws_bytes=1 << 30):
+    cin = lambda a, b: ssdc.ssdc_cin(a, b)
+    cout = lambda a, b: ssdc.ssdc_cout(a, b)
+    p = ptrs
+    return lib.ssd_complex_fwd_ws(cin(p[0], p[1]), cin(p[2], p[3]), cin(p[4], p[5]), cin(p[6], p[7]),
+                                  p[8], d, Q, cout(p[9], p[10]), cout(p[11], p[12]),
+                                  ws, ws_bytes, None)
+
+
+def fake_ptrs(d, base=1 << 32):
+    """Distinct, aligned, non-overlapping fake device addresses (never dereferenced:
+    every call below fails its host-side checks before touching the GPU)."""
+    BTH = d.B * d.T * d.H
+    sizes = [BTH * d.D] * 2 + [d.H] * 2 + [BTH * d.N] * 4 + [BTH] + [BTH * d.D] * 2 + [d.B * d.H * d.N * d.D] * 2
+    out, cur = [], base
+    for s in sizes:
+        out.append(cur)
+        cur += ((s * 4 + 4095) // 4096) * 4096
+    return out, cur
+
+
+def test_rejects_null_pointer(lib):
+    d = ssdc.dims(1, 128, 2, 64, 64, "fp32")
+    ptrs, end = fake_ptrs(d)
+    for i in range(13):
+        bad = list(ptrs)
+        bad[i] = None
+        assert _call(lib, bad, d, ws=end) == ssdc.SSDC_ERR_INVALID
+
+
+def test_rejects_misaligned_pointer(lib):
+    d = ssdc.dims(1, 128, 2, 64, 64, "fp32")
+    ptrs, end = fake_ptrs(d)
+    for i in range(13):
+        bad = list(ptrs)
+        bad[i] += 4
+        assert _call(lib, bad, d, ws=end) == ssdc.SSDC_ERR_ALIGN
+
+
+def test_rejects_bad_workspace(lib):
+    d = ssdc.dims(1, 128, 2, 64, 64, "fp32")
+    ptrs, end = fake_ptrs(d)
+    need = ssdc.ssd_complex_fwd_workspace_bytes(d, 64)
+    assert _call(lib, ptrs, d, ws=None) == ssdc.SSDC_ERR_WORKSPACE
+    assert _call(lib, ptrs, d, ws=end + 16) == ssdc.SSDC_ERR_WORKSPACE
+    assert _call(lib, ptrs, d, ws=end, ws_bytes=need - 1) == ssdc.SSDC_ERR_WORKSPACE
+
+
+def test_rejects_overlapping_outputs(lib):
+    d = ssdc.dims(1, 128, 2, 64, 64, "fp32")
+    ptrs, end = fake_ptrs(d)
+    bad = list(ptrs)
+    bad[9] = ptrs[0]          # y.re on top of x.re
+    assert _call(lib, bad, d, ws=end) == ssdc.SSDC_ERR_INVALID
+    bad = list(ptrs)
+    bad[12] = ptrs[11]        # final_state planes alias
+    assert _call(lib, bad, d, ws=end) == ssdc.SSDC_ERR_INVALID
+    bad = list(ptrs)
+    bad[9] = end              # y.re inside the workspace
+    assert _call(lib, bad, d, ws=end) == ssdc.SSDC_ERR_INVALID
+
+
+def test_rejects_unsupported_before_launch(lib):
+    d = ssdc.dims(1, 128, 2, 64, 64, "tf32")
+    ptrs, end = fake_ptrs(d)
+    assert _call(lib, ptrs, d, Q=16, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
+    d = ssdc.dims(1, 128, 2, 64, 64, 3)
+    assert _call(lib, ptrs, d, ws=end) == ssdc.SSDC_ERR_INVALID
+
+
+def test_status_null_workspace(lib):
+    assert lib.ssd_complex_status(None, None) == ssdc.SSDC_ERR_INVALID
