@@ -40,9 +40,14 @@
  * workspace and reported by ssd_complex_status().
  *
  * Precision. SSDC_PREC_TF32 runs the chunk contractions on the tcgen05 tensor
- * cores with TF32 operands and fp32 accumulation; SSDC_PREC_FP32 runs every
- * step in exact fp32 on the SIMT cores (the checking variant). The state pass
- * between chunks is fp32 in both.
+ * cores with TF32 operands and fp32 accumulation; for Q = 64, N = D = 64 it
+ * is one fused kernel that passes the chunk states between the CTAs of a
+ * thread-block cluster through distributed shared memory, otherwise the
+ * staged path below. SSDC_PREC_TF32_STAGED is the same arithmetic as three
+ * kernels (chunk states, state pass, chunk outputs) with the per-chunk states
+ * staged in the workspace. SSDC_PREC_FP32 runs every step in exact fp32 on
+ * the SIMT cores (the checking variant), staged the same way. The state pass
+ * between chunks is fp32 in all three.
  */
 #ifndef SSDC_H
 #define SSDC_H
@@ -67,9 +72,10 @@ extern "C" {
 
 #define SSDC_PREC_TF32 0
 #define SSDC_PREC_FP32 1
+#define SSDC_PREC_TF32_STAGED 2
 
 /* Problem sizes: batch B, sequence length T, heads H, complex state size N,
- * complex head dimension D; precision is SSDC_PREC_TF32 or SSDC_PREC_FP32. */
+ * complex head dimension D; precision is one of SSDC_PREC_*. */
 typedef struct {
     int64_t B, T, H, N, D;
     int32_t precision;
@@ -87,14 +93,15 @@ typedef struct {
  * Supported sizes.
  *   SSDC_PREC_FP32: chunk_size in {16, 32, 64, 128, 256};
  *                   N and D multiples of 8 in [8, 64].
- *   SSDC_PREC_TF32: chunk_size in {32, 64, 128, 256}; N = D = 64.
+ *   SSDC_PREC_TF32, SSDC_PREC_TF32_STAGED: chunk_size in {64, 128, 256};
+ *                   N = D = 64.
  * T need not be a multiple of chunk_size: the last chunk is partial.
  */
 int ssd_complex_fwd_supported(ssdc_dims dims, int chunk_size);
 
 /* Bytes of device workspace ssd_complex_fwd_ws needs for these sizes (0 on
- * invalid or unsupported sizes). It holds the per-chunk states, the per-chunk
- * decays and a device status word. */
+ * invalid or unsupported sizes). It holds a device status word and, on the
+ * staged paths, the per-chunk states and decays. */
 size_t ssd_complex_fwd_workspace_bytes(ssdc_dims dims, int chunk_size);
 
 /*

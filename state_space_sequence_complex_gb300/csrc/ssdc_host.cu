@@ -4,6 +4,7 @@
 // on the caller's stream. No allocation happens in ssd_complex_fwd_ws.
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include <cuda_runtime.h>
@@ -43,7 +44,8 @@ bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 int check_sizes(const ssdc_dims& d, int Q) {
     if (d.B <= 0 || d.T <= 0 || d.H <= 0 || d.N <= 0 || d.D <= 0 || Q <= 0) return SSDC_ERR_INVALID;
-    if (d.precision != SSDC_PREC_TF32 && d.precision != SSDC_PREC_FP32) return SSDC_ERR_INVALID;
+    if (d.precision != SSDC_PREC_TF32 && d.precision != SSDC_PREC_FP32 && d.precision != SSDC_PREC_TF32_STAGED)
+        return SSDC_ERR_INVALID;
     if (d.B > 65535 || d.H > 65535 || d.B * d.H > 65535) return SSDC_ERR_UNSUPPORTED;
     const int64_t nc = ssdc::ceil_div64(d.T, Q);
     if (nc * 4 > INT32_MAX) return SSDC_ERR_UNSUPPORTED;
@@ -59,7 +61,12 @@ int check_sizes(const ssdc_dims& d, int Q) {
     return SSDC_OK;
 }
 
+bool use_fused(const ssdc_dims& d, int Q) {
+    return d.precision == SSDC_PREC_TF32 && ssdc::fused_supported((int)d.N, (int)d.D, Q);
+}
+
 size_t ws_bytes_for(const ssdc_dims& d, int Q) {
+    if (use_fused(d, Q)) return 256;  // status word only
     const int64_t nc = ssdc::ceil_div64(d.T, Q);
     const int64_t chunks = d.B * d.H * nc;
     size_t s = (size_t)chunks * 2 * d.N * d.D * sizeof(float);
@@ -78,8 +85,13 @@ ssdc::Workspace carve(void* ws, const ssdc_dims& d, int Q) {
     char* base = static_cast<char*>(ws);
     ssdc::Workspace w;
     w.status = reinterpret_cast<int*>(base);
-    w.S = reinterpret_cast<float*>(base + 256);
-    w.a = reinterpret_cast<float*>(base + 256 + s);
+    if (use_fused(d, Q)) {
+        w.S = nullptr;
+        w.a = nullptr;
+    } else {
+        w.S = reinterpret_cast<float*>(base + 256);
+        w.a = reinterpret_cast<float*>(base + 256 + s);
+    }
     return w;
 }
 
@@ -177,6 +189,14 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const
         const dim3 cgrid((unsigned)(p.nc * lblocks), (unsigned)p.H, (unsigned)p.B);
         ssdc::ssdc_simt_chunk_scan<<<cgrid, 256, ssdc::simt_scan_smem(), stream>>>(p, w);
         record_event(++launches, stream);
+    } else if (use_fused(dims, chunk_size)) {
+        const char* env = getenv("SSDC_FUSED_CLUSTER");
+        const int force = env ? atoi(env) : 0;
+        if (force != 0 && force != 1 && force != 2 && force != 4 && force != 8) return SSDC_ERR_INVALID;
+        const int n = ssdc::fused_launch(p, w, stream, force);
+        if (n < 0) return n;
+        launches += n;
+        record_event(launches, stream);
     } else {
         int n = ssdc::tc_launch_chunk_state(p, w, stream);
         if (n < 0) return n;

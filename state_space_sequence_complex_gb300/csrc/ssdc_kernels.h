@@ -34,4 +34,10 @@ int tc_launch_chunk_state(const Problem& p, const Workspace& ws, cudaStream_t st
 int tc_launch_chunk_scan(const Problem& p, const Workspace& ws, cudaStream_t stream);
 bool tc_supported(int N, int D, int Q);
 
+// Fused single-pass TF32 kernel (state passed through distributed shared
+// memory inside thread-block clusters). force_cluster = 0 picks the cluster
+// size; 1, 2, 4 or 8 forces it.
+bool fused_supported(int N, int D, int Q);
+int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster);
+
 }  // namespace ssdc

@@ -23,89 +23,21 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include "ptx.cuh"
-#include "ssdc_common.cuh"
-#include "ssdc_kernels.h"
+#include "tc_common.cuh"
 
 namespace ssdc {
+namespace tc {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kRows = 64;                    // tokens per block (l or s)
-constexpr uint32_t kPlaneBytes = 64 * 64 * 4;  // one 64 x 64 fp32 plane: two 8 KB swizzle halves
-constexpr uint32_t kHalfBytes = kPlaneBytes / 2;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kWaitIters = 1u << 22;
-
 // Column offsets inside the CTA's TMEM allocation.
 constexpr uint32_t kW1 = 0, kW2 = 64, kAccA = 128, kAccB = 192;
 
-constexpr uint32_t kIdesc = ptx::idesc_tf32(128, 64, 0);  // M = 128, N = 64, B operand K-major
-
-// Element (r, c) of a 64 x 64 fp32 plane staged by TMA as two boxes of
-// 64 rows x 32 floats with the 128-byte swizzle (16-byte chunk index XOR row%8).
-__device__ __forceinline__ float plane_ld(const float* plane, int r, int c) {
-    const int half = c >> 5, cc = c & 31;
-    const char* p = reinterpret_cast<const char*>(plane) + half * kHalfBytes + r * 128 +
-                    ((((cc >> 2) ^ (r & 7)) << 4) | ((cc & 3) << 2));
-    return *reinterpret_cast<const float*>(p);
-}
-
-// B operand "K-major": the plane's rows are the MMA's N index, its columns
-// the K index (B[n][k]); K-step k covers columns 8k .. 8k+7.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t plane_saddr, int k) {
-    const uint32_t start = plane_saddr + (uint32_t)(k >> 2) * kHalfBytes + (uint32_t)(k & 3) * 32u;
-    return ptx::smem_desc_sw128(start, 16u, 1024u);
-}
-
-// Transpose the two planes of a staged 64 x 64 tile (rows r, columns c) into
-// the same swizzled layout with rows and columns exchanged, so that a tile
-// whose rows are the contraction index becomes a K-major MMA operand (the
-// TF32 MMA takes K-major operands only). Each thread moves 4 x 4 blocks with
-// 16-byte loads and stores; the caller synchronises and fences for the MMA.
-__device__ __forceinline__ void transpose_tile(const float* src, float* dst) {
-    for (int blk = threadIdx.x; blk < 2 * 256; blk += kThreads) {
-        const int plane = blk >> 8, rb = (blk >> 4) & 15, cb = blk & 15;
-        const char* sp = reinterpret_cast<const char*>(src) + plane * kPlaneBytes + (cb >> 3) * kHalfBytes;
-        char* dp = reinterpret_cast<char*>(dst) + plane * kPlaneBytes + (rb >> 3) * kHalfBytes;
-        float4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 4 * rb + i;
-            v[i] = *reinterpret_cast<const float4*>(sp + r * 128 + ((((cb & 7) ^ (r & 7))) << 4));
-        }
-        const float4 o0 = make_float4(v[0].x, v[1].x, v[2].x, v[3].x);
-        const float4 o1 = make_float4(v[0].y, v[1].y, v[2].y, v[3].y);
-        const float4 o2 = make_float4(v[0].z, v[1].z, v[2].z, v[3].z);
-        const float4 o3 = make_float4(v[0].w, v[1].w, v[2].w, v[3].w);
-        const float4 o[4] = {o0, o1, o2, o3};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = 4 * cb + j;
-            *reinterpret_cast<float4*>(dp + r * 128 + ((((rb & 7) ^ (r & 7))) << 4)) = o[j];
-        }
-    }
-}
-
-__device__ __forceinline__ uint32_t lane_base(uint32_t tmem) {
-    const uint32_t warp = threadIdx.x >> 5;
-    return tmem + ((warp * 32u) << 16);
-}
-
-__device__ __forceinline__ void fail(int* status) { atomicExch(status, SSDC_ERR_TIMEOUT); }
-
-// Store 64 columns (4 x 16) of this thread's lane.
-__device__ __forceinline__ void tmem_store64(uint32_t taddr, const float* v) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) ptx::tmem_st16(taddr + 16 * q, v + 16 * q);
-}
-
-__device__ __forceinline__ void tmem_load64(uint32_t taddr, float* v) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) ptx::tmem_ld16(taddr + 16 * q, v + 16 * q);
-    ptx::tmem_wait_ld();
-}
-
+// ------------------------------------------------------------------------
+// Chunk state: S_loc[n, d] = sum_s (dec[s] B[s, n]) x[s, d], written as
+// S_loc^T (d rows, n contiguous) per plane; a_c = exp(Acs[Q-1]).
+// TMEM: W1, W2 (the dec o B^T windows), kAccA = accumulator.
 // All threads: make this thread's tcgen05.st visible, then thread 0 may
 // issue MMAs reading them.
 __device__ __forceinline__ void publish_tmem_writes() {
@@ -115,25 +47,6 @@ __device__ __forceinline__ void publish_tmem_writes() {
     ptx::tc_fence_after();
 }
 
-// Issue D (+)= W1 * B1 + W2 * B2 over K = 64 (8 MMAs of K = 8 each); B1, B2
-// are K-major 64 x 64 planes in shared memory.
-__device__ __forceinline__ void issue_pair(uint32_t d, uint32_t w1, uint32_t w2, uint32_t b1, uint32_t b2,
-                                           bool accumulate) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        ptx::mma_tf32_ts(d, w1 + 8 * k, desc_kmajor(b1, k), kIdesc, (accumulate || k > 0) ? 1u : 0u);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) ptx::mma_tf32_ts(d, w2 + 8 * k, desc_kmajor(b2, k), kIdesc, 1u);
-}
-
-struct TcMaps {
-    CUtensorMap x_re, x_im, B_re, B_im, C_re, C_im, S;
-};
-
-// ------------------------------------------------------------------------
-// Chunk state: S_loc[n, d] = sum_s (dec[s] B[s, n]) x[s, d], written as
-// S_loc^T (d rows, n contiguous) per plane; a_c = exp(Acs[Q-1]).
-// TMEM: W1, W2 (the dec o B^T windows), kAccA = accumulator.
 struct StateSmem {
     float b[2][64 * 64];  // B block: re, im planes
     float x[2][64 * 64];  // x block: re, im planes
@@ -168,7 +81,7 @@ tc_chunk_state(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem;
-    const uint32_t my = lane_base(tmem);
+    const uint32_t my = lane_base(tmem, warp);
 
     const uint32_t sb_re = ptx::smem_addr(sm.b[0]), sb_im = ptx::smem_addr(sm.b[1]);
     const uint32_t sx_re = ptx::smem_addr(sm.x[0]), sx_im = ptx::smem_addr(sm.x[1]);
@@ -206,10 +119,10 @@ tc_chunk_state(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
             w1[s] = part ? a.y : a.x;
             w2[s] = part ? a.x : -a.y;
         }
-        tmem_store64(my + kW1, w1);
-        tmem_store64(my + kW2, w2);
+        tmem_store<64>(my + kW1, w1);
+        tmem_store<64>(my + kW2, w2);
         __syncthreads();  // every thread is done reading B
-        transpose_tile(sm.x[0], sm.b[0]);  // x^T (d rows, s contiguous) into the B buffer
+        transpose_tile<kThreads>(sm.x[0], sm.b[0], tid);  // x^T (d rows, s contiguous) into the B buffer
         ptx::fence_proxy_async_smem();
         publish_tmem_writes();
         if (tid == 0) {
@@ -227,7 +140,7 @@ tc_chunk_state(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
 
     // epilogue: lane 2n+part holds plane `part` of S_loc[n, 0..63]
     float v[64];
-    tmem_load64(my + kAccA, v);
+    tmem_load<64>(my + kAccA, v);
     const int64_t chunk = ((int64_t)b * H + h) * p.nc + c;
     float* S = ws.S + (chunk * 2 + part) * 64 * 64;
 #pragma unroll
@@ -287,7 +200,7 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem;
-    const uint32_t my = lane_base(tmem);
+    const uint32_t my = lane_base(tmem, warp);
 
     auto load_bx = [&](int s0) {
         ptx::mbar_arrive_expect_tx(&sm.bar_bx, 4 * kPlaneBytes);
@@ -333,8 +246,8 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
                 w1[k] = part ? ci : cr;
                 w2[k] = part ? cr : -ci;
             }
-            tmem_store64(my + kW1, w1);
-            tmem_store64(my + kW2, w2);
+            tmem_store<64>(my + kW1, w1);
+            tmem_store<64>(my + kW2, w2);
         }
         publish_tmem_writes();
         if (tid == 0) {
@@ -345,12 +258,12 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
         ph_mma ^= 1;
         ptx::tc_fence_after();
         // the C B^T MMA has consumed B: x^T (d rows, s contiguous) goes into its buffer
-        transpose_tile(sm.x[0], sm.b[0]);
+        transpose_tile<kThreads>(sm.x[0], sm.b[0], tid);
         ptx::fence_proxy_async_smem();
 
         // P = G o L; this thread takes columns s = 2j + part
         float g[64];
-        tmem_load64(my + kAccA, g);
+        tmem_load<64>(my + kAccA, g);
         float pr[32], pi[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -381,8 +294,8 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
                 w2[2 * j] = part ? re_e : -im_e;
                 w2[2 * j + 1] = part ? re_o : -im_o;
             }
-            tmem_store64(my + kW1, w1);
-            tmem_store64(my + kW2, w2);
+            tmem_store<64>(my + kW1, w1);
+            tmem_store<64>(my + kW2, w2);
         }
         publish_tmem_writes();
         if (tid == 0) {
@@ -418,8 +331,8 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
             w1[k] = part ? cv.y : cv.x;
             w2[k] = part ? cv.x : -cv.y;
         }
-        tmem_store64(my + kW1, w1);
-        tmem_store64(my + kW2, w2);
+        tmem_store<64>(my + kW1, w1);
+        tmem_store<64>(my + kW2, w2);
     }
     if (!ptx::mbar_wait(&sm.bar_s, 0, kWaitIters)) fail(ws.status);
     publish_tmem_writes();
@@ -431,7 +344,7 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
     ptx::tc_fence_after();
 
     float v[64];
-    tmem_load64(my + kAccB, v);
+    tmem_load<64>(my + kAccB, v);
     if (l0 + l < nvalid) {
         float* yp = (part ? p.y_im : p.y_re) + ((((int64_t)b * p.T + t0 + l0 + l) * H + h) * 64);
         float4* y4 = reinterpret_cast<float4*>(yp);
@@ -458,15 +371,24 @@ bool get_encoder() {
     return true;
 }
 
-// (F, H, T, B) fp32 plane, box (32, 1, 64, 1), 128-byte swizzle, zero fill.
-bool make_feature_map(CUtensorMap* m, const float* base, int F, int H, int64_t T, int B) {
+}  // namespace
+
+// (F, H, T, B) fp32 plane, box (32, 1, rows, 1), 128-byte swizzle, zero fill.
+bool encode_feature_map(CUtensorMap* m, const float* base, int F, int H, int64_t T, int B, int rows) {
+    if (!get_encoder()) return false;
     cuuint64_t dims[4] = {(cuuint64_t)F, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)F * 4, (cuuint64_t)F * H * 4, (cuuint64_t)F * H * 4 * (cuuint64_t)T};
-    cuuint32_t box[4] = {32, 1, 64, 1};
+    cuuint32_t box[4] = {32, 1, (cuuint32_t)rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+bool make_feature_map(CUtensorMap* m, const float* base, int F, int H, int64_t T, int B) {
+    return encode_feature_map(m, base, F, H, T, B, 64);
 }
 
 // Workspace states as rows of 64 floats, box (32, 64).
@@ -480,7 +402,9 @@ bool make_state_map(CUtensorMap* m, const float* base, int64_t rows) {
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int make_maps(const Problem& p, const Workspace& ws, TcMaps* m) {
+}  // namespace
+
+int make_maps(const Problem& p, const float* ws_S, TcMaps* m) {
     if (!get_encoder()) return SSDC_ERR_CUDA;
     bool ok = make_feature_map(&m->x_re, p.x_re, 64, p.H, p.T, p.B) &&
               make_feature_map(&m->x_im, p.x_im, 64, p.H, p.T, p.B) &&
@@ -488,9 +412,11 @@ int make_maps(const Problem& p, const Workspace& ws, TcMaps* m) {
               make_feature_map(&m->B_im, p.B_im, 64, p.H, p.T, p.B) &&
               make_feature_map(&m->C_re, p.C_re, 64, p.H, p.T, p.B) &&
               make_feature_map(&m->C_im, p.C_im, 64, p.H, p.T, p.B) &&
-              make_state_map(&m->S, ws.S, (int64_t)p.B * p.H * p.nc * 2 * 64);
+              (ws_S == nullptr || make_state_map(&m->S, ws_S, (int64_t)p.B * p.H * p.nc * 2 * 64));
     return ok ? SSDC_OK : SSDC_ERR_CUDA;
 }
+
+namespace {
 
 constexpr size_t kStateSmem = sizeof(StateSmem) + 1024;
 constexpr size_t kScanSmem = sizeof(ScanSmem) + 1024;
@@ -514,28 +440,29 @@ int set_attrs() {
 }
 
 }  // namespace
+}  // namespace tc
 
 bool tc_supported(int N, int D, int Q) { return N == 64 && D == 64 && (Q == 64 || Q == 128 || Q == 256); }
 
 int tc_launch_chunk_state(const Problem& p, const Workspace& ws, cudaStream_t stream) {
-    int rc = set_attrs();
+    int rc = tc::set_attrs();
     if (rc != SSDC_OK) return rc;
-    TcMaps maps;
-    rc = make_maps(p, ws, &maps);
+    tc::TcMaps maps;
+    rc = tc::make_maps(p, ws.S, &maps);
     if (rc != SSDC_OK) return rc;
     const dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
-    tc_chunk_state<<<grid, kThreads, kStateSmemLaunch, stream>>>(p, ws, maps);
+    tc::tc_chunk_state<<<grid, tc::kThreads, tc::kStateSmemLaunch, stream>>>(p, ws, maps);
     return 1;
 }
 
 int tc_launch_chunk_scan(const Problem& p, const Workspace& ws, cudaStream_t stream) {
-    int rc = set_attrs();
+    int rc = tc::set_attrs();
     if (rc != SSDC_OK) return rc;
-    TcMaps maps;
-    rc = make_maps(p, ws, &maps);
+    tc::TcMaps maps;
+    rc = tc::make_maps(p, ws.S, &maps);
     if (rc != SSDC_OK) return rc;
-    const dim3 grid((unsigned)(p.nc * (p.Q / kRows)), (unsigned)p.H, (unsigned)p.B);
-    tc_chunk_scan<<<grid, kThreads, kScanSmem, stream>>>(p, ws, maps);
+    const dim3 grid((unsigned)(p.nc * (p.Q / tc::kRows)), (unsigned)p.H, (unsigned)p.B);
+    tc::tc_chunk_scan<<<grid, tc::kThreads, tc::kScanSmem, stream>>>(p, ws, maps);
     return 1;
 }
 

@@ -21,7 +21,7 @@ SSDC_ERR_CUDA = -5
 SSDC_ERR_TIMEOUT = -6
 SSDC_ERR_DEVICE = -7
 
-PREC = {"tf32": 0, "fp32": 1}
+PREC = {"tf32": 0, "fp32": 1, "tf32_staged": 2}
 
 # Every symbol include/ssdc.h declares.
 EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_complex_fwd_ws",

@@ -54,13 +54,20 @@ def test_supported_sets(lib):
     assert ok(ssdc.dims(1, -1, 2, 64, 64, "fp32"), 64) == ssdc.SSDC_ERR_INVALID
     assert ok(ssdc.dims(1, 128, 2, 64, 64, 7), 64) == ssdc.SSDC_ERR_INVALID
     assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 0) == ssdc.SSDC_ERR_INVALID
+    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 64) == 0
+    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 32) == ssdc.SSDC_ERR_UNSUPPORTED
 
 
 def test_workspace_bytes(lib):
-    d = ssdc.dims(2, 2048, 16, 64, 64, "tf32")
-    nb = ssdc.ssd_complex_fwd_workspace_bytes(d, 64)
     chunks = 2 * 16 * 32
-    assert nb >= chunks * 2 * 64 * 64 * 4 + chunks * 8 + 4
+    for prec in ("fp32", "tf32_staged"):
+        d = ssdc.dims(2, 2048, 16, 64, 64, prec)
+        nb = ssdc.ssd_complex_fwd_workspace_bytes(d, 64)
+        assert nb >= chunks * 2 * 64 * 64 * 4 + chunks * 8 + 4
+    # the fused tensor-core path keeps the chunk states on chip: status word only
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == 256
+    # at other chunk sizes the TF32 path stages the states
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 128) > 256
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 48) == 0
     # uneven T rounds the chunk count up
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(1, 65, 1, 64, 64, "fp32"), 64) > \

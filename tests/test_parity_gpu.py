@@ -93,3 +93,31 @@ def test_launch_count_and_reuse():
     # a second call on the same workspace gives the same answer
     y, s, _ = run_library(inp, 64, "fp32", dev=dev, forward=f)
     assert_close(y, s, *ref, "fp32")
+
+
+@pytest.mark.parametrize("T,Q", [(64, 64), (1000, 64), (300, 128), (511, 256), (100, 64)])
+def test_staged_tf32_path(T, Q):
+    inp = inputs.custom(2, T, 3, 64, 64, seed=2000 + T + Q)
+    check(inp, Q, "tf32_staged", f"staged T={T} Q={Q}")
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+def test_fused_cluster_sizes(cluster, monkeypatch):
+    # several sequences per cluster, a partial last chunk, more chunks than CTAs
+    monkeypatch.setenv("SSDC_FUSED_CLUSTER", str(cluster))
+    inp = inputs.custom(2, 64 * 9 + 13, 3, 64, 64, seed=3000 + cluster)
+    check(inp, 64, "tf32", f"fused cluster {cluster}")
+
+
+def test_fused_fewer_chunks_than_cluster(monkeypatch):
+    monkeypatch.setenv("SSDC_FUSED_CLUSTER", "8")
+    inp = inputs.custom(1, 130, 2, 64, 64, seed=31)   # 3 chunks on an 8-CTA cluster
+    check(inp, 64, "tf32", "3 chunks, cluster 8")
+
+
+def test_fused_single_launch_and_small_workspace():
+    d = ssdc.dims(2, 2048, 16, 64, 64, "tf32")
+    assert ssdc.ssd_complex_fwd_workspace_bytes(d, 64) == 256
+    inp = inputs.custom(1, 256, 2, 64, 64, seed=8)
+    _, _, f = run_library(inp, 64, "tf32")
+    assert ssdc.last_launch_count() == 1
