@@ -20,23 +20,22 @@
 //
 // Complex products. Planar re/im operands are multiplied as real M=128 MMAs
 // whose A operand holds the real and imaginary rows of the left factor
-// interleaved in groups of eight (row 16g + 8p + i = plane p of row 8g + i).
-// Two accumulators, A * Br and A * Bi, then hold in TMEM lanes m and m ^ 8
-// (the same warp) all four real products, so
+// interleaved in groups of eight (row 16g + 8p + i = plane p of row 8g + i)
+// and whose B operand stacks or interleaves the right factor's two planes as
+// 128 rows (N = 128). One accumulator then holds, in TMEM lanes m and m ^ 8
+// (the same warp), all four real products, and
 //     Re = (A_r B_r)[lane p=0] - (A_i B_i)[lane p=1]
 //     Im = (A_r B_i)[lane p=0] + (A_i B_r)[lane p=1]
 // is one exchange between partner lanes. The C tile is loaded in that layout
-// by TMA (8-row boxes); x^T is written in it by a shared-memory transpose and
-// serves both as an interleaved A operand and, read with a 2 KB group
-// stride, as two planar B operands.
+// by TMA (8-row boxes); x^T is written in it by a shared-memory transpose.
+// The output accumulator takes both P x (Y_diag) and (C o exp(Acs)) S_in
+// (Y_off): the two A operands, P and C', are rows written to TMEM.
 //
-// Roles in a CTA (288 threads):
-//   warps 0-7  workers: transposes, decay mask, state hop, epilogue; worker
-//              thread 0 issues the tcgen05 MMAs
-//   warp 8     producer: TMA loads of the next chunk's C, B, x tiles into a
-//              two-stage ring, dt and the in-chunk cumulative log-decay
-// Worker warps w and w + 4 share TMEM lane quadrant w % 4 and split the
-// 64 columns of each accumulator row between them (h = w / 4).
+// Threads. 16 warps; warps w and w + 4k share TMEM lane quadrant w % 4 and
+// split a row's 64 columns in quarters (k = w / 4). Worker thread 0 issues
+// the MMAs and the TMA stores of y; warp 15 also issues the TMA loads of the
+// next chunk's C, B, x tiles into the other stage of a two-stage ring and
+// computes its cumulative log-decay.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,30 +48,29 @@ namespace {
 using namespace tc;
 
 constexpr int kQ = 64;
-constexpr int kWorkers = 256;
-constexpr int kThreads = kWorkers + 32;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kLoader = kWarps - 1;  // warp that prefetches the next chunk
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: pairs of 64-column accumulators (A * Br | A * Bi) and the
-// P operand (64 columns). The C B^T pair is reused for C S_in.
-constexpr uint32_t kAccG = 0, kAccS = 128, kAccY = 256, kPwin = 384;
+// TMEM columns: three 128-column accumulators and two 64-column A operands.
+constexpr uint32_t kAccG = 0, kAccS = 128, kAccY = 256, kPwin = 384, kCwin = 448;
 constexpr uint32_t kTileBytes = 2 * kPlaneBytes;  // 32 KB: one complex 64 x 64 tile
 constexpr uint32_t kStageTx = 3 * kTileBytes;     // C, B, x
 constexpr uint32_t kStateBytes = kTileBytes;
 constexpr uint32_t kIntHalf = 16384;  // one 32-column half of a 128-row tile
 constexpr uint32_t kIdesc128 = ptx::idesc_tf32(128, 128, 0);  // M = 128, N = 128, B operand K-major
-constexpr uint32_t kBarWorkers = 1;   // named barrier id of the worker warps
 
 struct Smem {
     float c[2][64 * 128];    // [stage] C, interleaved 128 rows (A operand)
     float b[2][64 * 128];    // [stage] B, stacked (rows s); after C B^T, (dec o B)^T stacked (rows n)
     float x[2][64 * 128];    // [stage] x, stacked (rows s); x^T interleaved (rows d); then y staging
-    float sin[64 * 128];     // incoming state S_in^T, stacked (rows d, n contiguous)
+    float sin[64 * 128];     // incoming state S_in^T, interleaved (rows d, n contiguous)
     float2 acs[2][kQ];       // in-chunk cumulative log-decay, per stage
     float2 dec[kQ];          // exp(Acs[Q-1] - Acs[s])
     float2 eacs[kQ];         // exp(Acs[l])
     float2 a_c;              // exp(Acs[Q-1])
-    uint64_t full[2], empty[2], sin_full, succ_empty;
-    uint64_t mma[4];         // one per MMA group (C B^T, S_loc^T, Y_diag, C S_in), one phase per chunk
+    uint64_t full[2], sin_full, succ_empty;
+    uint64_t mma[3];         // MMA groups C B^T, S_loc^T, y; one phase per chunk
     uint32_t tmem;
 };
 
@@ -100,10 +98,9 @@ struct Items {
 __device__ __forceinline__ float2 cdiff(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
 
 // Byte offsets. A "stacked" tile holds two 64 x 64 planes as one K-major
-// operand of 128 rows: [32-column half][plane][64 rows][128 B], so that a
-// descriptor over 128 rows covers plane 0 (rows 0-63) and plane 1 (rows
-// 64-127). An "interleaved" tile is [32-column half][128 rows][128 B] with
-// row 16g + 8p + i = plane p of row 8g + i. Rows are 128-byte swizzled.
+// operand of 128 rows: [32-column half][plane][64 rows][128 B]. An
+// "interleaved" tile is [32-column half][128 rows][128 B] with row
+// 16g + 8p + i = plane p of row 8g + i. Rows are 128-byte swizzled.
 __device__ __forceinline__ uint32_t stk_row(int khalf, int plane, int r) {
     return (uint32_t)(khalf * kIntHalf + plane * kHalfBytes + r * 128);
 }
@@ -122,6 +119,76 @@ __device__ __forceinline__ uint64_t desc_k(uint64_t d, int k) {
 __device__ __forceinline__ void issue_ss128(uint32_t d, uint64_t da, uint64_t db) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) ptx::mma_tf32_ss(d, desc_k(da, k), desc_k(db, k), kIdesc128, k > 0 ? 1u : 0u);
+}
+__device__ __forceinline__ void issue_ts128(uint32_t d, uint32_t a_tmem, uint64_t db, bool accumulate) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        ptx::mma_tf32_ts(d, a_tmem + 8 * k, desc_k(db, k), kIdesc128, (accumulate || k > 0) ? 1u : 0u);
+}
+
+// Loader warp: TMA of one chunk's C (8-row boxes, re/im interleaved), B and
+// x (stacked) into stage `st`, counted on `bar`. The 40 copies are issued by
+// the warp's lanes in parallel after lane 0 has announced the bytes.
+__device__ __forceinline__ void load_tiles(Smem& sm, int st, const TcMaps& maps, const CUtensorMap& c8_re,
+                                           const CUtensorMap& c8_im, int h, int t0, int b, int lane) {
+    uint64_t* bar = &sm.full[st];
+    if (lane == 0) ptx::mbar_expect_tx(bar, kStageTx);
+    __syncwarp();
+    char* cb = reinterpret_cast<char*>(sm.c[st]);
+    char* bb = reinterpret_cast<char*>(sm.b[st]);
+    char* xb = reinterpret_cast<char*>(sm.x[st]);
+    for (int op = lane; op < 40; op += 32) {
+        const int half = op / 20, k = op % 20, f0 = 32 * half;
+        if (k < 16) {  // C rows 8g .. 8g+7 of plane k & 1
+            const int g = k >> 1, pl = k & 1;
+            ptx::tma_load_4d(cb + inter_row(half, 16 * g + 8 * pl), pl ? &c8_im : &c8_re, bar, f0, h, t0 + 8 * g, b);
+        } else {
+            const int pl = k & 1;
+            const CUtensorMap* m = k < 18 ? (pl ? &maps.B_im : &maps.B_re) : (pl ? &maps.x_im : &maps.x_re);
+            ptx::tma_load_4d((k < 18 ? bb : xb) + stk_row(half, pl, 0), m, bar, f0, h, t0, b);
+        }
+    }
+}
+
+// Loader warp: dt of one chunk's 64 tokens (two per lane; tokens past T are
+// marked with NaN so that they get zero log-decay), and A of its head. The
+// loads are only issued here; their values are first used by store_acs.
+struct Alog {
+    float dt0, dt1, Ar, Ai;
+};
+__device__ __forceinline__ Alog load_alog(const Problem& p, int b, int h, int64_t t0, int lane) {
+    Alog a;
+    const int64_t ta = t0 + 2 * lane, tb = ta + 1;
+    a.dt0 = ta < p.T ? p.dt[((int64_t)b * p.T + ta) * p.H + h] : __int_as_float(0x7fffffff);
+    a.dt1 = tb < p.T ? p.dt[((int64_t)b * p.T + tb) * p.H + h] : __int_as_float(0x7fffffff);
+    a.Ar = p.A_re[h];
+    a.Ai = p.A_im[h];
+    return a;
+}
+
+// Loader warp: discretisation softplus(dt) * A and its inclusive cumulative
+// sum into acs, then arrive on the stage barrier (the tile bytes were
+// announced by load_tiles). The sum is fp32: its rounding (about 1e-7 of
+// |Acs|, so about 1e-5 relative on a decay factor) is far below TF32's.
+__device__ __forceinline__ void store_acs(Smem& sm, int st, const Alog& al, int lane) {
+    const float sp0 = al.dt0 == al.dt0 ? softplus_f(al.dt0) : 0.0f;
+    const float sp1 = al.dt1 == al.dt1 ? softplus_f(al.dt1) : 0.0f;
+    const float r0 = sp0 * al.Ar, i0 = sp0 * al.Ai, r1 = sp1 * al.Ar, i1 = sp1 * al.Ai;
+    float cr = r0 + r1, ci = i0 + i1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float ur = __shfl_up_sync(0xffffffffu, cr, off);
+        const float ui = __shfl_up_sync(0xffffffffu, ci, off);
+        if (lane >= off) {
+            cr += ur;
+            ci += ui;
+        }
+    }
+    const float er = cr - (r0 + r1), ei = ci - (i0 + i1);  // exclusive prefix
+    sm.acs[st][2 * lane] = make_float2(er + r0, ei + i0);
+    sm.acs[st][2 * lane + 1] = make_float2(cr, ci);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&sm.full[st]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -144,11 +211,8 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
         return;
     }
     if (tid == 0) {
-        for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(&sm.full[s], 1);
-            ptx::mbar_init(&sm.empty[s], 1);
-        }
-        for (int g = 0; g < 4; ++g) ptx::mbar_init(&sm.mma[g], 1);
+        for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.full[s], 1);
+        for (int g = 0; g < 3; ++g) ptx::mbar_init(&sm.mma[g], 1);
         ptx::mbar_init(&sm.sin_full, 1);
         ptx::mbar_init(&sm.succ_empty, 1);
         ptx::fence_mbar_init();
@@ -164,127 +228,85 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
     ptx::cluster_sync();  // peers' barriers are initialised before any remote access
     const uint32_t tmem = sm.tmem;
 
-    if (warp == kWorkers / 32) {
-        // ------------------------------------------------------- producer
-        for (int64_t it = 0; it < nitems; ++it) {
-            const int s = (int)(it & 1);
-            if (it >= 2 && !ptx::mbar_wait(&sm.empty[s], (uint32_t)(((it >> 1) & 1) ^ 1), kWaitIters))
-                fail(ws.status);
-            int64_t q, c;
-            items.get(it, q, c);
-            const int b = (int)(q / H), h = (int)(q % H);
-            const int64_t t0 = c * kQ;
-            if (lane == 0) {
-                ptx::mbar_expect_tx(&sm.full[s], kStageTx);
-                char* cb = reinterpret_cast<char*>(sm.c[s]);
-                char* bb = reinterpret_cast<char*>(sm.b[s]);
-                char* xb = reinterpret_cast<char*>(sm.x[s]);
-                for (int half = 0; half < 2; ++half) {
-                    const int f0 = 32 * half;
-                    // C as 8-row boxes, re and im groups interleaved
-                    for (int g = 0; g < 8; ++g) {
-                        ptx::tma_load_4d(cb + inter_row(half, 16 * g), &c8_re, &sm.full[s], f0, h, (int)t0 + 8 * g, b);
-                        ptx::tma_load_4d(cb + inter_row(half, 16 * g + 8), &c8_im, &sm.full[s], f0, h, (int)t0 + 8 * g, b);
-                    }
-                    ptx::tma_load_4d(bb + stk_row(half, 0, 0), &maps.B_re, &sm.full[s], f0, h, (int)t0, b);
-                    ptx::tma_load_4d(bb + stk_row(half, 1, 0), &maps.B_im, &sm.full[s], f0, h, (int)t0, b);
-                    ptx::tma_load_4d(xb + stk_row(half, 0, 0), &maps.x_re, &sm.full[s], f0, h, (int)t0, b);
-                    ptx::tma_load_4d(xb + stk_row(half, 1, 0), &maps.x_im, &sm.full[s], f0, h, (int)t0, b);
-                }
-            }
-            // discretisation and in-chunk inclusive cumulative sum (fp64 accumulation)
-            const float Ar = p.A_re[h], Ai = p.A_im[h];
-            double r0 = 0.0, i0 = 0.0, r1 = 0.0, i1 = 0.0;
-            {
-                const int64_t ta = t0 + 2 * lane, tb = ta + 1;
-                if (ta < p.T) {
-                    const float sp = softplus_f(p.dt[((int64_t)b * p.T + ta) * H + h]);
-                    r0 = (double)(sp * Ar);
-                    i0 = (double)(sp * Ai);
-                }
-                if (tb < p.T) {
-                    const float sp = softplus_f(p.dt[((int64_t)b * p.T + tb) * H + h]);
-                    r1 = (double)(sp * Ar);
-                    i1 = (double)(sp * Ai);
-                }
-            }
-            double cr = r0 + r1, ci = i0 + i1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const double ur = __shfl_up_sync(0xffffffffu, cr, off);
-                const double ui = __shfl_up_sync(0xffffffffu, ci, off);
-                if (lane >= off) {
-                    cr += ur;
-                    ci += ui;
-                }
-            }
-            const double er = cr - (r0 + r1), ei = ci - (i0 + i1);  // exclusive prefix
-            sm.acs[s][2 * lane] = make_float2((float)(er + r0), (float)(ei + i0));
-            sm.acs[s][2 * lane + 1] = make_float2((float)(er + r0 + r1), (float)(ei + i0 + i1));
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sm.full[s]);
+    // first chunk's tiles and decays
+    if (warp == kLoader && nitems > 0) {
+        int64_t q0, c0;
+        items.get(0, q0, c0);
+        const int b0 = (int)(q0 / H), h0 = (int)(q0 % H);
+        load_tiles(sm, 0, maps, c8_re, c8_im, h0, (int)(c0 * kQ), b0, lane);
+        store_acs(sm, 0, load_alog(p, b0, h0, c0 * kQ, lane), lane);
+    }
+
+    const int h4 = warp >> 2;                   // column quarter of this warp
+    const int m = (warp & 3) * 32 + lane;       // TMEM lane
+    const int r8 = 8 * (m >> 4) + (m & 7);      // complex row (l or d) of this lane
+    const int pl = (m >> 3) & 1;                // plane of this lane
+    const uint32_t my = lane_base(tmem, warp);
+    uint32_t n_recv = 0, n_send = 0;
+    const uint32_t sin_saddr = ptx::smem_addr(sm.sin);
+    const uint32_t remote_sin = ptx::mapa(sin_saddr, succ);
+    const uint32_t remote_sin_full = ptx::mapa(ptx::smem_addr(&sm.sin_full), succ);
+    const uint32_t remote_pred_empty = ptx::mapa(ptx::smem_addr(&sm.succ_empty), pred);
+
+    auto wait_mma = [&](int g, int64_t it) {
+        if (!ptx::mbar_wait(&sm.mma[g], (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
+        ptx::tc_fence_after();
+    };
+    auto publish = [&]() {  // tcgen05.st and smem writes of all threads -> MMA issue
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+    };
+
+    // dt of chunk it + 1 is loaded during chunk it - 1 and consumed during chunk it
+    Alog nal = {};
+    if (warp == kLoader && nitems > 1) {
+        int64_t q1, c1;
+        items.get(1, q1, c1);
+        nal = load_alog(p, (int)(q1 / H), (int)(q1 % H), c1 * kQ, lane);
+    }
+    for (int64_t it = 0; it < nitems; ++it) {
+        const int s = (int)(it & 1);
+        int64_t q, c;
+        items.get(it, q, c);
+        const int b = (int)(q / H), h = (int)(q % H);
+        const int64_t t0 = c * kQ;
+        const bool has_in = c > 0, last = c == p.nc - 1;
+        char* xbase = reinterpret_cast<char*>(sm.x[s]);
+        char* bbase = reinterpret_cast<char*>(sm.b[s]);
+        const char* cbase = reinterpret_cast<const char*>(sm.c[s]);
+        const uint32_t cs = ptx::smem_addr(cbase), bs = ptx::smem_addr(bbase), xs = ptx::smem_addr(xbase);
+        if (!ptx::mbar_wait(&sm.full[s], (uint32_t)((it >> 1) & 1), kWaitIters)) fail(ws.status);
+        if (tid == 0) {
+            // C B^T reads only TMA-loaded tiles: issue it first
+            ptx::tc_fence_after();
+            issue_ss128(tmem + kAccG, desc128(cs), desc128(bs));  // [C Br | C Bi]
+            ptx::mma_commit(&sm.mma[0]);
+            ptx::bulk_wait_read_all();  // the previous chunk's y store has read its stage
         }
-    } else {
-        // -------------------------------------------------------- workers
-        const int h2 = warp >> 2;                   // column half of this warp
-        const int m = (warp & 3) * 32 + lane;       // TMEM lane
-        const int r8 = 8 * (m >> 4) + (m & 7);      // complex row (l or d) of this lane
-        const int pl = (m >> 3) & 1;                // plane of this lane
-        const uint32_t my = lane_base(tmem, warp);
-        uint32_t n_recv = 0, n_send = 0;
-        const uint32_t sin_saddr = ptx::smem_addr(sm.sin);
-        const uint32_t remote_sin = ptx::mapa(sin_saddr, succ);
-        const uint32_t remote_sin_full = ptx::mapa(ptx::smem_addr(&sm.sin_full), succ);
-        const uint32_t remote_pred_empty = ptx::mapa(ptx::smem_addr(&sm.succ_empty), pred);
 
-        // MMA group g of item `it` completes phase `it` of barrier mma[g]
-        auto wait_mma = [&](int g, int64_t it) {
-            if (!ptx::mbar_wait(&sm.mma[g], (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
-            ptx::tc_fence_after();
-        };
-        auto publish = [&]() {  // tcgen05.st and smem writes of all workers -> MMA issue
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::named_sync(kBarWorkers, kWorkers);
-            ptx::tc_fence_after();
-        };
-
-        for (int64_t it = 0; it < nitems; ++it) {
-            const int s = (int)(it & 1);
-            int64_t q, c;
-            items.get(it, q, c);
-            const int b = (int)(q / H), h = (int)(q % H);
-            const int64_t t0 = c * kQ;
-            const bool has_in = c > 0, last = c == p.nc - 1;
-            char* cbase = reinterpret_cast<char*>(sm.c[s]);
-            char* bbase = reinterpret_cast<char*>(sm.b[s]);
-            char* xbase = reinterpret_cast<char*>(sm.x[s]);
-            const uint32_t cs = ptx::smem_addr(cbase), bs = ptx::smem_addr(bbase), xs = ptx::smem_addr(xbase);
-            if (!ptx::mbar_wait(&sm.full[s], (uint32_t)((it >> 1) & 1), kWaitIters)) fail(ws.status);
-
-            // ---- A: decays; x and B 4x4 blocks into registers. Lane bits pick the
-            // block so that the 16-byte loads and stores of a warp spread over all
-            // eight bank groups of the swizzled rows.
-            if (tid < kQ) {
-                sm.dec[tid] = cexp_fast(cdiff(sm.acs[s][kQ - 1], sm.acs[s][tid]));
-            } else if (tid < 2 * kQ) {
-                sm.eacs[tid - kQ] = cexp_fast(sm.acs[s][tid - kQ]);
-            } else if (tid == 2 * kQ) {
-                sm.a_c = cexp_fast(sm.acs[s][kQ - 1]);
-            }
-            const int blo = lane & 7, bmid = (lane >> 3) & 3;
-            float4 xv[2][4], bv[2][4];
+        // ---- A: decays; x and B 4x4 blocks into registers. Lane bits pick the
+        // block so that a warp's 16-byte accesses cover all eight bank groups.
+        if (tid < kQ) {
+            sm.dec[tid] = cexp_fast(cdiff(sm.acs[s][kQ - 1], sm.acs[s][tid]));
+        } else if (tid < 2 * kQ) {
+            sm.eacs[tid - kQ] = cexp_fast(sm.acs[s][tid - kQ]);
+        } else if (tid == 2 * kQ) {
+            sm.a_c = cexp_fast(sm.acs[s][kQ - 1]);
+        }
+        const int blo = lane & 7, bmid = (lane >> 3) & 3;
+        const int xsb = bmid + 4 * (warp & 3), xdb = blo + 8 * ((warp >> 2) & 1), xp = (warp >> 3) & 1;
+        float4 xv[4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {  // x block: rows s = 4 sbk + i, columns d = 4 dbk ..
-                const int wq = warp + 8 * u;
-                const int sbk = bmid + 4 * (wq & 3), dbk = blo + 8 * ((wq >> 2) & 1), xp = (wq >> 3) & 1;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int sr = 4 * sbk + i;
-                    xv[u][i] = *reinterpret_cast<const float4*>(xbase + stk_row(dbk >> 3, xp, sr) + chunk16(dbk & 7, sr));
-                }
-            }
-            const int bsb = bmid + 4 * (warp & 3), bnb = blo + 8 * ((warp >> 2) & 1);  // rows s = 4 bsb .., columns n = 4 bnb ..
+        for (int i = 0; i < 4; ++i) {  // x block: rows s = 4 xsb + i, columns d = 4 xdb ..
+            const int sr = 4 * xsb + i;
+            xv[i] = *reinterpret_cast<const float4*>(xbase + stk_row(xdb >> 3, xp, sr) + chunk16(xdb & 7, sr));
+        }
+        const bool bwork = warp < 8;  // (dec o B)^T: one block of both planes per thread of warps 0-7
+        const int bsb = bmid + 4 * (warp & 3), bnb = blo + 8 * ((warp >> 2) & 1);
+        float4 bv[2][4];
+        if (bwork) {
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
@@ -292,32 +314,46 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
                     const int sr = 4 * bsb + i;
                     bv[pp][i] = *reinterpret_cast<const float4*>(bbase + stk_row(bnb >> 3, pp, sr) + chunk16(bnb & 7, sr));
                 }
-            ptx::named_sync(kBarWorkers, kWorkers);
+        }
+        __syncthreads();
+        // the previous chunk's stage is free: prefetch the next chunk into it
+        const bool prefetch = it + 1 < nitems;
+        int64_t qn = 0, cn = 0;
+        if (warp == kLoader && prefetch) items.get(it + 1, qn, cn);
 
-            // ---- B: x^T (interleaved rows d) in place of x; then C B^T
+        // ---- B: x^T (interleaved rows d) in place of x; C' = C o exp(Acs[l]) rows into TMEM; C B^T
+        {
+            const float4 o[4] = {make_float4(xv[0].x, xv[1].x, xv[2].x, xv[3].x), make_float4(xv[0].y, xv[1].y, xv[2].y, xv[3].y),
+                                 make_float4(xv[0].z, xv[1].z, xv[2].z, xv[3].z), make_float4(xv[0].w, xv[1].w, xv[2].w, xv[3].w)};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int wq = warp + 8 * u;
-                const int sbk = bmid + 4 * (wq & 3), dbk = blo + 8 * ((wq >> 2) & 1), xp = (wq >> 3) & 1;
-                const float4 o[4] = {make_float4(xv[u][0].x, xv[u][1].x, xv[u][2].x, xv[u][3].x),
-                                     make_float4(xv[u][0].y, xv[u][1].y, xv[u][2].y, xv[u][3].y),
-                                     make_float4(xv[u][0].z, xv[u][1].z, xv[u][2].z, xv[u][3].z),
-                                     make_float4(xv[u][0].w, xv[u][1].w, xv[u][2].w, xv[u][3].w)};
+            for (int j = 0; j < 4; ++j) {
+                const int mm = inter_m(4 * xdb + j, xp);
+                *reinterpret_cast<float4*>(xbase + inter_row(xsb >> 3, mm) + chunk16(xsb & 7, mm)) = o[j];
+            }
+        }
+        {
+            // plane pl of C'[l, n] for n in [16 h4, 16 h4 + 16): row l of both C planes
+            const float2 e = sm.eacs[r8];
+            const int kh = h4 >> 1, j0 = 4 * (h4 & 1);
+            const int mre = inter_m(r8, 0), mim = inter_m(r8, 1);
+            float w[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int mm = inter_m(4 * dbk + j, xp);
-                    *reinterpret_cast<float4*>(xbase + inter_row(sbk >> 3, mm) + chunk16(sbk & 7, mm)) = o[j];
-                }
+            for (int j = 0; j < 4; ++j) {
+                const float4 cr = *reinterpret_cast<const float4*>(cbase + inter_row(kh, mre) + chunk16(j0 + j, mre));
+                const float4 ci = *reinterpret_cast<const float4*>(cbase + inter_row(kh, mim) + chunk16(j0 + j, mim));
+                const float crv[4] = {cr.x, cr.y, cr.z, cr.w}, civ[4] = {ci.x, ci.y, ci.z, ci.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    w[4 * j + k] = pl ? (crv[k] * e.y + civ[k] * e.x) : (crv[k] * e.x - civ[k] * e.y);
             }
-            ptx::fence_proxy_async_smem();
-            publish();
-            if (tid == 0) {
-                issue_ss128(tmem + kAccG, desc128(cs), desc128(bs));  // [C Br | C Bi]
-                ptx::mma_commit(&sm.mma[0]);
-            }
-            wait_mma(0, it);
+            ptx::tmem_st16(my + kCwin + 16 * h4, w);
+        }
+        if (warp == kLoader && prefetch)
+            load_tiles(sm, s ^ 1, maps, c8_re, c8_im, (int)(qn % H), (int)(cn * kQ), (int)(qn / H), lane);
+        wait_mma(0, it);  // C B^T has read B
 
-            // ---- C: (dec o B)^T stacked in place of B; then S_loc^T = x^T (dec o B)
+        // ---- C: (dec o B)^T stacked in place of B; then S_loc^T = x^T (dec o B)
+        if (bwork) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {  // column n = 4 bnb + j of B -> row n of the output
                 const int nr = 4 * bnb + j;
@@ -335,168 +371,166 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
                 *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 1, nr) + chunk16(bsb & 7, nr)) =
                     make_float4(oim[0], oim[1], oim[2], oim[3]);
             }
-            ptx::fence_proxy_async_smem();
-            publish();
-            if (tid == 0) {
-                issue_ss128(tmem + kAccS, desc128(xs), desc128(bs));  // [x^T B'r | x^T B'i]
-                ptx::mma_commit(&sm.mma[1]);
-            }
+        }
+        ptx::fence_proxy_async_smem();
+        publish();
+        if (tid == 0) {
+            issue_ss128(tmem + kAccS, desc128(xs), desc128(bs));  // [x^T B'r | x^T B'i]
+            ptx::mma_commit(&sm.mma[1]);
+        }
 
-            // ---- D: P = (C B^T) o L on this thread's columns; P operand rows into TMEM
-            {
-                float ga[32], gb[32];
-                ptx::tmem_ld16(my + kAccG + 16 * h2, ga);
-                ptx::tmem_ld16(my + kAccG + 32 + 16 * h2, ga + 16);
-                ptx::tmem_ld16(my + kAccG + 64 + 16 * h2, gb);
-                ptx::tmem_ld16(my + kAccG + 96 + 16 * h2, gb + 16);
-                ptx::tmem_wait_ld();
-                const float2 acs_l = sm.acs[s][r8];
-                float w[32];
+        // ---- D: P = (C B^T) o L on this thread's columns; P rows into TMEM; then P x
+        {
+            // columns [8 h4, 8 h4 + 8) and [32 + 8 h4, 32 + 8 h4 + 8), in pairs (e, e + 1)
+            float ga[16], gb[16];
+            ptx::tmem_ld8(my + kAccG + 8 * h4, ga);
+            ptx::tmem_ld8(my + kAccG + 32 + 8 * h4, ga + 8);
+            ptx::tmem_ld8(my + kAccG + 64 + 8 * h4, gb);
+            ptx::tmem_ld8(my + kAccG + 96 + 8 * h4, gb + 8);
+            ptx::tmem_wait_ld();
+            const float2 acs_l = sm.acs[s][r8];
+            float w[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int e = (jj < 8 ? 16 * h2 : 32 + 16 * h2) + 2 * (jj & 7);  // even column of the pair
-                    const float ra = __shfl_xor_sync(0xffffffffu, pl ? ga[2 * jj] : ga[2 * jj + 1], 8);
-                    const float rb = __shfl_xor_sync(0xffffffffu, pl ? gb[2 * jj] : gb[2 * jj + 1], 8);
-                    // plane-0 products (Cr B) and plane-1 products (Ci B) of this thread's column
-                    const float ga0 = pl ? ra : ga[2 * jj], gb0 = pl ? rb : gb[2 * jj];
-                    const float ga1 = pl ? ga[2 * jj + 1] : ra, gb1 = pl ? gb[2 * jj + 1] : rb;
-                    const int col = e + pl;
-                    float2 v = make_float2(0.0f, 0.0f);
-                    if (col <= r8)
-                        v = cmul(make_float2(ga0 - gb1, gb0 + ga1), cexp_fast(cdiff(acs_l, sm.acs[s][col])));
-                    // lane p keeps plane p of P: column e from the p = 0 lane, e + 1 from the p = 1 lane
-                    const float other = __shfl_xor_sync(0xffffffffu, pl ? v.x : v.y, 8);
-                    w[2 * jj] = pl ? other : v.x;
-                    w[2 * jj + 1] = pl ? v.y : other;
-                }
-                ptx::tmem_st16(my + kPwin + 16 * h2, w);
-                ptx::tmem_st16(my + kPwin + 32 + 16 * h2, w + 16);
+            for (int jj = 0; jj < 8; ++jj) {
+                const int e = (jj < 4 ? 8 * h4 : 32 + 8 * h4) + 2 * (jj & 3);
+                const float ra = __shfl_xor_sync(0xffffffffu, pl ? ga[2 * jj] : ga[2 * jj + 1], 8);
+                const float rb = __shfl_xor_sync(0xffffffffu, pl ? gb[2 * jj] : gb[2 * jj + 1], 8);
+                // plane-0 products (Cr B) and plane-1 products (Ci B) of this thread's column
+                const float ga0 = pl ? ra : ga[2 * jj], gb0 = pl ? rb : gb[2 * jj];
+                const float ga1 = pl ? ga[2 * jj + 1] : ra, gb1 = pl ? gb[2 * jj + 1] : rb;
+                const int col = e + pl;
+                float2 v = make_float2(0.0f, 0.0f);
+                if (col <= r8) v = cmul(make_float2(ga0 - gb1, gb0 + ga1), cexp_fast(cdiff(acs_l, sm.acs[s][col])));
+                // lane p keeps plane p of P: column e from the p = 0 lane, e + 1 from the p = 1 lane
+                const float other = __shfl_xor_sync(0xffffffffu, pl ? v.x : v.y, 8);
+                w[2 * jj] = pl ? other : v.x;
+                w[2 * jj + 1] = pl ? v.y : other;
             }
-            publish();
-            if (tid == 0) {
-                // Y_diag: columns 16g + 8p + i hold plane p of P x (row d = 8g + i)
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    ptx::mma_tf32_ts(tmem + kAccY, tmem + kPwin + 8 * k, desc_k(desc128(xs), k), kIdesc128, k > 0);
-                ptx::mma_commit(&sm.mma[2]);
-            }
+            ptx::tmem_st8(my + kPwin + 8 * h4, w);
+            ptx::tmem_st8(my + kPwin + 32 + 8 * h4, w + 8);
+        }
+        publish();
+        if (tid == 0) issue_ts128(tmem + kAccY, tmem + kPwin, desc128(xs), false);  // P x^T (interleaved columns)
 
-            // ---- E: S_loc^T and the state hop  S_out = a_c S_in + S_loc  (row d = r8)
-            wait_mma(1, it);  // S_loc^T
-            float out[32];
-            {
-                float sa[32], sb[32];
-                ptx::tmem_ld16(my + kAccS + 32 * h2, sa);
-                ptx::tmem_ld16(my + kAccS + 16 + 32 * h2, sa + 16);
-                ptx::tmem_ld16(my + kAccS + 64 + 32 * h2, sb);
-                ptx::tmem_ld16(my + kAccS + 80 + 32 * h2, sb + 16);
-                ptx::tmem_wait_ld();
-                if (has_in && CL > 1) {
-                    if (!ptx::mbar_wait(&sm.sin_full, n_recv & 1, kWaitIters)) fail(ws.status);
-                    ++n_recv;
-                }
-                const float2 a = sm.a_c;
-                const char* sinb = reinterpret_cast<const char*>(sm.sin);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float4 sr = make_float4(0.f, 0.f, 0.f, 0.f), si = sr;
-                    if (has_in) {
-                        sr = *reinterpret_cast<const float4*>(sinb + stk_row(h2, 0, r8) + chunk16(j, r8));
-                        si = *reinterpret_cast<const float4*>(sinb + stk_row(h2, 1, r8) + chunk16(j, r8));
-                    }
-                    const float srv[4] = {sr.x, sr.y, sr.z, sr.w}, siv[4] = {si.x, si.y, si.z, si.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 4 * j + e;
-                        const float other = __shfl_xor_sync(0xffffffffu, sb[k], 8);
-                        // Re: a S_in + (xr B'r)[p0] - (xi B'i)[p1];  Im: a S_in + (xr B'i)[p0] + (xi B'r)[p1]
-                        out[k] = pl ? (a.x * siv[e] + a.y * srv[e] + other + sa[k])
-                                    : (a.x * srv[e] - a.y * siv[e] + sa[k] - other);
-                    }
-                }
-            }
-            if (last) {
-                float* fs = (pl ? p.fs_im : p.fs_re) + (q * 64) * 64 + r8;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) fs[(int64_t)(32 * h2 + k) * 64] = out[k];
-            } else if (CL > 1) {
-                if (n_send > 0 && !ptx::mbar_wait(&sm.succ_empty, (n_send - 1) & 1, kWaitIters)) fail(ws.status);
-                ++n_send;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    ptx::st_async_v4(remote_sin + stk_row(h2, pl, r8) + chunk16(j, r8),
-                                     make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]),
-                                     remote_sin_full);
-            }
-
-            // ---- F: C S_in (reuses the C B^T accumulators)
-            publish();
-            if (tid == 0) {
-                if (has_in) issue_ss128(tmem + kAccG, desc128(cs), desc128(sin_saddr));  // [C Sr | C Si]
-                ptx::mma_commit(&sm.mma[3]);
-            }
-            wait_mma(2, it);  // Y_diag
-            wait_mma(3, it);  // C S_in
-            if (has_in && CL > 1 && tid == 0) {
-                // the incoming buffer is consumed: re-arm it and free it for the sender
-                ptx::mbar_arrive_expect_tx(&sm.sin_full, kStateBytes);
-                ptx::mbar_arrive_remote(remote_pred_empty);
-            }
-            if (!last && CL == 1) {
-                // keep the state for this CTA's next chunk
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<float4*>(reinterpret_cast<char*>(sm.sin) + stk_row(h2, pl, r8) + chunk16(j, r8)) =
-                        make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-                ptx::fence_proxy_async_smem();
-            }
-
-            // ---- G: y = Y_diag + exp(Acs[l]) (C S_in), staged in the x buffer
-            // (both MMAs reading x^T are done) and written by TMA.
-            {
-                const float2 e = sm.eacs[r8];
-#pragma unroll
-                for (int pass = 0; pass < 2; ++pass) {
-                    const int c0 = 32 * h2 + 16 * pass;  // first column d of this pass
-                    float yv[32], za[16], zb[16];
-                    ptx::tmem_ld16(my + kAccY + 2 * c0, yv);
-                    ptx::tmem_ld16(my + kAccY + 2 * c0 + 16, yv + 16);
-                    ptx::tmem_ld16(my + kAccG + c0, za);
-                    ptx::tmem_ld16(my + kAccG + 64 + c0, zb);
-                    ptx::tmem_wait_ld();
-                    float o[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int yi = 16 * (k >> 3) + (k & 7);  // Y column of plane 0; plane 1 is 8 further
-                        const float ya = yv[yi], yb = yv[yi + 8];
-                        const float zak = has_in ? za[k] : 0.0f, zbk = has_in ? zb[k] : 0.0f;
-                        // this lane's share of Re y and Im y (see the header comment)
-                        const float u = pl ? (-yb - e.x * zbk - e.y * zak) : (ya + e.x * zak - e.y * zbk);
-                        const float v = pl ? (ya + e.x * zak - e.y * zbk) : (yb + e.x * zbk + e.y * zak);
-                        const float other = __shfl_xor_sync(0xffffffffu, pl ? u : v, 8);
-                        o[k] = pl ? v + other : u + other;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        *reinterpret_cast<float4*>(xbase + stk_row(h2, pl, r8) + chunk16(4 * pass + k, r8)) =
-                            make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                }
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            ptx::named_sync(kBarWorkers, kWorkers);
-            if (tid == 0) {
-                for (int half = 0; half < 2; ++half) {
-                    ptx::tma_store_4d(&y_re, xbase + stk_row(half, 0, 0), 32 * half, h, (int)t0, b);
-                    ptx::tma_store_4d(&y_im, xbase + stk_row(half, 1, 0), 32 * half, h, (int)t0, b);
-                }
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();  // the stage may be refilled once the store has read it
-                ptx::mbar_arrive(&sm.empty[s]);
+        // ---- E: S_loc^T and the state hop  S_out = a_c S_in + S_loc  (row d = r8, n in [16 h4, +16))
+        if (warp == kLoader && prefetch) {
+            store_acs(sm, s ^ 1, nal, lane);  // next chunk's decays
+            if (it + 2 < nitems) {
+                int64_t q2, c2;
+                items.get(it + 2, q2, c2);
+                nal = load_alog(p, (int)(q2 / H), (int)(q2 % H), c2 * kQ, lane);
             }
         }
-        if (tid == 0) ptx::bulk_wait_all();
+        wait_mma(1, it);
+        float out[16];
+        {
+            float sa[16], sb[16];
+            ptx::tmem_ld16(my + kAccS + 16 * h4, sa);
+            ptx::tmem_ld16(my + kAccS + 64 + 16 * h4, sb);
+            ptx::tmem_wait_ld();
+            if (has_in && CL > 1) {
+                if (!ptx::mbar_wait(&sm.sin_full, n_recv & 1, kWaitIters)) fail(ws.status);
+                ++n_recv;
+            }
+            const float2 a = sm.a_c;
+            const char* sinb = reinterpret_cast<const char*>(sm.sin);
+            const int kh = h4 >> 1, j0 = 4 * (h4 & 1);
+            const int mre = inter_m(r8, 0), mim = inter_m(r8, 1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float4 sr = make_float4(0.f, 0.f, 0.f, 0.f), si = sr;
+                if (has_in) {
+                    sr = *reinterpret_cast<const float4*>(sinb + inter_row(kh, mre) + chunk16(j0 + j, mre));
+                    si = *reinterpret_cast<const float4*>(sinb + inter_row(kh, mim) + chunk16(j0 + j, mim));
+                }
+                const float srv[4] = {sr.x, sr.y, sr.z, sr.w}, siv[4] = {si.x, si.y, si.z, si.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 4 * j + e;
+                    const float other = __shfl_xor_sync(0xffffffffu, sb[k], 8);
+                    // Re: a S_in + (xr B'r)[p0] - (xi B'i)[p1];  Im: a S_in + (xr B'i)[p0] + (xi B'r)[p1]
+                    out[k] = pl ? (a.x * siv[e] + a.y * srv[e] + other + sa[k])
+                                : (a.x * srv[e] - a.y * siv[e] + sa[k] - other);
+                }
+            }
+        }
+        const int mo = inter_m(r8, pl);
+        if (last) {
+            float* fs = (pl ? p.fs_im : p.fs_re) + (q * 64) * 64 + r8;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) fs[(int64_t)(16 * h4 + k) * 64] = out[k];
+        } else if (CL > 1) {
+            // stage S_out in the C buffer (C was consumed by C B^T and the C' rows);
+            // worker thread 0 moves it to the next CTA with one bulk copy
+            char* stg = reinterpret_cast<char*>(sm.c[s]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float4*>(stg + inter_row(h4 >> 1, mo) + chunk16(4 * (h4 & 1) + j, mo)) =
+                    make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+        }
+
+        // ---- F: (C o exp(Acs)) S_in into the same accumulator
+        publish();
+        if (tid == 0) {
+            if (has_in) issue_ts128(tmem + kAccY, tmem + kCwin, desc128(sin_saddr), true);
+            ptx::mma_commit(&sm.mma[2]);
+            if (!last && CL > 1) {
+                if (n_send > 0 && !ptx::mbar_wait(&sm.succ_empty, (n_send - 1) & 1, kWaitIters)) fail(ws.status);
+                ++n_send;
+                ptx::bulk_copy_to_cluster(remote_sin, cs, kStateBytes, remote_sin_full);
+                ptx::bulk_commit();
+            }
+        }
+        wait_mma(2, it);
+        if (has_in && CL > 1 && tid == 0) {
+            // the incoming buffer is consumed: re-arm it and free it for the sender
+            ptx::mbar_arrive_expect_tx(&sm.sin_full, kStateBytes);
+            ptx::mbar_arrive_remote(remote_pred_empty);
+        }
+        if (!last && CL == 1) {
+            // keep the state for this CTA's next chunk
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float4*>(reinterpret_cast<char*>(sm.sin) + inter_row(h4 >> 1, mo) + chunk16(4 * (h4 & 1) + j, mo)) =
+                    make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+        }
+
+        // ---- G: y rows, staged in the x buffer and written by TMA. Columns
+        // 16g + 8p' + i of the accumulator hold plane-p' products of column 8g + i.
+        {
+            float yv[32];
+            ptx::tmem_ld16(my + kAccY + 32 * h4, yv);
+            ptx::tmem_ld16(my + kAccY + 32 * h4 + 16, yv + 16);
+            ptx::tmem_wait_ld();
+            float o[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int yi = 16 * (k >> 3) + (k & 7);
+                const float ya = yv[yi], yb = yv[yi + 8];
+                // Re y = ya[p0] - yb[p1], Im y = yb[p0] + ya[p1]
+                const float u = pl ? -yb : ya, v = pl ? ya : yb;
+                const float other = __shfl_xor_sync(0xffffffffu, pl ? u : v, 8);
+                o[k] = pl ? v + other : u + other;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<float4*>(xbase + stk_row(h4 >> 1, pl, r8) + chunk16(4 * (h4 & 1) + k, r8)) =
+                    make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            for (int half = 0; half < 2; ++half) {
+                ptx::tma_store_4d(&y_re, xbase + stk_row(half, 0, 0), 32 * half, h, (int)t0, b);
+                ptx::tma_store_4d(&y_im, xbase + stk_row(half, 1, 0), 32 * half, h, (int)t0, b);
+            }
+            ptx::bulk_commit();  // read-complete is awaited before the next prefetch
+        }
     }
+    if (tid == 0) ptx::bulk_wait_all();
 
     ptx::tc_fence_before();
     __syncthreads();
