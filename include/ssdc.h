@@ -69,6 +69,7 @@ extern "C" {
 #define SSDC_ERR_CUDA (-5)        /* a CUDA call or launch failed */
 #define SSDC_ERR_TIMEOUT (-6)     /* a bounded device wait gave up */
 #define SSDC_ERR_DEVICE (-7)      /* the current device is not sm_103 */
+#define SSDC_ERR_TOO_LARGE (-8)   /* needs more scratch than the static buffer holds */
 
 #define SSDC_PREC_TF32 0
 #define SSDC_PREC_FP32 1
@@ -152,6 +153,34 @@ int ssd_complex_last_launch_count(void);
  */
 int ssd_complex_timing_enable(int enable);
 int ssd_complex_timing_read(float *ms, int n);
+
+/*
+ * Forward pass that allocates nothing, for callers that cannot allocate
+ * device memory when they run the scan (code running inside a memory-pool or
+ * allocator hook, latency-critical paths that forbid allocator calls, or
+ * embedders with a fixed memory budget). There is no counterpart on the pages;
+ * it is an operational variant of the staged path.
+ *
+ * It runs the staged path (precision SSDC_PREC_FP32 or SSDC_PREC_TF32_STAGED;
+ * anything else is SSDC_ERR_UNSUPPORTED) with its workspace in a static device
+ * array of SSDC_NOALLOC_SCRATCH_BYTES that the library holds on every GPU that
+ * loads it, for the life of the process. Problems whose workspace
+ * (ssd_complex_fwd_workspace_bytes) exceeds it return SSDC_ERR_TOO_LARGE
+ * before anything is enqueued. Arguments, layout and outputs are those of
+ * ssd_complex_fwd_ws; it calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one array and leave their chunk states in it: calls
+ * whose work may overlap on the GPU (different streams, or threads without
+ * ordering) race on it and must be serialised by the caller. The array needs
+ * no clearing between calls.
+ */
+#define SSDC_NOALLOC_SCRATCH_BYTES ((size_t)32 * 1024 * 1024 + (size_t)64 * 1024)
+int ssd_complex_fwd_noalloc(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
+                            const float *dt, ssdc_dims dims, int chunk_size,
+                            ssdc_cout y, ssdc_cout final_state, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -247,6 +247,7 @@ const char* ssd_complex_strerror(int status) {
         case SSDC_ERR_CUDA: return "CUDA call or kernel launch failed";
         case SSDC_ERR_TIMEOUT: return "a bounded device wait gave up";
         case SSDC_ERR_DEVICE: return "current device is not a compute capability 10.3 GPU";
+        case SSDC_ERR_TOO_LARGE: return "problem needs more workspace than the static no-allocation buffer holds";
         default: return "unknown status";
     }
 }

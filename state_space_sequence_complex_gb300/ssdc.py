@@ -20,13 +20,16 @@ SSDC_ERR_WORKSPACE = -4
 SSDC_ERR_CUDA = -5
 SSDC_ERR_TIMEOUT = -6
 SSDC_ERR_DEVICE = -7
+SSDC_ERR_TOO_LARGE = -8
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024 + 64 * 1024
 
 PREC = {"tf32": 0, "fp32": 1, "tf32_staged": 2}
 
 # Every symbol include/ssdc.h declares.
 EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_complex_fwd_ws",
            "ssd_complex_fwd", "ssd_complex_status", "ssd_complex_strerror",
-           "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read")
+           "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read",
+           "ssd_complex_fwd_noalloc")
 
 
 class ssdc_dims(ctypes.Structure):
@@ -75,6 +78,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_strerror.restype = ctypes.c_char_p
     lib.ssd_complex_last_launch_count.argtypes = []
     lib.ssd_complex_last_launch_count.restype = ctypes.c_int
+    lib.ssd_complex_fwd_noalloc.argtypes = common + [vp]
+    lib.ssd_complex_fwd_noalloc.restype = ctypes.c_int
     lib.ssd_complex_timing_enable.argtypes = [ctypes.c_int]
     lib.ssd_complex_timing_enable.restype = ctypes.c_int
     lib.ssd_complex_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int]
@@ -132,6 +137,25 @@ def ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk
         int(workspace.numel()), ctypes.c_void_p(s.cuda_stream))
     if check and rc != SSDC_OK:
         raise SSDCError(rc, "ssd_complex_fwd_ws")
+    return rc
+
+
+def ssd_complex_fwd_noalloc(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
+                            precision="fp32", y_re, y_im, fs_re, fs_im, stream=None, check=True) -> int:
+    """Call ``ssd_complex_fwd_noalloc`` on torch CUDA tensors: the staged path
+    with the library's static scratch workspace, for callers that cannot
+    allocate device memory while they run the scan. Returns the status."""
+    import torch
+
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    d = dims(Bn, T, H, N, D, precision)
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_fwd_noalloc(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt), d,
+        int(chunk_size), _cout(y_re, y_im), _cout(fs_re, fs_im), ctypes.c_void_p(s.cuda_stream))
+    if check and rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_fwd_noalloc")
     return rc
 
 

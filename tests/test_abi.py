@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_strerror(lib):
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         s = ssdc.strerror(code)
         assert s and s != "unknown status"
     assert ssdc.strerror(-99) == "unknown status"
