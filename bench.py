@@ -1,8 +1,9 @@
 """Benchmark of the complex chunkwise SSD forward (libssdc) on GB300.
 
-One step = one forward pass of the whole scan (chunk-state kernel, state pass,
-chunk-scan kernel) over the single-layer production workload (B=2, T=2048,
-H=16, D=N=64 complex, Q=64), inputs resident in HBM. Metric: token-heads/s
+One step = one forward pass of the whole scan (every row of the chunked
+decomposition; one fused kernel launch on the TF32 path) over the single-layer
+production workload (B=2, T=2048, H=16, D=N=64 complex, Q=64), inputs resident
+in HBM. Metric: token-heads/s
 (B*T*H per step). L2 is flushed (a 512 MiB write) before every timed step and
 each step is timed on its stream with CUDA events.
 
@@ -51,6 +52,24 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def rank_layer(rank: int) -> int:
+    """Seed offset of rank `rank`'s batch: every rank runs its own independent
+    batch of the workload (weak scaling, no data-path collective)."""
+    return rank
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise max of a list of floats over all ranks (identity when not
+    distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
 
 
 def peaks():
@@ -215,7 +234,7 @@ def main():
     ssdc.load()
 
     # each rank processes its own independently seeded batch (weak scaling)
-    inp = inputs.generate(w, layer=rank)
+    inp = inputs.generate(w, layer=rank_layer(rank))
     host = {k: torch.from_numpy(np.ascontiguousarray(v)) for k, v in inp.arrays().items()}
     d_in = {k: v.to(dev) for k, v in host.items()}
     Bn, T, H, N, D = inp.dims
@@ -302,10 +321,7 @@ def main():
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
 
     # max over ranks
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev)
 
     units = w.token_heads * world
     value = units / (ms / 1000.0)

@@ -69,10 +69,14 @@ struct Smem {
     float2 dec[kQ];          // exp(Acs[Q-1] - Acs[s])
     float2 eacs[kQ];         // exp(Acs[l])
     float2 a_c;              // exp(Acs[Q-1])
+    float2 pair[kQ];         // exp(Acs[s+2] - Acs[s]): decay over tokens s+1, s+2
     uint64_t full[2], sin_full, succ_empty;
+    uint64_t xt_ready, bt_ready;  // x^T written (all warps), (dec o B)^T written (warps 0-7)
     uint64_t mma[3];         // MMA groups C B^T, S_loc^T, y; one phase per chunk
     uint32_t tmem;
 };
+
+static_assert(sizeof(Smem) <= 232448, "shared-memory plan exceeds the 227 KB a CTA can have");
 
 // The chunks this CTA processes, in order: for each sequence owned by its
 // cluster, the chunks congruent to its rank.
@@ -214,6 +218,8 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
         for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.full[s], 1);
         for (int g = 0; g < 3; ++g) ptx::mbar_init(&sm.mma[g], 1);
         ptx::mbar_init(&sm.sin_full, 1);
+        ptx::mbar_init(&sm.xt_ready, kWarps);
+        ptx::mbar_init(&sm.bt_ready, 8);
         ptx::mbar_init(&sm.succ_empty, 1);
         ptx::fence_mbar_init();
         if (CL > 1) ptx::mbar_arrive_expect_tx(&sm.sin_full, kStateBytes);  // first transfer
@@ -243,6 +249,7 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
     const int pl = (m >> 3) & 1;                // plane of this lane
     const uint32_t my = lane_base(tmem, warp);
     uint32_t n_recv = 0, n_send = 0;
+    bool recv_ok = true;
     const uint32_t sin_saddr = ptx::smem_addr(sm.sin);
     const uint32_t remote_sin = ptx::mapa(sin_saddr, succ);
     const uint32_t remote_sin_full = ptx::mapa(ptx::smem_addr(&sm.sin_full), succ);
@@ -294,6 +301,9 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
             sm.eacs[tid - kQ] = cexp_fast(sm.acs[s][tid - kQ]);
         } else if (tid == 2 * kQ) {
             sm.a_c = cexp_fast(sm.acs[s][kQ - 1]);
+        } else if (tid > 2 * kQ && tid <= 3 * kQ - 2) {
+            const int t = tid - 2 * kQ - 1;  // 0 .. Q-3
+            sm.pair[t] = cexp_fast(cdiff(sm.acs[s][t + 2], sm.acs[s][t]));
         }
         const int blo = lane & 7, bmid = (lane >> 3) & 3;
         const int xsb = bmid + 4 * (warp & 3), xdb = blo + 8 * ((warp >> 2) & 1), xp = (warp >> 3) & 1;
@@ -330,6 +340,9 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
                 const int mm = inter_m(4 * xdb + j, xp);
                 *reinterpret_cast<float4*>(xbase + inter_row(xsb >> 3, mm) + chunk16(xsb & 7, mm)) = o[j];
             }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.xt_ready);
         }
         {
             // plane pl of C'[l, n] for n in [16 h4, 16 h4 + 16): row l of both C planes
@@ -352,7 +365,8 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
             load_tiles(sm, s ^ 1, maps, c8_re, c8_im, (int)(qn % H), (int)(cn * kQ), (int)(qn / H), lane);
         wait_mma(0, it);  // C B^T has read B
 
-        // ---- C: (dec o B)^T stacked in place of B; then S_loc^T = x^T (dec o B)
+        // ---- C: (dec o B)^T stacked in place of B; then S_loc^T = x^T (dec o B), issued by
+        // thread 0 once every warp has announced its x^T and (dec o B)^T blocks
         if (bwork) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {  // column n = 4 bnb + j of B -> row n of the output
@@ -371,10 +385,14 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
                 *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 1, nr) + chunk16(bsb & 7, nr)) =
                     make_float4(oim[0], oim[1], oim[2], oim[3]);
             }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.bt_ready);
         }
-        ptx::fence_proxy_async_smem();
-        publish();
         if (tid == 0) {
+            if (!ptx::mbar_wait(&sm.xt_ready, (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
+            if (!ptx::mbar_wait(&sm.bt_ready, (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
+            ptx::tc_fence_after();
             issue_ss128(tmem + kAccS, desc128(xs), desc128(bs));  // [x^T B'r | x^T B'i]
             ptx::mma_commit(&sm.mma[1]);
         }
@@ -389,22 +407,47 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
             ptx::tmem_ld8(my + kAccG + 96 + 8 * h4, gb + 8);
             ptx::tmem_wait_ld();
             const float2 acs_l = sm.acs[s][r8];
-            float w[16];
+            // complex G on this thread's columns: column e + pl of each pair
+            float gre[8], gim[8];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
-                const int e = (jj < 4 ? 8 * h4 : 32 + 8 * h4) + 2 * (jj & 3);
                 const float ra = __shfl_xor_sync(0xffffffffu, pl ? ga[2 * jj] : ga[2 * jj + 1], 8);
                 const float rb = __shfl_xor_sync(0xffffffffu, pl ? gb[2 * jj] : gb[2 * jj + 1], 8);
                 // plane-0 products (Cr B) and plane-1 products (Ci B) of this thread's column
                 const float ga0 = pl ? ra : ga[2 * jj], gb0 = pl ? rb : gb[2 * jj];
                 const float ga1 = pl ? ga[2 * jj + 1] : ra, gb1 = pl ? gb[2 * jj + 1] : rb;
-                const int col = e + pl;
-                float2 v = make_float2(0.0f, 0.0f);
-                if (col <= r8) v = cmul(make_float2(ga0 - gb1, gb0 + ga1), cexp_fast(cdiff(acs_l, sm.acs[s][col])));
+                gre[jj] = ga0 - gb1;
+                gim[jj] = gb0 + ga1;
+            }
+            // L[l, col] for the four columns col = base + 2k + pl of each 8-column range, from
+            // the last one with col <= l down: one exponential of a difference of cumulative
+            // sums, then L[l, col - 2] = L[l, col] exp(Acs[col] - Acs[col - 2]).
+            float pr[8], pim[8];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int base = (rr ? 32 : 0) + 8 * h4 + pl;
+                float2 L = make_float2(0.0f, 0.0f);
+                bool started = false;
+#pragma unroll
+                for (int k = 3; k >= 0; --k) {
+                    const int col = base + 2 * k, jj = 4 * rr + k;
+                    float2 v = make_float2(0.0f, 0.0f);
+                    if (col <= r8) {
+                        L = started ? cmul(L, sm.pair[col]) : cexp_fast(cdiff(acs_l, sm.acs[s][col]));
+                        started = true;
+                        v = cmul(make_float2(gre[jj], gim[jj]), L);
+                    }
+                    pr[jj] = v.x;
+                    pim[jj] = v.y;
+                }
+            }
+            float w[16];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
                 // lane p keeps plane p of P: column e from the p = 0 lane, e + 1 from the p = 1 lane
-                const float other = __shfl_xor_sync(0xffffffffu, pl ? v.x : v.y, 8);
-                w[2 * jj] = pl ? other : v.x;
-                w[2 * jj + 1] = pl ? v.y : other;
+                const float other = __shfl_xor_sync(0xffffffffu, pl ? pr[jj] : pim[jj], 8);
+                w[2 * jj] = pl ? other : pr[jj];
+                w[2 * jj + 1] = pl ? pim[jj] : other;
             }
             ptx::tmem_st8(my + kPwin + 8 * h4, w);
             ptx::tmem_st8(my + kPwin + 32 + 8 * h4, w + 8);
@@ -429,7 +472,10 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
             ptx::tmem_ld16(my + kAccS + 64 + 16 * h4, sb);
             ptx::tmem_wait_ld();
             if (has_in && CL > 1) {
-                if (!ptx::mbar_wait(&sm.sin_full, n_recv & 1, kWaitIters)) fail(ws.status);
+                if (!ptx::mbar_wait(&sm.sin_full, n_recv & 1, kWaitIters)) {
+                    fail(ws.status);
+                    recv_ok = false;  // the buffer protocol stops here for this CTA
+                }
                 ++n_recv;
             }
             const float2 a = sm.a_c;
@@ -473,17 +519,18 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
         // ---- F: (C o exp(Acs)) S_in into the same accumulator
         publish();
         if (tid == 0) {
-            if (has_in) issue_ts128(tmem + kAccY, tmem + kCwin, desc128(sin_saddr), true);
-            ptx::mma_commit(&sm.mma[2]);
-            if (!last && CL > 1) {
+            // the state goes to the next CTA first: it is on the chain's critical path
+            if (!last && CL > 1 && c != p.drop_send_chunk) {
                 if (n_send > 0 && !ptx::mbar_wait(&sm.succ_empty, (n_send - 1) & 1, kWaitIters)) fail(ws.status);
                 ++n_send;
                 ptx::bulk_copy_to_cluster(remote_sin, cs, kStateBytes, remote_sin_full);
                 ptx::bulk_commit();
             }
+            if (has_in) issue_ts128(tmem + kAccY, tmem + kCwin, desc128(sin_saddr), true);
+            ptx::mma_commit(&sm.mma[2]);
         }
         wait_mma(2, it);
-        if (has_in && CL > 1 && tid == 0) {
+        if (has_in && CL > 1 && tid == 0 && recv_ok) {
             // the incoming buffer is consumed: re-arm it and free it for the sender
             ptx::mbar_arrive_expect_tx(&sm.sin_full, kStateBytes);
             ptx::mbar_arrive_remote(remote_pred_empty);

@@ -172,6 +172,10 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const
     p.T = dims.T; p.B = (int)dims.B; p.H = (int)dims.H; p.N = (int)dims.N; p.D = (int)dims.D;
     p.Q = chunk_size;
     p.nc = ssdc::ceil_div64(dims.T, chunk_size);
+    {
+        const char* drop = getenv("SSDC_TEST_DROP_STATE_CHUNK");
+        p.drop_send_chunk = drop ? atoll(drop) : -1;
+    }
     ssdc::Workspace w = carve(workspace, dims, chunk_size);
 
     (void)cudaGetLastError();  // clear a stale error from unrelated work

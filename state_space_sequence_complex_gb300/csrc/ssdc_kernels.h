@@ -16,6 +16,10 @@ struct Problem {
     int64_t T;
     int B, H, N, D, Q;
     int64_t nc;  // chunks per sequence, ceil(T / Q)
+    // Test hook of the fused kernel: the CTA of this chunk index does not send
+    // the state it computes (-1 = off), so that its successor's bounded wait
+    // gives up and reports SSDC_ERR_TIMEOUT.
+    int64_t drop_send_chunk;
 };
 
 // SIMT (exact fp32) kernels.
