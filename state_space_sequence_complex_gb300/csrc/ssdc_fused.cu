@@ -10,32 +10,40 @@
 // (b, h) sequence at a time; CTA rank r takes the chunks c = r, r + CL, ...
 // of it, in order. The state entering chunk c+1,
 //     S_in[c+1] = exp(Acs_c[Q-1]) S_in[c] + S_loc[c],
-// is computed by the CTA of chunk c and stored (st.async, 32 KB) straight
-// into the shared memory of the CTA of chunk c+1, rank (r+1) mod CL, whose
-// mbarrier counts the bytes; the receiver frees the buffer by arriving on the
-// sender's mbarrier. With CL = 1 the CTA keeps the state in its own shared
-// memory. All chunk-local work (C B^T, L, Y_diag, S_loc) is independent of
-// the incoming state, so the serial chain per sequence is one complex
-// multiply-add per state element and one 32 KB transfer per chunk.
+// is computed by the CTA of chunk c and copied (cp.async.bulk, 32 KB in four
+// 8 KB quarters of rows d) straight into the shared memory of the CTA of
+// chunk c+1, rank (r+1) mod CL, where one mbarrier per quarter counts the
+// bytes; the receiver frees the buffer by arriving on the sender's mbarrier.
+// Each quarter leaves as soon as the four warps that own its rows have it, so
+// the quarters of consecutive hops overlap. With CL = 1 the CTA keeps the
+// state in its own shared memory. All chunk-local work (C B^T, L, Y_diag,
+// S_loc) is independent of the incoming state, so the serial chain per
+// sequence is one complex multiply-add per state element and one transfer of
+// a quarter of the state per chunk.
 //
 // Complex products. Planar re/im operands are multiplied as real M=128 MMAs
 // whose A operand holds the real and imaginary rows of the left factor
 // interleaved in groups of eight (row 16g + 8p + i = plane p of row 8g + i)
 // and whose B operand stacks or interleaves the right factor's two planes as
-// 128 rows (N = 128). One accumulator then holds, in TMEM lanes m and m ^ 8
-// (the same warp), all four real products, and
+// 128 rows (N = 128). One accumulator then holds, in TMEM lanes m and m + 8,
+// all four real products, and
 //     Re = (A_r B_r)[lane p=0] - (A_i B_i)[lane p=1]
-//     Im = (A_r B_i)[lane p=0] + (A_i B_r)[lane p=1]
-// is one exchange between partner lanes. The C tile is loaded in that layout
-// by TMA (8-row boxes); x^T is written in it by a shared-memory transpose.
-// The output accumulator takes both P x (Y_diag) and (C o exp(Acs)) S_in
-// (Y_off): the two A operands, P and C', are rows written to TMEM.
+//     Im = (A_r B_i)[lane p=0] + (A_i B_r)[lane p=1].
+// The 16x256b TMEM access shape hands each thread lanes m and m + 8 of the
+// same columns, so every thread combines its own values: no exchange between
+// lanes. The C tile is loaded in that layout by TMA (8-row boxes); x^T is
+// written in it by a shared-memory transpose. The output accumulator takes
+// both P x (Y_diag) and (C o exp(Acs)) S_in (Y_off): the two A operands, P
+// and C', are rows written to TMEM.
 //
 // Threads. 16 warps; warps w and w + 4k share TMEM lane quadrant w % 4 and
 // split a row's 64 columns in quarters (k = w / 4). Worker thread 0 issues
-// the MMAs and the TMA stores of y; warp 15 also issues the TMA loads of the
-// next chunk's C, B, x tiles into the other stage of a two-stage ring and
-// computes its cumulative log-decay.
+// the MMAs; y goes from registers to global memory, four lanes per 32-byte
+// run of a row. Warp 15 also issues the TMA loads of the next chunk's C, B,
+// x tiles into the other stage of a two-stage ring and computes its
+// cumulative log-decay.
+#include <cstring>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -48,15 +56,19 @@ namespace {
 using namespace tc;
 
 constexpr int kQ = 64;
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kLoader = kWarps - 1;  // warp that prefetches the next chunk
+constexpr int kWorkers = 512;               // 16 worker warps
+constexpr int kWorkerWarps = kWorkers / 32;
+constexpr int kIssuer = kWorkerWarps;        // warp 16: issues the MMAs
+constexpr int kProducer = kWorkerWarps + 1;  // warp 17: TMA loads and decays
+constexpr int kThreads = kWorkers + 64;
+constexpr uint32_t kWorkerBar = 5;           // named barrier of the worker warps (1-4: quadrants)
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: three 128-column accumulators and two 64-column A operands.
 constexpr uint32_t kAccG = 0, kAccS = 128, kAccY = 256, kPwin = 384, kCwin = 448;
 constexpr uint32_t kTileBytes = 2 * kPlaneBytes;  // 32 KB: one complex 64 x 64 tile
 constexpr uint32_t kStageTx = 3 * kTileBytes;     // C, B, x
 constexpr uint32_t kStateBytes = kTileBytes;
+constexpr uint32_t kQuarterBytes = kStateBytes / 4;  // rows d of one TMEM lane quadrant (4 warps)
 constexpr uint32_t kIntHalf = 16384;  // one 32-column half of a 128-row tile
 constexpr uint32_t kIdesc128 = ptx::idesc_tf32(128, 128, 0);  // M = 128, N = 128, B operand K-major
 
@@ -69,33 +81,48 @@ struct Smem {
     float2 dec[kQ];          // exp(Acs[Q-1] - Acs[s])
     float2 eacs[kQ];         // exp(Acs[l])
     float2 a_c;              // exp(Acs[Q-1])
-    float2 pair[kQ];         // exp(Acs[s+2] - Acs[s]): decay over tokens s+1, s+2
-    uint64_t full[2], sin_full, succ_empty;
-    uint64_t xt_ready, bt_ready;  // x^T written (all warps), (dec o B)^T written (warps 0-7)
+    float2 step[kQ];         // exp(Acs[s] - Acs[s-1]): decay over token s (s >= 1)
+    uint64_t full[2], sin_full[4], succ_empty;  // sin_full[q]: rows d in [16q, 16q + 16) of S_in
+    uint64_t stage_free;          // workers are done with the previous chunk's stage
+    uint64_t xt_ready, bt_ready;  // x^T, (dec o B)^T written (one arrival per worker warp)
+    uint64_t p_ready;             // P and C' rows in TMEM (one arrival per worker warp)
     uint64_t mma[3];         // MMA groups C B^T, S_loc^T, y; one phase per chunk
     uint32_t tmem;
 };
 
 static_assert(sizeof(Smem) <= 232448, "shared-memory plan exceeds the 227 KB a CTA can have");
 
+// Position of an item: sequence q = b H + h and chunk c (all below 2^31: the
+// host limits B H to 65535 and the chunk count to 2^29).
+struct Pos {
+    int q, c, b, h;
+};
+
 // The chunks this CTA processes, in order: for each sequence owned by its
 // cluster, the chunks congruent to its rank.
 struct Items {
-    int64_t nseq, nc;
+    int nseq, nc;
     uint32_t cl, rank, cluster, nclusters;
-    int64_t per_seq;  // chunks of one sequence owned by this rank
-    __device__ Items(int64_t nseq_, int64_t nc_)
+    __device__ Items(int nseq_, int nc_)
         : nseq(nseq_), nc(nc_), cl(ptx::cluster_nctarank()), rank(ptx::cluster_ctarank()),
-          cluster(ptx::cluster_id_x()), nclusters(ptx::ncluster_x()) {
-        per_seq = nc > (int64_t)rank ? (nc - 1 - rank) / cl + 1 : 0;
-    }
-    __device__ int64_t count() const {
-        const int64_t seqs = nseq > (int64_t)cluster ? (nseq - 1 - cluster) / nclusters + 1 : 0;
+          cluster(ptx::cluster_id_x()), nclusters(ptx::ncluster_x()) {}
+    __device__ int count() const {
+        const int per_seq = nc > (int)rank ? (nc - 1 - (int)rank) / (int)cl + 1 : 0;
+        const int seqs = nseq > (int)cluster ? (nseq - 1 - (int)cluster) / (int)nclusters + 1 : 0;
         return seqs * per_seq;
     }
-    __device__ void get(int64_t i, int64_t& q, int64_t& c) const {
-        q = cluster + (i / per_seq) * nclusters;
-        c = rank + (i % per_seq) * cl;
+    __device__ static Pos at(int q, int c, int H) {
+        Pos p;
+        p.q = q;
+        p.c = c;
+        p.b = (int)((uint32_t)q / (uint32_t)H);
+        p.h = q - p.b * H;
+        return p;
+    }
+    __device__ Pos first(int H) const { return at((int)cluster, (int)rank, H); }
+    __device__ Pos next(const Pos& p, int H) const {
+        const int c = p.c + (int)cl;
+        return c < nc ? at(p.q, c, H) : at(p.q + (int)nclusters, (int)rank, H);
     }
 };
 
@@ -111,6 +138,10 @@ __device__ __forceinline__ uint32_t stk_row(int khalf, int plane, int r) {
 __device__ __forceinline__ uint32_t inter_row(int khalf, int m) { return (uint32_t)(khalf * kIntHalf + m * 128); }
 __device__ __forceinline__ uint32_t chunk16(int j, int r) { return (uint32_t)(((j ^ (r & 7)) & 7) << 4); }
 __device__ __forceinline__ int inter_m(int r8, int plane) { return 16 * (r8 >> 3) + 8 * plane + (r8 & 7); }
+// Column pair (n, n + 1), n even and below 32, of row m in 32-column half khalf of an interleaved tile.
+__device__ __forceinline__ uint32_t pair_off(int khalf, int m, int n) {
+    return inter_row(khalf, m) + chunk16(n >> 2, m) + (uint32_t)((n & 3) << 2);
+}
 
 // K-major SW128 descriptor of a 128-row operand; K-step k (8 fp32) adds
 // (k / 4) halves and (k % 4) 32-byte steps to the start address.
@@ -130,26 +161,54 @@ __device__ __forceinline__ void issue_ts128(uint32_t d, uint32_t a_tmem, uint64_
         ptx::mma_tf32_ts(d, a_tmem + 8 * k, desc_k(db, k), kIdesc128, (accumulate || k > 0) ? 1u : 0u);
 }
 
-// Loader warp: TMA of one chunk's C (8-row boxes, re/im interleaved), B and
-// x (stacked) into stage `st`, counted on `bar`. The 40 copies are issued by
-// the warp's lanes in parallel after lane 0 has announced the bytes.
-__device__ __forceinline__ void load_tiles(Smem& sm, int st, const TcMaps& maps, const CUtensorMap& c8_re,
-                                           const CUtensorMap& c8_im, int h, int t0, int b, int lane) {
+// Tensor maps of one launch. The fast maps fetch both planes of a tensor in
+// one copy per 32-column half, through a "plane" dimension whose stride is the
+// distance between the two planes' allocations; the C map also splits time
+// into 8-row groups so that its box lands in the interleaved layout. Where a
+// fast map cannot be made (planes not 16-byte spaced or too far apart, T not a
+// multiple of 8 for C), the per-plane maps are used.
+struct FusedMaps {
+    CUtensorMap x_re, x_im, B_re, B_im;  // (F, H, T, B), boxes (32, 1, 64, 1)
+    CUtensorMap c8_re, c8_im;            // (F, H, T, B), boxes (32, 1, 8, 1)
+    CUtensorMap x2, B2;                  // (F, H, T, plane, B), boxes (32, 1, 64, 2, 1)
+    CUtensorMap C2;                      // (F, H, T % 8, plane, (B T) / 8), boxes (32, 1, 8, 2, 8)
+    int fast;                            // bit 0: x2, bit 1: B2, bit 2: C2 in use
+    int swap;                            // bit k: the fast map's plane 0 is the imaginary plane (0 x, 1 B, 2 C)
+};
+
+// Issuer warp: TMA of one chunk's C (re/im interleaved), B and x (stacked)
+// into stage `st`, counted on `bar`. The copies are issued by the warp's lanes
+// in parallel after lane 0 has announced the bytes.
+__device__ __forceinline__ void load_tiles(Smem& sm, int st, const FusedMaps& fm, int h, int t0, int b, int64_t T,
+                                           int lane) {
     uint64_t* bar = &sm.full[st];
     if (lane == 0) ptx::mbar_expect_tx(bar, kStageTx);
     __syncwarp();
     char* cb = reinterpret_cast<char*>(sm.c[st]);
     char* bb = reinterpret_cast<char*>(sm.b[st]);
     char* xb = reinterpret_cast<char*>(sm.x[st]);
-    for (int op = lane; op < 40; op += 32) {
-        const int half = op / 20, k = op % 20, f0 = 32 * half;
-        if (k < 16) {  // C rows 8g .. 8g+7 of plane k & 1
-            const int g = k >> 1, pl = k & 1;
-            ptx::tma_load_4d(cb + inter_row(half, 16 * g + 8 * pl), pl ? &c8_im : &c8_re, bar, f0, h, t0 + 8 * g, b);
+    const bool fx = fm.fast & 1, fb = (fm.fast >> 1) & 1, fc = (fm.fast >> 2) & 1;
+    const int nc = fc ? 2 : 32, nb = fb ? 2 : 4, nx = fx ? 2 : 4;
+    for (int op = lane; op < nc + nb + nx; op += 32) {
+        if (op < nc) {
+            if (fc) {
+                ptx::tma_load_5d(cb + inter_row(op, 0), &fm.C2, bar, 32 * op, h, 0, 0, (int)(((int64_t)b * T + t0) >> 3));
+            } else {  // C rows 8g .. 8g+7 of plane pl
+                const int half = op >> 4, g = (op >> 1) & 7, pl = op & 1;
+                ptx::tma_load_4d(cb + inter_row(half, 16 * g + 8 * pl), pl ? &fm.c8_im : &fm.c8_re, bar, 32 * half, h,
+                                 t0 + 8 * g, b);
+            }
         } else {
-            const int pl = k & 1;
-            const CUtensorMap* m = k < 18 ? (pl ? &maps.B_im : &maps.B_re) : (pl ? &maps.x_im : &maps.x_re);
-            ptx::tma_load_4d((k < 18 ? bb : xb) + stk_row(half, pl, 0), m, bar, f0, h, t0, b);
+            const bool isb = op < nc + nb;
+            const int k = isb ? op - nc : op - nc - nb;
+            char* dst = isb ? bb : xb;
+            if (isb ? fb : fx) {
+                ptx::tma_load_5d(dst + stk_row(k, 0, 0), isb ? &fm.B2 : &fm.x2, bar, 32 * k, h, t0, 0, b);
+            } else {
+                const int half = k >> 1, pl = k & 1;
+                const CUtensorMap* m = isb ? (pl ? &fm.B_im : &fm.B_re) : (pl ? &fm.x_im : &fm.x_re);
+                ptx::tma_load_4d(dst + stk_row(half, pl, 0), m, bar, 32 * half, h, t0, b);
+            }
         }
     }
 }
@@ -195,16 +254,15 @@ __device__ __forceinline__ void store_acs(Smem& sm, int st, const Alog& al, int 
     if (lane == 0) ptx::mbar_arrive(&sm.full[st]);
 }
 
+template <bool kSwapC>
 __global__ void __launch_bounds__(kThreads, 1)
-fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const __grid_constant__ CUtensorMap c8_re,
-             const __grid_constant__ CUtensorMap c8_im, const __grid_constant__ CUtensorMap y_re,
-             const __grid_constant__ CUtensorMap y_im) {
+fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
-    const Items items((int64_t)p.B * H, p.nc);
-    const int64_t nitems = items.count();
+    const Items items(p.B * H, (int)p.nc);
+    const int nitems = items.count();
     const uint32_t CL = items.cl, rank = items.rank;
     const uint32_t succ = (rank + 1) % CL, pred = (rank + CL - 1) % CL;
 
@@ -217,12 +275,15 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) ptx::mbar_init(&sm.full[s], 1);
         for (int g = 0; g < 3; ++g) ptx::mbar_init(&sm.mma[g], 1);
-        ptx::mbar_init(&sm.sin_full, 1);
-        ptx::mbar_init(&sm.xt_ready, kWarps);
-        ptx::mbar_init(&sm.bt_ready, 8);
+        for (int k = 0; k < 4; ++k) ptx::mbar_init(&sm.sin_full[k], 1);
+        ptx::mbar_init(&sm.stage_free, 1);
+        ptx::mbar_init(&sm.xt_ready, kWorkerWarps);
+        ptx::mbar_init(&sm.bt_ready, kWorkerWarps);
+        ptx::mbar_init(&sm.p_ready, kWorkerWarps);
         ptx::mbar_init(&sm.succ_empty, 1);
         ptx::fence_mbar_init();
-        if (CL > 1) ptx::mbar_arrive_expect_tx(&sm.sin_full, kStateBytes);  // first transfer
+        if (CL > 1)  // first transfer
+            for (int k = 0; k < 4; ++k) ptx::mbar_arrive_expect_tx(&sm.sin_full[k], kQuarterBytes);
     }
     if (warp == 0) {
         ptx::tmem_alloc(&sm.tmem, kTmemCols);
@@ -231,354 +292,380 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    ptx::cluster_sync();  // peers' barriers are initialised before any remote access
     const uint32_t tmem = sm.tmem;
 
-    // first chunk's tiles and decays
-    if (warp == kLoader && nitems > 0) {
-        int64_t q0, c0;
-        items.get(0, q0, c0);
-        const int b0 = (int)(q0 / H), h0 = (int)(q0 % H);
-        load_tiles(sm, 0, maps, c8_re, c8_im, h0, (int)(c0 * kQ), b0, lane);
-        store_acs(sm, 0, load_alog(p, b0, h0, c0 * kQ, lane), lane);
-    }
-
-    const int h4 = warp >> 2;                   // column quarter of this warp
-    const int m = (warp & 3) * 32 + lane;       // TMEM lane
-    const int r8 = 8 * (m >> 4) + (m & 7);      // complex row (l or d) of this lane
-    const int pl = (m >> 3) & 1;                // plane of this lane
-    const uint32_t my = lane_base(tmem, warp);
-    uint32_t n_recv = 0, n_send = 0;
-    bool recv_ok = true;
-    const uint32_t sin_saddr = ptx::smem_addr(sm.sin);
-    const uint32_t remote_sin = ptx::mapa(sin_saddr, succ);
-    const uint32_t remote_sin_full = ptx::mapa(ptx::smem_addr(&sm.sin_full), succ);
-    const uint32_t remote_pred_empty = ptx::mapa(ptx::smem_addr(&sm.succ_empty), pred);
-
-    auto wait_mma = [&](int g, int64_t it) {
-        if (!ptx::mbar_wait(&sm.mma[g], (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
-        ptx::tc_fence_after();
-    };
-    auto publish = [&]() {  // tcgen05.st and smem writes of all threads -> MMA issue
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncthreads();
-        ptx::tc_fence_after();
-    };
-
-    // dt of chunk it + 1 is loaded during chunk it - 1 and consumed during chunk it
-    Alog nal = {};
-    if (warp == kLoader && nitems > 1) {
-        int64_t q1, c1;
-        items.get(1, q1, c1);
-        nal = load_alog(p, (int)(q1 / H), (int)(q1 % H), c1 * kQ, lane);
-    }
-    for (int64_t it = 0; it < nitems; ++it) {
-        const int s = (int)(it & 1);
-        int64_t q, c;
-        items.get(it, q, c);
-        const int b = (int)(q / H), h = (int)(q % H);
-        const int64_t t0 = c * kQ;
-        const bool has_in = c > 0, last = c == p.nc - 1;
-        char* xbase = reinterpret_cast<char*>(sm.x[s]);
-        char* bbase = reinterpret_cast<char*>(sm.b[s]);
-        const char* cbase = reinterpret_cast<const char*>(sm.c[s]);
-        const uint32_t cs = ptx::smem_addr(cbase), bs = ptx::smem_addr(bbase), xs = ptx::smem_addr(xbase);
-        if (!ptx::mbar_wait(&sm.full[s], (uint32_t)((it >> 1) & 1), kWaitIters)) fail(ws.status);
-        if (tid == 0) {
-            // C B^T reads only TMA-loaded tiles: issue it first
+    if (warp == kProducer) {
+        // ============ producer warp: TMA loads and cumulative log-decays ============
+        bool ok = true;  // false once a wait gave up: later waits are skipped
+        Pos ld = items.first(H);
+        Alog al = {};
+        if (nitems > 0) al = load_alog(p, ld.b, ld.h, (int64_t)ld.c * kQ, lane);
+        for (int j = 0; j < nitems; ++j) {  // item j into stage j & 1
+            if (j == 1) ptx::cluster_sync();  // peers' barriers are initialised before any remote access
+            const int st = j & 1;
+            if (j >= 2) {
+                // the workers have passed the first barrier of item j - 1: item j - 2 left the stage
+                if (lane == 0 && ok && !ptx::mbar_wait(&sm.stage_free, (uint32_t)((j - 2) & 1), kWaitIters)) {
+                    fail(ws.status);
+                    ok = false;
+                }
+                __syncwarp();
+            }
+            load_tiles(sm, st, fm, ld.h, ld.c * kQ, ld.b, p.T, lane);
+            const Alog now = al;
+            ld = items.next(ld, H);
+            if (j + 1 < nitems) al = load_alog(p, ld.b, ld.h, (int64_t)ld.c * kQ, lane);
+            store_acs(sm, st, now, lane);
+        }
+        if (nitems <= 1) ptx::cluster_sync();
+    } else if (warp == kIssuer) {
+        // ============ MMA warp: lane 0 issues every MMA in chunk order ============
+        ptx::cluster_sync();  // peers' barriers are initialised before any remote access
+        bool ok = true;  // false once a wait gave up: later waits are skipped
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (ok && !ptx::mbar_wait(bar, parity, kWaitIters)) {
+                fail(ws.status);
+                ok = false;
+            }
+        };
+        const uint32_t pred_empty = ptx::mapa(ptx::smem_addr(&sm.succ_empty), pred);
+        const uint32_t sin_saddr = ptx::smem_addr(sm.sin);
+        Pos cur = items.first(H);
+        bool prev_in = false;
+        uint32_t n_recv = 0;
+        for (int it = 0; it < nitems && lane == 0; ++it) {
+            const int s = it & 1;
+            const bool has_in = cur.c > 0;
+            const uint32_t cs = ptx::smem_addr(sm.c[s]), bs = ptx::smem_addr(sm.b[s]), xs = ptx::smem_addr(sm.x[s]);
+            wait(&sm.full[s], (uint32_t)((it >> 1) & 1));
             ptx::tc_fence_after();
             issue_ss128(tmem + kAccG, desc128(cs), desc128(bs));  // [C Br | C Bi]
             ptx::mma_commit(&sm.mma[0]);
-            ptx::bulk_wait_read_all();  // the previous chunk's y store has read its stage
+            if (it > 0) {
+                // the previous chunk's y MMAs are done: its incoming state buffer is free
+                wait(&sm.mma[2], (uint32_t)((it - 1) & 1));
+                if (prev_in && CL > 1 && ok) {
+                    for (int k = 0; k < 4; ++k) ptx::mbar_arrive_expect_tx(&sm.sin_full[k], kQuarterBytes);
+                    ptx::mbar_arrive_remote(pred_empty);
+                }
+            }
+            wait(&sm.xt_ready, (uint32_t)(it & 1));
+            wait(&sm.bt_ready, (uint32_t)(it & 1));
+            ptx::tc_fence_after();
+            issue_ss128(tmem + kAccS, desc128(xs), desc128(bs));  // [x^T B'r | x^T B'i]
+            ptx::mma_commit(&sm.mma[1]);
+            wait(&sm.p_ready, (uint32_t)(it & 1));
+            ptx::tc_fence_after();
+            issue_ts128(tmem + kAccY, tmem + kPwin, desc128(xs), false);  // P x^T (interleaved columns)
+            if (has_in) {
+                if (CL > 1) {
+                    for (int k = 0; k < 4; ++k) wait(&sm.sin_full[k], n_recv & 1);
+                    ++n_recv;
+                }
+                ptx::tc_fence_after();
+                issue_ts128(tmem + kAccY, tmem + kCwin, desc128(sin_saddr), true);  // + C' S_in
+            }
+            ptx::mma_commit(&sm.mma[2]);
+            prev_in = has_in;
+            cur = items.next(cur, H);
         }
+        __syncwarp();
+    } else {
+        // ===================== 16 worker warps =====================
+        ptx::cluster_sync();  // peers' barriers are initialised before any remote access
+        // Fragment of a warp: TMEM lane quadrant qd, 16-lane block blk of it (complex rows
+        // rr = 16 qd + 8 blk + i4: lane i4 holds plane 0, lane i4 + 8 plane 1) and the 32-column
+        // half kh (column pair n = 32 kh + 8 j + 2 lq + {0, 1}, j = 0 .. 3). In an interleaved
+        // tile these are 16 whole 128-byte rows; the four warps of a quadrant hold rows
+        // [32 qd, 32 qd + 32) of both halves, the quadrant's 2 x 4 KB of the state.
+        const int qd = warp & 3, blk = (warp >> 2) & 1, kh = warp >> 3;
+        const int i4 = lane >> 2, lq = lane & 3;
+        const int rr = 16 * qd + 8 * blk + i4;
+        const int mre = inter_m(rr, 0), mim = inter_m(rr, 1);
+        const uint32_t tl = lane_base(tmem, warp) + ((uint32_t)(16 * blk) << 16);
+        const bool leader = warp == qd && lane == 0;  // copies the quadrant's rows of the state
+        // physical plane order of the x and B tiles, and the C-tile rows and G-accumulator
+        // columns that hold the real planes
+        const int swx = fm.swap & 1, swb = (fm.swap >> 1) & 1;
+        constexpr int kCr = kSwapC ? 1 : 0;                 // C plane in TMEM lane plane 0 / 1
+        constexpr int kRr = 2 * kCr, kRi = 2 - 2 * kCr;     // register offset of the C_r / C_i lanes
+        const uint32_t gbr = kAccG + 64 * swb, gbi = kAccG + 64 * (1 - swb);  // B_r / B_i products
+        uint32_t n_recv = 0, n_send = 0;
+        const uint32_t remote_sin = ptx::mapa(ptx::smem_addr(sm.sin), succ);
+        const uint32_t remote_sin_full = ptx::mapa(ptx::smem_addr(&sm.sin_full[qd]), succ);
 
-        // ---- A: decays; x and B 4x4 blocks into registers. Lane bits pick the
-        // block so that a warp's 16-byte accesses cover all eight bank groups.
-        if (tid < kQ) {
-            sm.dec[tid] = cexp_fast(cdiff(sm.acs[s][kQ - 1], sm.acs[s][tid]));
-        } else if (tid < 2 * kQ) {
-            sm.eacs[tid - kQ] = cexp_fast(sm.acs[s][tid - kQ]);
-        } else if (tid == 2 * kQ) {
-            sm.a_c = cexp_fast(sm.acs[s][kQ - 1]);
-        } else if (tid > 2 * kQ && tid <= 3 * kQ - 2) {
-            const int t = tid - 2 * kQ - 1;  // 0 .. Q-3
-            sm.pair[t] = cexp_fast(cdiff(sm.acs[s][t + 2], sm.acs[s][t]));
-        }
-        const int blo = lane & 7, bmid = (lane >> 3) & 3;
-        const int xsb = bmid + 4 * (warp & 3), xdb = blo + 8 * ((warp >> 2) & 1), xp = (warp >> 3) & 1;
-        float4 xv[4];
+        auto wait_mma = [&](int g, int it) {
+            if (!ptx::mbar_wait(&sm.mma[g], (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
+            ptx::tc_fence_after();
+        };
+        // this thread's state values S^T[rr, n] in an interleaved tile, index 2 j + e
+        auto for_pairs = [&](char* base, float* vr, float* vi, bool store) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {  // x block: rows s = 4 xsb + i, columns d = 4 xdb ..
-            const int sr = 4 * xsb + i;
-            xv[i] = *reinterpret_cast<const float4*>(xbase + stk_row(xdb >> 3, xp, sr) + chunk16(xdb & 7, sr));
-        }
-        const bool bwork = warp < 8;  // (dec o B)^T: one block of both planes per thread of warps 0-7
-        const int bsb = bmid + 4 * (warp & 3), bnb = blo + 8 * ((warp >> 2) & 1);
-        float4 bv[2][4];
-        if (bwork) {
+            for (int j = 0; j < 4; ++j) {
+                float2* pr = reinterpret_cast<float2*>(base + pair_off(kh, mre, 8 * j + 2 * lq));
+                float2* pi = reinterpret_cast<float2*>(base + pair_off(kh, mim, 8 * j + 2 * lq));
+                if (store) {
+                    *pr = make_float2(vr[2 * j], vr[2 * j + 1]);
+                    *pi = make_float2(vi[2 * j], vi[2 * j + 1]);
+                } else {
+                    const float2 a = *pr, b = *pi;
+                    vr[2 * j] = a.x;
+                    vr[2 * j + 1] = a.y;
+                    vi[2 * j] = b.x;
+                    vi[2 * j + 1] = b.y;
+                }
+            }
+        };
+
+        // Work left over from the previous chunk, done at the start of the next one (or after
+        // the last): wait for its y MMAs, keep its outgoing state (CL = 1) and write its y row
+        // straight from the accumulator to global memory. Column 16g + 8p' + i of the
+        // accumulator holds the plane-p' products of column d = 8g + i; four consecutive lanes
+        // hold one 32-byte run of a row.
+        float outr[8], outi[8];
+        auto finish = [&](int it, const Pos& pos, bool keep_state) {
+            wait_mma(2, it);
+            if (keep_state) {
+                for_pairs(reinterpret_cast<char*>(sm.sin), outr, outi, true);
+                ptx::fence_proxy_async_smem();
+            }
+            float yv[32];
+            ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh, yv);
+            ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh + 32, yv + 16);
+            ptx::tmem_wait_ld();
+            const int64_t t = (int64_t)pos.c * kQ + rr;
+            if (t < p.T) {
+                const int64_t row = (((int64_t)pos.b * p.T + t) * H + pos.h) * 64;
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int dd = 0; dd < 2; ++dd) {
+                        const int jr = 16 * u + 8 * dd, ji = jr + 4;  // register blocks of planes x_r, x_i
+                        const int d = 32 * kh + 16 * u + 8 * dd + 2 * lq;
+                        // Re y = (P_r x_r)[p0] - (P_i x_i)[p1], Im y = (P_r x_i)[p0] + (P_i x_r)[p1]
+                        *reinterpret_cast<float2*>(p.y_re + row + d) =
+                            make_float2(yv[jr + 0] - yv[ji + 2], yv[jr + 1] - yv[ji + 3]);
+                        *reinterpret_cast<float2*>(p.y_im + row + d) =
+                            make_float2(yv[ji + 0] + yv[jr + 2], yv[ji + 1] + yv[jr + 3]);
+                    }
+            }
+        };
+
+        Pos cur = items.first(H), prev = cur;
+        bool prev_keep = false;
+        for (int it = 0; it < nitems; ++it) {
+            const int s = it & 1;
+            const bool has_in = cur.c > 0, last = cur.c == (int)p.nc - 1;
+            char* xbase = reinterpret_cast<char*>(sm.x[s]);
+            char* bbase = reinterpret_cast<char*>(sm.b[s]);
+            char* cbase = reinterpret_cast<char*>(sm.c[s]);
+            const uint32_t cs = ptx::smem_addr(cbase);
+            if (!ptx::mbar_wait(&sm.full[s], (uint32_t)((it >> 1) & 1), kWaitIters)) fail(ws.status);
+
+            // ---- A: decays; the previous chunk's y; x and B blocks into registers. Lane bits
+            // pick the blocks so that a warp's accesses cover all bank groups.
+            if (tid < kQ) {
+                sm.dec[tid] = cexp_fast(cdiff(sm.acs[s][kQ - 1], sm.acs[s][tid]));
+            } else if (tid < 2 * kQ) {
+                sm.eacs[tid - kQ] = cexp_fast(sm.acs[s][tid - kQ]);
+            } else if (tid == 2 * kQ) {
+                sm.a_c = cexp_fast(sm.acs[s][kQ - 1]);
+            } else if (tid < 3 * kQ) {
+                const int t = tid - 2 * kQ;  // 1 .. Q-1
+                sm.step[t] = cexp_fast(cdiff(sm.acs[s][t], sm.acs[s][t - 1]));
+            }
+            if (it > 0) finish(it - 1, prev, prev_keep);
+            const int blo = lane & 7, bmid = (lane >> 3) & 3;
+            const int xsb = bmid + 4 * (warp & 3), xdb = blo + 8 * ((warp >> 2) & 1), xp = (warp >> 3) & 1;
+            float4 xv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {  // x block: rows s = 4 xsb + i, columns d = 4 xdb ..
+                const int sr = 4 * xsb + i;
+                xv[i] = *reinterpret_cast<const float4*>(xbase + stk_row(xdb >> 3, xp ^ swx, sr) + chunk16(xdb & 7, sr));
+            }
+            // (dec o B)^T: rows s = 4 bsb + i, columns n = 4 bnb + 2 bjh + {0, 1}, both planes
+            const int bjh = (lane >> 3) & 1;
+            const int bsb = ((lane >> 4) & 1) + 2 * (warp >> 1), bnb = blo + 8 * (warp & 1);
+            float2 bv[2][4];
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int sr = 4 * bsb + i;
-                    bv[pp][i] = *reinterpret_cast<const float4*>(bbase + stk_row(bnb >> 3, pp, sr) + chunk16(bnb & 7, sr));
+                    bv[pp][i] = *reinterpret_cast<const float2*>(bbase + stk_row(bnb >> 3, pp ^ swb, sr) + chunk16(bnb & 7, sr) + 8 * bjh);
                 }
-        }
-        __syncthreads();
-        // the previous chunk's stage is free: prefetch the next chunk into it
-        const bool prefetch = it + 1 < nitems;
-        int64_t qn = 0, cn = 0;
-        if (warp == kLoader && prefetch) items.get(it + 1, qn, cn);
+            // the previous chunk's state copies have read their staging buffer (the
+            // other stage's C tile), which the producer's next prefetch overwrites
+            if (leader) ptx::bulk_wait_read_all();
+            ptx::named_sync(kWorkerBar, kWorkers);
+            if (tid == 0 && it >= 1) ptx::mbar_arrive(&sm.stage_free);
+            // The decay tables are rewritten at the start of the next chunk, which a warp can
+            // reach once every warp has announced its (dec o B)^T block: what is needed after
+            // that announcement is read now.
+            const float2 a_c = sm.a_c;
+            float2 step_j[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) step_j[j] = sm.step[32 * kh + 8 * j + 2 * lq + 1];
 
-        // ---- B: x^T (interleaved rows d) in place of x; C' = C o exp(Acs[l]) rows into TMEM; C B^T
-        {
-            const float4 o[4] = {make_float4(xv[0].x, xv[1].x, xv[2].x, xv[3].x), make_float4(xv[0].y, xv[1].y, xv[2].y, xv[3].y),
-                                 make_float4(xv[0].z, xv[1].z, xv[2].z, xv[3].z), make_float4(xv[0].w, xv[1].w, xv[2].w, xv[3].w)};
+            // ---- B: x^T (interleaved rows d) in place of x; C' = C o exp(Acs[l]) rows into TMEM
+            {
+                const float4 o[4] = {make_float4(xv[0].x, xv[1].x, xv[2].x, xv[3].x), make_float4(xv[0].y, xv[1].y, xv[2].y, xv[3].y),
+                                     make_float4(xv[0].z, xv[1].z, xv[2].z, xv[3].z), make_float4(xv[0].w, xv[1].w, xv[2].w, xv[3].w)};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int mm = inter_m(4 * xdb + j, xp);
-                *reinterpret_cast<float4*>(xbase + inter_row(xsb >> 3, mm) + chunk16(xsb & 7, mm)) = o[j];
-            }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sm.xt_ready);
-        }
-        {
-            // plane pl of C'[l, n] for n in [16 h4, 16 h4 + 16): row l of both C planes
-            const float2 e = sm.eacs[r8];
-            const int kh = h4 >> 1, j0 = 4 * (h4 & 1);
-            const int mre = inter_m(r8, 0), mim = inter_m(r8, 1);
-            float w[16];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 cr = *reinterpret_cast<const float4*>(cbase + inter_row(kh, mre) + chunk16(j0 + j, mre));
-                const float4 ci = *reinterpret_cast<const float4*>(cbase + inter_row(kh, mim) + chunk16(j0 + j, mim));
-                const float crv[4] = {cr.x, cr.y, cr.z, cr.w}, civ[4] = {ci.x, ci.y, ci.z, ci.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    w[4 * j + k] = pl ? (crv[k] * e.y + civ[k] * e.x) : (crv[k] * e.x - civ[k] * e.y);
-            }
-            ptx::tmem_st16(my + kCwin + 16 * h4, w);
-        }
-        if (warp == kLoader && prefetch)
-            load_tiles(sm, s ^ 1, maps, c8_re, c8_im, (int)(qn % H), (int)(cn * kQ), (int)(qn / H), lane);
-        wait_mma(0, it);  // C B^T has read B
-
-        // ---- C: (dec o B)^T stacked in place of B; then S_loc^T = x^T (dec o B), issued by
-        // thread 0 once every warp has announced its x^T and (dec o B)^T blocks
-        if (bwork) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {  // column n = 4 bnb + j of B -> row n of the output
-                const int nr = 4 * bnb + j;
-                float ore[4], oim[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float* r0v = reinterpret_cast<const float*>(&bv[0][i]);
-                    const float* r1v = reinterpret_cast<const float*>(&bv[1][i]);
-                    const float2 v = cmul(sm.dec[4 * bsb + i], make_float2(r0v[j], r1v[j]));
-                    ore[i] = v.x;
-                    oim[i] = v.y;
+                for (int j = 0; j < 4; ++j) {
+                    const int mm = inter_m(4 * xdb + j, xp);
+                    *reinterpret_cast<float4*>(xbase + inter_row(xsb >> 3, mm) + chunk16(xsb & 7, mm)) = o[j];
                 }
-                *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 0, nr) + chunk16(bsb & 7, nr)) =
-                    make_float4(ore[0], ore[1], ore[2], ore[3]);
-                *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 1, nr) + chunk16(bsb & 7, nr)) =
-                    make_float4(oim[0], oim[1], oim[2], oim[3]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm.xt_ready);
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sm.bt_ready);
-        }
-        if (tid == 0) {
-            if (!ptx::mbar_wait(&sm.xt_ready, (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
-            if (!ptx::mbar_wait(&sm.bt_ready, (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
-            ptx::tc_fence_after();
-            issue_ss128(tmem + kAccS, desc128(xs), desc128(bs));  // [x^T B'r | x^T B'i]
-            ptx::mma_commit(&sm.mma[1]);
-        }
+            {
+                // C'[rr, n] on this thread's eight columns, both planes
+                const float2 e = sm.eacs[rr];
+                const int cre = inter_m(rr, kCr), cim = inter_m(rr, 1 - kCr);
+                float w[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 cr = *reinterpret_cast<const float2*>(cbase + pair_off(kh, cre, 8 * j + 2 * lq));
+                    const float2 ci = *reinterpret_cast<const float2*>(cbase + pair_off(kh, cim, 8 * j + 2 * lq));
+                    w[4 * j + 0] = cr.x * e.x - ci.x * e.y;
+                    w[4 * j + 1] = cr.y * e.x - ci.y * e.y;
+                    w[4 * j + 2] = cr.x * e.y + ci.x * e.x;
+                    w[4 * j + 3] = cr.y * e.y + ci.y * e.x;
+                }
+                ptx::tmem_st_16x256b_x4(tl + kCwin + 32 * kh, w);
+            }
+            wait_mma(0, it);  // C B^T has read B
 
-        // ---- D: P = (C B^T) o L on this thread's columns; P rows into TMEM; then P x
-        {
-            // columns [8 h4, 8 h4 + 8) and [32 + 8 h4, 32 + 8 h4 + 8), in pairs (e, e + 1)
-            float ga[16], gb[16];
-            ptx::tmem_ld8(my + kAccG + 8 * h4, ga);
-            ptx::tmem_ld8(my + kAccG + 32 + 8 * h4, ga + 8);
-            ptx::tmem_ld8(my + kAccG + 64 + 8 * h4, gb);
-            ptx::tmem_ld8(my + kAccG + 96 + 8 * h4, gb + 8);
-            ptx::tmem_wait_ld();
-            const float2 acs_l = sm.acs[s][r8];
-            // complex G on this thread's columns: column e + pl of each pair
-            float gre[8], gim[8];
+            // ---- C: (dec o B)^T stacked in place of B (the MMA warp then starts S_loc^T = x^T (dec o B))
+            {
+                float2 dv[4];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const float ra = __shfl_xor_sync(0xffffffffu, pl ? ga[2 * jj] : ga[2 * jj + 1], 8);
-                const float rb = __shfl_xor_sync(0xffffffffu, pl ? gb[2 * jj] : gb[2 * jj + 1], 8);
-                // plane-0 products (Cr B) and plane-1 products (Ci B) of this thread's column
-                const float ga0 = pl ? ra : ga[2 * jj], gb0 = pl ? rb : gb[2 * jj];
-                const float ga1 = pl ? ga[2 * jj + 1] : ra, gb1 = pl ? gb[2 * jj + 1] : rb;
-                gre[jj] = ga0 - gb1;
-                gim[jj] = gb0 + ga1;
-            }
-            // L[l, col] for the four columns col = base + 2k + pl of each 8-column range, from
-            // the last one with col <= l down: one exponential of a difference of cumulative
-            // sums, then L[l, col - 2] = L[l, col] exp(Acs[col] - Acs[col - 2]).
-            float pr[8], pim[8];
+                for (int i = 0; i < 4; ++i) dv[i] = sm.dec[4 * bsb + i];
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                const int base = (rr ? 32 : 0) + 8 * h4 + pl;
-                float2 L = make_float2(0.0f, 0.0f);
-                bool started = false;
+                for (int j = 0; j < 2; ++j) {  // column n of B -> row n of the output
+                    const int nr = 4 * bnb + 2 * bjh + j;
+                    float ore[4], oim[4];
 #pragma unroll
-                for (int k = 3; k >= 0; --k) {
-                    const int col = base + 2 * k, jj = 4 * rr + k;
-                    float2 v = make_float2(0.0f, 0.0f);
-                    if (col <= r8) {
-                        L = started ? cmul(L, sm.pair[col]) : cexp_fast(cdiff(acs_l, sm.acs[s][col]));
-                        started = true;
-                        v = cmul(make_float2(gre[jj], gim[jj]), L);
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 v = cmul(dv[i], j ? make_float2(bv[0][i].y, bv[1][i].y) : make_float2(bv[0][i].x, bv[1][i].x));
+                        ore[i] = v.x;
+                        oim[i] = v.y;
                     }
-                    pr[jj] = v.x;
-                    pim[jj] = v.y;
+                    *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 0, nr) + chunk16(bsb & 7, nr)) =
+                        make_float4(ore[0], ore[1], ore[2], ore[3]);
+                    *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 1, nr) + chunk16(bsb & 7, nr)) =
+                        make_float4(oim[0], oim[1], oim[2], oim[3]);
                 }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm.bt_ready);
             }
-            float w[16];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                // lane p keeps plane p of P: column e from the p = 0 lane, e + 1 from the p = 1 lane
-                const float other = __shfl_xor_sync(0xffffffffu, pl ? pr[jj] : pim[jj], 8);
-                w[2 * jj] = pl ? other : pr[jj];
-                w[2 * jj + 1] = pl ? pim[jj] : other;
-            }
-            ptx::tmem_st8(my + kPwin + 8 * h4, w);
-            ptx::tmem_st8(my + kPwin + 32 + 8 * h4, w + 8);
-        }
-        publish();
-        if (tid == 0) issue_ts128(tmem + kAccY, tmem + kPwin, desc128(xs), false);  // P x^T (interleaved columns)
 
-        // ---- E: S_loc^T and the state hop  S_out = a_c S_in + S_loc  (row d = r8, n in [16 h4, +16))
-        if (warp == kLoader && prefetch) {
-            store_acs(sm, s ^ 1, nal, lane);  // next chunk's decays
-            if (it + 2 < nitems) {
-                int64_t q2, c2;
-                items.get(it + 2, q2, c2);
-                nal = load_alog(p, (int)(q2 / H), (int)(q2 % H), c2 * kQ, lane);
-            }
-        }
-        wait_mma(1, it);
-        float out[16];
-        {
-            float sa[16], sb[16];
-            ptx::tmem_ld16(my + kAccS + 16 * h4, sa);
-            ptx::tmem_ld16(my + kAccS + 64 + 16 * h4, sb);
-            ptx::tmem_wait_ld();
-            if (has_in && CL > 1) {
-                if (!ptx::mbar_wait(&sm.sin_full, n_recv & 1, kWaitIters)) {
-                    fail(ws.status);
-                    recv_ok = false;  // the buffer protocol stops here for this CTA
+            // ---- D: P = (C B^T) o L on this thread's row rr and columns col, col + 1 (col = 32 kh +
+            // 8 j + 2 lq); P rows into TMEM (the MMA warp then starts P x). In the accumulator, one
+            // 64-column half holds the products with B_r, the other with B_i; lane plane 0 / 1 of
+            // the row holds the products of C's plane 0 / 1 (C_r first unless kSwapC).
+            {
+                float ga[16], gb[16];
+                ptx::tmem_ld_16x256b_x4(tl + gbr + 32 * kh, ga);
+                ptx::tmem_ld_16x256b_x4(tl + gbi + 32 * kh, gb);
+                ptx::tmem_wait_ld();
+                const float2 acs_l = sm.acs[s][rr];
+                float w[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // L[rr, col + 1] from one exponential, L[rr, col] = L[rr, col + 1] exp(-dA[col + 1])
+                    const int col = 32 * kh + 8 * j + 2 * lq;
+                    float2 L1 = make_float2(0.0f, 0.0f), L0 = make_float2(0.0f, 0.0f);
+                    if (col + 1 <= rr) {
+                        L1 = cexp_fast(cdiff(acs_l, sm.acs[s][col + 1]));
+                        L0 = cmul(L1, step_j[j]);
+                    } else if (col == rr) {
+                        L0 = make_float2(1.0f, 0.0f);
+                    }
+                    // Re G = Cr Br - Ci Bi, Im G = Cr Bi + Ci Br
+                    const float2 g0 = make_float2(ga[4 * j + kRr] - gb[4 * j + kRi], gb[4 * j + kRr] + ga[4 * j + kRi]);
+                    const float2 g1 = make_float2(ga[4 * j + kRr + 1] - gb[4 * j + kRi + 1],
+                                                  gb[4 * j + kRr + 1] + ga[4 * j + kRi + 1]);
+                    const float2 p0 = cmul(g0, L0), p1 = cmul(g1, L1);
+                    w[4 * j + 0] = p0.x;
+                    w[4 * j + 1] = p1.x;
+                    w[4 * j + 2] = p0.y;
+                    w[4 * j + 3] = p1.y;
                 }
-                ++n_recv;
+                ptx::tmem_st_16x256b_x4(tl + kPwin + 32 * kh, w);
+                // P and C' rows of this warp are in TMEM
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm.p_ready);
             }
-            const float2 a = sm.a_c;
-            const char* sinb = reinterpret_cast<const char*>(sm.sin);
-            const int kh = h4 >> 1, j0 = 4 * (h4 & 1);
-            const int mre = inter_m(r8, 0), mim = inter_m(r8, 1);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float4 sr = make_float4(0.f, 0.f, 0.f, 0.f), si = sr;
-                if (has_in) {
-                    sr = *reinterpret_cast<const float4*>(sinb + inter_row(kh, mre) + chunk16(j0 + j, mre));
-                    si = *reinterpret_cast<const float4*>(sinb + inter_row(kh, mim) + chunk16(j0 + j, mim));
-                }
-                const float srv[4] = {sr.x, sr.y, sr.z, sr.w}, siv[4] = {si.x, si.y, si.z, si.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int k = 4 * j + e;
-                    const float other = __shfl_xor_sync(0xffffffffu, sb[k], 8);
-                    // Re: a S_in + (xr B'r)[p0] - (xi B'i)[p1];  Im: a S_in + (xr B'i)[p0] + (xi B'r)[p1]
-                    out[k] = pl ? (a.x * siv[e] + a.y * srv[e] + other + sa[k])
-                                : (a.x * srv[e] - a.y * siv[e] + sa[k] - other);
-                }
-            }
-        }
-        const int mo = inter_m(r8, pl);
-        if (last) {
-            float* fs = (pl ? p.fs_im : p.fs_re) + (q * 64) * 64 + r8;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) fs[(int64_t)(16 * h4 + k) * 64] = out[k];
-        } else if (CL > 1) {
-            // stage S_out in the C buffer (C was consumed by C B^T and the C' rows);
-            // worker thread 0 moves it to the next CTA with one bulk copy
-            char* stg = reinterpret_cast<char*>(sm.c[s]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<float4*>(stg + inter_row(h4 >> 1, mo) + chunk16(4 * (h4 & 1) + j, mo)) =
-                    make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-            ptx::fence_proxy_async_smem();
-        }
 
-        // ---- F: (C o exp(Acs)) S_in into the same accumulator
-        publish();
-        if (tid == 0) {
-            // the state goes to the next CTA first: it is on the chain's critical path
-            if (!last && CL > 1 && c != p.drop_send_chunk) {
-                if (n_send > 0 && !ptx::mbar_wait(&sm.succ_empty, (n_send - 1) & 1, kWaitIters)) fail(ws.status);
-                ++n_send;
-                ptx::bulk_copy_to_cluster(remote_sin, cs, kStateBytes, remote_sin_full);
-                ptx::bulk_commit();
-            }
-            if (has_in) issue_ts128(tmem + kAccY, tmem + kCwin, desc128(sin_saddr), true);
-            ptx::mma_commit(&sm.mma[2]);
-        }
-        wait_mma(2, it);
-        if (has_in && CL > 1 && tid == 0 && recv_ok) {
-            // the incoming buffer is consumed: re-arm it and free it for the sender
-            ptx::mbar_arrive_expect_tx(&sm.sin_full, kStateBytes);
-            ptx::mbar_arrive_remote(remote_pred_empty);
-        }
-        if (!last && CL == 1) {
-            // keep the state for this CTA's next chunk
+            // ---- E: S_loc^T and the state hop  S_out = a_c S_in + S_loc  (row d = rr, this thread's
+            // columns n). Each lane quadrant's rows travel to the next CTA as soon as its four warps
+            // have them, so the chain of states is pipelined across quadrants.
+            wait_mma(1, it);
+            {
+                float sa[16], sb[16];
+                ptx::tmem_ld_16x256b_x4(tl + kAccS + 32 * kh, sa);
+                ptx::tmem_ld_16x256b_x4(tl + kAccS + 64 + 32 * kh, sb);
+                ptx::tmem_wait_ld();
+                // Re: (xr B'r)[p0] - (xi B'i)[p1];  Im: (xr B'i)[p0] + (xi B'r)[p1]
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<float4*>(reinterpret_cast<char*>(sm.sin) + inter_row(h4 >> 1, mo) + chunk16(4 * (h4 & 1) + j, mo)) =
-                    make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-            ptx::fence_proxy_async_smem();
-        }
-
-        // ---- G: y rows, staged in the x buffer and written by TMA. Columns
-        // 16g + 8p' + i of the accumulator hold plane-p' products of column 8g + i.
-        {
-            float yv[32];
-            ptx::tmem_ld16(my + kAccY + 32 * h4, yv);
-            ptx::tmem_ld16(my + kAccY + 32 * h4 + 16, yv + 16);
-            ptx::tmem_wait_ld();
-            float o[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int yi = 16 * (k >> 3) + (k & 7);
-                const float ya = yv[yi], yb = yv[yi + 8];
-                // Re y = ya[p0] - yb[p1], Im y = yb[p0] + ya[p1]
-                const float u = pl ? -yb : ya, v = pl ? ya : yb;
-                const float other = __shfl_xor_sync(0xffffffffu, pl ? u : v, 8);
-                o[k] = pl ? v + other : u + other;
+                for (int k = 0; k < 8; ++k) {
+                    const int j = k >> 1, e = k & 1;
+                    outr[k] = sa[4 * j + e] - sb[4 * j + 2 + e];
+                    outi[k] = sb[4 * j + e] + sa[4 * j + 2 + e];
+                }
             }
+            if (has_in) {
+                if (CL > 1) {
+                    if (!ptx::mbar_wait(&sm.sin_full[qd], n_recv & 1, kWaitIters)) fail(ws.status);
+                    ++n_recv;
+                }
+                const float2 a = a_c;
+                float sr[8], si[8];
+                for_pairs(reinterpret_cast<char*>(sm.sin), sr, si, false);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<float4*>(xbase + stk_row(h4 >> 1, pl, r8) + chunk16(4 * (h4 & 1) + k, r8)) =
-                    make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            for (int half = 0; half < 2; ++half) {
-                ptx::tma_store_4d(&y_re, xbase + stk_row(half, 0, 0), 32 * half, h, (int)t0, b);
-                ptx::tma_store_4d(&y_im, xbase + stk_row(half, 1, 0), 32 * half, h, (int)t0, b);
+                for (int k = 0; k < 8; ++k) {
+                    outr[k] += a.x * sr[k] - a.y * si[k];
+                    outi[k] += a.x * si[k] + a.y * sr[k];
+                }
             }
-            ptx::bulk_commit();  // read-complete is awaited before the next prefetch
+            if (last) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int n = 32 * kh + 8 * (k >> 1) + 2 * lq + (k & 1);
+                    const int64_t o = ((int64_t)cur.q * 64 + n) * 64 + rr;
+                    p.fs_re[o] = outr[k];
+                    p.fs_im[o] = outi[k];
+                }
+            } else if (CL > 1) {
+                // stage S_out in the C buffer (C was consumed by C B^T and the C' rows), then the
+                // quadrant's leader copies its 2 x 4 KB of rows to the next CTA
+                for_pairs(cbase, outr, outi, true);
+                ptx::fence_proxy_async_smem();
+                ptx::named_sync(1 + qd, 128);
+                if (leader && cur.c != p.drop_send_chunk) {
+                    if (n_send > 0 && !ptx::mbar_wait(&sm.succ_empty, (n_send - 1) & 1, kWaitIters)) fail(ws.status);
+                    ++n_send;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t off = (uint32_t)half * kIntHalf + (uint32_t)(32 * qd) * 128u;
+                        ptx::bulk_copy_to_cluster(remote_sin + off, cs + off, kQuarterBytes / 2, remote_sin_full);
+                    }
+                    ptx::bulk_commit();
+                }
+            }
+            prev = cur;
+            prev_keep = !last && CL == 1;
+            cur = items.next(cur, H);
         }
+        if (nitems > 0) finish(nitems - 1, prev, false);
+        if (leader) ptx::bulk_wait_all();
     }
-    if (tid == 0) ptx::bulk_wait_all();
-
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
@@ -588,9 +675,74 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ TcMaps maps, const
 constexpr size_t kSmemBytes = sizeof(Smem);
 bool g_attr_set[64] = {};
 
-// (F, H, T, B) fp32 plane as 8-row boxes (32, 1, 8, 1), 128-byte swizzle.
-bool make_rows8_map(CUtensorMap* m, const float* base, int H, int64_t T, int B) {
-    return tc::encode_feature_map(m, base, 64, H, T, B, 8);
+// Plane pair (re, im) as one map dimension: base = the lower address, stride =
+// the distance, swap = the imaginary plane comes first.
+bool plane_pair(const float* re, const float* im, const float** base, cuuint64_t* stride, bool* swap) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(re), b = reinterpret_cast<uintptr_t>(im);
+    if (a == b) return false;
+    *swap = b < a;
+    *base = reinterpret_cast<const float*>(b < a ? b : a);
+    const uint64_t d = b < a ? a - b : b - a;
+    if (d % 16 != 0 || d >= (uint64_t(1) << 40)) return false;
+    *stride = d;
+    return true;
+}
+
+// Both planes of an (F, H, T, B) tensor, boxes (32, 1, 64, 2, 1): the stacked layout.
+bool make_pair_map(CUtensorMap* m, const float* re, const float* im, const Problem& p, bool* swap) {
+    const float* base;
+    cuuint64_t ps;
+    if (!plane_pair(re, im, &base, &ps, swap)) return false;
+    const cuuint64_t row = 64 * 4;
+    const cuuint64_t dims[5] = {64, (cuuint64_t)p.H, (cuuint64_t)p.T, 2, (cuuint64_t)p.B};
+    const cuuint64_t strides[4] = {row, row * p.H, ps, row * p.H * (cuuint64_t)p.T};
+    const cuuint32_t box[5] = {32, 1, 64, 2, 1};
+    return tc::encode_tiled_f32(m, base, 5, dims, strides, box);
+}
+
+// Both planes of C, time split into 8-row groups (T a multiple of 8, so that
+// batch and group merge into one dimension), boxes (32, 1, 8, 2, 8): the
+// interleaved layout, row 16g + 8p + i.
+bool make_interleaved_map(CUtensorMap* m, const Problem& p, bool* swap) {
+    if (p.T % 8 != 0 || (int64_t)p.B * p.T / 8 >= (int64_t(1) << 31)) return false;
+    const float* base;
+    cuuint64_t ps;
+    if (!plane_pair(p.C_re, p.C_im, &base, &ps, swap)) return false;
+    const cuuint64_t row = 64 * 4;
+    const cuuint64_t dims[5] = {64, (cuuint64_t)p.H, 8, 2, (cuuint64_t)p.B * (cuuint64_t)p.T / 8};
+    const cuuint64_t strides[4] = {row, row * p.H, ps, 8 * row * p.H};
+    const cuuint32_t box[5] = {32, 1, 8, 2, 8};
+    return tc::encode_tiled_f32(m, base, 5, dims, strides, box);
+}
+
+int make_fused_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
+    memset(fm, 0, sizeof(*fm));
+    bool sw = false;
+    if (allow_fast && make_pair_map(&fm->x2, p.x_re, p.x_im, p, &sw)) fm->fast |= 1, fm->swap |= sw ? 1 : 0;
+    if (allow_fast && make_pair_map(&fm->B2, p.B_re, p.B_im, p, &sw)) fm->fast |= 2, fm->swap |= sw ? 2 : 0;
+    if (allow_fast && make_interleaved_map(&fm->C2, p, &sw)) fm->fast |= 4, fm->swap |= sw ? 4 : 0;
+    bool ok = true;
+    if (!(fm->fast & 1))
+        ok = ok && tc::encode_feature_map(&fm->x_re, p.x_re, 64, p.H, p.T, p.B, 64) &&
+             tc::encode_feature_map(&fm->x_im, p.x_im, 64, p.H, p.T, p.B, 64);
+    if (!(fm->fast & 2))
+        ok = ok && tc::encode_feature_map(&fm->B_re, p.B_re, 64, p.H, p.T, p.B, 64) &&
+             tc::encode_feature_map(&fm->B_im, p.B_im, 64, p.H, p.T, p.B, 64);
+    if (!(fm->fast & 4))
+        ok = ok && tc::encode_feature_map(&fm->c8_re, p.C_re, 64, p.H, p.T, p.B, 8) &&
+             tc::encode_feature_map(&fm->c8_im, p.C_im, 64, p.H, p.T, p.B, 8);
+    return ok ? SSDC_OK : SSDC_ERR_CUDA;
+}
+
+int set_attrs(int dev) {
+    if (g_attr_set[dev]) return SSDC_OK;
+    if (cudaFuncSetAttribute(fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess)
+        return SSDC_ERR_CUDA;
+    g_attr_set[dev] = true;
+    return SSDC_OK;
 }
 
 }  // namespace
@@ -600,12 +752,8 @@ bool make_rows8_map(CUtensorMap* m, const float* base, int H, int64_t T, int B) 
 int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSDC_ERR_CUDA;
-    if (!g_attr_set[dev]) {
-        if (cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
-            return SSDC_ERR_CUDA;
-        g_attr_set[dev] = true;
-    }
+    const int arc = set_attrs(dev);
+    if (arc != SSDC_OK) return arc;
     const int64_t nseq = (int64_t)p.B * p.H;
     double best = 1e300;
     int best_cl = 1, best_n = 1;
@@ -623,7 +771,7 @@ int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, fused_kernel, &cfg) != cudaSuccess || active <= 0) {
+        if (cudaOccupancyMaxActiveClusters(&active, fused_kernel<false>, &cfg) != cudaSuccess || active <= 0) {
             (void)cudaGetLastError();
             continue;
         }
@@ -648,7 +796,7 @@ int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
 
 bool fused_supported(int N, int D, int Q) { return N == 64 && D == 64 && Q == 64; }
 
-int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster) {
+int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster, bool plane_maps) {
     int cl = 1, nclusters = 1;
     int rc = fused::pick_cluster(p, &cl, &nclusters);
     if (rc != SSDC_OK) return rc;
@@ -662,14 +810,9 @@ int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int
         const int64_t fit = sms / cl > 0 ? sms / cl : 1;
         nclusters = (int)(nseq < fit ? nseq : fit);
     }
-    tc::TcMaps maps;
-    rc = tc::make_maps(p, nullptr, &maps);
+    fused::FusedMaps fm;
+    rc = fused::make_fused_maps(p, plane_maps, &fm);
     if (rc != SSDC_OK) return rc;
-    CUtensorMap c8_re, c8_im, y_re, y_im;
-    if (!fused::make_rows8_map(&c8_re, p.C_re, p.H, p.T, p.B) || !fused::make_rows8_map(&c8_im, p.C_im, p.H, p.T, p.B) ||
-        !tc::encode_feature_map(&y_re, p.y_re, 64, p.H, p.T, p.B, 64) ||
-        !tc::encode_feature_map(&y_im, p.y_im, 64, p.H, p.T, p.B, 64))
-        return SSDC_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -682,8 +825,9 @@ int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, fused::fused_kernel, p, ws, maps, c8_re, c8_im, y_re, y_im) != cudaSuccess) return SSDC_ERR_CUDA;
-    return 1;
+    const cudaError_t e = (fm.swap & 4) ? cudaLaunchKernelEx(&cfg, fused::fused_kernel<true>, p, ws, fm)
+                                        : cudaLaunchKernelEx(&cfg, fused::fused_kernel<false>, p, ws, fm);
+    return e == cudaSuccess ? 1 : SSDC_ERR_CUDA;
 }
 
 }  // namespace ssdc

@@ -197,7 +197,11 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const
         const char* env = getenv("SSDC_FUSED_CLUSTER");
         const int force = env ? atoi(env) : 0;
         if (force != 0 && force != 1 && force != 2 && force != 4 && force != 8) return SSDC_ERR_INVALID;
-        const int n = ssdc::fused_launch(p, w, stream, force);
+        // SSDC_FUSED_PLANE_MAPS=0 makes the kernel fetch each plane with its own copies (the
+        // path taken when the two planes of a tensor cannot share one tensor map)
+        const char* pm = getenv("SSDC_FUSED_PLANE_MAPS");
+        const bool plane_maps = !(pm && pm[0] == '0' && pm[1] == 0);
+        const int n = ssdc::fused_launch(p, w, stream, force, plane_maps);
         if (n < 0) return n;
         launches += n;
         record_event(launches, stream);

@@ -40,8 +40,9 @@ bool tc_supported(int N, int D, int Q);
 
 // Fused single-pass TF32 kernel (state passed through distributed shared
 // memory inside thread-block clusters). force_cluster = 0 picks the cluster
-// size; 1, 2, 4 or 8 forces it.
+// size; 1, 2, 4 or 8 forces it. plane_maps = false fetches every plane with
+// its own tensor map even where one map could fetch both.
 bool fused_supported(int N, int D, int Q);
-int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster);
+int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster, bool plane_maps);
 
 }  // namespace ssdc

@@ -121,3 +121,31 @@ def test_fused_single_launch_and_small_workspace():
     inp = inputs.custom(1, 256, 2, 64, 64, seed=8)
     _, _, f = run_library(inp, 64, "tf32")
     assert ssdc.last_launch_count() == 1
+
+
+def _planes_in_order(t, name, imag_first):
+    """Both planes of one tensor in one allocation, in the given address order."""
+    import torch
+    re, im = t[name + "_re"], t[name + "_im"]
+    buf = torch.empty((2,) + tuple(re.shape), dtype=re.dtype, device=re.device)
+    first, second = (im, re) if imag_first else (re, im)
+    buf[0].copy_(first)
+    buf[1].copy_(second)
+    t[name + "_re"], t[name + "_im"] = (buf[1], buf[0]) if imag_first else (buf[0], buf[1])
+
+
+@pytest.mark.parametrize("plane_maps", ["1", "0"])
+@pytest.mark.parametrize("order", ["re_first", "im_first", "mixed"])
+def test_fused_tensor_map_paths(order, plane_maps, monkeypatch):
+    # T a multiple of 8 (the interleaved C map applies) with a partial last chunk; each
+    # tensor's planes either in one map (in either address order) or in one map per plane
+    monkeypatch.setenv("SSDC_FUSED_CLUSTER", "2")
+    monkeypatch.setenv("SSDC_FUSED_PLANE_MAPS", plane_maps)
+    inp = inputs.custom(2, 64 * 5 + 24, 3, 64, 64, seed=3100)
+    y_ref, s_ref = naive_scan_inputs(inp)
+    t = to_device(inp)
+    flips = {"re_first": (False, False, False), "im_first": (True, True, True), "mixed": (True, False, True)}[order]
+    for name, flip in zip(["x", "B", "C"], flips):
+        _planes_in_order(t, name, flip)
+    y, s, _ = run_library(inp, 64, "tf32", dev=t)
+    assert_close(y, s, y_ref, s_ref, "tf32", f"planes {order}, plane maps {plane_maps}")
