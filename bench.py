@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -42,7 +43,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--precision", choices=["auto", "tf32", "fp32"], default="auto")
-    ap.add_argument("--workload", choices=["layer"], default="layer")
+    ap.add_argument("--workload", choices=["layer", "train28", "qsweep", "long"], default="layer",
+                    help="layer: the headline single-layer workload; the others are measurement modes "
+                         "with device-generated inputs (no CPU baseline, no end-to-end figure)")
+    ap.add_argument("--chunk", type=int, default=0, help="chunk size Q (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -213,8 +217,103 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+def other_workload(args, w):
+    """Measurement mode for the training-batch, chunk-sweep and long-memory workloads: inputs
+    drawn on the device from the same distributions (torch generator seeded per layer), one
+    step = every layer of the workload back to back, L2 flushed before each step."""
+    import torch
+    from state_space_sequence_complex_gb300 import build, ssdc
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build.build()
+    ssdc.load()
+    Q = args.chunk or w.Q
+    g = torch.Generator(device=dev)
+
+    def layer_inputs(layer):
+        g.manual_seed(w.seed + layer)
+        Bn, T, H, D, N = w.B, w.T, w.H, w.D, w.N
+        s = math.sqrt(0.5)
+        A_re = torch.empty(H, device=dev).uniform_(w.re_lo, w.re_hi, generator=g)
+        sign = torch.where(torch.rand(H, device=dev, generator=g) < 0.5, -1.0, 1.0)
+        A_im = torch.empty(H, device=dev).uniform_(0.35, 2.20, generator=g) * sign
+        dt = torch.randn(Bn, T, H, device=dev, generator=g) * w.dt_std + w.dt_mean
+        cp = lambda F: [torch.randn(Bn, T, H, F, device=dev, generator=g) * s for _ in range(2)]
+        (x_re, x_im), (B_re, B_im), (C_re, C_im) = cp(D), cp(N), cp(N)
+        return [x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt]
+
+    layers = [layer_inputs(i) for i in range(w.layers)]
+    precision = args.precision
+    if precision == "auto":
+        precision = "tf32" if ssdc.ssd_complex_fwd_supported(ssdc.dims(w.B, w.T, w.H, w.N, w.D, "tf32"), Q) == 0 else "fp32"
+    f = ssdc.Forward(w.B, w.T, w.H, w.N, w.D, Q, precision, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(max(args.warmup, 3)):
+        flush.fill_(float(i))
+        for L in layers:
+            f(*L)
+    torch.cuda.synchronize()
+    ssdc.timing_enable(True)
+    per_kernel, ev = [], []
+    sampler = ClockSampler(dev.index)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.1)
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for L in layers:
+            f(*L)
+            per_kernel.append(ssdc.timing_read())
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ssdc.timing_enable(False)
+    st = f.status()
+    if st != ssdc.SSDC_OK:
+        raise SystemExit(f"device status after timed steps: {ssdc.strerror(st)}")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    nk = min(len(p) for p in per_kernel)
+    kmeans = [sum(p[i] for p in per_kernel) / len(per_kernel) for i in range(nk)]
+    names = {1: ["fused_kernel"], 3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
+        nk, [f"launch{i}" for i in range(nk)])
+    top = int(np.argmax(kmeans))
+    peak, peak_kind = peaks()
+    wq = w.with_(Q=Q)
+    bytes_per_launch = algorithmic_bytes_per_unit(wq) * w.token_heads
+    launch_ms = sum(kmeans)
+    units = w.token_heads * w.layers
+    line = {
+        "metric": METRIC, "value": units / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32",
+        "data": "synthetic, drawn on the device per layer",
+        "config": {"workload": f"{w.name} Q{Q}", "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
+                   "chunk_size": Q, "layers": w.layers, "precision": precision,
+                   "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)"},
+        "roofline": {"bound": "hbm", "kernel": names[top], "achieved": bytes_per_launch / (launch_ms / 1000.0) / 1e9,
+                     "peak": peak, "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
+                     "frac": bytes_per_launch / (launch_ms / 1000.0) / 1e9 / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_per_launch,
+                     "kernel_ms": {n: m for n, m in zip(names, kmeans)}},
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": nk * w.layers * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload != "layer":
+        if args.impl == "reference" or args.gpus != 1:
+            raise SystemExit("the measurement workloads run on one GPU with --impl ours")
+        other_workload(args, inputs.ALL[args.workload])
+        return
     w = inputs.LAYER
     if args.impl == "reference":
         reference_arm(args, w)

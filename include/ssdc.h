@@ -94,7 +94,7 @@ typedef struct {
  * Supported sizes.
  *   SSDC_PREC_FP32: chunk_size in {16, 32, 64, 128, 256};
  *                   N and D multiples of 8 in [8, 64].
- *   SSDC_PREC_TF32, SSDC_PREC_TF32_STAGED: chunk_size in {64, 128, 256};
+ *   SSDC_PREC_TF32, SSDC_PREC_TF32_STAGED: chunk_size in {32, 64, 128, 256};
  *                   N = D = 64.
  * T need not be a multiple of chunk_size: the last chunk is partial.
  */

@@ -18,7 +18,8 @@
 //
 // Kernels (128 threads = 4 warps; thread t owns TMEM lane t):
 //   tc_chunk_state  grid (nc, H, B): S_loc^T and a_c of one chunk
-//   tc_chunk_scan   grid (nc * Q/64, H, B): 64 output rows of one chunk
+//   tc_chunk_scan   grid (nc * ceil(Q/64), H, B): 64 output rows of one chunk (Q = 32: the
+//                   first 32 rows of a 64-row tile)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -106,7 +107,9 @@ tc_chunk_state(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
 
     const int n = tid >> 1, part = tid & 1;
     uint32_t ph_in = 0, ph_mma = 0;
-    const int nblocks = Q / kRows;
+    // 64-row blocks of the chunk; with Q = 32 the block's last 32 rows belong to the next chunk
+    // and get a zero window (they add nothing to S_loc)
+    const int nblocks = (Q + kRows - 1) / kRows;
     for (int sb = 0; sb < nblocks; ++sb) {
         if (!ptx::mbar_wait(&sm.bar_in, ph_in, kWaitIters)) fail(ws.status);
         ph_in ^= 1;
@@ -115,7 +118,8 @@ tc_chunk_state(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
 #pragma unroll
         for (int s = 0; s < 64; ++s) {
             const float2 bv = make_float2(plane_ld(sm.b[0], s, n), plane_ld(sm.b[1], s, n));
-            const float2 a = cmul(sm.dec[sb * kRows + s], bv);
+            const int sg = sb * kRows + s;
+            const float2 a = sg < Q ? cmul(sm.dec[sg], bv) : make_float2(0.0f, 0.0f);
             w1[s] = part ? a.y : a.x;
             w2[s] = part ? a.x : -a.y;
         }
@@ -176,7 +180,9 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
     ScanSmem& sm = *reinterpret_cast<ScanSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int Q = p.Q, H = p.H;
-    const int lblocks = Q / kRows;
+    // 64-row output blocks; with Q = 32 the block's last 32 rows (the next chunk's) are computed
+    // from clamped decays and never stored
+    const int lblocks = (Q + kRows - 1) / kRows;
     const int c = blockIdx.x / lblocks, lb = blockIdx.x % lblocks;
     const int h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -227,7 +233,7 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
     __syncthreads();
 
     const int l = tid >> 1, part = tid & 1;
-    const Acs acs_l = sm.acs[l0 + l];
+    const Acs acs_l = sm.acs[l0 + l < Q ? l0 + l : Q - 1];
     const uint32_t sb_re = ptx::smem_addr(sm.b[0]), sb_im = ptx::smem_addr(sm.b[1]);
     const uint32_t sx_re = ptx::smem_addr(sm.x[0]), sx_im = ptx::smem_addr(sm.x[1]);
     uint32_t ph_bx = 0, ph_mma = 0;
@@ -274,7 +280,7 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
             const int s = 2 * j + part;
             float2 v = make_float2(0.0f, 0.0f);
             if (s0 + s <= l0 + l) {
-                const float2 L = cexp_fast(acs_diff(acs_l, sm.acs[s0 + s]));
+                const float2 L = cexp_fast(acs_diff(acs_l, sm.acs[s0 + s < Q ? s0 + s : Q - 1]));
                 v = cmul(make_float2(gre, gim), L);
             }
             pr[j] = v.x;
@@ -451,7 +457,7 @@ int set_attrs() {
 }  // namespace
 }  // namespace tc
 
-bool tc_supported(int N, int D, int Q) { return N == 64 && D == 64 && (Q == 64 || Q == 128 || Q == 256); }
+bool tc_supported(int N, int D, int Q) { return N == 64 && D == 64 && (Q == 32 || Q == 64 || Q == 128 || Q == 256); }
 
 int tc_launch_chunk_state(const Problem& p, const Workspace& ws, cudaStream_t stream) {
     int rc = tc::set_attrs();
@@ -470,7 +476,7 @@ int tc_launch_chunk_scan(const Problem& p, const Workspace& ws, cudaStream_t str
     tc::TcMaps maps;
     rc = tc::make_maps(p, ws.S, &maps);
     if (rc != SSDC_OK) return rc;
-    const dim3 grid((unsigned)(p.nc * (p.Q / tc::kRows)), (unsigned)p.H, (unsigned)p.B);
+    const dim3 grid((unsigned)(p.nc * ((p.Q + tc::kRows - 1) / tc::kRows)), (unsigned)p.H, (unsigned)p.B);
     tc::tc_chunk_scan<<<grid, tc::kThreads, tc::kScanSmem, stream>>>(p, ws, maps);
     return 1;
 }

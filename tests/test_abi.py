@@ -55,7 +55,9 @@ def test_supported_sets(lib):
     assert ok(ssdc.dims(1, 128, 2, 64, 64, 7), 64) == ssdc.SSDC_ERR_INVALID
     assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 0) == ssdc.SSDC_ERR_INVALID
     assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 64) == 0
-    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 32) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 32) == 0
+    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 32) == 0
+    assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 16) == ssdc.SSDC_ERR_UNSUPPORTED
 
 
 def test_workspace_bytes(lib):

@@ -95,7 +95,8 @@ def test_launch_count_and_reuse():
     assert_close(y, s, *ref, "fp32")
 
 
-@pytest.mark.parametrize("T,Q", [(64, 64), (1000, 64), (300, 128), (511, 256), (100, 64)])
+@pytest.mark.parametrize("T,Q", [(64, 64), (1000, 64), (300, 128), (511, 256), (100, 64), (257, 32), (32, 32),
+                                 (31, 32), (1000, 32)])
 def test_staged_tf32_path(T, Q):
     inp = inputs.custom(2, T, 3, 64, 64, seed=2000 + T + Q)
     check(inp, Q, "tf32_staged", f"staged T={T} Q={Q}")
