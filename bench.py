@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 
 from state_space_sequence_complex_gb300 import inputs  # noqa: E402
 
-METRIC = "complex-SSD fwd token·heads/s at Q=64"
+METRIC = "complex-SSD fwd token·heads/s at Q=64 and % of roofline (HBM or TF32)"  # the value is token·heads/s; the fraction is roofline.frac
 UNIT = "token·heads/s"
 FLUSH_BYTES = 512 << 20
 
