@@ -31,17 +31,19 @@
 //     Im = (A_r B_i)[lane p=0] + (A_i B_r)[lane p=1].
 // The 16x256b TMEM access shape hands each thread lanes m and m + 8 of the
 // same columns, so every thread combines its own values: no exchange between
-// lanes. The C tile is loaded in that layout by TMA (8-row boxes); x^T is
-// written in it by a shared-memory transpose. The output accumulator takes
-// both P x (Y_diag) and (C o exp(Acs)) S_in (Y_off): the two A operands, P
-// and C', are rows written to TMEM.
+// lanes. The C tile is loaded in that layout by TMA (one 5-D copy per 32-column
+// half, or 8-row boxes); x^T is written in it by a shared-memory transpose. The
+// output accumulator takes both P x (Y_diag) and (C o exp(Acs)) S_in (Y_off):
+// the two A operands, P and C', are rows written to TMEM.
 //
-// Threads. 16 warps; warps w and w + 4k share TMEM lane quadrant w % 4 and
-// split a row's 64 columns in quarters (k = w / 4). Worker thread 0 issues
-// the MMAs; y goes from registers to global memory, four lanes per 32-byte
-// run of a row. Warp 15 also issues the TMA loads of the next chunk's C, B,
-// x tiles into the other stage of a two-stage ring and computes its
-// cumulative log-decay.
+// Threads. 16 worker warps: warp w owns TMEM lane quadrant w % 4, its 16-lane
+// block (w / 4) % 2 (8 complex rows) and the 32-column half w / 8, which is a
+// contiguous 2 KB of every interleaved tile. They write the transposes, the C'
+// and P rows and the state hop, and store y from registers to global memory,
+// four lanes per 32-byte run of a row (the previous chunk's y, early in the
+// next chunk). Warp 16 issues every MMA, in chunk order, on mbarrier hand-offs
+// from the workers; warp 17 issues the TMA loads of the next chunk into the
+// other stage of a two-stage ring and computes its cumulative log-decay.
 #include <cstring>
 
 #include <cuda.h>
