@@ -182,6 +182,39 @@ int ssd_complex_fwd_noalloc(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
                             const float *dt, ssdc_dims dims, int chunk_size,
                             ssdc_cout y, ssdc_cout final_state, cudaStream_t stream);
 
+/*
+ * Forward pass on HOST buffers: the library copies the inputs to the device,
+ * runs the forward pass of ssd_complex_fwd_ws and copies y and the final
+ * state back. There is no counterpart on the pages; it is the path for callers
+ * whose data live in host memory.
+ *
+ * The problem is cut into pieces (batch rows, and head groups when the batch
+ * is small; every (b, h) sequence is independent) that go through internal
+ * streams copy-in -> compute -> copy-out with two pieces in flight, so that
+ * the host-device copies and the compute overlap. Host buffers should be
+ * pinned (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous
+ * and overlap; pageable buffers give the same results, slower.
+ *
+ *   x, A, B_t, C_t, dt, y, final_state   host pointers, layout as for
+ *                                        ssd_complex_fwd_ws
+ *   dev_scratch    device memory, 256-byte aligned, at least
+ *                  ssd_complex_fwd_host_scratch_bytes(dims, chunk_size) bytes;
+ *                  it holds the device copies of two pieces and their
+ *                  workspaces (no initialisation needed)
+ *   stream         the work starts after the caller's earlier work on
+ *                  `stream`, and `stream` continues after the last copy-out
+ *
+ * The call returns when y and the final state are in the host buffers, with
+ * SSDC_OK, a host-side argument error (before anything is enqueued), or the
+ * first device status that is not SSDC_OK. Calls on one device are
+ * serialised by the library; calls sharing one dev_scratch must not overlap.
+ */
+size_t ssd_complex_fwd_host_scratch_bytes(ssdc_dims dims, int chunk_size);
+int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
+                         const float *dt, ssdc_dims dims, int chunk_size,
+                         ssdc_cout y, ssdc_cout final_state, void *dev_scratch,
+                         size_t scratch_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

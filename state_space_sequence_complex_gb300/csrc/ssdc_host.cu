@@ -284,3 +284,7 @@ int ssd_complex_timing_read(float* ms, int n) {
 }
 
 }  // extern "C"
+
+namespace ssdc {
+void set_last_launch_count(int n) { g_last_launches = n; }
+}  // namespace ssdc

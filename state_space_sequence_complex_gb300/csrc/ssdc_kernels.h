@@ -45,4 +45,7 @@ bool tc_supported(int N, int D, int Q);
 bool fused_supported(int N, int D, int Q);
 int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster, bool plane_maps);
 
+// Launch count reported by ssd_complex_last_launch_count() for the calling thread.
+void set_last_launch_count(int n);
+
 }  // namespace ssdc

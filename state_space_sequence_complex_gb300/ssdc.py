@@ -29,7 +29,7 @@ PREC = {"tf32": 0, "fp32": 1, "tf32_staged": 2}
 EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_complex_fwd_ws",
            "ssd_complex_fwd", "ssd_complex_status", "ssd_complex_strerror",
            "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read",
-           "ssd_complex_fwd_noalloc")
+           "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host")
 
 
 class ssdc_dims(ctypes.Structure):
@@ -80,6 +80,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_last_launch_count.restype = ctypes.c_int
     lib.ssd_complex_fwd_noalloc.argtypes = common + [vp]
     lib.ssd_complex_fwd_noalloc.restype = ctypes.c_int
+    lib.ssd_complex_fwd_host_scratch_bytes.argtypes = [ssdc_dims, ctypes.c_int]
+    lib.ssd_complex_fwd_host_scratch_bytes.restype = sz
+    lib.ssd_complex_fwd_host.argtypes = common + [vp, sz, vp]
+    lib.ssd_complex_fwd_host.restype = ctypes.c_int
     lib.ssd_complex_timing_enable.argtypes = [ctypes.c_int]
     lib.ssd_complex_timing_enable.restype = ctypes.c_int
     lib.ssd_complex_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int]
@@ -159,6 +163,32 @@ def ssd_complex_fwd_noalloc(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, 
     return rc
 
 
+def ssd_complex_fwd_host_scratch_bytes(d: ssdc_dims, chunk_size: int) -> int:
+    return int(load().ssd_complex_fwd_host_scratch_bytes(d, int(chunk_size)))
+
+
+def ssd_complex_fwd_host(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
+                         precision="tf32", y_re, y_im, fs_re, fs_im, scratch, stream=None,
+                         check=True) -> int:
+    """Call ``ssd_complex_fwd_host``: inputs and outputs are contiguous float32
+    CPU tensors (pinned for overlapped copies), ``scratch`` a uint8 CUDA tensor
+    of at least ``ssd_complex_fwd_host_scratch_bytes`` bytes. Returns when the
+    outputs are in the host tensors, with the status."""
+    import torch
+
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    d = dims(Bn, T, H, N, D, precision)
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_fwd_host(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt), d,
+        int(chunk_size), _cout(y_re, y_im), _cout(fs_re, fs_im), _ptr(scratch),
+        int(scratch.numel()), ctypes.c_void_p(s.cuda_stream))
+    if check and rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_fwd_host")
+    return rc
+
+
 def ssd_complex_status(workspace, stream=None) -> int:
     import torch
 
@@ -226,3 +256,37 @@ def ssd_complex_fwd(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_si
     N = B_re.shape[-1]
     f = Forward(Bn, T, H, N, D, chunk_size, precision, device=x_re.device)
     return f(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt)
+
+
+class HostForward:
+    """The host-buffer form of ``Forward``: holds pinned host outputs and the
+    device scratch of one problem size. ``__call__`` takes the planar inputs as
+    contiguous float32 CPU tensors (pinned for overlapped copies) and returns
+    ``(y_re, y_im, final_state_re, final_state_im)`` as CPU tensors, filled
+    when the call returns."""
+
+    def __init__(self, Bn, T, H, N, D, chunk_size, precision="tf32", device="cuda"):
+        import torch
+
+        self.shape = (Bn, T, H, N, D)
+        self.chunk_size = int(chunk_size)
+        self.precision = precision
+        d = dims(Bn, T, H, N, D, precision)
+        rc = ssd_complex_fwd_supported(d, chunk_size)
+        if rc != SSDC_OK:
+            raise SSDCError(rc, "ssd_complex_fwd_supported")
+        pin = torch.cuda.is_available()
+        f32 = dict(dtype=torch.float32, pin_memory=pin)
+        self.y_re = torch.empty((Bn, T, H, D), **f32)
+        self.y_im = torch.empty((Bn, T, H, D), **f32)
+        self.fs_re = torch.empty((Bn, H, N, D), **f32)
+        self.fs_im = torch.empty((Bn, H, N, D), **f32)
+        nbytes = ssd_complex_fwd_host_scratch_bytes(d, chunk_size)
+        self.scratch = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, stream=None):
+        ssd_complex_fwd_host(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, self.chunk_size,
+                             precision=self.precision, y_re=self.y_re, y_im=self.y_im,
+                             fs_re=self.fs_re, fs_im=self.fs_im, scratch=self.scratch,
+                             stream=stream)
+        return self.y_re, self.y_im, self.fs_re, self.fs_im

@@ -148,3 +148,48 @@ def test_rejects_unsupported_before_launch(lib):
 
 def test_status_null_workspace(lib):
     assert lib.ssd_complex_status(None, None) == ssdc.SSDC_ERR_INVALID
+
+
+def test_host_scratch_bytes(lib):
+    hb = ssdc.ssd_complex_fwd_host_scratch_bytes
+    per_token_head = (2 * 64 + 4 * 64 + 1 + 2 * 64) * 4  # x, B, C, dt in; y out
+    for prec in ("tf32", "fp32"):
+        # 134 MB of inputs and outputs: 2 pieces of one batch row, one device slot each
+        # (plus, per slot, the final state and the staged chunk states on the fp32 path)
+        nb = hb(ssdc.dims(2, 2048, 16, 64, 64, prec), 64)
+        assert 2 * 2048 * 16 * per_token_head <= nb < 2 * 2048 * 16 * per_token_head + (40 << 20)
+    # 4.3 GB: 8 pieces of 8 batch rows, two of them on the device at a time
+    big = hb(ssdc.dims(64, 2048, 16, 64, 64, "tf32"), 64)
+    assert 2 * 8 * 2048 * 16 * per_token_head <= big < 3 * 8 * 2048 * 16 * per_token_head
+    assert hb(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 48) == 0
+    assert hb(ssdc.dims(0, 2048, 16, 64, 64, "tf32"), 64) == 0
+
+
+def _call_host(lib, ptrs, d, Q=64, scratch=None, nbytes=1 << 30):
+    cin = lambda a, b: ssdc.ssdc_cin(a, b)
+    cout = lambda a, b: ssdc.ssdc_cout(a, b)
+    p = ptrs
+    return lib.ssd_complex_fwd_host(cin(p[0], p[1]), cin(p[2], p[3]), cin(p[4], p[5]), cin(p[6], p[7]),
+                                    p[8], d, Q, cout(p[9], p[10]), cout(p[11], p[12]),
+                                    scratch, nbytes, None)
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    """Host-side checks of the host-buffer entry point: null pointers, overlapping
+    outputs, unsupported sizes and a bad scratch buffer, all before any copy."""
+    d = ssdc.dims(1, 128, 2, 64, 64, "fp32")
+    ptrs, end = fake_ptrs(d)
+    scratch = 1 << 44
+    for i in range(13):
+        bad = list(ptrs)
+        bad[i] = None
+        assert _call_host(lib, bad, d, scratch=scratch) == ssdc.SSDC_ERR_INVALID
+    for o, i in ((9, 0), (10, 8), (11, 12), (12, 9)):
+        bad = list(ptrs)
+        bad[o] = ptrs[i]
+        assert _call_host(lib, bad, d, scratch=scratch) == ssdc.SSDC_ERR_INVALID
+    assert _call_host(lib, ptrs, d, Q=48, scratch=scratch) == ssdc.SSDC_ERR_UNSUPPORTED
+    need = ssdc.ssd_complex_fwd_host_scratch_bytes(d, 64)
+    assert _call_host(lib, ptrs, d, scratch=None) == ssdc.SSDC_ERR_WORKSPACE
+    assert _call_host(lib, ptrs, d, scratch=scratch + 16) == ssdc.SSDC_ERR_WORKSPACE
+    assert _call_host(lib, ptrs, d, scratch=scratch, nbytes=need - 1) == ssdc.SSDC_ERR_WORKSPACE
