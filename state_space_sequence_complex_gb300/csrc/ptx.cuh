@@ -368,6 +368,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// The same with any layout: 0 = none, 2 = 128-byte, 4 = 64-byte, 6 = 32-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)(layout & 7u) << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::tf32, fp32 accumulate, A and B TF32.
 //   [4,6) D format 1 = F32; [7,10) A format 2 = TF32; [10,13) B format 2;
 //   [15] A major (0 = K); [16] B major (0 = K, 1 = MN);

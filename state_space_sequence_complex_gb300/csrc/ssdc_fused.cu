@@ -78,7 +78,7 @@ struct Smem {
     float c[2][64 * 128];    // [stage] C, interleaved 128 rows (A operand)
     float b[2][64 * 128];    // [stage] B, stacked (rows s); after C B^T, (dec o B)^T stacked (rows n)
     float x[2][64 * 128];    // [stage] x, stacked (rows s); x^T interleaved (rows d); then y staging
-    float sin[64 * 128];     // incoming state S_in^T, interleaved (rows d, n contiguous)
+    float sin[64 * 128];     // incoming state S_in^T, interleaved rows d, K = n, state layout (st_off)
     float2 acs[2][kQ];       // in-chunk cumulative log-decay, per stage
     float2 dec[kQ];          // exp(Acs[Q-1] - Acs[s])
     float2 eacs[kQ];         // exp(Acs[l])
@@ -145,6 +145,17 @@ __device__ __forceinline__ uint32_t pair_off(int khalf, int m, int n) {
     return inter_row(khalf, m) + chunk16(n >> 2, m) + (uint32_t)((n & 3) << 2);
 }
 
+// The state tiles (S_in^T and the outgoing state, rows d interleaved, K = n) use
+// a 32-byte swizzle instead: 8-row groups of 2 KB holding the eight 32-byte
+// K-blocks one after another, so that the per-thread pair accesses of the
+// 16x256b fragments hit 16 distinct 8-byte bank positions per half-warp (with
+// the 128-byte swizzle two rows of a half-warp share each position), and the
+// rows of one TMEM lane quadrant are one contiguous 8 KB.
+__device__ __forceinline__ uint32_t st_off(int m, int n) {
+    return (uint32_t)((m >> 3) * 2048 + (n >> 3) * 256 + (m & 7) * 32 + ((((n >> 2) ^ (m >> 2)) & 1) << 4) + ((n & 3) << 2));
+}
+__device__ __forceinline__ uint64_t desc_state(uint32_t base) { return ptx::smem_desc(base, 16u, 2048u, 6u); }
+
 // K-major SW128 descriptor of a 128-row operand; K-step k (8 fp32) adds
 // (k / 4) halves and (k % 4) 32-byte steps to the start address.
 __device__ __forceinline__ uint64_t desc128(uint32_t base) { return ptx::smem_desc_sw128(base, 16u, 1024u); }
@@ -161,6 +172,11 @@ __device__ __forceinline__ void issue_ts128(uint32_t d, uint32_t a_tmem, uint64_
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         ptx::mma_tf32_ts(d, a_tmem + 8 * k, desc_k(db, k), kIdesc128, (accumulate || k > 0) ? 1u : 0u);
+}
+// The same with the B operand in the state layout: K-step k is the next 256-byte block.
+__device__ __forceinline__ void issue_ts128_state(uint32_t d, uint32_t a_tmem, uint64_t db) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ptx::mma_tf32_ts(d, a_tmem + 8 * k, db + (uint64_t)(16 * k), kIdesc128, 1u);
 }
 
 // Tensor maps of one launch. The fast maps fetch both planes of a tensor in
@@ -365,7 +381,7 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     ++n_recv;
                 }
                 ptx::tc_fence_after();
-                issue_ts128(tmem + kAccY, tmem + kCwin, desc128(sin_saddr), true);  // + C' S_in
+                issue_ts128_state(tmem + kAccY, tmem + kCwin, desc_state(sin_saddr));  // + C' S_in
             }
             ptx::mma_commit(&sm.mma[2]);
             prev_in = has_in;
@@ -379,7 +395,7 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         // rr = 16 qd + 8 blk + i4: lane i4 holds plane 0, lane i4 + 8 plane 1) and the 32-column
         // half kh (column pair n = 32 kh + 8 j + 2 lq + {0, 1}, j = 0 .. 3). In an interleaved
         // tile these are 16 whole 128-byte rows; the four warps of a quadrant hold rows
-        // [32 qd, 32 qd + 32) of both halves, the quadrant's 2 x 4 KB of the state.
+        // [32 qd, 32 qd + 32) of both halves; in the state layout, the quadrant's contiguous 8 KB.
         const int qd = warp & 3, blk = (warp >> 2) & 1, kh = warp >> 3;
         const int i4 = lane >> 2, lq = lane & 3;
         const int rr = 16 * qd + 8 * blk + i4;
@@ -400,12 +416,14 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             if (!ptx::mbar_wait(&sm.mma[g], (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
             ptx::tc_fence_after();
         };
-        // this thread's state values S^T[rr, n] in an interleaved tile, index 2 j + e
+        // this thread's state values S^T[rr, n] in a state tile, index 2 j + e (column pair
+        // n = 32 kh + 8 j + 2 lq: K-block 4 kh + j, 256 bytes apart)
         auto for_pairs = [&](char* base, float* vr, float* vi, bool store) {
+            const uint32_t soff_re = st_off(mre, 32 * kh + 2 * lq), soff_im = st_off(mim, 32 * kh + 2 * lq);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float2* pr = reinterpret_cast<float2*>(base + pair_off(kh, mre, 8 * j + 2 * lq));
-                float2* pi = reinterpret_cast<float2*>(base + pair_off(kh, mim, 8 * j + 2 * lq));
+                float2* pr = reinterpret_cast<float2*>(base + soff_re + 256 * j);
+                float2* pi = reinterpret_cast<float2*>(base + soff_im + 256 * j);
                 if (store) {
                     *pr = make_float2(vr[2 * j], vr[2 * j + 1]);
                     *pi = make_float2(vi[2 * j], vi[2 * j + 1]);
@@ -477,17 +495,22 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 sm.step[t] = cexp_fast(cdiff(sm.acs[s][t], sm.acs[s][t - 1]));
             }
             if (it > 0) finish(it - 1, prev, prev_keep);
-            const int blo = lane & 7, bmid = (lane >> 3) & 3;
-            const int xsb = bmid + 4 * (warp & 3), xdb = blo + 8 * ((warp >> 2) & 1), xp = (warp >> 3) & 1;
+            // Lane bits L0..L4. 128-bit accesses are served eight lanes at a time, so within
+            // each group of eight (L0..L2) the 16-byte chunk positions of both the block loads
+            // (rows s, swizzle by s) and the transposed stores (rows d, swizzle by d) are distinct.
+            const int L0 = lane & 1, L1 = (lane >> 1) & 1, L2 = (lane >> 2) & 1, L3 = (lane >> 3) & 1, L4 = lane >> 4;
+            const int xdb = L0 + 2 * L1 + 4 * L4 + 8 * ((warp >> 2) & 1);
+            const int xsb = L2 + 2 * (L1 ^ L3) + 4 * (warp & 3), xp = (warp >> 3) & 1;
             float4 xv[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {  // x block: rows s = 4 xsb + i, columns d = 4 xdb ..
                 const int sr = 4 * xsb + i;
                 xv[i] = *reinterpret_cast<const float4*>(xbase + stk_row(xdb >> 3, xp ^ swx, sr) + chunk16(xdb & 7, sr));
             }
-            // (dec o B)^T: rows s = 4 bsb + i, columns n = 4 bnb + 2 bjh + {0, 1}, both planes
-            const int bjh = (lane >> 3) & 1;
-            const int bsb = ((lane >> 4) & 1) + 2 * (warp >> 1), bnb = blo + 8 * (warp & 1);
+            // (dec o B)^T: rows s = 4 bsb + i, columns n = 4 bnb + 2 bjh + {0, 1}, both planes; the
+            // 64-bit loads (16 lanes at a time) and the 128-bit stores (8 at a time) are conflict-free
+            const int bjh = L1;
+            const int bsb = L2 + 2 * (warp >> 1), bnb = L0 + 2 * L3 + 4 * L4 + 8 * (warp & 1);
             float2 bv[2][4];
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp)
@@ -646,18 +669,15 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 }
             } else if (CL > 1) {
                 // stage S_out in the C buffer (C was consumed by C B^T and the C' rows), then the
-                // quadrant's leader copies its 2 x 4 KB of rows to the next CTA
+                // quadrant's leader copies its 8 KB of rows to the next CTA
                 for_pairs(cbase, outr, outi, true);
                 ptx::fence_proxy_async_smem();
                 ptx::named_sync(1 + qd, 128);
                 if (leader && cur.c != p.drop_send_chunk) {
                     if (n_send > 0 && !ptx::mbar_wait(&sm.succ_empty, (n_send - 1) & 1, kWaitIters)) fail(ws.status);
                     ++n_send;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const uint32_t off = (uint32_t)half * kIntHalf + (uint32_t)(32 * qd) * 128u;
-                        ptx::bulk_copy_to_cluster(remote_sin + off, cs + off, kQuarterBytes / 2, remote_sin_full);
-                    }
+                    const uint32_t off = (uint32_t)qd * kQuarterBytes;
+                    ptx::bulk_copy_to_cluster(remote_sin + off, cs + off, kQuarterBytes, remote_sin_full);
                     ptx::bulk_commit();
                 }
             }
