@@ -47,6 +47,9 @@ def parse():
                     help="layer: the headline single-layer workload; the others are measurement modes "
                          "with device-generated inputs (no CPU baseline, no end-to-end figure)")
     ap.add_argument("--chunk", type=int, default=0, help="chunk size Q (default: the workload's)")
+    ap.add_argument("--segments", type=int, default=1,
+                    help="measurement mode: process T in this many segments, each started from the "
+                         "previous segment's final state (the initial-state entry point)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -220,7 +223,9 @@ def reference_arm(args, w):
 def other_workload(args, w):
     """Measurement mode for the training-batch, chunk-sweep and long-memory workloads: inputs
     drawn on the device from the same distributions (torch generator seeded per layer), one
-    step = every layer of the workload back to back, L2 flushed before each step."""
+    step = every layer of the workload back to back, L2 flushed before each step. With
+    --segments K each layer's sequence is processed as K consecutive segments, every segment
+    started from the previous one's final state (updated in place)."""
     import torch
     from state_space_sequence_complex_gb300 import build, ssdc
     torch.cuda.set_device(0)
@@ -242,20 +247,36 @@ def other_workload(args, w):
         (x_re, x_im), (B_re, B_im), (C_re, C_im) = cp(D), cp(N), cp(N)
         return [x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt]
 
-    layers = [layer_inputs(i) for i in range(w.layers)]
+    K = max(1, args.segments)
+    if w.T % K != 0:
+        raise SystemExit(f"--segments {K} does not divide T={w.T}")
+    Ts = w.T // K
+
+    def split(L):  # contiguous per-segment copies of the (B, T, ...) inputs; A is per head
+        return [[t if t.dim() == 1 else t[:, k * Ts:(k + 1) * Ts].contiguous() for t in L] for k in range(K)]
+
+    layers = [split(layer_inputs(i)) for i in range(w.layers)]
     precision = args.precision
     if precision == "auto":
-        precision = "tf32" if ssdc.ssd_complex_fwd_supported(ssdc.dims(w.B, w.T, w.H, w.N, w.D, "tf32"), Q) == 0 else "fp32"
-    f = ssdc.Forward(w.B, w.T, w.H, w.N, w.D, Q, precision, device=dev)
+        precision = "tf32" if ssdc.ssd_complex_fwd_supported(ssdc.dims(w.B, Ts, w.H, w.N, w.D, "tf32"), Q) == 0 else "fp32"
+    f = ssdc.Forward(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev)
+
+    def run_layer(L, timed=False):
+        for k, seg in enumerate(L):
+            if k == 0:
+                f(*seg)
+            else:
+                f(*seg, s0_re=f.fs_re, s0_im=f.fs_im)
+            if timed:
+                per_kernel.append(ssdc.timing_read())
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    per_kernel, ev = [], []
     for i in range(max(args.warmup, 3)):
         flush.fill_(float(i))
         for L in layers:
-            f(*L)
+            run_layer(L)
     torch.cuda.synchronize()
-    ssdc.timing_enable(True)
-    per_kernel, ev = [], []
     sampler = ClockSampler(dev.index)
     torch.cuda.synchronize()
     sampler.start()
@@ -265,25 +286,33 @@ def other_workload(args, w):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for L in layers:
-            f(*L)
-            per_kernel.append(ssdc.timing_read())
+            run_layer(L)
         e1.record(stream)
         ev.append((e0, e1))
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ssdc.timing_enable(False)
     st = f.status()
     if st != ssdc.SSDC_OK:
         raise SystemExit(f"device status after timed steps: {ssdc.strerror(st)}")
     ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    # per-launch device times from the library's own events, in a separate pass (reading
+    # them waits for each call, which would stall the timed steps)
+    ssdc.timing_enable(True)
+    for k in range(min(args.steps, 50)):
+        flush.fill_(float(k))
+        for L in layers:
+            run_layer(L, timed=True)
+    ssdc.timing_enable(False)
     nk = min(len(p) for p in per_kernel)
     kmeans = [sum(p[i] for p in per_kernel) / len(per_kernel) for i in range(nk)]
     names = {1: ["fused_kernel"], 3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
         nk, [f"launch{i}" for i in range(nk)])
     top = int(np.argmax(kmeans))
     peak, peak_kind = peaks()
-    wq = w.with_(Q=Q)
-    bytes_per_launch = algorithmic_bytes_per_unit(wq) * w.token_heads
+    wq = w.with_(Q=Q, T=Ts)
+    # per launch; a segment after the first also reads its initial state (8 N D bytes per sequence)
+    bytes_per_launch = (algorithmic_bytes_per_unit(wq) * wq.token_heads
+                        + 8.0 * w.N * w.D * w.B * w.H * (K - 1) / K)
     launch_ms = sum(kmeans)
     units = w.token_heads * w.layers
     line = {
@@ -291,8 +320,9 @@ def other_workload(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32",
         "data": "synthetic, drawn on the device per layer",
-        "config": {"workload": f"{w.name} Q{Q}", "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
-                   "chunk_size": Q, "layers": w.layers, "precision": precision,
+        "config": {"workload": f"{w.name} Q{Q}" + (f" in {K} segments of T={Ts}, state carried" if K > 1 else ""),
+                   "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
+                   "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)"},
         "roofline": {"bound": "hbm", "kernel": names[top], "achieved": bytes_per_launch / (launch_ms / 1000.0) / 1e9,
                      "peak": peak, "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
@@ -301,7 +331,7 @@ def other_workload(args, w):
                      "kernel_ms": {n: m for n, m in zip(names, kmeans)}},
         "cpu_baseline": None,
         "e2e": None,
-        "gpu_launches": nk * w.layers * args.steps,
+        "gpu_launches": nk * w.layers * K * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -309,7 +339,7 @@ def other_workload(args, w):
 
 def main():
     args = parse()
-    if args.workload != "layer":
+    if args.workload != "layer" or args.segments > 1:
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
         other_workload(args, inputs.ALL[args.workload])
@@ -355,10 +385,7 @@ def main():
     if st != ssdc.SSDC_OK:
         raise SystemExit(f"device status after warm-up: {ssdc.strerror(st)}")
 
-    # ---- timed region: device-resident inputs ----
-    ssdc.timing_enable(True)
-    names = None
-    per_kernel = []
+    # ---- timed region: device-resident inputs, one library call per step ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
@@ -373,18 +400,25 @@ def main():
         ev[k][0].record(stream)
         call()
         ev[k][1].record(stream)
-        per_kernel.append(ssdc.timing_read())
         launches_per_step = ssdc.last_launch_count()
     torch.cuda.synchronize()
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    ssdc.timing_enable(False)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = sum(step_ms) / len(step_ms)
     st = f.status()
     if st != ssdc.SSDC_OK:
         raise SystemExit(f"device status after timed steps: {ssdc.strerror(st)}")
+    # per-launch device times from the library's own events (the roofline's kernel time), in
+    # a separate pass: reading them waits for each call, which would stall the timed steps
+    ssdc.timing_enable(True)
+    per_kernel = []
+    for k in range(min(args.steps, 200)):
+        flush.fill_(float(k))
+        call()
+        per_kernel.append(ssdc.timing_read())
+    ssdc.timing_enable(False)
 
     # ---- end to end through the C ABI with host buffers (ssd_complex_fwd_host): every
     # step copies its inputs from pinned host memory, runs the scan and copies y and the

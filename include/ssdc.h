@@ -123,6 +123,27 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
                        size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Forward pass from a given initial state: s_{-1} = initial_state instead of
+ * zero. The pages' scan starts from a zero state; this form continues a
+ * sequence from the state an earlier call returned, so that a long sequence
+ * can be processed in segments: the segment [T1, T) started from the final
+ * state of [0, T1) gives the y rows and the final state of the whole scan, up
+ * to rounding.
+ *
+ *   initial_state  (B,H,N,D) complex, planar device arrays, 16-byte aligned.
+ *                  Both planes null means a zero initial state (the call is
+ *                  then ssd_complex_fwd_ws). It may be the final_state buffer
+ *                  itself (an in-place update, plane for plane); otherwise it
+ *                  must not overlap an output or the workspace.
+ * The other arguments, the workspace, the errors and the precisions are those
+ * of ssd_complex_fwd_ws; one null plane is SSDC_ERR_INVALID.
+ */
+int ssd_complex_fwd_init(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
+                         const float *dt, ssdc_cin initial_state, ssdc_dims dims,
+                         int chunk_size, ssdc_cout y, ssdc_cout final_state,
+                         void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Forward pass that allocates its workspace on `stream` (cudaMallocAsync /
  * cudaFreeAsync, stream-ordered). A device-side error cannot be queried after
  * it returns; use the _ws form with ssd_complex_status() to read one.

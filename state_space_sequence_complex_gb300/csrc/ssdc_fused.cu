@@ -353,7 +353,8 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         uint32_t n_recv = 0;
         for (int it = 0; it < nitems && lane == 0; ++it) {
             const int s = it & 1;
-            const bool has_in = cur.c > 0;
+            const bool self_fill = cur.c == 0 && p.s0_re != nullptr;  // S_in[0] is the initial state
+            const bool has_in = cur.c > 0 || self_fill;
             const uint32_t cs = ptx::smem_addr(sm.c[s]), bs = ptx::smem_addr(sm.b[s]), xs = ptx::smem_addr(sm.x[s]);
             wait(&sm.full[s], (uint32_t)((it >> 1) & 1));
             ptx::tc_fence_after();
@@ -364,7 +365,9 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 wait(&sm.mma[2], (uint32_t)((it - 1) & 1));
                 if (prev_in && CL > 1 && ok) {
                     for (int k = 0; k < 4; ++k) ptx::mbar_arrive_expect_tx(&sm.sin_full[k], kQuarterBytes);
-                    ptx::mbar_arrive_remote(pred_empty);
+                    // the buffer is free for the predecessor's next state, unless this chunk fills
+                    // it with an initial state first (then the signal follows that chunk)
+                    if (!self_fill) ptx::mbar_arrive_remote(pred_empty);
                 }
             }
             wait(&sm.xt_ready, (uint32_t)(it & 1));
@@ -411,6 +414,10 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         uint32_t n_recv = 0, n_send = 0;
         const uint32_t remote_sin = ptx::mapa(ptx::smem_addr(sm.sin), succ);
         const uint32_t remote_sin_full = ptx::mapa(ptx::smem_addr(&sm.sin_full[qd]), succ);
+        const uint32_t self_sin = ptx::mapa(ptx::smem_addr(sm.sin), rank);
+        const uint32_t self_sin_full = ptx::mapa(ptx::smem_addr(&sm.sin_full[qd]), rank);
+        // the successor fills its buffer with an initial state before its first state from here
+        const bool succ_self_fills = p.s0_re != nullptr && succ == 0;
 
         auto wait_mma = [&](int g, int it) {
             if (!ptx::mbar_wait(&sm.mma[g], (uint32_t)(it & 1), kWaitIters)) fail(ws.status);
@@ -475,7 +482,8 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         bool prev_keep = false;
         for (int it = 0; it < nitems; ++it) {
             const int s = it & 1;
-            const bool has_in = cur.c > 0, last = cur.c == (int)p.nc - 1;
+            const bool self_fill = cur.c == 0 && p.s0_re != nullptr;
+            const bool has_in = cur.c > 0 || self_fill, last = cur.c == (int)p.nc - 1;
             char* xbase = reinterpret_cast<char*>(sm.x[s]);
             char* bbase = reinterpret_cast<char*>(sm.b[s]);
             char* cbase = reinterpret_cast<char*>(sm.c[s]);
@@ -560,6 +568,30 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     w[4 * j + 3] = cr.y * e.y + ci.y * e.x;
                 }
                 ptx::tmem_st_16x256b_x4(tl + kCwin + 32 * kh, w);
+            }
+            if (self_fill) {
+                // S_in[0] = the given initial state (N, D) of this sequence, into the incoming
+                // state tile: directly with CL = 1; otherwise staged in the C buffer (C' has been
+                // read) and copied by the quadrant's leader like a state from a predecessor, so
+                // that its arrival is counted on the same barrier
+                float vr[8], vi[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int n = 32 * kh + 8 * (k >> 1) + 2 * lq + (k & 1);
+                    const int64_t o = ((int64_t)cur.q * 64 + n) * 64 + rr;
+                    vr[k] = p.s0_re[o];
+                    vi[k] = p.s0_im[o];
+                }
+                for_pairs(CL > 1 ? cbase : reinterpret_cast<char*>(sm.sin), vr, vi, true);
+                ptx::fence_proxy_async_smem();
+                if (CL > 1) {
+                    ptx::named_sync(1 + qd, 128);
+                    if (leader) {
+                        const uint32_t off = (uint32_t)qd * kQuarterBytes;
+                        ptx::bulk_copy_to_cluster(self_sin + off, cs + off, kQuarterBytes, self_sin_full);
+                        ptx::bulk_commit();
+                    }
+                }
             }
             wait_mma(0, it);  // C B^T has read B
 
@@ -674,7 +706,10 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 ptx::fence_proxy_async_smem();
                 ptx::named_sync(1 + qd, 128);
                 if (leader && cur.c != p.drop_send_chunk) {
-                    if (n_send > 0 && !ptx::mbar_wait(&sm.succ_empty, (n_send - 1) & 1, kWaitIters)) fail(ws.status);
+                    // send k waits for the successor's k-th buffer release (its (k-1)-th when the
+                    // buffer starts out free)
+                    const int sig = succ_self_fills ? (int)n_send : (int)n_send - 1;
+                    if (sig >= 0 && !ptx::mbar_wait(&sm.succ_empty, (uint32_t)sig & 1, kWaitIters)) fail(ws.status);
                     ++n_send;
                     const uint32_t off = (uint32_t)qd * kQuarterBytes;
                     ptx::bulk_copy_to_cluster(remote_sin + off, cs + off, kQuarterBytes, remote_sin_full);

@@ -115,6 +115,12 @@ int setup_device_attrs() {
     return SSDC_OK;
 }
 
+// The forward pass behind ssd_complex_fwd_ws and ssd_complex_fwd_init: s0 = the
+// initial state's planes, or both null for a zero initial state.
+int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt, ssdc_cin s0, ssdc_dims dims,
+             int chunk_size, ssdc_cout y, ssdc_cout final_state, void* workspace, size_t ws_bytes,
+             cudaStream_t stream);
+
 }  // namespace
 
 extern "C" {
@@ -129,6 +135,24 @@ size_t ssd_complex_fwd_workspace_bytes(ssdc_dims dims, int chunk_size) {
 int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt,
                        ssdc_dims dims, int chunk_size, ssdc_cout y, ssdc_cout final_state,
                        void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    return fwd_impl(x, A, B_t, C_t, dt, ssdc_cin{nullptr, nullptr}, dims, chunk_size, y, final_state, workspace,
+                    ws_bytes, stream);
+}
+
+int ssd_complex_fwd_init(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt,
+                         ssdc_cin initial_state, ssdc_dims dims, int chunk_size, ssdc_cout y,
+                         ssdc_cout final_state, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    return fwd_impl(x, A, B_t, C_t, dt, initial_state, dims, chunk_size, y, final_state, workspace, ws_bytes,
+                    stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt, ssdc_cin s0, ssdc_dims dims,
+             int chunk_size, ssdc_cout y, ssdc_cout final_state, void* workspace, size_t ws_bytes,
+             cudaStream_t stream) {
     int rc = check_sizes(dims, chunk_size);
     if (rc != SSDC_OK) return rc;
     const void* ptrs[] = {x.re, x.im, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt,
@@ -137,6 +161,9 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const
         if (q == nullptr) return SSDC_ERR_INVALID;
     for (const void* q : ptrs)
         if (!aligned16(q)) return SSDC_ERR_ALIGN;
+    const bool has_s0 = s0.re != nullptr;
+    if ((s0.re == nullptr) != (s0.im == nullptr) || (has_s0 && s0.re == s0.im)) return SSDC_ERR_INVALID;
+    if (has_s0 && (!aligned16(s0.re) || !aligned16(s0.im))) return SSDC_ERR_ALIGN;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return SSDC_ERR_WORKSPACE;
     if (ws_bytes < ws_bytes_for(dims, chunk_size)) return SSDC_ERR_WORKSPACE;
@@ -161,6 +188,17 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const
     for (int i = 0; i < 4; ++i)
         for (int j = i + 1; j < 4; ++j)
             if (overlaps(out[i], out[j])) return SSDC_ERR_INVALID;
+    if (has_s0) {
+        // the initial state may be the final-state buffer itself (updated in place), plane for
+        // plane; it must not otherwise overlap an output or the workspace
+        const bool in_place = s0.re == final_state.re && s0.im == final_state.im;
+        const Range st[] = {rng(s0.re, fsn), rng(s0.im, fsn)};
+        if (overlaps(st[0], st[1])) return SSDC_ERR_INVALID;
+        for (const Range& r : st) {
+            if (overlaps(r, out[0]) || overlaps(r, out[1]) || overlaps(r, in[9])) return SSDC_ERR_INVALID;
+            if (!in_place && (overlaps(r, out[2]) || overlaps(r, out[3]))) return SSDC_ERR_INVALID;
+        }
+    }
 
     rc = setup_device_attrs();
     if (rc != SSDC_OK) return rc;
@@ -168,6 +206,7 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const
     ssdc::Problem p;
     p.x_re = x.re; p.x_im = x.im; p.A_re = A.re; p.A_im = A.im;
     p.B_re = B_t.re; p.B_im = B_t.im; p.C_re = C_t.re; p.C_im = C_t.im; p.dt = dt;
+    p.s0_re = s0.re; p.s0_im = s0.im;
     p.y_re = y.re; p.y_im = y.im; p.fs_re = final_state.re; p.fs_im = final_state.im;
     p.T = dims.T; p.B = (int)dims.B; p.H = (int)dims.H; p.N = (int)dims.N; p.D = (int)dims.D;
     p.Q = chunk_size;
@@ -222,6 +261,10 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const
     if (g_timing) g_timed_launches = launches;
     return SSDC_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int ssd_complex_fwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt,
                     ssdc_dims dims, int chunk_size, ssdc_cout y, ssdc_cout final_state,

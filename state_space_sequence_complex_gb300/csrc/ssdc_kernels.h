@@ -12,6 +12,7 @@ namespace ssdc {
 // Sizes and device pointers of one forward call (planar complex planes).
 struct Problem {
     const float *x_re, *x_im, *A_re, *A_im, *B_re, *B_im, *C_re, *C_im, *dt;
+    const float *s0_re, *s0_im;  // initial state (B, H, N, D), or null: zero
     float *y_re, *y_im, *fs_re, *fs_im;
     int64_t T;
     int B, H, N, D, Q;

@@ -1,7 +1,8 @@
 // Inter-chunk state pass (landing page, "03 Chunkwise SSD", STATE line: the
 // chunk states are carried across chunks by the chunk decays).
 //
-//   S_in[0] = 0,  S_in[c+1] = a_c * S_in[c] + S_loc[c],  a_c = exp(Acs_c[Q-1])
+//   S_in[0] = 0 (or the given initial state),
+//   S_in[c+1] = a_c * S_in[c] + S_loc[c],  a_c = exp(Acs_c[Q-1])
 //   final_state = a_last * S_in[last] + S_loc[last]
 //
 // This is the sequential form of the pages' "decay_chunk matrix" recurrence.
@@ -26,7 +27,13 @@ ssdc_state_pass(Problem p, Workspace ws) {
     const int64_t nc = p.nc;
     float* S = ws.S + bh * nc * 2 * ND + j;
     const float* a = ws.a + bh * nc * 2;
+    const int d = j / p.N, n = j % p.N;
+    const int64_t o = (bh * p.N + n) * p.D + d;  // (b, h, n, d) of the initial and final states
     float sr = 0.0f, si = 0.0f;
+    if (p.s0_re != nullptr) {
+        sr = p.s0_re[o];
+        si = p.s0_im[o];
+    }
     for (int64_t c0 = 0; c0 < nc; c0 += kPassAhead) {
         float lr[kPassAhead], li[kPassAhead], ar[kPassAhead], ai[kPassAhead];
 #pragma unroll
@@ -52,8 +59,6 @@ ssdc_state_pass(Problem p, Workspace ws) {
             }
         }
     }
-    const int d = j / p.N, n = j % p.N;
-    const int64_t o = (bh * p.N + n) * p.D + d;
     p.fs_re[o] = sr;
     p.fs_im[o] = si;
 }

@@ -29,7 +29,8 @@ PREC = {"tf32": 0, "fp32": 1, "tf32_staged": 2}
 EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_complex_fwd_ws",
            "ssd_complex_fwd", "ssd_complex_status", "ssd_complex_strerror",
            "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read",
-           "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host")
+           "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host",
+           "ssd_complex_fwd_init")
 
 
 class ssdc_dims(ctypes.Structure):
@@ -70,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     common = [ssdc_cin, ssdc_cin, ssdc_cin, ssdc_cin, vp, ssdc_dims, ctypes.c_int, ssdc_cout, ssdc_cout]
     lib.ssd_complex_fwd_ws.argtypes = common + [vp, sz, vp]
     lib.ssd_complex_fwd_ws.restype = ctypes.c_int
+    lib.ssd_complex_fwd_init.argtypes = common[:5] + [ssdc_cin] + common[5:] + [vp, sz, vp]
+    lib.ssd_complex_fwd_init.restype = ctypes.c_int
     lib.ssd_complex_fwd.argtypes = common + [vp]
     lib.ssd_complex_fwd.restype = ctypes.c_int
     lib.ssd_complex_status.argtypes = [vp, vp]
@@ -141,6 +144,28 @@ def ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk
         int(workspace.numel()), ctypes.c_void_p(s.cuda_stream))
     if check and rc != SSDC_OK:
         raise SSDCError(rc, "ssd_complex_fwd_ws")
+    return rc
+
+
+def ssd_complex_fwd_init(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, s0_re, s0_im, chunk_size, *,
+                         precision="tf32", y_re, y_im, fs_re, fs_im, workspace, stream=None,
+                         check=True) -> int:
+    """Call ``ssd_complex_fwd_init`` on torch CUDA tensors: the forward pass from
+    the initial state (s0_re, s0_im) of shape (B,H,N,D) (None, None: zero). The
+    initial state may be the (fs_re, fs_im) tensors themselves. Returns the status."""
+    import torch
+
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    d = dims(Bn, T, H, N, D, precision)
+    s = torch.cuda.current_stream() if stream is None else stream
+    s0 = ssdc_cin(None if s0_re is None else s0_re.data_ptr(), None if s0_im is None else s0_im.data_ptr())
+    rc = load().ssd_complex_fwd_init(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt), s0, d,
+        int(chunk_size), _cout(y_re, y_im), _cout(fs_re, fs_im), _ptr(workspace),
+        int(workspace.numel()), ctypes.c_void_p(s.cuda_stream))
+    if check and rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_fwd_init")
     return rc
 
 
@@ -239,11 +264,20 @@ class Forward:
         self.fs_im = torch.empty((Bn, H, N, D), **f32)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
 
-    def __call__(self, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, stream=None):
-        ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, self.chunk_size,
-                           precision=self.precision, y_re=self.y_re, y_im=self.y_im,
-                           fs_re=self.fs_re, fs_im=self.fs_im, workspace=self.workspace,
-                           stream=stream)
+    def __call__(self, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, stream=None,
+                 s0_re=None, s0_im=None):
+        """``s0_re, s0_im``: an optional initial state (B,H,N,D); passing this
+        object's own ``fs_re, fs_im`` continues the previous call in place."""
+        if s0_re is None and s0_im is None:
+            ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, self.chunk_size,
+                               precision=self.precision, y_re=self.y_re, y_im=self.y_im,
+                               fs_re=self.fs_re, fs_im=self.fs_im, workspace=self.workspace,
+                               stream=stream)
+        else:
+            ssd_complex_fwd_init(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, s0_re, s0_im,
+                                 self.chunk_size, precision=self.precision, y_re=self.y_re,
+                                 y_im=self.y_im, fs_re=self.fs_re, fs_im=self.fs_im,
+                                 workspace=self.workspace, stream=stream)
         return self.y_re, self.y_im, self.fs_re, self.fs_im
 
     def status(self, stream=None) -> int:

@@ -193,3 +193,33 @@ def test_host_entry_rejects_bad_arguments(lib):
     assert _call_host(lib, ptrs, d, scratch=None) == ssdc.SSDC_ERR_WORKSPACE
     assert _call_host(lib, ptrs, d, scratch=scratch + 16) == ssdc.SSDC_ERR_WORKSPACE
     assert _call_host(lib, ptrs, d, scratch=scratch, nbytes=need - 1) == ssdc.SSDC_ERR_WORKSPACE
+
+
+def _call_init(lib, ptrs, s0, d, Q=64, ws=None, ws_bytes=1 << 30):
+    cin = lambda a, b: ssdc.ssdc_cin(a, b)
+    cout = lambda a, b: ssdc.ssdc_cout(a, b)
+    p = ptrs
+    return lib.ssd_complex_fwd_init(cin(p[0], p[1]), cin(p[2], p[3]), cin(p[4], p[5]), cin(p[6], p[7]),
+                                    p[8], cin(s0[0], s0[1]), d, Q, cout(p[9], p[10]), cout(p[11], p[12]),
+                                    ws, ws_bytes, None)
+
+
+def test_init_entry_rejects_bad_initial_state(lib):
+    d = ssdc.dims(1, 128, 2, 64, 64, "fp32")
+    ptrs, end = fake_ptrs(d)
+    ws = end
+    s0 = (end + (4 << 20), end + (8 << 20))  # after the workspace, apart from everything
+    need = ssdc.ssd_complex_fwd_workspace_bytes(d, 64)
+    call = lambda s: _call_init(lib, ptrs, s, d, ws=ws, ws_bytes=need)
+    assert call((s0[0], None)) == ssdc.SSDC_ERR_INVALID          # one plane missing
+    assert call((None, s0[1])) == ssdc.SSDC_ERR_INVALID
+    assert call((s0[0], s0[0])) == ssdc.SSDC_ERR_INVALID         # one buffer for both planes
+    assert call((s0[0] + 4, s0[1])) == ssdc.SSDC_ERR_ALIGN
+    assert call((ptrs[9], s0[1])) == ssdc.SSDC_ERR_INVALID       # on top of y.re
+    assert call((ws, s0[1])) == ssdc.SSDC_ERR_INVALID            # inside the workspace
+    assert call((ptrs[11] + 16, s0[1])) == ssdc.SSDC_ERR_INVALID  # part of the final state
+    assert call((ptrs[12], ptrs[11])) == ssdc.SSDC_ERR_INVALID   # the final state's planes swapped
+    # the final-state buffer itself (in place) and a separate buffer pass the argument checks;
+    # without a GPU the call then fails on the device
+    for ok in ((ptrs[11], ptrs[12]), s0, (None, None)):
+        assert call(ok) not in (ssdc.SSDC_ERR_INVALID, ssdc.SSDC_ERR_ALIGN, ssdc.SSDC_ERR_WORKSPACE)
