@@ -89,6 +89,28 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def fp32_flops_per_unit(w) -> dict:
+    """Algorithmic real flops per token-head of each launch of the exact fp32 path (causal
+    triangle only): chunk state S_loc = B^T (dec o x): 8 N D; state pass: 8 N D / Q; chunk
+    scan: C B^T and P x over the causal triangle, 4 (Q+1) (N + D), and (C o e^Acs) S_in, 8 N D."""
+    N, D, Q = w.N, w.D, w.Q
+    return {"chunk_state": 8.0 * N * D, "state_pass": 8.0 * N * D / Q,
+            "chunk_scan": 4.0 * (Q + 1) * (N + D) + 8.0 * N * D}
+
+
+def fp32_alu_peak_tflops(dev_index: int):
+    """FP32 FMA peak of the CUDA cores: SMs x 128 FP32 lanes x 2 flops x the maximum SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except Exception:
+        pass
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x {mhz:.0f} MHz"
+
+
 def profiled_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary of `kernel`, or
     None if the kernel source changed since that capture."""
@@ -464,6 +486,23 @@ def main():
     achieved = bytes_per_launch / (kmeans[top] / 1000.0) / 1e9
     step_achieved = bytes_per_launch / (ms / 1000.0) / 1e9 / 1.0
 
+    roofline = {"bound": "hbm", "kernel": names[top], "achieved": achieved, "peak": peak,
+                "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(names[top]),
+                "algorithmic_bytes_per_launch": bytes_per_launch,
+                "kernel_ms": {n: m for n, m in zip(names, kmeans)},
+                "step_frac": step_achieved / peak}
+    if precision == "fp32" and names[top] in ("chunk_state", "state_pass", "chunk_scan"):
+        # the exact path computes on the CUDA cores: its dominant launch against the FP32 FMA peak
+        fl = fp32_flops_per_unit(w)[names[top]] * w.token_heads
+        alu_peak, alu_kind = fp32_alu_peak_tflops(dev.index)
+        tf = fl / (kmeans[top] / 1000.0) / 1e12
+        roofline = {"bound": "alu", "kernel": names[top], "achieved": tf, "peak": alu_peak,
+                    "peak_kind": alu_kind, "unit": "TFLOP/s", "frac": tf / alu_peak, "traffic": None,
+                    "algorithmic_flops_per_launch": fl,
+                    "kernel_ms": {n: m for n, m in zip(names, kmeans)},
+                    "hbm_step_frac": step_achieved / peak}
+
     if rank != 0:
         return
     cpu = None
@@ -477,12 +516,7 @@ def main():
                    "chunk_size": w.Q, "seed": w.seed, "precision": precision,
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
                    "parallelism": f"weak: {world} independent batch(es), no collective"},
-        "roofline": {"bound": "hbm", "kernel": names[top], "achieved": achieved, "peak": peak,
-                     "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(names[top]),
-                     "algorithmic_bytes_per_launch": bytes_per_launch,
-                     "kernel_ms": {n: m for n, m in zip(names, kmeans)},
-                     "step_frac": step_achieved / peak},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},

@@ -153,14 +153,16 @@ def test_status_null_workspace(lib):
 def test_host_scratch_bytes(lib):
     hb = ssdc.ssd_complex_fwd_host_scratch_bytes
     per_token_head = (2 * 64 + 4 * 64 + 1 + 2 * 64) * 4  # x, B, C, dt in; y out
+    whole = 2 * 2048 * 16 * per_token_head
     for prec in ("tf32", "fp32"):
-        # 134 MB of inputs and outputs: 2 pieces of one batch row, one device slot each
-        # (plus, per slot, the final state and the staged chunk states on the fp32 path)
+        # 134 MB of inputs and outputs, 2 batch rows: 4 segments of 512 tokens of both rows,
+        # two on the device at a time (plus, per slot, the final state and, on the fp32
+        # path, the staged chunk states)
         nb = hb(ssdc.dims(2, 2048, 16, 64, 64, prec), 64)
-        assert 2 * 2048 * 16 * per_token_head <= nb < 2 * 2048 * 16 * per_token_head + (40 << 20)
-    # 4.3 GB: 8 pieces of 8 batch rows, two of them on the device at a time
+        assert 2 * 2 * 512 * 16 * per_token_head <= nb < whole
+    # 4.3 GB: 16 groups of 4 batch rows, two on the device at a time
     big = hb(ssdc.dims(64, 2048, 16, 64, 64, "tf32"), 64)
-    assert 2 * 8 * 2048 * 16 * per_token_head <= big < 3 * 8 * 2048 * 16 * per_token_head
+    assert 2 * 4 * 2048 * 16 * per_token_head <= big < 3 * 4 * 2048 * 16 * per_token_head
     assert hb(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 48) == 0
     assert hb(ssdc.dims(0, 2048, 16, 64, 64, "tf32"), 64) == 0
 

@@ -1,10 +1,11 @@
 """The host-buffer entry point (ssd_complex_fwd_host): inputs and outputs in
 host memory, the library copying pieces of the problem in and out around the
 scan. Checked against the oracle on small cases that exercise each way of
-cutting the problem (head groups for a small batch, batch rows for a large
-one, more pieces than device slots, a partial last piece), with pinned and
-with pageable host buffers, and against the device entry point at the
-single-layer size."""
+cutting the problem (segments of the sequence carried by the initial-state
+path for a small batch, groups of batch rows for a large one, a partial last
+segment or group), with pinned and with pageable host buffers, and against the
+device entry point at the single-layer size and with more pieces than device
+slots."""
 import numpy as np
 import pytest
 import torch
@@ -42,9 +43,10 @@ def run_host(inp, Q, precision, pinned=True):
     return y, s
 
 
-# (B, T, H, D, N, Q, precision). Problems this small go in 2 pieces: along the
-# batch when B >= 2 (B = 5 and 9 give a smaller last piece), else along the
-# heads (H = 2: 2 pieces of 1 head; H = 3 has no divisor to split by: 1 piece).
+# (B, T, H, D, N, Q, precision). A batch of fewer than 4 rows goes as up to 4
+# segments of the sequence (a multiple of Q tokens each, the last partial), each
+# started from the previous one's final state; 4 rows or more go as up to 4 row
+# groups (B = 5 and 9 give a smaller last group).
 CASES = [
     (1, 200, 2, 16, 16, 32, "fp32"),
     (1, 100, 3, 8, 8, 16, "fp32"),
@@ -66,7 +68,8 @@ def test_host_entry_matches_oracle(case):
     y, s = run_host(inp, Q, precision)
     assert_close(y, s, y_ref, s_ref, precision, "host buffers")
     if precision == "fp32":
-        # each (b, h) sequence runs the same exact-fp32 kernels whatever piece it is in
+        # each (b, h) sequence runs the same exact-fp32 arithmetic whatever piece it is in:
+        # segments start at chunk boundaries and carry the state the whole scan would
         yd, sd, _ = run_library(inp, Q, precision)
         assert np.array_equal(y, yd) and np.array_equal(s, sd)
 
@@ -81,17 +84,17 @@ def test_host_entry_pageable_buffers():
 def test_host_entry_single_layer_matches_device_entry():
     inp = inputs.generate(inputs.LAYER)
     y, s = run_host(inp, 64, "tf32")
-    assert ssdc.last_launch_count() == 2  # 2 pieces of one batch row, one fused launch each
+    assert ssdc.last_launch_count() == 4  # 4 segments of 512 tokens, one fused launch each
     yd, sd, _ = run_library(inp, 64, "tf32")
     assert rel_fro(y, yd) <= 1e-6 and rel_fro(s, sd) <= 1e-6
 
 
 @pytest.mark.parametrize("precision", ["fp32", "tf32"])
 def test_host_entry_more_pieces_than_slots(precision):
-    # 538 MB of inputs and outputs: 4 pieces of 2 batch rows through the 2 device slots
+    # 538 MB of inputs and outputs: 8 pieces of 1 batch row through the 2 device slots
     inp = inputs.custom(8, 2048, 16, 64, 64, seed=351)
     y, s = run_host(inp, 64, precision)
-    assert ssdc.last_launch_count() == 4 * (1 if precision == "tf32" else 3)
+    assert ssdc.last_launch_count() == 8 * (1 if precision == "tf32" else 3)
     yd, sd, _ = run_library(inp, 64, precision)
     if precision == "fp32":
         assert np.array_equal(y, yd) and np.array_equal(s, sd)
