@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--segments", type=int, default=1,
                     help="measurement mode: process T in this many segments, each started from the "
                          "previous segment's final state (the initial-state entry point)")
+    ap.add_argument("--real-x", action="store_true",
+                    help="measurement mode: x real (x.im = NULL, only x.re is read), as in the model")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -278,6 +280,10 @@ def other_workload(args, w):
         return [[t if t.dim() == 1 else t[:, k * Ts:(k + 1) * Ts].contiguous() for t in L] for k in range(K)]
 
     layers = [split(layer_inputs(i)) for i in range(w.layers)]
+    if args.real_x:  # no imaginary plane for x
+        for L in layers:
+            for seg in L:
+                seg[1] = None
     precision = args.precision
     if precision == "auto":
         precision = "tf32" if ssdc.ssd_complex_fwd_supported(ssdc.dims(w.B, Ts, w.H, w.N, w.D, "tf32"), Q) == 0 else "fp32"
@@ -333,7 +339,7 @@ def other_workload(args, w):
     peak, peak_kind = peaks()
     wq = w.with_(Q=Q, T=Ts)
     # per launch; a segment after the first also reads its initial state (8 N D bytes per sequence)
-    bytes_per_launch = (algorithmic_bytes_per_unit(wq) * wq.token_heads
+    bytes_per_launch = ((algorithmic_bytes_per_unit(wq) - (4.0 * w.D if args.real_x else 0.0)) * wq.token_heads
                         + 8.0 * w.N * w.D * w.B * w.H * (K - 1) / K)
     launch_ms = sum(kmeans)
     units = w.token_heads * w.layers
@@ -342,7 +348,8 @@ def other_workload(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32",
         "data": "synthetic, drawn on the device per layer",
-        "config": {"workload": f"{w.name} Q{Q}" + (f" in {K} segments of T={Ts}, state carried" if K > 1 else ""),
+        "config": {"workload": f"{w.name} Q{Q}" + (f" in {K} segments of T={Ts}, state carried" if K > 1 else "")
+                   + (", real x" if args.real_x else ""), "real_x": bool(args.real_x),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
                    "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)"},
@@ -361,7 +368,7 @@ def other_workload(args, w):
 
 def main():
     args = parse()
-    if args.workload != "layer" or args.segments > 1:
+    if args.workload != "layer" or args.segments > 1 or args.real_x:
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
         other_workload(args, inputs.ALL[args.workload])

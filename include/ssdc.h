@@ -29,6 +29,11 @@
  * All pointers are device pointers, 16-byte aligned. Outputs must not
  * overlap inputs or each other.
  *
+ * Real x. x.im may be NULL: x is then real (its imaginary plane is zero and
+ * is not read), as in the model, where x is a real H*D slice of the input
+ * projection. Every path and entry point accepts it; y and the state stay
+ * complex. Any other NULL pointer is SSDC_ERR_INVALID.
+ *
  * Ownership. The caller owns every buffer; the library keeps no pointer after
  * a call returns. Work is enqueued on `stream` and runs asynchronously: inputs
  * must stay unchanged, and outputs unread, until the stream reaches that point.

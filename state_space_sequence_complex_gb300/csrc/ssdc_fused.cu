@@ -192,6 +192,7 @@ struct FusedMaps {
     CUtensorMap C2;                      // (F, H, T % 8, plane, (B T) / 8), boxes (32, 1, 8, 2, 8)
     int fast;                            // bit 0: x2, bit 1: B2, bit 2: C2 in use
     int swap;                            // bit k: the fast map's plane 0 is the imaginary plane (0 x, 1 B, 2 C)
+    int real_x;                          // x has no imaginary plane (x_re only)
 };
 
 // Issuer warp: TMA of one chunk's C (re/im interleaved), B and x (stacked)
@@ -200,13 +201,14 @@ struct FusedMaps {
 __device__ __forceinline__ void load_tiles(Smem& sm, int st, const FusedMaps& fm, int h, int t0, int b, int64_t T,
                                            int lane) {
     uint64_t* bar = &sm.full[st];
-    if (lane == 0) ptx::mbar_expect_tx(bar, kStageTx);
+    // real x: only its real plane is loaded (the workers take the imaginary one as zero)
+    if (lane == 0) ptx::mbar_expect_tx(bar, fm.real_x ? kStageTx - kPlaneBytes : kStageTx);
     __syncwarp();
     char* cb = reinterpret_cast<char*>(sm.c[st]);
     char* bb = reinterpret_cast<char*>(sm.b[st]);
     char* xb = reinterpret_cast<char*>(sm.x[st]);
     const bool fx = fm.fast & 1, fb = (fm.fast >> 1) & 1, fc = (fm.fast >> 2) & 1;
-    const int nc = fc ? 2 : 32, nb = fb ? 2 : 4, nx = fx ? 2 : 4;
+    const int nc = fc ? 2 : 32, nb = fb ? 2 : 4, nx = fx ? 2 : fm.real_x ? 2 : 4;
     for (int op = lane; op < nc + nb + nx; op += 32) {
         if (op < nc) {
             if (fc) {
@@ -223,7 +225,9 @@ __device__ __forceinline__ void load_tiles(Smem& sm, int st, const FusedMaps& fm
             if (isb ? fb : fx) {
                 ptx::tma_load_5d(dst + stk_row(k, 0, 0), isb ? &fm.B2 : &fm.x2, bar, 32 * k, h, t0, 0, b);
             } else {
-                const int half = k >> 1, pl = k & 1;
+                // per-plane copies: k = 2 half + plane (for real x, k = half and the real plane only)
+                const bool ronly = !isb && fm.real_x;
+                const int half = ronly ? k : k >> 1, pl = ronly ? 0 : k & 1;
                 const CUtensorMap* m = isb ? (pl ? &fm.B_im : &fm.B_re) : (pl ? &fm.x_im : &fm.x_re);
                 ptx::tma_load_4d(dst + stk_row(half, pl, 0), m, bar, 32 * half, h, t0, b);
             }
@@ -510,10 +514,13 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             const int xdb = L0 + 2 * L1 + 4 * L4 + 8 * ((warp >> 2) & 1);
             const int xsb = L2 + 2 * (L1 ^ L3) + 4 * (warp & 3), xp = (warp >> 3) & 1;
             float4 xv[4];
+            const bool zero_plane = xp == 1 && fm.real_x;  // the imaginary plane of a real x
 #pragma unroll
             for (int i = 0; i < 4; ++i) {  // x block: rows s = 4 xsb + i, columns d = 4 xdb ..
                 const int sr = 4 * xsb + i;
-                xv[i] = *reinterpret_cast<const float4*>(xbase + stk_row(xdb >> 3, xp ^ swx, sr) + chunk16(xdb & 7, sr));
+                xv[i] = zero_plane ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                                   : *reinterpret_cast<const float4*>(xbase + stk_row(xdb >> 3, xp ^ swx, sr) +
+                                                                      chunk16(xdb & 7, sr));
             }
             // (dec o B)^T: rows s = 4 bsb + i, columns n = 4 bnb + 2 bjh + {0, 1}, both planes; the
             // 64-bit loads (16 lanes at a time) and the 128-bit stores (8 at a time) are conflict-free
@@ -774,14 +781,15 @@ bool make_interleaved_map(CUtensorMap* m, const Problem& p, bool* swap) {
 
 int make_fused_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
     memset(fm, 0, sizeof(*fm));
+    fm->real_x = p.x_im == nullptr;
     bool sw = false;
-    if (allow_fast && make_pair_map(&fm->x2, p.x_re, p.x_im, p, &sw)) fm->fast |= 1, fm->swap |= sw ? 1 : 0;
+    if (allow_fast && !fm->real_x && make_pair_map(&fm->x2, p.x_re, p.x_im, p, &sw)) fm->fast |= 1, fm->swap |= sw ? 1 : 0;
     if (allow_fast && make_pair_map(&fm->B2, p.B_re, p.B_im, p, &sw)) fm->fast |= 2, fm->swap |= sw ? 2 : 0;
     if (allow_fast && make_interleaved_map(&fm->C2, p, &sw)) fm->fast |= 4, fm->swap |= sw ? 4 : 0;
     bool ok = true;
     if (!(fm->fast & 1))
         ok = ok && tc::encode_feature_map(&fm->x_re, p.x_re, 64, p.H, p.T, p.B, 64) &&
-             tc::encode_feature_map(&fm->x_im, p.x_im, 64, p.H, p.T, p.B, 64);
+             (fm->real_x || tc::encode_feature_map(&fm->x_im, p.x_im, 64, p.H, p.T, p.B, 64));
     if (!(fm->fast & 2))
         ok = ok && tc::encode_feature_map(&fm->B_re, p.B_re, 64, p.H, p.T, p.B, 64) &&
              tc::encode_feature_map(&fm->B_im, p.B_im, 64, p.H, p.T, p.B, 64);

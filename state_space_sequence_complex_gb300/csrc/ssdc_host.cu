@@ -155,12 +155,15 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
              cudaStream_t stream) {
     int rc = check_sizes(dims, chunk_size);
     if (rc != SSDC_OK) return rc;
-    const void* ptrs[] = {x.re, x.im, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt,
+    // x.im may be null: a real x (its imaginary plane is zero and is not read)
+    const void* ptrs[] = {x.re, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt,
                           y.re, y.im, final_state.re, final_state.im};
     for (const void* q : ptrs)
         if (q == nullptr) return SSDC_ERR_INVALID;
     for (const void* q : ptrs)
         if (!aligned16(q)) return SSDC_ERR_ALIGN;
+    if (!aligned16(x.im)) return SSDC_ERR_ALIGN;
+    if (x.im == x.re) return SSDC_ERR_INVALID;
     const bool has_s0 = s0.re != nullptr;
     if ((s0.re == nullptr) != (s0.im == nullptr) || (has_s0 && s0.re == s0.im)) return SSDC_ERR_INVALID;
     if (has_s0 && (!aligned16(s0.re) || !aligned16(s0.im))) return SSDC_ERR_ALIGN;
@@ -172,7 +175,7 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     const int64_t BTH = dims.B * dims.T * dims.H;
     auto rng = [](const void* p, int64_t n) {
         const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-        return Range{lo, lo + (uintptr_t)n * sizeof(float)};
+        return Range{lo, p == nullptr ? lo : lo + (uintptr_t)n * sizeof(float)};  // null: empty
     };
     const Range in[] = {rng(x.re, BTH * dims.D), rng(x.im, BTH * dims.D), rng(A.re, dims.H),
                         rng(A.im, dims.H), rng(B_t.re, BTH * dims.N), rng(B_t.im, BTH * dims.N),

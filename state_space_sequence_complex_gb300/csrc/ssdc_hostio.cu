@@ -154,8 +154,10 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, con
     if (rc != SSDC_OK) return rc;
     const void* ins[] = {x.re, x.im, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt, y.re, y.im,
                          final_state.re, final_state.im};
-    for (const void* q : ins)
-        if (q == nullptr) return SSDC_ERR_INVALID;
+    for (int i = 0; i < 13; ++i)
+        if (ins[i] == nullptr && i != 1) return SSDC_ERR_INVALID;  // only x.im may be null: a real x
+    const bool real_x = x.im == nullptr;
+    if (x.im == x.re) return SSDC_ERR_INVALID;
     {  // host outputs must not overlap the inputs or each other
         const size_t tok = (size_t)dims.B * dims.T * dims.H;
         const size_t ib[] = {tok * dims.D * 4, tok * dims.D * 4, (size_t)dims.H * 4, (size_t)dims.H * 4,
@@ -169,7 +171,7 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, con
         };
         for (int o = 0; o < 4; ++o) {
             for (int i = 0; i < 9; ++i)
-                if (hit(outs[o], ob[o], ins[i], ib[i])) return SSDC_ERR_INVALID;
+                if (ins[i] != nullptr && hit(outs[o], ob[o], ins[i], ib[i])) return SSDC_ERR_INVALID;
             for (int j = o + 1; j < 4; ++j)
                 if (hit(outs[o], ob[o], outs[j], ob[j])) return SSDC_ERR_INVALID;
         }
@@ -231,7 +233,8 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, con
             const size_t tk0 = (size_t)((b0 * T + t0) * H);            // first (b, t, h) of the piece
             const size_t hrow = (size_t)(T * H), drow = (size_t)(Ts * H);  // tokens per host / device row
             bool ok = copy2d(dx_re, drow * D * 4, x.re + tk0 * D, hrow * D * 4, drow * D * 4, Bp, h2d, pipe.in) &&
-                      copy2d(dx_im, drow * D * 4, x.im + tk0 * D, hrow * D * 4, drow * D * 4, Bp, h2d, pipe.in) &&
+                      (real_x ||
+                       copy2d(dx_im, drow * D * 4, x.im + tk0 * D, hrow * D * 4, drow * D * 4, Bp, h2d, pipe.in)) &&
                       copy2d(dB_re, drow * N * 4, B_t.re + tk0 * N, hrow * N * 4, drow * N * 4, Bp, h2d, pipe.in) &&
                       copy2d(dB_im, drow * N * 4, B_t.im + tk0 * N, hrow * N * 4, drow * N * 4, Bp, h2d, pipe.in) &&
                       copy2d(dC_re, drow * N * 4, C_t.re + tk0 * N, hrow * N * 4, drow * N * 4, Bp, h2d, pipe.in) &&
@@ -248,7 +251,8 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, con
             ssdc_dims pd = dims;
             pd.B = Bp;
             pd.T = Ts;
-            rc = ssd_complex_fwd_init(ssdc_cin{dx_re, dx_im}, ssdc_cin{dA_re, dA_im}, ssdc_cin{dB_re, dB_im},
+            rc = ssd_complex_fwd_init(ssdc_cin{dx_re, real_x ? nullptr : dx_im}, ssdc_cin{dA_re, dA_im},
+                                      ssdc_cin{dB_re, dB_im},
                                       ssdc_cin{dC_re, dC_im}, ddt, ssdc_cin{ds0_re, ds0_im}, pd, chunk_size,
                                       ssdc_cout{dy_re, dy_im}, ssdc_cout{dfs_re, dfs_im}, s + sl.ws, sl.ws_bytes,
                                       pipe.comp);

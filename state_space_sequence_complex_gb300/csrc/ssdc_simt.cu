@@ -62,7 +62,7 @@ ssdc_simt_chunk_state(Problem p, Workspace ws) {
             if (s0 + s < nvalid) {
                 const int64_t o = ((int64_t)b * p.T + t) * H * D + (int64_t)h * D + d;
                 vr = p.x_re[o];
-                vi = p.x_im[o];
+                vi = p.x_im != nullptr ? p.x_im[o] : 0.0f;  // real x: no imaginary plane
             }
             sm.xr[s][d] = vr;
             sm.xi[s][d] = vi;
@@ -196,7 +196,7 @@ ssdc_simt_chunk_scan(Problem p, Workspace ws) {
             if (s0 + s < nvalid) {
                 const int64_t o = ((int64_t)b * p.T + t0 + s0 + s) * H * D + (int64_t)h * D + d;
                 vr = p.x_re[o];
-                vi = p.x_im[o];
+                vi = p.x_im != nullptr ? p.x_im[o] : 0.0f;  // real x: no imaginary plane
             }
             sm.xr[s][d] = vr;
             sm.xi[s][d] = vi;

@@ -86,14 +86,19 @@ tc_chunk_state(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
 
     const uint32_t sb_re = ptx::smem_addr(sm.b[0]), sb_im = ptx::smem_addr(sm.b[1]);
     const uint32_t sx_re = ptx::smem_addr(sm.x[0]), sx_im = ptx::smem_addr(sm.x[1]);
+    const bool real_x = p.x_im == nullptr;  // x real: its imaginary plane stays zero in shared memory
+    if (real_x) {
+        for (int i = tid; i < 64 * 64; i += kThreads) sm.x[1][i] = 0.0f;
+    }
     auto load_block = [&](int s0) {
-        ptx::mbar_arrive_expect_tx(&sm.bar_in, 4 * kPlaneBytes);
+        ptx::mbar_arrive_expect_tx(&sm.bar_in, (real_x ? 3 : 4) * kPlaneBytes);
         const int t = (int)(t0 + s0);
         for (int half = 0; half < 2; ++half) {
             ptx::tma_load_4d(reinterpret_cast<char*>(sm.b[0]) + half * kHalfBytes, &maps.B_re, &sm.bar_in, 32 * half, h, t, b);
             ptx::tma_load_4d(reinterpret_cast<char*>(sm.b[1]) + half * kHalfBytes, &maps.B_im, &sm.bar_in, 32 * half, h, t, b);
             ptx::tma_load_4d(reinterpret_cast<char*>(sm.x[0]) + half * kHalfBytes, &maps.x_re, &sm.bar_in, 32 * half, h, t, b);
-            ptx::tma_load_4d(reinterpret_cast<char*>(sm.x[1]) + half * kHalfBytes, &maps.x_im, &sm.bar_in, 32 * half, h, t, b);
+            if (!real_x)
+                ptx::tma_load_4d(reinterpret_cast<char*>(sm.x[1]) + half * kHalfBytes, &maps.x_im, &sm.bar_in, 32 * half, h, t, b);
         }
     };
     if (tid == 0) load_block(0);
@@ -208,14 +213,19 @@ tc_chunk_scan(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
     const uint32_t tmem = sm.tmem;
     const uint32_t my = lane_base(tmem, warp);
 
+    const bool real_x = p.x_im == nullptr;  // x real: its imaginary plane stays zero in shared memory
+    if (real_x) {
+        for (int i = tid; i < 64 * 64; i += kThreads) sm.x[1][i] = 0.0f;
+    }
     auto load_bx = [&](int s0) {
-        ptx::mbar_arrive_expect_tx(&sm.bar_bx, 4 * kPlaneBytes);
+        ptx::mbar_arrive_expect_tx(&sm.bar_bx, (real_x ? 3 : 4) * kPlaneBytes);
         const int t = (int)(t0 + s0);
         for (int half = 0; half < 2; ++half) {
             ptx::tma_load_4d(reinterpret_cast<char*>(sm.b[0]) + half * kHalfBytes, &maps.B_re, &sm.bar_bx, 32 * half, h, t, b);
             ptx::tma_load_4d(reinterpret_cast<char*>(sm.b[1]) + half * kHalfBytes, &maps.B_im, &sm.bar_bx, 32 * half, h, t, b);
             ptx::tma_load_4d(reinterpret_cast<char*>(sm.x[0]) + half * kHalfBytes, &maps.x_re, &sm.bar_bx, 32 * half, h, t, b);
-            ptx::tma_load_4d(reinterpret_cast<char*>(sm.x[1]) + half * kHalfBytes, &maps.x_im, &sm.bar_bx, 32 * half, h, t, b);
+            if (!real_x)
+                ptx::tma_load_4d(reinterpret_cast<char*>(sm.x[1]) + half * kHalfBytes, &maps.x_im, &sm.bar_bx, 32 * half, h, t, b);
         }
     };
     const int64_t chunk = ((int64_t)b * H + h) * p.nc + c;
@@ -422,7 +432,7 @@ bool make_state_map(CUtensorMap* m, const float* base, int64_t rows) {
 int make_maps(const Problem& p, const float* ws_S, TcMaps* m) {
     if (!get_encoder()) return SSDC_ERR_CUDA;
     bool ok = make_feature_map(&m->x_re, p.x_re, 64, p.H, p.T, p.B) &&
-              make_feature_map(&m->x_im, p.x_im, 64, p.H, p.T, p.B) &&
+              (p.x_im == nullptr || make_feature_map(&m->x_im, p.x_im, 64, p.H, p.T, p.B)) &&
               make_feature_map(&m->B_re, p.B_re, 64, p.H, p.T, p.B) &&
               make_feature_map(&m->B_im, p.B_im, 64, p.H, p.T, p.B) &&
               make_feature_map(&m->C_re, p.C_re, 64, p.H, p.T, p.B) &&

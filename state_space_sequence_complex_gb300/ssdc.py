@@ -116,7 +116,8 @@ def _ptr(t):
 
 
 def _cin(re, im):
-    return ssdc_cin(re.data_ptr(), im.data_ptr())
+    """Planar input; ``im`` may be None for a real x."""
+    return ssdc_cin(re.data_ptr(), None if im is None else im.data_ptr())
 
 
 def _cout(re, im):

@@ -101,9 +101,26 @@ def test_rejects_null_pointer(lib):
     d = ssdc.dims(1, 128, 2, 64, 64, "fp32")
     ptrs, end = fake_ptrs(d)
     for i in range(13):
+        if i == 1:
+            continue  # a null x.im means a real x
         bad = list(ptrs)
         bad[i] = None
         assert _call(lib, bad, d, ws=end) == ssdc.SSDC_ERR_INVALID
+
+
+def test_real_x_passes_argument_checks(lib):
+    """x.im = NULL is a real x: it passes the host checks (without a GPU the call then
+    fails on the device); x.im equal to x.re is rejected."""
+    for prec in ("fp32", "tf32", "tf32_staged"):
+        d = ssdc.dims(1, 128, 2, 64, 64, prec)
+        ptrs, end = fake_ptrs(d)
+        real = list(ptrs)
+        real[1] = None
+        assert _call(lib, real, d, ws=end) not in (ssdc.SSDC_ERR_INVALID, ssdc.SSDC_ERR_ALIGN,
+                                                   ssdc.SSDC_ERR_WORKSPACE, ssdc.SSDC_OK)
+        same = list(ptrs)
+        same[1] = ptrs[0]
+        assert _call(lib, same, d, ws=end) == ssdc.SSDC_ERR_INVALID
 
 
 def test_rejects_misaligned_pointer(lib):
@@ -183,9 +200,14 @@ def test_host_entry_rejects_bad_arguments(lib):
     ptrs, end = fake_ptrs(d)
     scratch = 1 << 44
     for i in range(13):
+        if i == 1:
+            continue  # a null x.im means a real x
         bad = list(ptrs)
         bad[i] = None
         assert _call_host(lib, bad, d, scratch=scratch) == ssdc.SSDC_ERR_INVALID
+    same = list(ptrs)
+    same[1] = ptrs[0]
+    assert _call_host(lib, same, d, scratch=scratch) == ssdc.SSDC_ERR_INVALID
     for o, i in ((9, 0), (10, 8), (11, 12), (12, 9)):
         bad = list(ptrs)
         bad[o] = ptrs[i]
