@@ -448,18 +448,23 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             }
         };
 
-        // Work left over from the previous chunk, done at the start of the next one (or after
-        // the last): wait for its y MMAs, keep its outgoing state (CL = 1) and write its y row
-        // straight from the accumulator to global memory. Column 16g + 8p' + i of the
-        // accumulator holds the plane-p' products of column d = 8g + i; four consecutive lanes
-        // hold one 32-byte run of a row.
+        // Work left over from the previous chunk, done during the next one (or after the last):
+        // (a) at its start, wait for its y MMAs and keep its outgoing state (CL = 1); (b) before
+        // the next P x, write its y row straight from the accumulator to global memory, late
+        // enough that these stores do not share the SM's outbound link with the state copy that
+        // ended the chunk. Column 16g + 8p' + i of the accumulator holds the plane-p' products of
+        // column d = 8g + i; four consecutive lanes hold one 32-byte run of a row.
         float outr[8], outi[8];
-        auto finish = [&](int it, const Pos& pos, bool keep_state) {
+        // (a) wait for its y MMAs (they read its stage, C' and S_in) and keep its state
+        auto finish_wait = [&](int it, bool keep_state) {
             wait_mma(2, it);
             if (keep_state) {
                 for_pairs(reinterpret_cast<char*>(sm.sin), outr, outi, true);
                 ptx::fence_proxy_async_smem();
             }
+        };
+        // (b) its y, from the accumulator (free until this chunk's P x)
+        auto finish_y = [&](const Pos& pos) {
             float yv[32];
             ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh, yv);
             ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh + 32, yv + 16);
@@ -506,7 +511,7 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 const int t = tid - 2 * kQ;  // 1 .. Q-1
                 sm.step[t] = cexp_fast(cdiff(sm.acs[s][t], sm.acs[s][t - 1]));
             }
-            if (it > 0) finish(it - 1, prev, prev_keep);
+            if (it > 0) finish_wait(it - 1, prev_keep);
             // Lane bits L0..L4. 128-bit accesses are served eight lanes at a time, so within
             // each group of eight (L0..L2) the 16-byte chunk positions of both the block loads
             // (rows s, swizzle by s) and the transposed stores (rows d, swizzle by d) are distinct.
@@ -627,6 +632,8 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 if (lane == 0) ptx::mbar_arrive(&sm.bt_ready);
             }
 
+            if (it > 0) finish_y(prev);  // the previous chunk's y (see finish_y)
+
             // ---- D: P = (C B^T) o L on this thread's row rr and columns col, col + 1 (col = 32 kh +
             // 8 j + 2 lq); P rows into TMEM (the MMA warp then starts P x). In the accumulator, one
             // 64-column half holds the products with B_r, the other with B_i; lane plane 0 / 1 of
@@ -727,7 +734,10 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             prev_keep = !last && CL == 1;
             cur = items.next(cur, H);
         }
-        if (nitems > 0) finish(nitems - 1, prev, false);
+        if (nitems > 0) {
+            finish_wait(nitems - 1, false);
+            finish_y(prev);
+        }
         if (leader) ptx::bulk_wait_all();
     }
     ptx::tc_fence_before();
