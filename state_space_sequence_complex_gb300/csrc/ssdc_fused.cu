@@ -40,8 +40,8 @@
 // block (w / 4) % 2 (8 complex rows) and the 32-column half w / 8, which is a
 // contiguous 2 KB of every interleaved tile. They write the transposes, the C'
 // and P rows and the state hop, and store y from registers to global memory,
-// four lanes per 32-byte run of a row (the previous chunk's y, early in the
-// next chunk). Warp 16 issues every MMA, in chunk order, on mbarrier hand-offs
+// four lanes per 32-byte run of a row (the previous chunk's y, in the next
+// chunk just before its P rows). Warp 16 issues every MMA, in chunk order, on mbarrier hand-offs
 // from the workers; warp 17 issues the TMA loads of the next chunk into the
 // other stage of a two-stage ring and computes its cumulative log-decay.
 #include <cstring>
