@@ -116,6 +116,12 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The two halves of it, for a thread that publishes nothing through the barrier: a
+// relaxed arrival (it does not wait for the thread's outstanding loads) and the wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
 // shared::cluster address, completion counted on the destination's mbarrier.

@@ -319,11 +319,15 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     if (warp == kProducer) {
         // ============ producer warp: TMA loads and cumulative log-decays ============
         bool ok = true;  // false once a wait gave up: later waits are skipped
+        // This warp touches no peer's shared memory: it joins the cluster barrier that guards
+        // the other warps' first remote accesses with a relaxed arrival, before its first loads
+        // (a releasing arrival would wait for them), and completes it later.
+        ptx::cluster_arrive_relaxed();
         Pos ld = items.first(H);
         Alog al = {};
         if (nitems > 0) al = load_alog(p, ld.b, ld.h, (int64_t)ld.c * kQ, lane);
         for (int j = 0; j < nitems; ++j) {  // item j into stage j & 1
-            if (j == 1) ptx::cluster_sync();  // peers' barriers are initialised before any remote access
+            if (j == 1) ptx::cluster_wait();
             const int st = j & 1;
             if (j >= 2) {
                 // the workers have passed the first barrier of item j - 1: item j - 2 left the stage
@@ -339,7 +343,7 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             if (j + 1 < nitems) al = load_alog(p, ld.b, ld.h, (int64_t)ld.c * kQ, lane);
             store_acs(sm, st, now, lane);
         }
-        if (nitems <= 1) ptx::cluster_sync();
+        if (nitems <= 1) ptx::cluster_wait();
     } else if (warp == kIssuer) {
         // ============ MMA warp: lane 0 issues every MMA in chunk order ============
         ptx::cluster_sync();  // peers' barriers are initialised before any remote access
