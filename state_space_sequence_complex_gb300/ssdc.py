@@ -285,12 +285,26 @@ class Forward:
         return ssd_complex_status(self.workspace, stream)
 
 
-def ssd_complex_fwd(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, precision="tf32"):
-    """One forward call on torch CUDA tensors; returns (y_re, y_im, fs_re, fs_im)."""
+def ssd_complex_fwd(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, precision="tf32",
+                    stream=None):
+    """Call ``ssd_complex_fwd`` (workspace allocated stream-ordered by the library) on
+    torch CUDA tensors; returns new (y_re, y_im, fs_re, fs_im) tensors. ``x_im`` may be
+    None for a real x."""
+    import torch
+
     Bn, T, H, D = x_re.shape
     N = B_re.shape[-1]
-    f = Forward(Bn, T, H, N, D, chunk_size, precision, device=x_re.device)
-    return f(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt)
+    f32 = dict(dtype=torch.float32, device=x_re.device)
+    y_re, y_im = torch.empty((Bn, T, H, D), **f32), torch.empty((Bn, T, H, D), **f32)
+    fs_re, fs_im = torch.empty((Bn, H, N, D), **f32), torch.empty((Bn, H, N, D), **f32)
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_fwd(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt),
+        dims(Bn, T, H, N, D, precision), int(chunk_size), _cout(y_re, y_im), _cout(fs_re, fs_im),
+        ctypes.c_void_p(s.cuda_stream))
+    if rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_fwd")
+    return y_re, y_im, fs_re, fs_im
 
 
 class HostForward:
