@@ -100,6 +100,15 @@ def fp32_flops_per_unit(w) -> dict:
             "chunk_scan": 4.0 * (Q + 1) * (N + D) + 8.0 * N * D}
 
 
+def bf16_peak_tflops() -> float:
+    """The measured burst BF16 dense peak of MEASURED_PEAKS.json (0 if absent)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 0.0
+
+
 def fp32_alu_peak_tflops(dev_index: int):
     """FP32 FMA peak of the CUDA cores: SMs x 128 FP32 lanes x 2 flops x the maximum SM clock."""
     import torch
@@ -499,6 +508,13 @@ def main():
                 "algorithmic_bytes_per_launch": bytes_per_launch,
                 "kernel_ms": {n: m for n, m in zip(names, kmeans)},
                 "step_frac": step_achieved / peak}
+    if precision == "tf32" and len(kmeans) == 1:
+        # context: the same launch against the TF32 tensor peak (the file's BF16 peak times the
+        # nominal TF32 / BF16 ratio), with the algorithmic (causal) flops
+        fl = sum(fp32_flops_per_unit(w).values()) * w.token_heads
+        tf32_peak = bf16_peak_tflops() * 1.1 / 2.25
+        roofline["tf32_flops_per_launch"] = fl
+        roofline["tf32_frac"] = fl / (kmeans[top] / 1000.0) / 1e12 / tf32_peak if tf32_peak else None
     if precision == "fp32" and names[top] in ("chunk_state", "state_pass", "chunk_scan"):
         # the exact path computes on the CUDA cores: its dominant launch against the FP32 FMA peak
         fl = fp32_flops_per_unit(w)[names[top]] * w.token_heads
