@@ -206,7 +206,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def run_oracle_baseline(w, inp, max_seconds=12.0, max_reps=20):
+def run_oracle_baseline(w, inp, max_seconds=12.0, max_reps=400):
     """Time the CPU oracle, as it stands, on the full workload, repeated."""
     from oracle import naive_scan_inputs
     from oracle.ssd_oracle import default_threads

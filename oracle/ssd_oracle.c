@@ -25,6 +25,11 @@
  * row-major over the shapes given. Inputs are float32 (the configs fix
  * complex64 inputs); all arithmetic and all outputs are double.
  *
+ * ssd_oracle_naive_bwd (end of this file) gives the gradients of that scan
+ * with respect to every input, by the adjoint of the same recurrence (the
+ * pages' training path; page "Extending -- SSM variants & Triton kernels",
+ * Step 3, the autograd wrapper seeded with the true output gradients).
+ *
  * Parity pins: every function here is pinned by tests that do not call it to
  * get the expected values (brute-force SSD matrix, closed forms, library IIR
  * filter, invariants, chunk-size invariance of an independent chunkwise form).
@@ -167,6 +172,267 @@ int ssd_oracle_naive(const float *x_re, const float *x_im, const float *A_re,
     }
     if (rc == 0 && started == 0) rc = -2;
     free(th);
+    pthread_mutex_destroy(&J.lock);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------
+ * Backward pass (gradients) of the scan above, by the adjoint of the
+ * recurrence, in double precision. TEST INFRASTRUCTURE ONLY.
+ *
+ * Convention for complex gradients (the one PyTorch uses for complex
+ * tensors): for a real loss L and a complex quantity z, the gradient dz holds
+ * dL/dRe(z) in its real part and dL/dIm(z) in its imaginary part. For a
+ * holomorphic step w = f(z) this gives dz += conj(f'(z)) * dw.
+ *
+ * Given dy (B,T,H,D) and d_final_state (B,H,N,D), with g the gradient of the
+ * state s_t (N x D):
+ *   g = d_final_state
+ *   for t = T-1 .. 0:
+ *       g[n,d] += conj(C_t[n]) * dy_t[d]                  (y_t = C_t s_t)
+ *       dC_t[n]  = sum_d dy_t[d] * conj(s_t[n,d])
+ *       dx_t[d]  = sum_n g[n,d] * conj(B_t[n])             (B_t (outer) x_t)
+ *       dB_t[n]  = sum_d g[n,d] * conj(x_t[d])
+ *       dz_t     = sum_{n,d} g[n,d] * conj(A_bar_t s_{t-1}[n,d])
+ *                  (z_t = delta_t A the log-decay, ds_t/dz_t = A_bar_t s_{t-1})
+ *       ddt_t    = Re(dz_t * conj(A)) * sigmoid(dt_t)     (delta = softplus(dt))
+ *       dA      += delta_t * dz_t                          (summed over b and t)
+ *       g        = conj(A_bar_t) * g                       (s_t = A_bar_t s_{t-1} + ...)
+ *   d_initial_state = g
+ * The states s_t are those of the forward scan, kept for every t.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    const float *x_re, *x_im, *A_re, *A_im, *B_re, *B_im, *C_re, *C_im, *dt;
+    const float *dy_re, *dy_im, *dfs_re, *dfs_im; /* dfs may be NULL: zero */
+    const double *s0_re, *s0_im;                  /* may be NULL: zero */
+    int64_t Bn, T, H, N, D;
+    double *dx_re, *dx_im, *dB_re, *dB_im, *dC_re, *dC_im, *ddt;
+    double *dAp_re, *dAp_im; /* per (b,h) partial sums of dA */
+    double *ds0_re, *ds0_im; /* (B,H,N,D) */
+    int64_t next_job;
+    pthread_mutex_t lock;
+} bjob_t;
+
+static double sigmoid(double v) {
+    return v >= 0.0 ? 1.0 / (1.0 + exp(-v)) : exp(v) / (1.0 + exp(v));
+}
+
+/* One (b,h) sequence. st holds (T+1) states of N*D complex values:
+ * st[0] = s_{-1}, st[t+1] = s_t. */
+static void grad_one(const bjob_t *J, int64_t b, int64_t h, double *str, double *sti,
+                     double *gr, double *gi) {
+    const int64_t T = J->T, H = J->H, N = J->N, D = J->D, ND = N * D;
+    const double Ar = J->A_re[h], Ai = J->A_im[h];
+    const int64_t bh = b * H + h;
+    /* forward, keeping every state */
+    if (J->s0_re) {
+        memcpy(str, J->s0_re + bh * ND, sizeof(double) * ND);
+        memcpy(sti, J->s0_im + bh * ND, sizeof(double) * ND);
+    } else {
+        memset(str, 0, sizeof(double) * ND);
+        memset(sti, 0, sizeof(double) * ND);
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t bth = (b * T + t) * H + h;
+        const double delta = softplus((double)J->dt[bth]);
+        const double mag = exp(delta * Ar);
+        const double abr = mag * cos(delta * Ai), abi = mag * sin(delta * Ai);
+        const float *xr = J->x_re + bth * D, *xi = J->x_im + bth * D;
+        const float *br = J->B_re + bth * N, *bi = J->B_im + bth * N;
+        const double *pr = str + t * ND, *pi = sti + t * ND;
+        double *qr = str + (t + 1) * ND, *qi = sti + (t + 1) * ND;
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t d = 0; d < D; ++d) {
+                const int64_t k = n * D + d;
+                qr[k] = (abr * pr[k] - abi * pi[k]) + ((double)br[n] * xr[d] - (double)bi[n] * xi[d]);
+                qi[k] = (abr * pi[k] + abi * pr[k]) + ((double)br[n] * xi[d] + (double)bi[n] * xr[d]);
+            }
+    }
+    /* backward */
+    if (J->dfs_re) {
+        for (int64_t k = 0; k < ND; ++k) {
+            gr[k] = J->dfs_re[bh * ND + k];
+            gi[k] = J->dfs_im[bh * ND + k];
+        }
+    } else {
+        memset(gr, 0, sizeof(double) * ND);
+        memset(gi, 0, sizeof(double) * ND);
+    }
+    double dAr = 0.0, dAi = 0.0;
+    for (int64_t t = T - 1; t >= 0; --t) {
+        const int64_t bth = (b * T + t) * H + h;
+        const double delta = softplus((double)J->dt[bth]);
+        const double mag = exp(delta * Ar);
+        const double abr = mag * cos(delta * Ai), abi = mag * sin(delta * Ai);
+        const float *xr = J->x_re + bth * D, *xi = J->x_im + bth * D;
+        const float *br = J->B_re + bth * N, *bi = J->B_im + bth * N;
+        const float *cr = J->C_re + bth * N, *ci = J->C_im + bth * N;
+        const float *yr = J->dy_re + bth * D, *yi = J->dy_im + bth * D;
+        const double *sr = str + (t + 1) * ND, *si = sti + (t + 1) * ND; /* s_t */
+        const double *pr = str + t * ND, *pi = sti + t * ND;             /* s_{t-1} */
+        /* g += conj(C_t) (outer) dy_t */
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t d = 0; d < D; ++d) {
+                const int64_t k = n * D + d;
+                gr[k] += (double)cr[n] * yr[d] + (double)ci[n] * yi[d];
+                gi[k] += (double)cr[n] * yi[d] - (double)ci[n] * yr[d];
+            }
+        /* dC_t[n] = sum_d dy_t[d] conj(s_t[n,d]) */
+        for (int64_t n = 0; n < N; ++n) {
+            double ar = 0.0, ai = 0.0;
+            for (int64_t d = 0; d < D; ++d) {
+                const int64_t k = n * D + d;
+                ar += yr[d] * sr[k] + yi[d] * si[k];
+                ai += yi[d] * sr[k] - yr[d] * si[k];
+            }
+            J->dC_re[bth * N + n] = ar;
+            J->dC_im[bth * N + n] = ai;
+        }
+        /* dx_t[d] = sum_n g[n,d] conj(B_t[n]) */
+        for (int64_t d = 0; d < D; ++d) {
+            double ar = 0.0, ai = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const int64_t k = n * D + d;
+                ar += gr[k] * br[n] + gi[k] * bi[n];
+                ai += gi[k] * br[n] - gr[k] * bi[n];
+            }
+            J->dx_re[bth * D + d] = ar;
+            J->dx_im[bth * D + d] = ai;
+        }
+        /* dB_t[n] = sum_d g[n,d] conj(x_t[d]) */
+        for (int64_t n = 0; n < N; ++n) {
+            double ar = 0.0, ai = 0.0;
+            for (int64_t d = 0; d < D; ++d) {
+                const int64_t k = n * D + d;
+                ar += gr[k] * xr[d] + gi[k] * xi[d];
+                ai += gi[k] * xr[d] - gr[k] * xi[d];
+            }
+            J->dB_re[bth * N + n] = ar;
+            J->dB_im[bth * N + n] = ai;
+        }
+        /* dz_t = sum g conj(A_bar_t s_{t-1}) */
+        double zr = 0.0, zi = 0.0;
+        for (int64_t k = 0; k < ND; ++k) {
+            const double ur = abr * pr[k] - abi * pi[k];
+            const double ui = abr * pi[k] + abi * pr[k];
+            zr += gr[k] * ur + gi[k] * ui;
+            zi += gi[k] * ur - gr[k] * ui;
+        }
+        J->ddt[bth] = (zr * Ar + zi * Ai) * sigmoid((double)J->dt[bth]);
+        dAr += delta * zr;
+        dAi += delta * zi;
+        /* g = conj(A_bar_t) g */
+        for (int64_t k = 0; k < ND; ++k) {
+            const double r = gr[k], i = gi[k];
+            gr[k] = abr * r + abi * i;
+            gi[k] = abr * i - abi * r;
+        }
+    }
+    J->dAp_re[bh] = dAr;
+    J->dAp_im[bh] = dAi;
+    if (J->ds0_re) {
+        memcpy(J->ds0_re + bh * ND, gr, sizeof(double) * ND);
+        memcpy(J->ds0_im + bh * ND, gi, sizeof(double) * ND);
+    }
+}
+
+static void *grad_worker(void *arg) {
+    bjob_t *J = (bjob_t *)arg;
+    const size_t ND = (size_t)(J->N * J->D);
+    const size_t sts = (size_t)(J->T + 1) * ND;
+    double *str = (double *)malloc(sizeof(double) * sts);
+    double *sti = (double *)malloc(sizeof(double) * sts);
+    double *gr = (double *)malloc(sizeof(double) * ND);
+    double *gi = (double *)malloc(sizeof(double) * ND);
+    void *ret = NULL;
+    if (!str || !sti || !gr || !gi) {
+        ret = (void *)1;
+    } else {
+        for (;;) {
+            pthread_mutex_lock(&J->lock);
+            const int64_t j = J->next_job++;
+            pthread_mutex_unlock(&J->lock);
+            if (j >= J->Bn * J->H) break;
+            grad_one(J, j / J->H, j % J->H, str, sti, gr, gi);
+        }
+    }
+    free(str);
+    free(sti);
+    free(gr);
+    free(gi);
+    return ret;
+}
+
+/*
+ * Gradients of the scan. Inputs as for ssd_oracle_naive plus dy (B,T,H,D)
+ * and d_final_state (B,H,N,D, may be NULL for zero). Outputs (double):
+ * dx (B,T,H,D), dA (H), dB and dC (B,T,H,N), ddt (B,T,H) and, when ds0_re /
+ * ds0_im are not NULL, d_initial_state (B,H,N,D). dA sums the (b,h) partials
+ * in order of b. Returns 0, -1 on bad arguments, -2 when out of threads or
+ * memory.
+ */
+int ssd_oracle_naive_bwd(const float *x_re, const float *x_im, const float *A_re,
+                         const float *A_im, const float *B_re, const float *B_im,
+                         const float *C_re, const float *C_im, const float *dt,
+                         const double *s0_re, const double *s0_im, const float *dy_re,
+                         const float *dy_im, const float *dfs_re, const float *dfs_im,
+                         int64_t Bn, int64_t T, int64_t H, int64_t N, int64_t D,
+                         double *dx_re, double *dx_im, double *dA_re, double *dA_im,
+                         double *dB_re, double *dB_im, double *dC_re, double *dC_im,
+                         double *ddt, double *ds0_re, double *ds0_im, int nthreads) {
+    if (Bn <= 0 || T <= 0 || H <= 0 || N <= 0 || D <= 0 || nthreads <= 0) return -1;
+    if ((s0_re == NULL) != (s0_im == NULL) || (dfs_re == NULL) != (dfs_im == NULL) ||
+        (ds0_re == NULL) != (ds0_im == NULL))
+        return -1;
+    bjob_t J;
+    J.x_re = x_re; J.x_im = x_im; J.A_re = A_re; J.A_im = A_im;
+    J.B_re = B_re; J.B_im = B_im; J.C_re = C_re; J.C_im = C_im; J.dt = dt;
+    J.dy_re = dy_re; J.dy_im = dy_im; J.dfs_re = dfs_re; J.dfs_im = dfs_im;
+    J.s0_re = s0_re; J.s0_im = s0_im;
+    J.Bn = Bn; J.T = T; J.H = H; J.N = N; J.D = D;
+    J.dx_re = dx_re; J.dx_im = dx_im; J.dB_re = dB_re; J.dB_im = dB_im;
+    J.dC_re = dC_re; J.dC_im = dC_im; J.ddt = ddt;
+    J.ds0_re = ds0_re; J.ds0_im = ds0_im;
+    J.dAp_re = (double *)calloc((size_t)(Bn * H), sizeof(double));
+    J.dAp_im = (double *)calloc((size_t)(Bn * H), sizeof(double));
+    J.next_job = 0;
+    if (!J.dAp_re || !J.dAp_im) {
+        free(J.dAp_re);
+        free(J.dAp_im);
+        return -2;
+    }
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads > Bn * H) nthreads = (int)(Bn * H);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nthreads);
+    int rc = 0, started = 0;
+    if (!th) rc = -2;
+    for (int i = 0; rc == 0 && i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, grad_worker, &J) != 0) {
+            rc = -2;
+            break;
+        }
+        ++started;
+    }
+    for (int i = 0; i < started; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret != NULL) rc = -2;
+    }
+    if (rc == 0 && started == 0) rc = -2;
+    if (rc == 0) {
+        for (int64_t h = 0; h < H; ++h) {
+            double ar = 0.0, ai = 0.0;
+            for (int64_t b = 0; b < Bn; ++b) {
+                ar += J.dAp_re[b * H + h];
+                ai += J.dAp_im[b * H + h];
+            }
+            dA_re[h] = ar;
+            dA_im[h] = ai;
+        }
+    }
+    free(th);
+    free(J.dAp_re);
+    free(J.dAp_im);
     pthread_mutex_destroy(&J.lock);
     return rc;
 }

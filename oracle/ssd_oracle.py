@@ -4,6 +4,8 @@
 "Extending -- SSM variants & Triton kernels" (Path A, Step 1) with the
 discretisation A_bar = exp(softplus(dt) * A). It returns y (B,T,H,D) and the
 final state (B,H,N,D) as complex128 numpy arrays; Re(y) is ``y.real``.
+``naive_grad`` runs the adjoint of the same recurrence: the gradients of a
+real loss with respect to every input, given the output gradients.
 """
 from __future__ import annotations
 
@@ -97,6 +99,72 @@ def naive_scan(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, *,
     if rc != 0:
         raise RuntimeError(f"ssd_oracle_naive failed with status {rc}")
     return y_re + 1j * y_im, s_re + 1j * s_im
+
+
+def _load_bwd():
+    lib = _load()
+    f = lib.ssd_oracle_naive_bwd
+    if f.argtypes is None:
+        fp = ctypes.POINTER(ctypes.c_float)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        f.argtypes = [fp] * 9 + [dp, dp] + [fp] * 4 + [i64] * 5 + [dp] * 11 + [ctypes.c_int]
+        f.restype = ctypes.c_int
+    return lib
+
+
+def naive_grad(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, dy, dfs=None, *,
+               s0: np.ndarray | None = None, threads: int | None = None) -> dict:
+    """Gradients of the sequential scan for the output gradients ``dy``
+    (B,T,H,D complex) and ``dfs`` (B,H,N,D complex, None: zero), by the
+    adjoint recurrence in complex128. A complex gradient holds dL/dRe in its
+    real part and dL/dIm in its imaginary part. Returns a dict with complex128
+    ``dx``, ``dA``, ``dB``, ``dC``, ``ds0`` and float64 ``ddt``."""
+    lib = _load_bwd()
+    Bn, T, H, D = np.shape(x_re)
+    N = np.shape(B_re)[-1]
+    keep, ptrs = [], []
+    for a in (x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt):
+        arr, p = _f32(a)
+        keep.append(arr)
+        ptrs.append(p)
+    null_d = ctypes.POINTER(ctypes.c_double)()
+    null_f = ctypes.POINTER(ctypes.c_float)()
+    if s0 is not None:
+        s0r = np.ascontiguousarray(np.real(s0), dtype=np.float64)
+        s0i = np.ascontiguousarray(np.imag(s0), dtype=np.float64)
+        assert s0r.shape == (Bn, H, N, D)
+        p0 = [_f64(s0r), _f64(s0i)]
+    else:
+        p0 = [null_d, null_d]
+    gy = [_f32(np.real(dy)), _f32(np.imag(dy))]
+    assert gy[0][0].shape == (Bn, T, H, D)
+    if dfs is not None:
+        gs = [_f32(np.real(dfs)), _f32(np.imag(dfs))]
+        assert gs[0][0].shape == (Bn, H, N, D)
+    else:
+        gs = [(None, null_f), (None, null_f)]
+    out = {k: np.zeros(s, np.float64) for k, s in (
+        ("dx_re", (Bn, T, H, D)), ("dx_im", (Bn, T, H, D)), ("dA_re", (H,)), ("dA_im", (H,)),
+        ("dB_re", (Bn, T, H, N)), ("dB_im", (Bn, T, H, N)), ("dC_re", (Bn, T, H, N)),
+        ("dC_im", (Bn, T, H, N)), ("ddt", (Bn, T, H)), ("ds0_re", (Bn, H, N, D)),
+        ("ds0_im", (Bn, H, N, D)))}
+    order = ("dx_re", "dx_im", "dA_re", "dA_im", "dB_re", "dB_im", "dC_re", "dC_im", "ddt",
+             "ds0_re", "ds0_im")
+    rc = lib.ssd_oracle_naive_bwd(*ptrs, *p0, gy[0][1], gy[1][1], gs[0][1], gs[1][1],
+                                  Bn, T, H, N, D, *[_f64(out[k]) for k in order],
+                                  int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"ssd_oracle_naive_bwd failed with status {rc}")
+    return {"dx": out["dx_re"] + 1j * out["dx_im"], "dA": out["dA_re"] + 1j * out["dA_im"],
+            "dB": out["dB_re"] + 1j * out["dB_im"], "dC": out["dC_re"] + 1j * out["dC_im"],
+            "ddt": out["ddt"], "ds0": out["ds0_re"] + 1j * out["ds0_im"]}
+
+
+def naive_grad_inputs(inp, dy, dfs=None, **kw) -> dict:
+    """``naive_grad`` on an ``inputs.Inputs`` bundle."""
+    return naive_grad(inp.x_re, inp.x_im, inp.A_re, inp.A_im, inp.B_re, inp.B_im,
+                      inp.C_re, inp.C_im, inp.dt, dy, dfs, **kw)
 
 
 def naive_scan_inputs(inp, **kw):

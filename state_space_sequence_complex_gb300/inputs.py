@@ -137,3 +137,33 @@ def custom(Bn, T, H, D, N, seed, dt_mode="normal", dt_mean=0.0, dt_std=1.0,
     """Inputs of an arbitrary shape with the standard distributions."""
     w = Workload("custom", Bn, T, H, D, N, 1, seed, dt_mode, dt_mean, dt_std, re_lo, re_hi)
     return generate(w)
+
+
+@dataclasses.dataclass
+class OutputGrads:
+    """Planar float32 gradients of a loss with respect to the outputs:
+    dy (B,T,H,D) and d_final_state (B,H,N,D). A complex gradient holds
+    dL/dRe in its real plane and dL/dIm in its imaginary plane."""
+
+    dy_re: np.ndarray
+    dy_im: np.ndarray
+    dfs_re: np.ndarray
+    dfs_im: np.ndarray
+
+    def complex(self):
+        c = lambda r, i: r.astype(np.float64) + 1j * i.astype(np.float64)
+        return dict(dy=c(self.dy_re, self.dy_im), dfs=c(self.dfs_re, self.dfs_im))
+
+
+def output_grads(Bn, T, H, D, N, seed) -> OutputGrads:
+    """Output gradients with i.i.d. N(0, 1/2) real and imaginary parts, drawn
+    dy first, then d_final_state, from ``default_rng(seed)``."""
+    rng = np.random.default_rng(seed)
+    dy_re, dy_im = _cnormal_planes(rng, (Bn, T, H, D))
+    dfs_re, dfs_im = _cnormal_planes(rng, (Bn, H, N, D))
+    return OutputGrads(dy_re, dy_im, dfs_re, dfs_im)
+
+
+def initial_state(Bn, H, N, D, seed) -> tuple[np.ndarray, np.ndarray]:
+    """A planar float32 initial state (B,H,N,D), i.i.d. N(0, 1/2) parts."""
+    return _cnormal_planes(np.random.default_rng(seed), (Bn, H, N, D))
