@@ -1,6 +1,7 @@
 /*
  * ssdc.h -- C ABI of libssdc.so: forward pass of the complex-valued chunkwise
- * SSD scan (the core scan of a Mamba-3 block) on one GB300 (sm_103a).
+ * SSD scan (the core scan of a Mamba-3 block) on one GB300 (sm_103a), and
+ * its backward pass (ssd_complex_bwd, at the end of this header).
  *
  * The operation (page "Extending -- SSM variants & Triton kernels", Path A,
  * Step 1, the naive O(T) scan and the discretisation it calls; landing page
@@ -240,6 +241,62 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
                          const float *dt, ssdc_dims dims, int chunk_size,
                          ssdc_cout y, ssdc_cout final_state, void *dev_scratch,
                          size_t scratch_bytes, cudaStream_t stream);
+
+/*
+ * Backward pass: the gradients of a real loss L with respect to every input
+ * of the forward pass, given the gradients with respect to its outputs. The
+ * pages' training path (page "Extending -- SSM variants & Triton kernels",
+ * Step 3: the backward recomputes the forward and is seeded with the true
+ * output gradients; every differentiated input gets a gradient).
+ *
+ * Convention. A complex gradient holds dL/dRe(z) in its real plane and
+ * dL/dIm(z) in its imaginary plane (PyTorch's convention for complex
+ * tensors). With g_t the gradient of the state s_t, the adjoint recurrence is
+ *   g_{T-1} = d_final_state + conj(C_{T-1}) (outer) dy_{T-1}
+ *   g_{t-1} = conj(A_bar_t) g_t + conj(C_{t-1}) (outer) dy_{t-1}
+ *   dx_t[d] = sum_n g_t[n,d] conj(B_t[n])     dB_t[n] = sum_d g_t[n,d] conj(x_t[d])
+ *   dC_t[n] = sum_d dy_t[d] conj(s_t[n,d])
+ *   dz_t = sum g_t conj(A_bar_t s_{t-1})      (z_t = softplus(dt_t) A)
+ *   ddt_t = Re(dz_t conj(A)) sigmoid(dt_t),  dA = sum_{b,t} softplus(dt_t) dz_t
+ *   d_initial_state = conj(A_bar_0) g_0
+ * The library computes it chunk by chunk: it recomputes the chunk states
+ * S_in[c], runs the adjoint state recurrence backwards over the chunks, forms
+ * dx, dB_t and dC_t per chunk, and obtains dz_t from the identity
+ *   dz_t = <d_final_state, final_state> + sum_{t' >= t} (<dC_t', C_t'> - <dB_t', B_t'>)
+ * with <u, v> = sum u conj(v) (accumulated in fp64).
+ *
+ *   x, A, B_t, C_t, dt, initial_state   the forward pass's inputs, as for
+ *                        ssd_complex_fwd_init (initial_state: both planes null
+ *                        for zero; x.im NULL for a real x)
+ *   dy                   (B,T,H,D) gradient of y. dy.im may be NULL: a loss of
+ *                        Re(y) alone (the pages' model takes Re(y))
+ *   d_final_state        (B,H,N,D) gradient of the final state; both planes
+ *                        NULL for zero
+ *   dx                   output (B,T,H,D). dx.im may be NULL: not written (for
+ *                        a real x, dx.re is the gradient of x)
+ *   dA                   output (H) complex, summed over b and t
+ *   dB_t, dC_t           outputs (B,T,H,N) complex
+ *   ddt                  output (B,T,H) real
+ *   d_initial_state      output (B,H,N,D) complex; both planes NULL: not
+ *                        written
+ *   workspace            device memory, 256-byte aligned, at least
+ *                        ssd_complex_bwd_workspace_bytes() bytes; no
+ *                        initialisation needed
+ * All pointers are device pointers, 16-byte aligned. Outputs must not overlap
+ * each other, an input or the workspace. One null plane of a pair that must
+ * be given together is SSDC_ERR_INVALID.
+ *
+ * Precision: SSDC_PREC_FP32 only (exact fp32 on the SIMT cores, every decay
+ * with the accurate expf / sincosf); the other precisions return
+ * SSDC_ERR_UNSUPPORTED. Sizes as for SSDC_PREC_FP32 in the forward pass.
+ * Errors, streams and ownership as for ssd_complex_fwd_ws.
+ */
+size_t ssd_complex_bwd_workspace_bytes(ssdc_dims dims, int chunk_size);
+int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float *dt,
+                    ssdc_cin initial_state, ssdc_cin dy, ssdc_cin d_final_state,
+                    ssdc_dims dims, int chunk_size, ssdc_cout dx, ssdc_cout dA,
+                    ssdc_cout dB_t, ssdc_cout dC_t, float *ddt, ssdc_cout d_initial_state,
+                    void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

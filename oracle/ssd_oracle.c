@@ -193,7 +193,7 @@ int ssd_oracle_naive(const float *x_re, const float *x_im, const float *A_re,
  *       dC_t[n]  = sum_d dy_t[d] * conj(s_t[n,d])
  *       dx_t[d]  = sum_n g[n,d] * conj(B_t[n])             (B_t (outer) x_t)
  *       dB_t[n]  = sum_d g[n,d] * conj(x_t[d])
- *       dz_t     = sum_{n,d} g[n,d] * conj(A_bar_t s_{t-1}[n,d])
+ *       dz_t     = sum_{n,d} g[n,d] * conj(A_bar_t s_{t-1}[n,d])   (also returned)
  *                  (z_t = delta_t A the log-decay, ds_t/dz_t = A_bar_t s_{t-1})
  *       ddt_t    = Re(dz_t * conj(A)) * sigmoid(dt_t)     (delta = softplus(dt))
  *       dA      += delta_t * dz_t                          (summed over b and t)
@@ -209,6 +209,7 @@ typedef struct {
     double *dx_re, *dx_im, *dB_re, *dB_im, *dC_re, *dC_im, *ddt;
     double *dAp_re, *dAp_im; /* per (b,h) partial sums of dA */
     double *ds0_re, *ds0_im; /* (B,H,N,D) */
+    double *dz_re, *dz_im;   /* (B,T,H): gradient of the log-decay z_t */
     int64_t next_job;
     pthread_mutex_t lock;
 } bjob_t;
@@ -318,6 +319,8 @@ static void grad_one(const bjob_t *J, int64_t b, int64_t h, double *str, double 
             zr += gr[k] * ur + gi[k] * ui;
             zi += gi[k] * ur - gr[k] * ui;
         }
+        J->dz_re[bth] = zr;
+        J->dz_im[bth] = zi;
         J->ddt[bth] = (zr * Ar + zi * Ai) * sigmoid((double)J->dt[bth]);
         dAr += delta * zr;
         dAi += delta * zi;
@@ -366,9 +369,10 @@ static void *grad_worker(void *arg) {
 /*
  * Gradients of the scan. Inputs as for ssd_oracle_naive plus dy (B,T,H,D)
  * and d_final_state (B,H,N,D, may be NULL for zero). Outputs (double):
- * dx (B,T,H,D), dA (H), dB and dC (B,T,H,N), ddt (B,T,H) and, when ds0_re /
- * ds0_im are not NULL, d_initial_state (B,H,N,D). dA sums the (b,h) partials
- * in order of b. Returns 0, -1 on bad arguments, -2 when out of threads or
+ * dx (B,T,H,D), dA (H), dB and dC (B,T,H,N), ddt (B,T,H), dz (B,T,H), the
+ * gradient of each token's log-decay z_t = softplus(dt_t) A, and, when
+ * ds0_re / ds0_im are not NULL, d_initial_state (B,H,N,D). dA sums the (b,h)
+ * partials in order of b. Returns 0, -1 on bad arguments, -2 when out of threads or
  * memory.
  */
 int ssd_oracle_naive_bwd(const float *x_re, const float *x_im, const float *A_re,
@@ -379,8 +383,10 @@ int ssd_oracle_naive_bwd(const float *x_re, const float *x_im, const float *A_re
                          int64_t Bn, int64_t T, int64_t H, int64_t N, int64_t D,
                          double *dx_re, double *dx_im, double *dA_re, double *dA_im,
                          double *dB_re, double *dB_im, double *dC_re, double *dC_im,
-                         double *ddt, double *ds0_re, double *ds0_im, int nthreads) {
+                         double *ddt, double *ds0_re, double *ds0_im, double *dz_re,
+                         double *dz_im, int nthreads) {
     if (Bn <= 0 || T <= 0 || H <= 0 || N <= 0 || D <= 0 || nthreads <= 0) return -1;
+    if (dz_re == NULL || dz_im == NULL) return -1;
     if ((s0_re == NULL) != (s0_im == NULL) || (dfs_re == NULL) != (dfs_im == NULL) ||
         (ds0_re == NULL) != (ds0_im == NULL))
         return -1;
@@ -393,6 +399,7 @@ int ssd_oracle_naive_bwd(const float *x_re, const float *x_im, const float *A_re
     J.dx_re = dx_re; J.dx_im = dx_im; J.dB_re = dB_re; J.dB_im = dB_im;
     J.dC_re = dC_re; J.dC_im = dC_im; J.ddt = ddt;
     J.ds0_re = ds0_re; J.ds0_im = ds0_im;
+    J.dz_re = dz_re; J.dz_im = dz_im;
     J.dAp_re = (double *)calloc((size_t)(Bn * H), sizeof(double));
     J.dAp_im = (double *)calloc((size_t)(Bn * H), sizeof(double));
     J.next_job = 0;

@@ -108,7 +108,7 @@ def _load_bwd():
         fp = ctypes.POINTER(ctypes.c_float)
         dp = ctypes.POINTER(ctypes.c_double)
         i64 = ctypes.c_int64
-        f.argtypes = [fp] * 9 + [dp, dp] + [fp] * 4 + [i64] * 5 + [dp] * 11 + [ctypes.c_int]
+        f.argtypes = [fp] * 9 + [dp, dp] + [fp] * 4 + [i64] * 5 + [dp] * 13 + [ctypes.c_int]
         f.restype = ctypes.c_int
     return lib
 
@@ -119,7 +119,8 @@ def naive_grad(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, dy, dfs=None,
     (B,T,H,D complex) and ``dfs`` (B,H,N,D complex, None: zero), by the
     adjoint recurrence in complex128. A complex gradient holds dL/dRe in its
     real part and dL/dIm in its imaginary part. Returns a dict with complex128
-    ``dx``, ``dA``, ``dB``, ``dC``, ``ds0`` and float64 ``ddt``."""
+    ``dx``, ``dA``, ``dB``, ``dC``, ``ds0``, ``dz`` (the gradient of each token's
+    log-decay z_t = softplus(dt_t) A, shape (B,T,H)) and float64 ``ddt``."""
     lib = _load_bwd()
     Bn, T, H, D = np.shape(x_re)
     N = np.shape(B_re)[-1]
@@ -148,9 +149,9 @@ def naive_grad(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, dy, dfs=None,
         ("dx_re", (Bn, T, H, D)), ("dx_im", (Bn, T, H, D)), ("dA_re", (H,)), ("dA_im", (H,)),
         ("dB_re", (Bn, T, H, N)), ("dB_im", (Bn, T, H, N)), ("dC_re", (Bn, T, H, N)),
         ("dC_im", (Bn, T, H, N)), ("ddt", (Bn, T, H)), ("ds0_re", (Bn, H, N, D)),
-        ("ds0_im", (Bn, H, N, D)))}
+        ("ds0_im", (Bn, H, N, D)), ("dz_re", (Bn, T, H)), ("dz_im", (Bn, T, H)))}
     order = ("dx_re", "dx_im", "dA_re", "dA_im", "dB_re", "dB_im", "dC_re", "dC_im", "ddt",
-             "ds0_re", "ds0_im")
+             "ds0_re", "ds0_im", "dz_re", "dz_im")
     rc = lib.ssd_oracle_naive_bwd(*ptrs, *p0, gy[0][1], gy[1][1], gs[0][1], gs[1][1],
                                   Bn, T, H, N, D, *[_f64(out[k]) for k in order],
                                   int(threads or default_threads()))
@@ -158,7 +159,8 @@ def naive_grad(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, dy, dfs=None,
         raise RuntimeError(f"ssd_oracle_naive_bwd failed with status {rc}")
     return {"dx": out["dx_re"] + 1j * out["dx_im"], "dA": out["dA_re"] + 1j * out["dA_im"],
             "dB": out["dB_re"] + 1j * out["dB_im"], "dC": out["dC_re"] + 1j * out["dC_im"],
-            "ddt": out["ddt"], "ds0": out["ds0_re"] + 1j * out["ds0_im"]}
+            "ddt": out["ddt"], "ds0": out["ds0_re"] + 1j * out["ds0_im"],
+            "dz": out["dz_re"] + 1j * out["dz_im"]}
 
 
 def naive_grad_inputs(inp, dy, dfs=None, **kw) -> dict:

@@ -1,7 +1,11 @@
 // Host side of the C ABI declared in include/ssdc.h: argument checks,
-// workspace carving and the launch sequence
-//   chunk-state kernel -> state pass -> chunk-scan kernel
-// on the caller's stream. No allocation happens in ssd_complex_fwd_ws.
+// workspace carving and the launch sequences
+//   forward:  chunk-state kernel -> state pass -> chunk-scan kernel
+//             (or the fused kernel)
+//   backward: chunk-state kernel -> state pass -> chunk adjoint -> adjoint
+//             pass -> chunk gradients -> step-size gradients
+// on the caller's stream. No allocation happens in ssd_complex_fwd_ws or
+// ssd_complex_bwd.
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -110,6 +114,12 @@ int setup_device_attrs() {
         return SSDC_ERR_CUDA;
     if (cudaFuncSetAttribute(ssdc::ssdc_simt_chunk_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ssdc::simt_scan_smem()) != cudaSuccess)
+        return SSDC_ERR_CUDA;
+    if (cudaFuncSetAttribute(ssdc::ssdc_bwd_chunk_adjoint, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssdc::bwd_adjoint_smem()) != cudaSuccess)
+        return SSDC_ERR_CUDA;
+    if (cudaFuncSetAttribute(ssdc::ssdc_bwd_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssdc::bwd_chunk_smem()) != cudaSuccess)
         return SSDC_ERR_CUDA;
     g_attr_done[dev].store(1, std::memory_order_release);
     return SSDC_OK;
@@ -327,6 +337,163 @@ int ssd_complex_timing_read(float* ms, int n) {
     for (int i = 0; i < k && i < n; ++i)
         if (cudaEventElapsedTime(&ms[i], g_events[i], g_events[i + 1]) != cudaSuccess) return SSDC_ERR_CUDA;
     return k;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward pass: recompute the chunk states (forward chunk-state kernel and
+// state pass), then the four backward kernels of csrc/ssdc_bwd.cu.
+
+namespace {
+
+struct BwdLayout {
+    size_t S, a, R, fs, r, anchor, total;  // byte offsets (total = size)
+};
+
+size_t pad256(size_t v) { return (v + 255) & ~size_t(255); }
+
+BwdLayout bwd_layout(const ssdc_dims& d, int Q) {
+    const int64_t nc = ssdc::ceil_div64(d.T, Q);
+    const size_t chunks = (size_t)(d.B * d.H * nc);
+    const size_t states = pad256(chunks * 2 * d.N * d.D * sizeof(float));
+    BwdLayout l;
+    l.S = 256;  // after the status word
+    l.a = l.S + states;
+    l.R = l.a + pad256(chunks * 2 * sizeof(float));
+    l.fs = l.R + states;
+    l.r = l.fs + pad256((size_t)(d.B * d.H * d.N * d.D) * 2 * sizeof(float));
+    l.anchor = l.r + pad256((size_t)(d.B * d.H * d.T) * 2 * sizeof(float));
+    l.total = l.anchor + pad256(chunks * 2 * sizeof(double));
+    return l;
+}
+
+int check_bwd_sizes(const ssdc_dims& d, int Q) {
+    const int rc = check_sizes(d, Q);
+    if (rc != SSDC_OK) return rc;
+    return d.precision == SSDC_PREC_FP32 ? SSDC_OK : SSDC_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssd_complex_bwd_workspace_bytes(ssdc_dims dims, int chunk_size) {
+    if (check_bwd_sizes(dims, chunk_size) != SSDC_OK) return 0;
+    return bwd_layout(dims, chunk_size).total;
+}
+
+int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt,
+                    ssdc_cin initial_state, ssdc_cin dy, ssdc_cin d_final_state, ssdc_dims dims,
+                    int chunk_size, ssdc_cout dx, ssdc_cout dA, ssdc_cout dB_t, ssdc_cout dC_t,
+                    float* ddt, ssdc_cout d_initial_state, void* workspace, size_t ws_bytes,
+                    cudaStream_t stream) {
+    int rc = check_bwd_sizes(dims, chunk_size);
+    if (rc != SSDC_OK) return rc;
+    // required pointers; x.im, dy.im and dx.im may be null, the three state pairs both or neither
+    const void* req[] = {x.re, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt, dy.re,
+                         dx.re, dA.re, dA.im, dB_t.re, dB_t.im, dC_t.re, dC_t.im, ddt};
+    for (const void* q : req)
+        if (q == nullptr) return SSDC_ERR_INVALID;
+    const ssdc_cin pairs[] = {initial_state, d_final_state,
+                              ssdc_cin{d_initial_state.re, d_initial_state.im}};
+    for (const ssdc_cin& q : pairs)
+        if ((q.re == nullptr) != (q.im == nullptr) || (q.re != nullptr && q.re == q.im)) return SSDC_ERR_INVALID;
+    const void* opt[] = {x.im, dy.im, dx.im, initial_state.re, initial_state.im, d_final_state.re,
+                         d_final_state.im, d_initial_state.re, d_initial_state.im};
+    for (const void* q : req)
+        if (!aligned16(q)) return SSDC_ERR_ALIGN;
+    for (const void* q : opt)
+        if (!aligned16(q)) return SSDC_ERR_ALIGN;
+    if (x.im == x.re || dy.im == dy.re) return SSDC_ERR_INVALID;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return SSDC_ERR_WORKSPACE;
+    const BwdLayout lay = bwd_layout(dims, chunk_size);
+    if (ws_bytes < lay.total) return SSDC_ERR_WORKSPACE;
+
+    // outputs must not overlap an input, the workspace or each other
+    const int64_t BTH = dims.B * dims.T * dims.H;
+    const int64_t fsn = dims.B * dims.H * dims.N * dims.D;
+    auto rng = [](const void* p, int64_t n) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{lo, p == nullptr ? lo : lo + (uintptr_t)n * sizeof(float)};  // null: empty
+    };
+    const Range in[] = {rng(x.re, BTH * dims.D), rng(x.im, BTH * dims.D), rng(A.re, dims.H),
+                        rng(A.im, dims.H), rng(B_t.re, BTH * dims.N), rng(B_t.im, BTH * dims.N),
+                        rng(C_t.re, BTH * dims.N), rng(C_t.im, BTH * dims.N), rng(dt, BTH),
+                        rng(initial_state.re, fsn), rng(initial_state.im, fsn),
+                        rng(dy.re, BTH * dims.D), rng(dy.im, BTH * dims.D),
+                        rng(d_final_state.re, fsn), rng(d_final_state.im, fsn),
+                        Range{reinterpret_cast<uintptr_t>(workspace),
+                              reinterpret_cast<uintptr_t>(workspace) + ws_bytes}};
+    const Range out[] = {rng(dx.re, BTH * dims.D), rng(dx.im, BTH * dims.D), rng(dA.re, dims.H),
+                         rng(dA.im, dims.H), rng(dB_t.re, BTH * dims.N), rng(dB_t.im, BTH * dims.N),
+                         rng(dC_t.re, BTH * dims.N), rng(dC_t.im, BTH * dims.N), rng(ddt, BTH),
+                         rng(d_initial_state.re, fsn), rng(d_initial_state.im, fsn)};
+    constexpr int kOut = sizeof(out) / sizeof(out[0]);
+    for (const Range& o : out)
+        for (const Range& i : in)
+            if (overlaps(o, i)) return SSDC_ERR_INVALID;
+    for (int i = 0; i < kOut; ++i)
+        for (int j = i + 1; j < kOut; ++j)
+            if (overlaps(out[i], out[j])) return SSDC_ERR_INVALID;
+
+    rc = setup_device_attrs();
+    if (rc != SSDC_OK) return rc;
+
+    char* base = static_cast<char*>(workspace);
+    ssdc::Workspace w;
+    w.status = reinterpret_cast<int*>(base);
+    w.S = reinterpret_cast<float*>(base + lay.S);
+    w.a = reinterpret_cast<float*>(base + lay.a);
+    ssdc::GradWorkspace gw;
+    gw.R = reinterpret_cast<float*>(base + lay.R);
+    gw.r = reinterpret_cast<float*>(base + lay.r);
+    gw.anchor = reinterpret_cast<double*>(base + lay.anchor);
+    float* fs = reinterpret_cast<float*>(base + lay.fs);
+
+    ssdc::GradProblem g;
+    ssdc::Problem& p = g.f;
+    p.x_re = x.re; p.x_im = x.im; p.A_re = A.re; p.A_im = A.im;
+    p.B_re = B_t.re; p.B_im = B_t.im; p.C_re = C_t.re; p.C_im = C_t.im; p.dt = dt;
+    p.s0_re = initial_state.re; p.s0_im = initial_state.im;
+    p.y_re = nullptr; p.y_im = nullptr;  // the forward rows are not needed
+    p.fs_re = fs; p.fs_im = fs + fsn;
+    p.T = dims.T; p.B = (int)dims.B; p.H = (int)dims.H; p.N = (int)dims.N; p.D = (int)dims.D;
+    p.Q = chunk_size;
+    p.nc = ssdc::ceil_div64(dims.T, chunk_size);
+    p.drop_send_chunk = -1;
+    g.dy_re = dy.re; g.dy_im = dy.im;
+    g.dfs_re = d_final_state.re; g.dfs_im = d_final_state.im;
+    g.dx_re = dx.re; g.dx_im = dx.im;
+    g.dA_re = dA.re; g.dA_im = dA.im;
+    g.dB_re = dB_t.re; g.dB_im = dB_t.im; g.dC_re = dC_t.re; g.dC_im = dC_t.im; g.ddt = ddt;
+    g.ds0_re = d_initial_state.re; g.ds0_im = d_initial_state.im;
+
+    (void)cudaGetLastError();  // clear a stale error from unrelated work
+    int launches = 0;
+    if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
+    const dim3 chunk_grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
+    const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
+                         (unsigned)(p.B * p.H));
+    ssdc::ssdc_simt_chunk_state<<<chunk_grid, 256, ssdc::simt_state_smem(), stream>>>(p, w);
+    record_event(++launches, stream);
+    ssdc::ssdc_state_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(p, w);
+    record_event(++launches, stream);
+    ssdc::ssdc_bwd_chunk_adjoint<<<chunk_grid, 256, ssdc::bwd_adjoint_smem(), stream>>>(g, w, gw);
+    record_event(++launches, stream);
+    ssdc::ssdc_adjoint_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(g, w, gw);
+    record_event(++launches, stream);
+    const int nb = (p.Q + 63) / 64;
+    const dim3 bgrid((unsigned)(p.nc * nb), (unsigned)p.H, (unsigned)p.B);
+    ssdc::ssdc_bwd_chunk<<<bgrid, 256, ssdc::bwd_chunk_smem(), stream>>>(g, w, gw);
+    record_event(++launches, stream);
+    ssdc::ssdc_bwd_dt<<<(unsigned)p.H, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);
+    record_event(++launches, stream);
+    if (cudaGetLastError() != cudaSuccess) return SSDC_ERR_CUDA;
+    g_last_launches = launches;
+    if (g_timing) g_timed_launches = launches;
+    return SSDC_OK;
 }
 
 }  // extern "C"

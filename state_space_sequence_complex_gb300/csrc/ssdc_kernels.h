@@ -23,6 +23,39 @@ struct Problem {
     int64_t drop_send_chunk;
 };
 
+// Sizes and device pointers of one backward call: the forward problem (its
+// y is unused; fs points into the backward workspace, where the recomputed
+// final state goes) plus the output gradients and the input gradients.
+struct GradProblem {
+    Problem f;
+    const float *dy_re, *dy_im;    // dy_im may be null: zero
+    const float *dfs_re, *dfs_im;  // both null: zero
+    float *dx_re, *dx_im;          // dx_im may be null: not written
+    float *dA_re, *dA_im;
+    float *dB_re, *dB_im, *dC_re, *dC_im, *ddt;
+    float *ds0_re, *ds0_im;  // both null: not written
+};
+
+// Backward workspace beyond the forward one (S, a, status).
+//   R  [B*H*nc][2][D][N] floats: U_c, replaced in place by R_c, the gradient
+//      of the state leaving chunk c (transposed like S)
+//   r  [B*H][2][T] floats: r_t = <dC_t, C_t> - <dB_t, B_t> of every token
+//   anchor [B*H*nc][2] doubles: <R_c, S_out(c)>, S_out(c) the state leaving chunk c
+struct GradWorkspace {
+    float* R;
+    float* r;
+    double* anchor;
+};
+
+// Backward kernels (exact fp32, SIMT).
+__global__ void ssdc_bwd_chunk_adjoint(GradProblem g, Workspace ws, GradWorkspace gw);
+__global__ void ssdc_adjoint_pass(GradProblem g, Workspace ws, GradWorkspace gw);
+__global__ void ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw);
+__global__ void ssdc_bwd_dt(GradProblem g, Workspace ws, GradWorkspace gw);
+size_t bwd_adjoint_smem();
+size_t bwd_chunk_smem();
+constexpr int kBwdDtThreads = 256;
+
 // SIMT (exact fp32) kernels.
 __global__ void ssdc_simt_chunk_state(Problem p, Workspace ws);
 __global__ void ssdc_simt_chunk_scan(Problem p, Workspace ws);

@@ -30,7 +30,7 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
            "ssd_complex_fwd", "ssd_complex_status", "ssd_complex_strerror",
            "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read",
            "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host",
-           "ssd_complex_fwd_init")
+           "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd")
 
 
 class ssdc_dims(ctypes.Structure):
@@ -87,6 +87,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_fwd_host_scratch_bytes.restype = sz
     lib.ssd_complex_fwd_host.argtypes = common + [vp, sz, vp]
     lib.ssd_complex_fwd_host.restype = ctypes.c_int
+    lib.ssd_complex_bwd_workspace_bytes.argtypes = [ssdc_dims, ctypes.c_int]
+    lib.ssd_complex_bwd_workspace_bytes.restype = sz
+    lib.ssd_complex_bwd.argtypes = ([ssdc_cin] * 4 + [vp] + [ssdc_cin] * 3 + [ssdc_dims, ctypes.c_int]
+                                    + [ssdc_cout] * 4 + [vp, ssdc_cout, vp, sz, vp])
+    lib.ssd_complex_bwd.restype = ctypes.c_int
     lib.ssd_complex_timing_enable.argtypes = [ctypes.c_int]
     lib.ssd_complex_timing_enable.restype = ctypes.c_int
     lib.ssd_complex_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int]
@@ -122,6 +127,15 @@ def _cin(re, im):
 
 def _cout(re, im):
     return ssdc_cout(re.data_ptr(), im.data_ptr())
+
+
+def _opt_in(re, im):
+    """Planar input where either plane may be None (a null pointer)."""
+    return ssdc_cin(None if re is None else re.data_ptr(), None if im is None else im.data_ptr())
+
+
+def _opt_out(re, im):
+    return ssdc_cout(None if re is None else re.data_ptr(), None if im is None else im.data_ptr())
 
 
 def ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
@@ -213,6 +227,147 @@ def ssd_complex_fwd_host(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chu
     if check and rc != SSDC_OK:
         raise SSDCError(rc, "ssd_complex_fwd_host")
     return rc
+
+
+def ssd_complex_bwd_workspace_bytes(d: ssdc_dims, chunk_size: int) -> int:
+    return int(load().ssd_complex_bwd_workspace_bytes(d, int(chunk_size)))
+
+
+def ssd_complex_bwd(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
+                    dy_re, dy_im=None, dfs_re=None, dfs_im=None, s0_re=None, s0_im=None,
+                    dx_re, dx_im=None, dA_re, dA_im, dB_re, dB_im, dC_re, dC_im, ddt,
+                    ds0_re=None, ds0_im=None, workspace, precision="fp32", stream=None,
+                    check=True) -> int:
+    """Call ``ssd_complex_bwd`` on torch CUDA tensors (planar float32): the
+    gradients of every input given ``dy`` (and ``dfs``, the gradient of the
+    final state; None: zero). ``x_im``, ``dy_im`` and ``dx_im`` may be None;
+    ``s0``, ``dfs`` and ``ds0`` are pairs given together or not at all.
+    Returns the status (raises on a non-zero one unless ``check`` is False)."""
+    import torch
+
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    d = dims(Bn, T, H, N, D, precision)
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_bwd(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt),
+        _opt_in(s0_re, s0_im), _opt_in(dy_re, dy_im), _opt_in(dfs_re, dfs_im), d, int(chunk_size),
+        _opt_out(dx_re, dx_im), _cout(dA_re, dA_im), _cout(dB_re, dB_im), _cout(dC_re, dC_im),
+        _ptr(ddt), _opt_out(ds0_re, ds0_im), _ptr(workspace), int(workspace.numel()),
+        ctypes.c_void_p(s.cuda_stream))
+    if check and rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_bwd")
+    return rc
+
+
+class Backward:
+    """Holds the input gradients and the workspace of one problem size, so
+    repeated backward calls allocate nothing. ``__call__`` takes the forward
+    inputs and the output gradients as CUDA tensors and returns a dict of
+    gradients: ``dx_re``, ``dx_im``, ``dA_re``, ``dA_im``, ``dB_re``, ``dB_im``,
+    ``dC_re``, ``dC_im``, ``ddt`` and, with an initial state, ``ds0_re`` and
+    ``ds0_im``."""
+
+    def __init__(self, Bn, T, H, N, D, chunk_size, precision="fp32", device="cuda"):
+        import torch
+
+        self.shape = (Bn, T, H, N, D)
+        self.chunk_size = int(chunk_size)
+        self.precision = precision
+        d = dims(Bn, T, H, N, D, precision)
+        nbytes = ssd_complex_bwd_workspace_bytes(d, chunk_size)
+        if nbytes == 0:
+            raise SSDCError(SSDC_ERR_UNSUPPORTED, "ssd_complex_bwd_workspace_bytes")
+        f32 = dict(dtype=torch.float32, device=device)
+        self.grads = {
+            "dx_re": torch.empty((Bn, T, H, D), **f32), "dx_im": torch.empty((Bn, T, H, D), **f32),
+            "dA_re": torch.empty((H,), **f32), "dA_im": torch.empty((H,), **f32),
+            "dB_re": torch.empty((Bn, T, H, N), **f32), "dB_im": torch.empty((Bn, T, H, N), **f32),
+            "dC_re": torch.empty((Bn, T, H, N), **f32), "dC_im": torch.empty((Bn, T, H, N), **f32),
+            "ddt": torch.empty((Bn, T, H), **f32),
+            "ds0_re": torch.empty((Bn, H, N, D), **f32), "ds0_im": torch.empty((Bn, H, N, D), **f32)}
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, dy_re, dy_im=None,
+                 dfs_re=None, dfs_im=None, s0_re=None, s0_im=None, stream=None):
+        g = self.grads
+        with_s0 = s0_re is not None
+        ssd_complex_bwd(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, self.chunk_size,
+                        dy_re=dy_re, dy_im=dy_im, dfs_re=dfs_re, dfs_im=dfs_im, s0_re=s0_re,
+                        s0_im=s0_im, dx_re=g["dx_re"], dx_im=None if x_im is None else g["dx_im"],
+                        dA_re=g["dA_re"], dA_im=g["dA_im"], dB_re=g["dB_re"], dB_im=g["dB_im"],
+                        dC_re=g["dC_re"], dC_im=g["dC_im"], ddt=g["ddt"],
+                        ds0_re=g["ds0_re"] if with_s0 else None,
+                        ds0_im=g["ds0_im"] if with_s0 else None,
+                        workspace=self.workspace, precision=self.precision, stream=stream)
+        out = {k: v for k, v in g.items() if not k.startswith("ds0") or with_s0}
+        if x_im is None:
+            out.pop("dx_im")
+        return out
+
+
+def _scan_function():
+    """The torch.autograd.Function over the library's forward and backward
+    passes (built on first use so that importing this module needs no torch)."""
+    import torch
+
+    class SSDComplexScan(torch.autograd.Function):
+        """Forward: ``ssd_complex_fwd_ws`` / ``_init``. Backward: ``ssd_complex_bwd``,
+        seeded with the true gradients of all four outputs (zeros where autograd
+        passes None), returning a gradient for every tensor input."""
+
+        @staticmethod
+        def forward(ctx, chunk_size, precision, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt,
+                    s0_re, s0_im):
+            Bn, T, H, D = x_re.shape
+            N = B_re.shape[-1]
+            f = Forward(Bn, T, H, N, D, chunk_size, precision, device=x_re.device)
+            y_re, y_im, fs_re, fs_im = f(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt,
+                                         s0_re=s0_re, s0_im=s0_im)
+            ctx.chunk_size = chunk_size
+            ctx.real_x = x_im is None
+            ctx.with_s0 = s0_re is not None
+            ctx.save_for_backward(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, s0_re, s0_im)
+            return y_re, y_im, fs_re, fs_im
+
+        @staticmethod
+        def backward(ctx, gy_re, gy_im, gfs_re, gfs_im):
+            x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, s0_re, s0_im = ctx.saved_tensors
+            Bn, T, H, D = x_re.shape
+            N = B_re.shape[-1]
+            z = lambda shape: torch.zeros(shape, dtype=torch.float32, device=x_re.device)
+            gy_re = z((Bn, T, H, D)) if gy_re is None else gy_re.contiguous()
+            gy_im = None if gy_im is None else gy_im.contiguous()
+            if gfs_re is None and gfs_im is None:
+                gfs = (None, None)
+            else:
+                gfs = (z((Bn, H, N, D)) if gfs_re is None else gfs_re.contiguous(),
+                       z((Bn, H, N, D)) if gfs_im is None else gfs_im.contiguous())
+            b = Backward(Bn, T, H, N, D, ctx.chunk_size, "fp32", device=x_re.device)
+            g = b(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, gy_re, gy_im, *gfs,
+                  s0_re=s0_re if ctx.with_s0 else None, s0_im=s0_im if ctx.with_s0 else None)
+            return (None, None, g["dx_re"], None if ctx.real_x else g["dx_im"], g["dA_re"],
+                    g["dA_im"], g["dB_re"], g["dB_im"], g["dC_re"], g["dC_im"], g["ddt"],
+                    g["ds0_re"] if ctx.with_s0 else None, g["ds0_im"] if ctx.with_s0 else None)
+
+    return SSDComplexScan
+
+
+_SCAN_FN = None
+
+
+def ssd_complex_scan(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
+                     s0_re=None, s0_im=None, precision="tf32"):
+    """Differentiable complex SSD scan on planar float32 CUDA tensors: returns
+    ``(y_re, y_im, final_state_re, final_state_im)``; ``y_re`` is Re(y). The
+    forward runs at ``precision``; the backward is the library's exact-fp32
+    backward pass. ``x_im`` may be None (a real x); the initial state
+    ``(s0_re, s0_im)`` is optional."""
+    global _SCAN_FN
+    if _SCAN_FN is None:
+        _SCAN_FN = _scan_function()
+    return _SCAN_FN.apply(int(chunk_size), precision, x_re, x_im, A_re, A_im, B_re, B_im, C_re,
+                          C_im, dt, s0_re, s0_im)
 
 
 def ssd_complex_status(workspace, stream=None) -> int:

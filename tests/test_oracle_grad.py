@@ -127,6 +127,22 @@ def test_grad_matches_autograd_of_ssd_matrix():
     ref = dt.grad.numpy()
     assert np.linalg.norm(g["ddt"] - ref) <= 1e-11 * np.linalg.norm(ref)
 
+    # dz: the same loss as a function of the per-token log-decays z_t = softplus(dt_t) A
+    z = (torch.nn.functional.softplus(dt).to(torch.complex128) * A).detach().requires_grad_(True)
+    lam = torch.cumsum(z, dim=1)
+    diff = lam[:, :, None, :] - lam[:, None, :, :]
+    decay = torch.where(causal, torch.exp(torch.where(causal, diff, torch.zeros_like(diff))),
+                        torch.zeros_like(diff))
+    y = torch.einsum("btsh,bshd->bthd", cb.detach() * decay, x.detach())
+    y = y + torch.exp(lam)[..., None] * torch.einsum("bthn,bhnd->bthd", Ct.detach(), s0.detach())
+    last = lam[:, -1, :]
+    dec = torch.exp(last[:, None, :] - lam)
+    st = (torch.exp(last)[..., None, None] * s0.detach()
+          + torch.einsum("bsh,bshn,bshd->bhnd", dec, Bt.detach(), x.detach()))
+    ((gy.conj() * y).real.sum() + (gs.conj() * st).real.sum()).backward()
+    ref = z.grad.numpy()
+    assert np.linalg.norm(g["dz"] - ref) <= 1e-11 * np.linalg.norm(ref)
+
 
 def test_grad_homogeneity_identities():
     Bn, T, H, D, N = 2, 40, 2, 6, 5
