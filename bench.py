@@ -8,6 +8,7 @@ in HBM. Metric: token-heads/s
 each step is timed on its stream with CUDA events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --backward [--workload ...] [--real-x]   (the backward pass)
 
 Under torchrun each rank runs its own independent batch (weak scaling, no
 collective on the data path); rank 0 prints one JSON line.
@@ -52,6 +53,9 @@ def parse():
                          "previous segment's final state (the initial-state entry point)")
     ap.add_argument("--real-x", action="store_true",
                     help="measurement mode: x real (x.im = NULL, only x.re is read), as in the model")
+    ap.add_argument("--backward", action="store_true",
+                    help="measurement mode: time the backward pass (ssd_complex_bwd, exact fp32) "
+                         "on the workload, seeded with random output gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -98,6 +102,23 @@ def fp32_flops_per_unit(w) -> dict:
     N, D, Q = w.N, w.D, w.Q
     return {"chunk_state": 8.0 * N * D, "state_pass": 8.0 * N * D / Q,
             "chunk_scan": 4.0 * (Q + 1) * (N + D) + 8.0 * N * D}
+
+
+def bwd_flops_per_unit(w) -> dict:
+    """Algorithmic real flops per token-head of each launch of the backward pass (causal
+    triangle, every product counted once). Recomputed chunk states: 8 N D, state pass
+    8 N D / Q; chunk adjoint U = C'^H dY: 8 N D; reverse pass: 8 N D / Q; chunk gradients:
+    per causal pair C B^T, P^H dY, dY x^H, V^T conj(C) and V conj(B) (24 N + 16 D), i.e.
+    (Q+1)(12 N + 8 D) per token, plus the three state terms (24 N D); step-size gradients:
+    about 12 per token."""
+    N, D, Q = w.N, w.D, w.Q
+    return {"chunk_state": 8.0 * N * D, "state_pass": 8.0 * N * D / Q,
+            "chunk_adjoint": 8.0 * N * D, "adjoint_pass": 8.0 * N * D / Q,
+            "bwd_chunk": (Q + 1) * (12.0 * N + 8.0 * D) + 24.0 * N * D + 16.0 * N + 8.0 * N * D / Q,
+            "bwd_dt": 12.0}
+
+
+BWD_NAMES = ["chunk_state", "state_pass", "chunk_adjoint", "adjoint_pass", "bwd_chunk", "bwd_dt"]
 
 
 def bf16_peak_tflops() -> float:
@@ -253,6 +274,136 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+def device_layer_inputs(w, layer, dev, g):
+    """The inputs of one layer of `w` drawn on the device (torch generator seeded with
+    seed + layer) from the distributions of `inputs`: x, A, B_t, C_t planes and dt."""
+    import torch
+    g.manual_seed(w.seed + layer)
+    Bn, T, H, D, N = w.B, w.T, w.H, w.D, w.N
+    s = math.sqrt(0.5)
+    A_re = torch.empty(H, device=dev).uniform_(w.re_lo, w.re_hi, generator=g)
+    sign = torch.where(torch.rand(H, device=dev, generator=g) < 0.5, -1.0, 1.0)
+    A_im = torch.empty(H, device=dev).uniform_(0.35, 2.20, generator=g) * sign
+    dt = torch.randn(Bn, T, H, device=dev, generator=g) * w.dt_std + w.dt_mean
+    cp = lambda F: [torch.randn(Bn, T, H, F, device=dev, generator=g) * s for _ in range(2)]
+    (x_re, x_im), (B_re, B_im), (C_re, C_im) = cp(D), cp(N), cp(N)
+    return [x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt]
+
+
+def backward_workload(args, w):
+    """Measurement mode for the backward pass: one step = ssd_complex_bwd over every layer
+    of the workload (inputs and output gradients drawn on the device), L2 flushed before
+    each step. With --real-x the model's case: x real, a loss of Re(y) alone (dy.im null)
+    and no final-state gradient."""
+    import torch
+    from state_space_sequence_complex_gb300 import build, ssdc
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build.build()
+    ssdc.load()
+    Q = args.chunk or w.Q
+    g = torch.Generator(device=dev)
+    s = math.sqrt(0.5)
+    layers = []
+    for i in range(w.layers):
+        L = device_layer_inputs(w, i, dev, g)
+        dy = [torch.randn(w.B, w.T, w.H, w.D, device=dev, generator=g) * s for _ in range(2)]
+        dfs = [torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=g) * s for _ in range(2)]
+        if args.real_x:
+            L[1], dy[1], dfs = None, None, [None, None]
+        layers.append(L + dy + dfs)
+    b = ssdc.Backward(w.B, w.T, w.H, w.N, w.D, Q, "fp32", device=dev)
+    run = lambda: [b(*L) for L in layers]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(max(args.warmup, 3)):
+        flush.fill_(float(i))
+        run()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.1)
+    ev = []
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st = ssdc.ssd_complex_status(b.workspace)
+    if st != ssdc.SSDC_OK:
+        raise SystemExit(f"device status after timed steps: {ssdc.strerror(st)}")
+    ms = sum(a.elapsed_time(e) for a, e in ev) / len(ev)
+    ssdc.timing_enable(True)
+    per_kernel = []
+    for k in range(min(args.steps, 50)):
+        flush.fill_(float(k))
+        for L in layers:
+            b(*L)
+            per_kernel.append(ssdc.timing_read())
+    ssdc.timing_enable(False)
+    nk = min(len(p) for p in per_kernel)
+    kmeans = [sum(p[i] for p in per_kernel) / len(per_kernel) for i in range(nk)]
+    names = BWD_NAMES if nk == len(BWD_NAMES) else [f"launch{i}" for i in range(nk)]
+    top = int(np.argmax(kmeans))
+    wq = w.with_(Q=Q)
+    fl_unit = bwd_flops_per_unit(wq)
+    fl = fl_unit.get(names[top], 0.0) * w.token_heads
+    alu_peak, alu_kind = fp32_alu_peak_tflops(dev.index)
+    tf = fl / (kmeans[top] / 1000.0) / 1e12
+    # minimum HBM bytes per token-head: x, dy, dx (8 D each, 4 D when real), B_t, C_t, dB_t,
+    # dC_t (8 N each), dt and ddt (4 each)
+    xb = 4.0 if args.real_x else 8.0
+    bytes_unit = 3 * xb * w.D + 32.0 * w.N + 8.0
+    units = w.token_heads * w.layers
+    cpu = None
+    if w.name == inputs.LAYER.name and Q == w.Q and not args.no_cpu_baseline and not args.real_x:
+        cpu = run_oracle_grad_baseline(w)
+    line = {
+        "metric": "complex-SSD bwd token·heads/s (exact fp32 gradients of every input)",
+        "value": units / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic, drawn on the device per layer",
+        "config": {"workload": f"{w.name} Q{Q} backward" + (", real x, Re(y) loss" if args.real_x else ""),
+                   "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N, "chunk_size": Q,
+                   "layers": w.layers, "real_x": bool(args.real_x), "precision": "fp32",
+                   "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)"},
+        "roofline": {"bound": "alu", "kernel": names[top], "achieved": tf, "peak": alu_peak,
+                     "peak_kind": alu_kind, "unit": "TFLOP/s", "frac": tf / alu_peak, "traffic": None,
+                     "algorithmic_flops_per_launch": fl,
+                     "step_alu_frac": sum(fl_unit.values()) * units / (ms / 1000.0) / 1e12 / alu_peak,
+                     "hbm_step_frac": bytes_unit * units / (ms / 1000.0) / 1e9 / peaks()[0],
+                     "kernel_ms": {n: m for n, m in zip(names, kmeans)}},
+        "cpu_baseline": cpu,
+        "e2e": None,
+        "gpu_launches": nk * w.layers * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_oracle_grad_baseline(w, max_seconds=12.0, max_reps=100):
+    """Time the gradient oracle, as it stands, on the full workload, repeated."""
+    from oracle import naive_grad_inputs
+    from oracle.ssd_oracle import default_threads
+    inp = inputs.generate(w)
+    og = inputs.output_grads(w.B, w.T, w.H, w.D, w.N, seed=w.seed + 1000)
+    dy = og.dy_re + 1j * og.dy_im
+    dfs = og.dfs_re + 1j * og.dfs_im
+    cores = default_threads()
+    reps, t_total = 0, 0.0
+    while reps < max_reps and t_total < max_seconds:
+        t0 = time.perf_counter()
+        naive_grad_inputs(inp, dy, dfs, threads=cores)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": w.token_heads * reps / t_total, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"full workload ({w.name}) backward x {reps} passes, {t_total:.1f} s"}
+
+
 def other_workload(args, w):
     """Measurement mode for the training-batch, chunk-sweep and long-memory workloads: inputs
     drawn on the device from the same distributions (torch generator seeded per layer), one
@@ -269,16 +420,7 @@ def other_workload(args, w):
     g = torch.Generator(device=dev)
 
     def layer_inputs(layer):
-        g.manual_seed(w.seed + layer)
-        Bn, T, H, D, N = w.B, w.T, w.H, w.D, w.N
-        s = math.sqrt(0.5)
-        A_re = torch.empty(H, device=dev).uniform_(w.re_lo, w.re_hi, generator=g)
-        sign = torch.where(torch.rand(H, device=dev, generator=g) < 0.5, -1.0, 1.0)
-        A_im = torch.empty(H, device=dev).uniform_(0.35, 2.20, generator=g) * sign
-        dt = torch.randn(Bn, T, H, device=dev, generator=g) * w.dt_std + w.dt_mean
-        cp = lambda F: [torch.randn(Bn, T, H, F, device=dev, generator=g) * s for _ in range(2)]
-        (x_re, x_im), (B_re, B_im), (C_re, C_im) = cp(D), cp(N), cp(N)
-        return [x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt]
+        return device_layer_inputs(w, layer, dev, g)
 
     K = max(1, args.segments)
     if w.T % K != 0:
@@ -377,6 +519,11 @@ def other_workload(args, w):
 
 def main():
     args = parse()
+    if args.backward:
+        if args.impl == "reference" or args.gpus != 1 or args.segments > 1:
+            raise SystemExit("the backward measurement runs on one GPU with --impl ours, unsegmented")
+        backward_workload(args, inputs.ALL[args.workload])
+        return
     if args.workload != "layer" or args.segments > 1 or args.real_x:
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
