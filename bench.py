@@ -106,19 +106,18 @@ def fp32_flops_per_unit(w) -> dict:
 
 def bwd_flops_per_unit(w) -> dict:
     """Algorithmic real flops per token-head of each launch of the backward pass (causal
-    triangle, every product counted once). Recomputed chunk states: 8 N D, state pass
-    8 N D / Q; chunk adjoint U = C'^H dY: 8 N D; reverse pass: 8 N D / Q; chunk gradients:
-    per causal pair C B^T, P^H dY, dY x^H, V^T conj(C) and V conj(B) (24 N + 16 D), i.e.
-    (Q+1)(12 N + 8 D) per token, plus the three state terms (24 N D); step-size gradients:
-    about 12 per token."""
+    triangle, every product counted once). Chunk states: the forward's S_loc = B^T (dec o x)
+    (recomputed) and U = C'^H dY, 8 N D each; the two chunk recurrences: 8 N D / Q each;
+    chunk gradients: per causal pair C B^T, P^H dY, dY x^H, V^T conj(C) and V conj(B)
+    (24 N + 16 D), i.e. (Q+1)(12 N + 8 D) per token, plus the three state terms (24 N D);
+    step-size gradients: about 12 per token; the per-head sum of dA: 2 per chunk."""
     N, D, Q = w.N, w.D, w.Q
-    return {"chunk_state": 8.0 * N * D, "state_pass": 8.0 * N * D / Q,
-            "chunk_adjoint": 8.0 * N * D, "adjoint_pass": 8.0 * N * D / Q,
+    return {"chunk_states": 16.0 * N * D, "passes": 16.0 * N * D / Q,
             "bwd_chunk": (Q + 1) * (12.0 * N + 8.0 * D) + 24.0 * N * D + 16.0 * N + 8.0 * N * D / Q,
-            "bwd_dt": 12.0}
+            "bwd_dt": 12.0, "bwd_dA": 2.0 / Q}
 
 
-BWD_NAMES = ["chunk_state", "state_pass", "chunk_adjoint", "adjoint_pass", "bwd_chunk", "bwd_dt"]
+BWD_NAMES = ["chunk_states", "passes", "bwd_chunk", "bwd_dt", "bwd_dA"]
 
 
 def bf16_peak_tflops() -> float:

@@ -27,13 +27,15 @@
 // chunk's last token. Anchoring every chunk keeps each sum within Q tokens,
 // so fp32 rounding in r_t does not accumulate along the sequence.
 //
-// Kernels, in launch order after the forward chunk-state kernel and state
-// pass have put S_in[c], a_c and the final state in the workspace:
-//   ssdc_bwd_chunk_adjoint  grid (nc, H, B)            U_c into the R slots
-//   ssdc_adjoint_pass       grid (ceil(N*D/256), B*H)  R_c in place, d_initial_state
-//   ssdc_bwd_chunk          grid (nc * ceil(Q/64), H, B) dx, dB_t, dC_t, r_t,
-//                                                       <R_c, S_out(c)>
-//   ssdc_bwd_dt             grid (H)                   dz -> ddt, dA
+// Kernels, in launch order:
+//   ssdc_bwd_chunk_states  grid (nc, H, B)             S_loc[c], a_c (the forward's,
+//                                                      recomputed) and U_c per chunk
+//   ssdc_bwd_passes        grid (2 ceil(N*D/256), B*H) S_in[c] and the final state;
+//                                                      R_c and d_initial_state
+//   ssdc_bwd_chunk         grid (nc * ceil(Q/64), H, B), 512 threads: dx, dB_t, dC_t, r_t,
+//                                                      <R_c, S_out(c)>
+//   ssdc_bwd_dt            grid (B*H*nc / 8)           dz -> ddt and each chunk's share of dA
+//   ssdc_bwd_dA            grid (H)                    dA
 #include <cuda_runtime.h>
 
 #include "ssdc_common.cuh"
@@ -45,57 +47,129 @@ constexpr int kBwdThreads = 256;
 constexpr int kRows = 64;  // token rows per shared-memory block
 constexpr int kCols = 64;  // max N, D
 
-struct Plane2 {
-    float re[kRows][kCols + 1];  // one float of padding against bank conflicts
-    float im[kRows][kCols + 1];
+// A tile of 64 rows x up to 64 complex values, real and imaginary parts
+// interleaved so that one 64-bit shared load fetches a value. Rows are 65
+// values long: 16 lanes reading one column of 16 different rows then touch
+// all 32 banks once.
+struct CTile {
+    float2 v[kRows][kCols + 1];
 };
+
+// acc += a * b, acc += a * conj(b), acc += conj(a) * b (complex, fp32 FMAs)
+__device__ __forceinline__ void cmac(float2& acc, float2 a, float2 b) {
+    acc.x = fmaf(a.x, b.x, fmaf(-a.y, b.y, acc.x));
+    acc.y = fmaf(a.x, b.y, fmaf(a.y, b.x, acc.y));
+}
+__device__ __forceinline__ void cmac_cb(float2& acc, float2 a, float2 b) {
+    acc.x = fmaf(a.x, b.x, fmaf(a.y, b.y, acc.x));
+    acc.y = fmaf(a.y, b.x, fmaf(-a.x, b.y, acc.y));
+}
+__device__ __forceinline__ void cmac_ca(float2& acc, float2 a, float2 b) {
+    acc.x = fmaf(a.x, b.x, fmaf(a.y, b.y, acc.x));
+    acc.y = fmaf(a.x, b.y, fmaf(-a.y, b.x, acc.y));
+}
+__device__ __forceinline__ float2 conjf2(float2 a) { return make_float2(a.x, -a.y); }
 
 __device__ __forceinline__ int chunk_valid(const Problem& p, int64_t t0) {
     return (int)(p.T - t0 < (int64_t)p.Q ? p.T - t0 : (int64_t)p.Q);
 }
 
 // Rows [r0, r0 + 64) of one chunk of a (B, T, H, F) plane pair into dst,
-// zero past the chunk's valid tokens (`valid`), past F and past the chunk.
+// zero past the chunk's valid tokens (`valid`) and past F. F is a multiple
+// of 8 and the planes are 16-byte aligned, so every row is read as float4s.
 // im may be null (a zero imaginary plane).
-__device__ __forceinline__ void load_rows(Plane2& dst, const float* __restrict__ re,
+template <int NT = kBwdThreads>
+__device__ __forceinline__ void load_rows(CTile& dst, const float* __restrict__ re,
                                           const float* __restrict__ im, int64_t bt0, int H, int h,
                                           int F, int r0, int valid) {
-    for (int e = threadIdx.x; e < kRows * kCols; e += kBwdThreads) {
-        const int r = e / kCols, f = e % kCols;
-        float vr = 0.0f, vi = 0.0f;
+    constexpr int kQuads = kRows * kCols / 4;  // float4 groups of the tile
+#pragma unroll
+    for (int it = 0; it < kQuads / NT; ++it) {
+        const int e = threadIdx.x + it * NT;
+        const int r = e / (kCols / 4), f = 4 * (e % (kCols / 4));
+        float4 vr = make_float4(0.0f, 0.0f, 0.0f, 0.0f), vi = vr;
         if (r0 + r < valid && f < F) {
             const int64_t o = ((bt0 + r0 + r) * H + h) * (int64_t)F + f;
-            vr = re[o];
-            vi = im != nullptr ? im[o] : 0.0f;
+            vr = __ldg(reinterpret_cast<const float4*>(re + o));
+            if (im != nullptr) vi = __ldg(reinterpret_cast<const float4*>(im + o));
         }
-        dst.re[r][f] = vr;
-        dst.im[r][f] = vi;
+        dst.v[r][f] = make_float2(vr.x, vi.x);
+        dst.v[r][f + 1] = make_float2(vr.y, vi.y);
+        dst.v[r][f + 2] = make_float2(vr.z, vi.z);
+        dst.v[r][f + 3] = make_float2(vr.w, vi.w);
+    }
+}
+
+// A per-chunk (D, N) state slot [2][D][N], fetched into registers (this
+// thread's share) and later stored into a tile as dst[d][n].
+template <int NT>
+struct StateRegs {
+    float4 re[kRows * kCols / 4 / NT], im[kRows * kCols / 4 / NT];
+};
+
+template <int NT>
+__device__ __forceinline__ void fetch_state(StateRegs<NT>& q, const float* __restrict__ slot, int D, int N) {
+    const float* si = slot + (int64_t)D * N;
+#pragma unroll
+    for (int it = 0; it < kRows * kCols / 4 / NT; ++it) {
+        const int e = threadIdx.x + it * NT;
+        const int d = e / (kCols / 4), n = 4 * (e % (kCols / 4));
+        q.re[it] = q.im[it] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (d < D && n < N) {
+            q.re[it] = __ldcg(reinterpret_cast<const float4*>(slot + d * N + n));
+            q.im[it] = __ldcg(reinterpret_cast<const float4*>(si + d * N + n));
+        }
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void store_state(CTile& dst, const StateRegs<NT>& q) {
+#pragma unroll
+    for (int it = 0; it < kRows * kCols / 4 / NT; ++it) {
+        const int e = threadIdx.x + it * NT;
+        const int d = e / (kCols / 4), n = 4 * (e % (kCols / 4));
+        dst.v[d][n] = make_float2(q.re[it].x, q.im[it].x);
+        dst.v[d][n + 1] = make_float2(q.re[it].y, q.im[it].y);
+        dst.v[d][n + 2] = make_float2(q.re[it].z, q.im[it].z);
+        dst.v[d][n + 3] = make_float2(q.re[it].w, q.im[it].w);
     }
 }
 
 // A per-chunk (D, N) state slot [2][D][N] into dst as dst[d][n].
-__device__ __forceinline__ void load_state(Plane2& dst, const float* __restrict__ slot, int D, int N) {
+template <int NT = kBwdThreads>
+__device__ __forceinline__ void load_state(CTile& dst, const float* __restrict__ slot, int D, int N) {
+    constexpr int kQuads = kRows * kCols / 4;
     const float* si = slot + (int64_t)D * N;
-    for (int e = threadIdx.x; e < kRows * kCols; e += kBwdThreads) {
-        const int d = e / kCols, n = e % kCols;
-        const bool ok = d < D && n < N;
-        dst.re[d][n] = ok ? slot[d * N + n] : 0.0f;
-        dst.im[d][n] = ok ? si[d * N + n] : 0.0f;
+#pragma unroll
+    for (int it = 0; it < kQuads / NT; ++it) {
+        const int e = threadIdx.x + it * NT;
+        const int d = e / (kCols / 4), n = 4 * (e % (kCols / 4));
+        float4 vr = make_float4(0.0f, 0.0f, 0.0f, 0.0f), vi = vr;
+        if (d < D && n < N) {
+            vr = __ldcg(reinterpret_cast<const float4*>(slot + d * N + n));
+            vi = __ldcg(reinterpret_cast<const float4*>(si + d * N + n));
+        }
+        dst.v[d][n] = make_float2(vr.x, vi.x);
+        dst.v[d][n + 1] = make_float2(vr.y, vi.y);
+        dst.v[d][n + 2] = make_float2(vr.z, vi.z);
+        dst.v[d][n + 3] = make_float2(vr.w, vi.w);
     }
 }
 
 // ---------------------------------------------------------------------------
-// U_c^T[d, n] = sum_l dY[l, d] conj(C'[l, n]), C'[l] = exp(Acs[l]) C[l].
+// Per chunk: the forward's local state S_loc^T[d, n] = sum_s x[s, d] dec[s] B[s, n]
+// and a_c = exp(Acs[Q-1]) (recomputed), then U_c^T[d, n] = sum_l dY[l, d]
+// conj(C'[l, n]), C'[l] = exp(Acs[l]) C[l]. Two tiles, reused by the two halves.
 
-struct AdjSmem {
+struct StatesSmem {
     Acs acs[kMaxQ];
-    Plane2 dy, cc;  // dY rows; C' rows
+    CTile a, b;  // x and dec o B; then dY and C'
 };
 
 __global__ void __launch_bounds__(kBwdThreads)
-ssdc_bwd_chunk_adjoint(GradProblem g, Workspace ws, GradWorkspace gw) {
+ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    AdjSmem& sm = *reinterpret_cast<AdjSmem*>(smem_raw);
+    StatesSmem& sm = *reinterpret_cast<StatesSmem*>(smem_raw);
     const Problem& p = g.f;
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int Q = p.Q, N = p.N, D = p.D, H = p.H;
@@ -103,116 +177,114 @@ ssdc_bwd_chunk_adjoint(GradProblem g, Workspace ws, GradWorkspace gw) {
     const int valid = chunk_valid(p, t0);
     const int tid = threadIdx.x;
     const int64_t bt0 = (int64_t)b * p.T + t0;
+    const int64_t chunk = ((int64_t)b * H + h) * p.nc + c;
+    if (c == 0 && h == 0 && b == 0 && tid == 0) *ws.status = SSDC_OK;
 
     if (tid < 32)
         chunk_cumsum_warp(p.dt + bt0 * H + h, H, valid, Q, p.A_re[h], p.A_im[h], sm.acs);
 
     const int dg = tid / 16, ng = tid % 16;  // micro-tile: d = dg + 16 i, n = ng + 16 j
-    float ur[4][4], ui[4][4];
+    for (int half = 0; half < 2; ++half) {
+        // half 0: acc = sum_s x[s] (outer) dec[s] B[s];  half 1: acc = sum_l dY[l] (outer) conj(C'[l])
+        float2 acc[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ur[i][j] = ui[i][j] = 0.0f;
-
-    for (int r0 = 0; r0 < Q; r0 += kRows) {
-        const int rows = min(kRows, Q - r0);
-        __syncthreads();  // the cumsum is written; the previous block's reads are done
-        load_rows(sm.dy, g.dy_re, g.dy_im, bt0, H, h, D, r0, valid);
-        load_rows(sm.cc, p.C_re, p.C_im, bt0, H, h, N, r0, valid);
-        __syncthreads();
-        for (int e = tid; e < rows * kCols; e += kBwdThreads) {
-            const int r = e / kCols, n = e % kCols;
-            if (r0 + r < valid && n < N) {
-                const float2 v = cmul(make_float2(sm.cc.re[r][n], sm.cc.im[r][n]),
-                                      cexp_exact(acs_value(sm.acs[r0 + r])));
-                sm.cc.re[r][n] = v.x;
-                sm.cc.im[r][n] = v.y;
+            for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+        for (int r0 = 0; r0 < Q; r0 += kRows) {
+            const int rows = min(kRows, Q - r0);
+            __syncthreads();  // the cumsum is written; the previous tiles' reads are done
+            if (half == 0) {
+                load_rows(sm.a, p.x_re, p.x_im, bt0, H, h, D, r0, valid);
+                load_rows(sm.b, p.B_re, p.B_im, bt0, H, h, N, r0, valid);
+            } else {
+                load_rows(sm.a, g.dy_re, g.dy_im, bt0, H, h, D, r0, valid);
+                load_rows(sm.b, p.C_re, p.C_im, bt0, H, h, N, r0, valid);
+            }
+            __syncthreads();
+            const Acs last = sm.acs[Q - 1];
+            for (int e = tid; e < rows * kCols; e += kBwdThreads) {
+                const int r = e / kCols, n = e % kCols;
+                if (r0 + r < valid && n < N) {
+                    // dec[s] = exp(Acs[Q-1] - Acs[s]) or exp(Acs[l]), conjugated for C'
+                    const float2 f = half == 0 ? cexp_exact(acs_diff(last, sm.acs[r0 + r]))
+                                               : conjf2(cexp_exact(acs_value(sm.acs[r0 + r])));
+                    const float2 v = sm.b.v[r][n];
+                    sm.b.v[r][n] = half == 0 ? cmul(f, v) : cmul(f, conjf2(v));
+                }
+            }
+            __syncthreads();
+            for (int l = 0; l < rows; ++l) {
+                float2 u[4], w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) u[i] = sm.a.v[l][dg + 16 * i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) w[j] = sm.b.v[l][ng + 16 * j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cmac(acc[i][j], u[i], w[j]);
             }
         }
-        __syncthreads();
-        for (int l = 0; l < rows; ++l) {
-            float yr[4], yi[4], cr[4], ci[4];
+        float* out = (half == 0 ? ws.S : gw.R) + chunk * 2 * D * N;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                yr[i] = sm.dy.re[l][dg + 16 * i];
-                yi[i] = sm.dy.im[l][dg + 16 * i];
-            }
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                cr[j] = sm.cc.re[l][ng + 16 * j];
-                ci[j] = sm.cc.im[l][ng + 16 * j];
-            }
-            // dY conj(C')
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    ur[i][j] = fmaf(yr[i], cr[j], fmaf(yi[i], ci[j], ur[i][j]));
-                    ui[i][j] = fmaf(yi[i], cr[j], fmaf(-yr[i], ci[j], ui[i][j]));
+                const int d = dg + 16 * i, n = ng + 16 * j;
+                if (d < D && n < N) {
+                    out[d * N + n] = acc[i][j].x;
+                    out[(int64_t)D * N + d * N + n] = acc[i][j].y;
                 }
-        }
-    }
-
-    const int64_t chunk = ((int64_t)b * H + h) * p.nc + c;
-    float* Rr = gw.R + chunk * 2 * D * N;
-    float* Ri = Rr + (int64_t)D * N;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int d = dg + 16 * i, n = ng + 16 * j;
-            if (d < D && n < N) {
-                Rr[d * N + n] = ur[i][j];
-                Ri[d * N + n] = ui[i][j];
             }
-        }
+    }
+    if (tid == 0) {
+        const float2 a = cexp_exact(acs_value(sm.acs[Q - 1]));
+        ws.a[2 * chunk] = a.x;
+        ws.a[2 * chunk + 1] = a.y;
+    }
 }
 
 // ---------------------------------------------------------------------------
-// Reverse state pass: one thread per complex (d, n) lane of one (b, h)
-// sequence walks the chunks from last to first, replacing U_c in its slot by
-// R_c (the gradient of the state leaving chunk c).
+// The two chunk recurrences, one thread per complex (d, n) lane of one (b, h)
+// sequence; the first half of the grid's x blocks runs the forward one, the
+// second half the backward one, concurrently. Forwards, S_loc[c] in its slot
+// becomes S_in[c] (the forward's state pass, from the initial state) and the
+// final state is written; backwards, U_c in its slot becomes R_c (the
+// gradient of the state leaving chunk c) and conj(a_0) R_0 + U_0 is the
+// initial-state gradient. The loads do not depend on the chain, so they are
+// issued a group of chunks ahead.
 
-constexpr int kAdjAhead = 8;
+constexpr int kPassAhead = 8;
 
-__global__ void __launch_bounds__(kPassThreads)
-ssdc_adjoint_pass(GradProblem g, Workspace ws, GradWorkspace gw) {
-    const Problem& p = g.f;
-    const int64_t bh = blockIdx.y;
-    const int ND = p.N * p.D;
-    const int j = blockIdx.x * kPassThreads + threadIdx.x;  // lane = d * N + n
-    if (j >= ND) return;
-    const int64_t nc = p.nc;
+// backwards: R_{c-1} = conj(a_c) R_c + U_c, lane j of sequence bh
+__device__ __forceinline__ void adjoint_chain(const GradProblem& g, const GradWorkspace& gw,
+                                              const float* a, int64_t bh, int64_t nc, int ND, int j,
+                                              int64_t o) {
     float* R = gw.R + bh * nc * 2 * ND + j;
-    const float* a = ws.a + bh * nc * 2;
-    const int d = j / p.N, n = j % p.N;
-    const int64_t o = (bh * p.N + n) * p.D + d;  // (b, h, n, d) of the state gradients
     float rr = 0.0f, ri = 0.0f;
     if (g.dfs_re != nullptr) {
         rr = g.dfs_re[o];
         ri = g.dfs_im[o];
     }
-    for (int64_t c1 = nc - 1; c1 >= 0; c1 -= kAdjAhead) {
-        float ur[kAdjAhead], ui[kAdjAhead], ar[kAdjAhead], ai[kAdjAhead];
+    for (int64_t c1 = nc - 1; c1 >= 0; c1 -= kPassAhead) {
+        float ur[kPassAhead], ui[kPassAhead], ar[kPassAhead], ai[kPassAhead];
 #pragma unroll
-        for (int k = 0; k < kAdjAhead; ++k) {
+        for (int k = 0; k < kPassAhead; ++k) {
             const int64_t c = c1 - k;
             if (c >= 0) {
-                const float* s = R + c * 2 * ND;
-                ur[k] = __ldcg(s);
-                ui[k] = __ldcg(s + ND);
+                ur[k] = __ldcg(R + c * 2 * ND);
+                ui[k] = __ldcg(R + c * 2 * ND + ND);
                 ar[k] = __ldg(a + 2 * c);
                 ai[k] = __ldg(a + 2 * c + 1);
             }
         }
 #pragma unroll
-        for (int k = 0; k < kAdjAhead; ++k) {
+        for (int k = 0; k < kPassAhead; ++k) {
             const int64_t c = c1 - k;
             if (c >= 0) {
-                float* s = R + c * 2 * ND;
-                __stcg(s, rr);
-                __stcg(s + ND, ri);
-                // conj(a_c) R_c + U_c
+                __stcg(R + c * 2 * ND, rr);
+                __stcg(R + c * 2 * ND + ND, ri);
                 const float nr = fmaf(ar[k], rr, fmaf(ai[k], ri, ur[k]));
                 const float ni = fmaf(ar[k], ri, fmaf(-ai[k], rr, ui[k]));
                 rr = nr;
@@ -226,30 +298,90 @@ ssdc_adjoint_pass(GradProblem g, Workspace ws, GradWorkspace gw) {
     }
 }
 
+__global__ void __launch_bounds__(kPassThreads)
+ssdc_bwd_passes(GradProblem g, Workspace ws, GradWorkspace gw) {
+    const Problem& p = g.f;
+    const int64_t bh = blockIdx.y;
+    const int ND = p.N * p.D;
+    const int half_blocks = (ND + kPassThreads - 1) / kPassThreads;
+    const bool backwards = (int)blockIdx.x >= half_blocks;
+    const int j = (blockIdx.x - (backwards ? half_blocks : 0)) * kPassThreads + threadIdx.x;  // d * N + n
+    if (j >= ND) return;
+    const int64_t nc = p.nc;
+    const float* a = ws.a + bh * nc * 2;
+    const int d = j / p.N, n = j % p.N;
+    const int64_t o = (bh * p.N + n) * p.D + d;  // (b, h, n, d) of the state arrays
+    if (backwards) {
+        adjoint_chain(g, gw, a, bh, nc, ND, j, o);
+        return;
+    }
+
+    // forwards: S_in[c+1] = a_c S_in[c] + S_loc[c]
+    float* S = ws.S + bh * nc * 2 * ND + j;
+    float sr = 0.0f, si = 0.0f;
+    if (p.s0_re != nullptr) {
+        sr = p.s0_re[o];
+        si = p.s0_im[o];
+    }
+    for (int64_t c0 = 0; c0 < nc; c0 += kPassAhead) {
+        float lr[kPassAhead], li[kPassAhead], ar[kPassAhead], ai[kPassAhead];
+#pragma unroll
+        for (int k = 0; k < kPassAhead; ++k)
+            if (c0 + k < nc) {
+                lr[k] = __ldcg(S + (c0 + k) * 2 * ND);
+                li[k] = __ldcg(S + (c0 + k) * 2 * ND + ND);
+                ar[k] = __ldg(a + 2 * (c0 + k));
+                ai[k] = __ldg(a + 2 * (c0 + k) + 1);
+            }
+#pragma unroll
+        for (int k = 0; k < kPassAhead; ++k)
+            if (c0 + k < nc) {
+                __stcg(S + (c0 + k) * 2 * ND, sr);
+                __stcg(S + (c0 + k) * 2 * ND + ND, si);
+                const float nr = fmaf(ar[k], sr, fmaf(-ai[k], si, lr[k]));
+                const float ni = fmaf(ar[k], si, fmaf(ai[k], sr, li[k]));
+                sr = nr;
+                si = ni;
+            }
+    }
+    p.fs_re[o] = sr;
+    p.fs_im[o] = si;
+}
+
 // ---------------------------------------------------------------------------
 // dx, dB_t, dC_t and r_t for the 64 token rows of one block `ib` of a chunk.
 //   part 1 (rows l of block ib): dX and dB over the token blocks jb >= ib,
 //          then the R_c terms;
 //   part 2 (rows t of block ib): dC over the blocks jb <= ib, then the S_in
 //          term, and r_t.
+// A chunk of one block (Q <= 64) has a single block pair: part 2 then reuses
+// part 1's tiles (C, dY, B) and V instead of loading and forming them again.
+// 512 threads: warp w owns the 4 rows 4w .. 4w+3 of every 64 x 64 result and
+// lane c its columns c and c + 32, so on the diagonal block pair, where P and
+// V vanish above the diagonal, a warp's row sums start (or stop) at its rows.
+
+constexpr int kChunkThreads = kBwdChunkThreads;
+constexpr int kChunkWarps = kChunkThreads / 32;
 
 struct BwdSmem {
     Acs acs[kMaxQ];
-    Plane2 own1, own2;  // part 1: B, x of block ib;   part 2: C, dY of block ib
-    Plane2 str1, str2;  // part 1: C, dY of block jb;  part 2: B, x of block jb
-    Plane2 pv;          // P or V of the block pair, [t][l]
-    Plane2 st;          // part 1: R_c^T [d][n];       part 2: S_in^T [d][n]
-    float nbb_re[kRows], nbb_im[kRows];  // -<dB_l, B_l> of the rows of block ib
-    double anc[kBwdThreads / 32][2];     // per-warp partial sums of <R_c, S_out(c)>
+    CTile own1, own2;  // part 1: B, x of block ib;   part 2: C, dY of block ib
+    CTile str1, str2;  // part 1: C, dY of block jb;  part 2: B, x of block jb
+    CTile pv;          // P or V of the block pair, [t][l]
+    CTile st;          // part 1: R_c^T [d][n];       part 2: S_in^T [d][n]
+    float2 nbb[kRows];                // -<dB_l, B_l> of the rows of block ib
+    double anc[kChunkWarps][2];       // per-warp partial sums of <R_c, S_out(c)>
 };
 
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kChunkThreads)
 ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
+    constexpr int NT = kChunkThreads;
     const Problem& p = g.f;
     const int Q = p.Q, N = p.N, D = p.D, H = p.H;
     const int nb = (Q + kRows - 1) / kRows;
+    const bool single = nb == 1;
     const int c = blockIdx.x / nb, ib = blockIdx.x % nb;
     const int h = blockIdx.y, b = blockIdx.z;
     const int64_t t0 = (int64_t)c * Q;
@@ -259,266 +391,203 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
     const int tid = threadIdx.x;
     const int64_t bt0 = (int64_t)b * p.T + t0;
     const int64_t chunk = ((int64_t)b * H + h) * p.nc + c;
+    // micro-tile: rows rb + i (i < 4), cols cg + 32 j (j < 2)
+    const int warp = tid >> 5, cg = tid & 31, rb = 4 * warp;
 
     if (tid < 32)
         chunk_cumsum_warp(p.dt + bt0 * H + h, H, valid, Q, p.A_re[h], p.A_im[h], sm.acs);
-    load_rows(sm.own1, p.B_re, p.B_im, bt0, H, h, N, r0, valid);
-    load_rows(sm.own2, p.x_re, p.x_im, bt0, H, h, D, r0, valid);
-    load_state(sm.st, gw.R + chunk * 2 * D * N, D, N);
+    load_rows<NT>(sm.own1, p.B_re, p.B_im, bt0, H, h, N, r0, valid);
+    load_rows<NT>(sm.own2, p.x_re, p.x_im, bt0, H, h, D, r0, valid);
+    load_state<NT>(sm.st, gw.R + chunk * 2 * D * N, D, N);
+    load_rows<NT>(sm.str1, p.C_re, p.C_im, bt0, H, h, N, r0, valid);  // the first pair's (jb = ib) C, dY
+    load_rows<NT>(sm.str2, g.dy_re, g.dy_im, bt0, H, h, D, r0, valid);
 
-    const int rg = tid / 16, cg = tid % 16;  // micro-tile: rows rg + 16 i, cols cg + 16 j
-    float xr[4][4], xi[4][4], br[4][4], bi[4][4];  // dX[l][d], dB[l][n]
+    float2 dx[4][2], db[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) xr[i][j] = xi[i][j] = br[i][j] = bi[i][j] = 0.0f;
+        for (int j = 0; j < 2; ++j) dx[i][j] = db[i][j] = make_float2(0.0f, 0.0f);
 
     // ---- part 1: token blocks jb >= ib (rows t), own rows l
     for (int jb = ib; jb < nb; ++jb) {
         const int s0 = jb * kRows;
         if (s0 >= valid) break;
         const int trows = min(kRows, valid - s0);
-        __syncthreads();  // previous pair's reads are done
-        load_rows(sm.str1, p.C_re, p.C_im, bt0, H, h, N, s0, valid);
-        load_rows(sm.str2, g.dy_re, g.dy_im, bt0, H, h, D, s0, valid);
+        if (jb != ib) {
+            __syncthreads();  // previous pair's reads are done
+            load_rows<NT>(sm.str1, p.C_re, p.C_im, bt0, H, h, N, s0, valid);
+            load_rows<NT>(sm.str2, g.dy_re, g.dy_im, bt0, H, h, D, s0, valid);
+        }
         __syncthreads();
-        // decay factors of the pair: L[t][l] for t = rg + 16 i (block jb), l = cg + 16 j (block ib)
-        float lr[4][4], li[4][4];
+        // decay factors of the pair: L[t][l] for t = rb + i (block jb), l = cg + 32 j (block ib)
+        float2 L[4][2];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int tt = s0 + rg + 16 * i, ll = r0 + cg + 16 * j;
-                float2 v = make_float2(0.0f, 0.0f);
-                if (tt >= ll && tt < valid && ll < valid) v = cexp_exact(acs_diff(sm.acs[tt], sm.acs[ll]));
-                lr[i][j] = v.x;
-                li[i][j] = v.y;
+            for (int j = 0; j < 2; ++j) {
+                const int tt = s0 + rb + i, ll = r0 + cg + 32 * j;
+                L[i][j] = make_float2(0.0f, 0.0f);
+                if (tt >= ll && tt < valid && ll < valid) L[i][j] = cexp_exact(acs_diff(sm.acs[tt], sm.acs[ll]));
             }
         // P[t][l] = (sum_n C[t,n] B[l,n]) L[t][l]
         {
-            float gr[4][4], gi[4][4];
+            float2 G[4][2];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) gr[i][j] = gi[i][j] = 0.0f;
+                for (int j = 0; j < 2; ++j) G[i][j] = make_float2(0.0f, 0.0f);
             for (int n = 0; n < N; ++n) {
-                float cr[4], ci[4], qr[4], qi[4];
+                float2 a[4], q[2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    cr[i] = sm.str1.re[rg + 16 * i][n];
-                    ci[i] = sm.str1.im[rg + 16 * i][n];
-                }
+                for (int i = 0; i < 4; ++i) a[i] = sm.str1.v[rb + i][n];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    qr[j] = sm.own1.re[cg + 16 * j][n];
-                    qi[j] = sm.own1.im[cg + 16 * j][n];
-                }
+                for (int j = 0; j < 2; ++j) q[j] = sm.own1.v[cg + 32 * j][n];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        gr[i][j] = fmaf(cr[i], qr[j], fmaf(-ci[i], qi[j], gr[i][j]));
-                        gi[i][j] = fmaf(cr[i], qi[j], fmaf(ci[i], qr[j], gi[i][j]));
-                    }
+                    for (int j = 0; j < 2; ++j) cmac(G[i][j], a[i], q[j]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 v = cmul(make_float2(gr[i][j], gi[i][j]), make_float2(lr[i][j], li[i][j]));
-                    sm.pv.re[rg + 16 * i][cg + 16 * j] = v.x;
-                    sm.pv.im[rg + 16 * i][cg + 16 * j] = v.y;
-                }
+                for (int j = 0; j < 2; ++j) sm.pv.v[rb + i][cg + 32 * j] = cmul(G[i][j], L[i][j]);
         }
         __syncthreads();
-        // dX[l][d] += sum_t conj(P[t][l]) dY[t][d]
-        for (int t = 0; t < trows; ++t) {
-            float pr[4], pi[4], yr[4], yi[4];
+        // dX[l][d] += sum_t conj(P[t][l]) dY[t][d]; on the diagonal pair P[t][l] = 0 for t < l,
+        // so a warp starts at its first row
+        const int t_lo = jb == ib ? rb : 0;
+        for (int t = t_lo; t < trows; ++t) {
+            float2 a[4], y[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                pr[i] = sm.pv.re[t][rg + 16 * i];
-                pi[i] = sm.pv.im[t][rg + 16 * i];
-            }
+            for (int i = 0; i < 4; ++i) a[i] = sm.pv.v[t][rb + i];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                yr[j] = sm.str2.re[t][cg + 16 * j];
-                yi[j] = sm.str2.im[t][cg + 16 * j];
-            }
+            for (int j = 0; j < 2; ++j) y[j] = sm.str2.v[t][cg + 32 * j];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    xr[i][j] = fmaf(pr[i], yr[j], fmaf(pi[i], yi[j], xr[i][j]));
-                    xi[i][j] = fmaf(pr[i], yi[j], fmaf(-pi[i], yr[j], xi[i][j]));
-                }
+                for (int j = 0; j < 2; ++j) cmac_ca(dx[i][j], a[i], y[j]);
         }
         __syncthreads();
         // V[t][l] = (sum_d dY[t,d] conj(x[l,d])) conj(L[t][l])
         {
-            float wr[4][4], wi[4][4];
+            float2 W[4][2];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) wr[i][j] = wi[i][j] = 0.0f;
+                for (int j = 0; j < 2; ++j) W[i][j] = make_float2(0.0f, 0.0f);
             for (int d = 0; d < D; ++d) {
-                float yr[4], yi[4], qr[4], qi[4];
+                float2 y[4], q[2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    yr[i] = sm.str2.re[rg + 16 * i][d];
-                    yi[i] = sm.str2.im[rg + 16 * i][d];
-                }
+                for (int i = 0; i < 4; ++i) y[i] = sm.str2.v[rb + i][d];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    qr[j] = sm.own2.re[cg + 16 * j][d];
-                    qi[j] = sm.own2.im[cg + 16 * j][d];
-                }
+                for (int j = 0; j < 2; ++j) q[j] = sm.own2.v[cg + 32 * j][d];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        wr[i][j] = fmaf(yr[i], qr[j], fmaf(yi[i], qi[j], wr[i][j]));
-                        wi[i][j] = fmaf(yi[i], qr[j], fmaf(-yr[i], qi[j], wi[i][j]));
-                    }
+                    for (int j = 0; j < 2; ++j) cmac_cb(W[i][j], y[i], q[j]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 v = cmul(make_float2(wr[i][j], wi[i][j]), make_float2(lr[i][j], -li[i][j]));
-                    sm.pv.re[rg + 16 * i][cg + 16 * j] = v.x;
-                    sm.pv.im[rg + 16 * i][cg + 16 * j] = v.y;
-                }
+                for (int j = 0; j < 2; ++j) sm.pv.v[rb + i][cg + 32 * j] = cmul(W[i][j], conjf2(L[i][j]));
         }
         __syncthreads();
-        // dB[l][n] += sum_t V[t][l] conj(C[t][n])
-        for (int t = 0; t < trows; ++t) {
-            float vr[4], vi[4], cr[4], ci[4];
+        // dB[l][n] += sum_t V[t][l] conj(C[t][n])  (V[t][l] = 0 for t < l, as P)
+        for (int t = t_lo; t < trows; ++t) {
+            float2 v[4], cc[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                vr[i] = sm.pv.re[t][rg + 16 * i];
-                vi[i] = sm.pv.im[t][rg + 16 * i];
-            }
+            for (int i = 0; i < 4; ++i) v[i] = sm.pv.v[t][rb + i];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                cr[j] = sm.str1.re[t][cg + 16 * j];
-                ci[j] = sm.str1.im[t][cg + 16 * j];
-            }
+            for (int j = 0; j < 2; ++j) cc[j] = sm.str1.v[t][cg + 32 * j];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    br[i][j] = fmaf(vr[i], cr[j], fmaf(vi[i], ci[j], br[i][j]));
-                    bi[i][j] = fmaf(vi[i], cr[j], fmaf(-vr[i], ci[j], bi[i][j]));
-                }
+                for (int j = 0; j < 2; ++j) cmac_cb(db[i][j], v[i], cc[j]);
         }
     }
+
+    // S_in of the chunk, for part 2: fetched now, stored into st once R_c is no longer read
+    StateRegs<NT> sin_regs;
+    fetch_state<NT>(sin_regs, ws.S + chunk * 2 * D * N, D, N);
 
     // R_c terms: dX += conj(dec[l]) sum_n conj(B[l,n]) R[n,d];  dB += conj(dec[l]) sum_d conj(x[l,d]) R[n,d]
     {
         const Acs last = sm.acs[Q - 1];
-        float er[4], ei[4];  // conj(dec[l]) of the rows l = rg + 16 i
+        float2 e[4];  // conj(dec[l]) of the rows l = rb + i
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 v = cexp_exact(acs_diff(last, sm.acs[min(r0 + rg + 16 * i, Q - 1)]));
-            er[i] = v.x;
-            ei[i] = -v.y;
-        }
-        float ar[4][4], ai[4][4];
+        for (int i = 0; i < 4; ++i) e[i] = conjf2(cexp_exact(acs_diff(last, sm.acs[min(r0 + rb + i, Q - 1)])));
+        float2 acc[4][2];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ar[i][j] = ai[i][j] = 0.0f;
+            for (int j = 0; j < 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
         for (int n = 0; n < N; ++n) {
-            float qr[4], qi[4], sr[4], si[4];
+            float2 q[4], r[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                qr[i] = sm.own1.re[rg + 16 * i][n];
-                qi[i] = sm.own1.im[rg + 16 * i][n];
-            }
+            for (int i = 0; i < 4; ++i) q[i] = sm.own1.v[rb + i][n];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sr[j] = sm.st.re[cg + 16 * j][n];
-                si[j] = sm.st.im[cg + 16 * j][n];
-            }
+            for (int j = 0; j < 2; ++j) r[j] = sm.st.v[cg + 32 * j][n];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    ar[i][j] = fmaf(qr[i], sr[j], fmaf(qi[i], si[j], ar[i][j]));
-                    ai[i][j] = fmaf(qr[i], si[j], fmaf(-qi[i], sr[j], ai[i][j]));
-                }
+                for (int j = 0; j < 2; ++j) cmac_ca(acc[i][j], q[i], r[j]);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 v = cmul(make_float2(er[i], ei[i]), make_float2(ar[i][j], ai[i][j]));
-                xr[i][j] += v.x;
-                xi[i][j] += v.y;
-                ar[i][j] = ai[i][j] = 0.0f;
+            for (int j = 0; j < 2; ++j) {
+                const float2 v = cmul(e[i], acc[i][j]);
+                dx[i][j].x += v.x;
+                dx[i][j].y += v.y;
+                acc[i][j] = make_float2(0.0f, 0.0f);
             }
         for (int d = 0; d < D; ++d) {
-            float qr[4], qi[4], sr[4], si[4];
+            float2 q[4], r[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                qr[i] = sm.own2.re[rg + 16 * i][d];
-                qi[i] = sm.own2.im[rg + 16 * i][d];
-            }
+            for (int i = 0; i < 4; ++i) q[i] = sm.own2.v[rb + i][d];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sr[j] = sm.st.re[d][cg + 16 * j];
-                si[j] = sm.st.im[d][cg + 16 * j];
-            }
+            for (int j = 0; j < 2; ++j) r[j] = sm.st.v[d][cg + 32 * j];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    ar[i][j] = fmaf(qr[i], sr[j], fmaf(qi[i], si[j], ar[i][j]));
-                    ai[i][j] = fmaf(qr[i], si[j], fmaf(-qi[i], sr[j], ai[i][j]));
-                }
+                for (int j = 0; j < 2; ++j) cmac_ca(acc[i][j], q[i], r[j]);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 v = cmul(make_float2(er[i], ei[i]), make_float2(ar[i][j], ai[i][j]));
-                br[i][j] += v.x;
-                bi[i][j] += v.y;
+            for (int j = 0; j < 2; ++j) {
+                const float2 v = cmul(e[i], acc[i][j]);
+                db[i][j].x += v.x;
+                db[i][j].y += v.y;
             }
     }
 
     // write dX, dB; -<dB_l, B_l> per row into shared memory
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int l = rg + 16 * i;
+        const int l = rb + i;
         const bool row_ok = r0 + l < valid;
         const int64_t tok = (bt0 + r0 + l) * H + h;
-        float sr = 0.0f, si = 0.0f;
+        float2 sum = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int f = cg + 16 * j;
+        for (int j = 0; j < 2; ++j) {
+            const int f = cg + 32 * j;
             if (row_ok && f < D) {
-                g.dx_re[tok * D + f] = xr[i][j];
-                if (g.dx_im != nullptr) g.dx_im[tok * D + f] = xi[i][j];
+                g.dx_re[tok * D + f] = dx[i][j].x;
+                if (g.dx_im != nullptr) g.dx_im[tok * D + f] = dx[i][j].y;
             }
             if (row_ok && f < N) {
-                g.dB_re[tok * N + f] = br[i][j];
-                g.dB_im[tok * N + f] = bi[i][j];
+                g.dB_re[tok * N + f] = db[i][j].x;
+                g.dB_im[tok * N + f] = db[i][j].y;
             }
-            // dB conj(B); B is zero past N
-            const float qr = sm.own1.re[l][f], qi = sm.own1.im[l][f];
-            sr = fmaf(br[i][j], qr, fmaf(bi[i][j], qi, sr));
-            si = fmaf(bi[i][j], qr, fmaf(-br[i][j], qi, si));
+            cmac_cb(sum, db[i][j], sm.own1.v[l][f]);  // dB conj(B); B is zero past N
         }
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) {
-            sr += __shfl_xor_sync(0xffffffffu, sr, off);
-            si += __shfl_xor_sync(0xffffffffu, si, off);
+        for (int off = 16; off >= 1; off >>= 1) {
+            sum.x += __shfl_xor_sync(0xffffffffu, sum.x, off);
+            sum.y += __shfl_xor_sync(0xffffffffu, sum.y, off);
         }
-        if (cg == 0) {
-            sm.nbb_re[l] = -sr;
-            sm.nbb_im[l] = -si;
-        }
+        if (cg == 0) sm.nbb[l] = make_float2(-sum.x, -sum.y);
     }
 
     // <R_c, S_out(c)>, once per chunk (row block 0); st holds R_c^T. S_out is the
@@ -527,35 +596,31 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
         const int64_t bh = (int64_t)b * H + h;
         const bool last_chunk = c == p.nc - 1;
         const float* nxt = ws.S + (chunk + 1) * 2 * D * N;
-        float ar = 0.0f, ai = 0.0f;
-        for (int e = tid; e < D * N; e += kBwdThreads) {
+        float2 acc = make_float2(0.0f, 0.0f);
+        for (int e = tid; e < D * N; e += NT) {
             const int d = e / N, n = e % N;
-            float sr, si;
+            float2 so;
             if (last_chunk) {
                 const int64_t o = (bh * N + n) * D + d;
-                sr = p.fs_re[o];
-                si = p.fs_im[o];
+                so = make_float2(p.fs_re[o], p.fs_im[o]);
             } else {
-                sr = nxt[e];
-                si = nxt[(int64_t)D * N + e];
+                so = make_float2(nxt[e], nxt[(int64_t)D * N + e]);
             }
-            const float rr = sm.st.re[d][n], ri = sm.st.im[d][n];
-            ar = fmaf(rr, sr, fmaf(ri, si, ar));
-            ai = fmaf(ri, sr, fmaf(-rr, si, ai));
+            cmac_cb(acc, sm.st.v[d][n], so);
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {
-            ar += __shfl_xor_sync(0xffffffffu, ar, off);
-            ai += __shfl_xor_sync(0xffffffffu, ai, off);
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
         }
-        if ((tid & 31) == 0) {
-            sm.anc[tid >> 5][0] = ar;
-            sm.anc[tid >> 5][1] = ai;
+        if (cg == 0) {
+            sm.anc[warp][0] = acc.x;
+            sm.anc[warp][1] = acc.y;
         }
         __syncthreads();
         if (tid == 0) {
             double sr = 0.0, si = 0.0;
-            for (int w = 0; w < kBwdThreads / 32; ++w) {
+            for (int w = 0; w < kChunkWarps; ++w) {
                 sr += sm.anc[w][0];
                 si += sm.anc[w][1];
             }
@@ -565,121 +630,102 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
     }
 
     // ---- part 2: own rows t of block ib, blocks jb <= ib (rows l)
+    // With a single block, C and dY of the rows are part 1's str1 / str2, the B rows
+    // are own1 and V of the pair is still in pv.
+    CTile& Cown = single ? sm.str1 : sm.own1;
+    CTile& Yown = single ? sm.str2 : sm.own2;
+    CTile& Bsrc = single ? sm.own1 : sm.str1;
     __syncthreads();
-    load_rows(sm.own1, p.C_re, p.C_im, bt0, H, h, N, r0, valid);
-    load_rows(sm.own2, g.dy_re, g.dy_im, bt0, H, h, D, r0, valid);
-    load_state(sm.st, ws.S + chunk * 2 * D * N, D, N);
-    float cr_[4][4], ci_[4][4];  // dC[t][n]
+    if (!single) {
+        load_rows<NT>(sm.own1, p.C_re, p.C_im, bt0, H, h, N, r0, valid);
+        load_rows<NT>(sm.own2, g.dy_re, g.dy_im, bt0, H, h, D, r0, valid);
+    }
+    store_state<NT>(sm.st, sin_regs);
+    float2 dc[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cr_[i][j] = ci_[i][j] = 0.0f;
+        for (int j = 0; j < 2; ++j) dc[i][j] = make_float2(0.0f, 0.0f);
     for (int jb = 0; jb <= ib; ++jb) {
         const int s0 = jb * kRows;
         const int lrows = min(kRows, valid - s0);
         __syncthreads();
-        load_rows(sm.str1, p.B_re, p.B_im, bt0, H, h, N, s0, valid);
-        load_rows(sm.str2, p.x_re, p.x_im, bt0, H, h, D, s0, valid);
-        __syncthreads();
-        // V[t][l] = (sum_d dY[t,d] conj(x[l,d])) conj(L[t][l]), t = rg + 16 i (block ib), l = cg + 16 j (block jb)
-        {
-            float wr[4][4], wi[4][4];
+        if (!single) {
+            load_rows<NT>(sm.str1, p.B_re, p.B_im, bt0, H, h, N, s0, valid);
+            load_rows<NT>(sm.str2, p.x_re, p.x_im, bt0, H, h, D, s0, valid);
+            __syncthreads();
+            // V[t][l] = (sum_d dY[t,d] conj(x[l,d])) conj(L[t][l]), t = rb + i (block ib),
+            // l = cg + 32 j (block jb)
+            float2 W[4][2];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) wr[i][j] = wi[i][j] = 0.0f;
+                for (int j = 0; j < 2; ++j) W[i][j] = make_float2(0.0f, 0.0f);
             for (int d = 0; d < D; ++d) {
-                float yr[4], yi[4], qr[4], qi[4];
+                float2 y[4], q[2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    yr[i] = sm.own2.re[rg + 16 * i][d];
-                    yi[i] = sm.own2.im[rg + 16 * i][d];
-                }
+                for (int i = 0; i < 4; ++i) y[i] = sm.own2.v[rb + i][d];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    qr[j] = sm.str2.re[cg + 16 * j][d];
-                    qi[j] = sm.str2.im[cg + 16 * j][d];
-                }
+                for (int j = 0; j < 2; ++j) q[j] = sm.str2.v[cg + 32 * j][d];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        wr[i][j] = fmaf(yr[i], qr[j], fmaf(yi[i], qi[j], wr[i][j]));
-                        wi[i][j] = fmaf(yi[i], qr[j], fmaf(-yr[i], qi[j], wi[i][j]));
-                    }
+                    for (int j = 0; j < 2; ++j) cmac_cb(W[i][j], y[i], q[j]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int tt = r0 + rg + 16 * i, ll = s0 + cg + 16 * j;
+                for (int j = 0; j < 2; ++j) {
+                    const int tt = r0 + rb + i, ll = s0 + cg + 32 * j;
                     float2 v = make_float2(0.0f, 0.0f);
-                    if (tt >= ll && tt < valid && ll < valid) {
-                        const float2 L = cexp_exact(acs_diff(sm.acs[tt], sm.acs[ll]));
-                        v = cmul(make_float2(wr[i][j], wi[i][j]), make_float2(L.x, -L.y));
-                    }
-                    sm.pv.re[rg + 16 * i][cg + 16 * j] = v.x;
-                    sm.pv.im[rg + 16 * i][cg + 16 * j] = v.y;
+                    if (tt >= ll && tt < valid && ll < valid)
+                        v = cmul(W[i][j], conjf2(cexp_exact(acs_diff(sm.acs[tt], sm.acs[ll]))));
+                    sm.pv.v[rb + i][cg + 32 * j] = v;
                 }
+            __syncthreads();
         }
-        __syncthreads();
-        // dC[t][n] += sum_l V[t][l] conj(B[l][n])
-        for (int l = 0; l < lrows; ++l) {
-            float vr[4], vi[4], qr[4], qi[4];
+        // dC[t][n] += sum_l V[t][l] conj(B[l][n]); on the diagonal pair V[t][l] = 0 for l > t,
+        // so a warp stops after its last row
+        const int l_hi = jb == ib ? min(lrows, rb + 4) : lrows;
+        for (int l = 0; l < l_hi; ++l) {
+            float2 v[4], q[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                vr[i] = sm.pv.re[rg + 16 * i][l];
-                vi[i] = sm.pv.im[rg + 16 * i][l];
-            }
+            for (int i = 0; i < 4; ++i) v[i] = sm.pv.v[rb + i][l];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                qr[j] = sm.str1.re[l][cg + 16 * j];
-                qi[j] = sm.str1.im[l][cg + 16 * j];
-            }
+            for (int j = 0; j < 2; ++j) q[j] = Bsrc.v[l][cg + 32 * j];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    cr_[i][j] = fmaf(vr[i], qr[j], fmaf(vi[i], qi[j], cr_[i][j]));
-                    ci_[i][j] = fmaf(vi[i], qr[j], fmaf(-vr[i], qi[j], ci_[i][j]));
-                }
+                for (int j = 0; j < 2; ++j) cmac_cb(dc[i][j], v[i], q[j]);
         }
     }
+    if (single) __syncthreads();  // S_in is in st
     // S_in term: dC[t][n] += conj(exp(Acs[t])) sum_d dY[t,d] conj(S_in[n,d])
     {
-        float ar[4][4], ai[4][4];
+        float2 acc[4][2];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ar[i][j] = ai[i][j] = 0.0f;
+            for (int j = 0; j < 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
         for (int d = 0; d < D; ++d) {
-            float yr[4], yi[4], sr[4], si[4];
+            float2 y[4], sv[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                yr[i] = sm.own2.re[rg + 16 * i][d];
-                yi[i] = sm.own2.im[rg + 16 * i][d];
-            }
+            for (int i = 0; i < 4; ++i) y[i] = Yown.v[rb + i][d];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sr[j] = sm.st.re[d][cg + 16 * j];
-                si[j] = sm.st.im[d][cg + 16 * j];
-            }
+            for (int j = 0; j < 2; ++j) sv[j] = sm.st.v[d][cg + 32 * j];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    ar[i][j] = fmaf(yr[i], sr[j], fmaf(yi[i], si[j], ar[i][j]));
-                    ai[i][j] = fmaf(yi[i], sr[j], fmaf(-yr[i], si[j], ai[i][j]));
-                }
+                for (int j = 0; j < 2; ++j) cmac_cb(acc[i][j], y[i], sv[j]);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 e = cexp_exact(acs_value(sm.acs[min(r0 + rg + 16 * i, Q - 1)]));
+            const float2 e = conjf2(cexp_exact(acs_value(sm.acs[min(r0 + rb + i, Q - 1)])));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 v = cmul(make_float2(e.x, -e.y), make_float2(ar[i][j], ai[i][j]));
-                cr_[i][j] += v.x;
-                ci_[i][j] += v.y;
+            for (int j = 0; j < 2; ++j) {
+                const float2 v = cmul(e, acc[i][j]);
+                dc[i][j].x += v.x;
+                dc[i][j].y += v.y;
             }
         }
     }
@@ -689,93 +735,138 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
     float* rim = rre + p.T;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int t = rg + 16 * i;
+        const int t = rb + i;
         const bool row_ok = r0 + t < valid;
         const int64_t tok = (bt0 + r0 + t) * H + h;
-        float sr = 0.0f, si = 0.0f;
+        float2 sum = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = cg + 16 * j;
+        for (int j = 0; j < 2; ++j) {
+            const int n = cg + 32 * j;
             if (row_ok && n < N) {
-                g.dC_re[tok * N + n] = cr_[i][j];
-                g.dC_im[tok * N + n] = ci_[i][j];
+                g.dC_re[tok * N + n] = dc[i][j].x;
+                g.dC_im[tok * N + n] = dc[i][j].y;
             }
-            const float qr = sm.own1.re[t][n], qi = sm.own1.im[t][n];
-            sr = fmaf(cr_[i][j], qr, fmaf(ci_[i][j], qi, sr));
-            si = fmaf(ci_[i][j], qr, fmaf(-cr_[i][j], qi, si));
+            cmac_cb(sum, dc[i][j], Cown.v[t][n]);
         }
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) {
-            sr += __shfl_xor_sync(0xffffffffu, sr, off);
-            si += __shfl_xor_sync(0xffffffffu, si, off);
+        for (int off = 16; off >= 1; off >>= 1) {
+            sum.x += __shfl_xor_sync(0xffffffffu, sum.x, off);
+            sum.y += __shfl_xor_sync(0xffffffffu, sum.y, off);
         }
         if (cg == 0 && row_ok) {
-            rre[t0 + r0 + t] = sr + sm.nbb_re[t];
-            rim[t0 + r0 + t] = si + sm.nbb_im[t];
+            rre[t0 + r0 + t] = sum.x + sm.nbb[t].x;
+            rim[t0 + r0 + t] = sum.y + sm.nbb[t].y;
         }
     }
 }
 
 // ---------------------------------------------------------------------------
 // dz_t = <R_c, S_out(c)> + sum_{t' >= t in chunk c} r_t' (fp64), then
-// ddt_t = Re(dz_t conj(A)) sigmoid(dt_t) and dA = sum_{b,t} softplus(dt_t) dz_t.
-// One CTA per head; its threads take the (b, chunk) pairs of the head in turn.
+// ddt_t = Re(dz_t conj(A)) sigmoid(dt_t) and the chunk's share of
+// dA = sum_{b,t} softplus(dt_t) dz_t. One warp per chunk: each lane takes a run
+// of consecutive tokens, the runs' totals are suffix-summed across the warp.
+// ssdc_bwd_dA then adds the chunk shares of each head in a fixed order.
 
 constexpr int kDtThreads = kBwdDtThreads;
+constexpr int kDtWarps = kDtThreads / 32;
 
 __global__ void __launch_bounds__(kDtThreads)
 ssdc_bwd_dt(GradProblem g, Workspace ws, GradWorkspace gw) {
-    __shared__ double red[kDtThreads / 32][2];
     const Problem& p = g.f;
-    const int h = blockIdx.x, tid = threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t nc = p.nc;
+    const int64_t task = (int64_t)blockIdx.x * kDtWarps + (threadIdx.x >> 5);  // chunk index (b, h, c)
+    if (task >= (int64_t)p.B * p.H * nc) return;
     const int H = p.H, Q = p.Q;
-    const int64_t T = p.T, nc = p.nc;
+    const int64_t T = p.T;
+    const int64_t bh = task / nc, c = task % nc;
+    const int64_t b = bh / H;
+    const int h = (int)(bh % H);
+    const int64_t t0 = c * Q;
+    const int valid = (int)(T - t0 < (int64_t)Q ? T - t0 : (int64_t)Q);
+    const int per = (Q + 31) / 32;  // tokens per lane (Q <= 256: at most 8)
+    const int la = min(valid, lane * per), lb = min(valid, la + per);
+    const float* rre = gw.r + bh * 2 * T + t0;
+    const float* rim = rre + T;
+    double tr = 0.0, ti = 0.0;  // this lane's run total
+    for (int l = la; l < lb; ++l) {
+        tr += rre[l];
+        ti += rim[l];
+    }
+    // inclusive suffix sum of the run totals over the lanes
+    double sr = tr, si = ti;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double ur = __shfl_down_sync(0xffffffffu, sr, off);
+        const double ui = __shfl_down_sync(0xffffffffu, si, off);
+        if (lane + off < 32) {
+            sr += ur;
+            si += ui;
+        }
+    }
+    // dz at the end of this lane's run: anchor + the runs after it
+    double zr = gw.anchor[2 * task] + (sr - tr), zi = gw.anchor[2 * task + 1] + (si - ti);
     const float Ar = p.A_re[h], Ai = p.A_im[h];
     double dAr = 0.0, dAi = 0.0;
-    for (int64_t k = tid; k < (int64_t)p.B * nc; k += kDtThreads) {
-        const int64_t b = k / nc, c = k % nc;
-        const int64_t bh = b * H + h;
-        const int64_t chunk = bh * nc + c;
-        const int64_t t0 = c * Q;
-        const int valid = (int)(T - t0 < (int64_t)Q ? T - t0 : (int64_t)Q);
-        const float* rre = gw.r + bh * 2 * T;
-        const float* rim = rre + T;
-        double zr = gw.anchor[2 * chunk], zi = gw.anchor[2 * chunk + 1];
-        for (int l = valid - 1; l >= 0; --l) {
-            const int64_t t = t0 + l;
-            zr += rre[t];
-            zi += rim[t];
-            const int64_t bth = (b * T + t) * H + h;
-            const float v = p.dt[bth];
-            const float sig = 1.0f / (1.0f + expf(-v));
-            g.ddt[bth] = (float)(zr * Ar + zi * Ai) * sig;
-            const double delta = (double)softplus_f(v);
-            dAr += delta * zr;
-            dAi += delta * zi;
-        }
+    for (int l = lb - 1; l >= la; --l) {
+        zr += rre[l];
+        zi += rim[l];
+        const int64_t bth = (b * T + t0 + l) * H + h;
+        const float v = p.dt[bth];
+        const float sig = 1.0f / (1.0f + expf(-v));
+        g.ddt[bth] = (float)(zr * Ar + zi * Ai) * sig;
+        const double delta = (double)softplus_f(v);
+        dAr += delta * zr;
+        dAi += delta * zi;
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         dAr += __shfl_xor_sync(0xffffffffu, dAr, off);
         dAi += __shfl_xor_sync(0xffffffffu, dAi, off);
     }
-    if ((tid & 31) == 0) {
-        red[tid >> 5][0] = dAr;
-        red[tid >> 5][1] = dAi;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        double sr = 0.0, si = 0.0;
-        for (int w = 0; w < kDtThreads / 32; ++w) {
-            sr += red[w][0];
-            si += red[w][1];
-        }
-        g.dA_re[h] = (float)sr;
-        g.dA_im[h] = (float)si;
+    if (lane == 0) {
+        gw.dA_part[2 * task] = dAr;
+        gw.dA_part[2 * task + 1] = dAi;
     }
 }
 
-size_t bwd_adjoint_smem() { return sizeof(AdjSmem); }
+// dA[h] = sum over b and c of the chunk shares, one CTA per head: each thread
+// sums a strided set of chunks, then a fixed-order reduction.
+__global__ void __launch_bounds__(kDtThreads)
+ssdc_bwd_dA(GradProblem g, Workspace ws, GradWorkspace gw) {
+    __shared__ double red[kDtWarps][2];
+    const Problem& p = g.f;
+    const int h = blockIdx.x, tid = threadIdx.x;
+    const int64_t nc = p.nc, per_head = (int64_t)p.B * nc;
+    double sr = 0.0, si = 0.0;
+    for (int64_t k = tid; k < per_head; k += kDtThreads) {
+        const int64_t b = k / nc, c = k % nc;
+        const int64_t task = (b * p.H + h) * nc + c;
+        sr += gw.dA_part[2 * task];
+        si += gw.dA_part[2 * task + 1];
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        sr += __shfl_xor_sync(0xffffffffu, sr, off);
+        si += __shfl_xor_sync(0xffffffffu, si, off);
+    }
+    if ((tid & 31) == 0) {
+        red[tid >> 5][0] = sr;
+        red[tid >> 5][1] = si;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double ar = 0.0, ai = 0.0;
+        for (int w = 0; w < kDtWarps; ++w) {
+            ar += red[w][0];
+            ai += red[w][1];
+        }
+        g.dA_re[h] = (float)ar;
+        g.dA_im[h] = (float)ai;
+    }
+}
+
+size_t bwd_states_smem() { return sizeof(StatesSmem); }
 size_t bwd_chunk_smem() { return sizeof(BwdSmem); }
 
 }  // namespace ssdc

@@ -2,8 +2,8 @@
 // workspace carving and the launch sequences
 //   forward:  chunk-state kernel -> state pass -> chunk-scan kernel
 //             (or the fused kernel)
-//   backward: chunk-state kernel -> state pass -> chunk adjoint -> adjoint
-//             pass -> chunk gradients -> step-size gradients
+//   backward: chunk states and adjoints -> both chunk recurrences -> chunk
+//             gradients -> step-size gradients -> per-head dA
 // on the caller's stream. No allocation happens in ssd_complex_fwd_ws or
 // ssd_complex_bwd.
 #include <atomic>
@@ -115,8 +115,8 @@ int setup_device_attrs() {
     if (cudaFuncSetAttribute(ssdc::ssdc_simt_chunk_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ssdc::simt_scan_smem()) != cudaSuccess)
         return SSDC_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssdc::ssdc_bwd_chunk_adjoint, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssdc::bwd_adjoint_smem()) != cudaSuccess)
+    if (cudaFuncSetAttribute(ssdc::ssdc_bwd_chunk_states, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ssdc::bwd_states_smem()) != cudaSuccess)
         return SSDC_ERR_CUDA;
     if (cudaFuncSetAttribute(ssdc::ssdc_bwd_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ssdc::bwd_chunk_smem()) != cudaSuccess)
@@ -342,13 +342,14 @@ int ssd_complex_timing_read(float* ms, int n) {
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// Backward pass: recompute the chunk states (forward chunk-state kernel and
-// state pass), then the four backward kernels of csrc/ssdc_bwd.cu.
+// Backward pass: the five kernels of csrc/ssdc_bwd.cu (chunk states and
+// adjoints, the two chunk recurrences, chunk gradients, step-size gradients,
+// the per-head sum of dA).
 
 namespace {
 
 struct BwdLayout {
-    size_t S, a, R, fs, r, anchor, total;  // byte offsets (total = size)
+    size_t S, a, R, fs, r, anchor, dA_part, total;  // byte offsets (total = size)
 };
 
 size_t pad256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -364,7 +365,8 @@ BwdLayout bwd_layout(const ssdc_dims& d, int Q) {
     l.fs = l.R + states;
     l.r = l.fs + pad256((size_t)(d.B * d.H * d.N * d.D) * 2 * sizeof(float));
     l.anchor = l.r + pad256((size_t)(d.B * d.H * d.T) * 2 * sizeof(float));
-    l.total = l.anchor + pad256(chunks * 2 * sizeof(double));
+    l.dA_part = l.anchor + pad256(chunks * 2 * sizeof(double));
+    l.total = l.dA_part + pad256(chunks * 2 * sizeof(double));
     return l;
 }
 
@@ -450,6 +452,7 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     gw.R = reinterpret_cast<float*>(base + lay.R);
     gw.r = reinterpret_cast<float*>(base + lay.r);
     gw.anchor = reinterpret_cast<double*>(base + lay.anchor);
+    gw.dA_part = reinterpret_cast<double*>(base + lay.dA_part);
     float* fs = reinterpret_cast<float*>(base + lay.fs);
 
     ssdc::GradProblem g;
@@ -476,19 +479,19 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     const dim3 chunk_grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
-    ssdc::ssdc_simt_chunk_state<<<chunk_grid, 256, ssdc::simt_state_smem(), stream>>>(p, w);
+    ssdc::ssdc_bwd_chunk_states<<<chunk_grid, 256, ssdc::bwd_states_smem(), stream>>>(g, w, gw);
     record_event(++launches, stream);
-    ssdc::ssdc_state_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(p, w);
-    record_event(++launches, stream);
-    ssdc::ssdc_bwd_chunk_adjoint<<<chunk_grid, 256, ssdc::bwd_adjoint_smem(), stream>>>(g, w, gw);
-    record_event(++launches, stream);
-    ssdc::ssdc_adjoint_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(g, w, gw);
+    const dim3 passes_grid(2 * pass_grid.x, pass_grid.y);  // forward and backward chains side by side
+    ssdc::ssdc_bwd_passes<<<passes_grid, ssdc::kPassThreads, 0, stream>>>(g, w, gw);
     record_event(++launches, stream);
     const int nb = (p.Q + 63) / 64;
     const dim3 bgrid((unsigned)(p.nc * nb), (unsigned)p.H, (unsigned)p.B);
-    ssdc::ssdc_bwd_chunk<<<bgrid, 256, ssdc::bwd_chunk_smem(), stream>>>(g, w, gw);
+    ssdc::ssdc_bwd_chunk<<<bgrid, ssdc::kBwdChunkThreads, ssdc::bwd_chunk_smem(), stream>>>(g, w, gw);
     record_event(++launches, stream);
-    ssdc::ssdc_bwd_dt<<<(unsigned)p.H, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);
+    const int64_t dt_blocks = ssdc::ceil_div64((int64_t)p.B * p.H * p.nc, ssdc::kBwdDtThreads / 32);
+    ssdc::ssdc_bwd_dt<<<(unsigned)dt_blocks, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);
+    record_event(++launches, stream);
+    ssdc::ssdc_bwd_dA<<<(unsigned)p.H, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);
     record_event(++launches, stream);
     if (cudaGetLastError() != cudaSuccess) return SSDC_ERR_CUDA;
     g_last_launches = launches;

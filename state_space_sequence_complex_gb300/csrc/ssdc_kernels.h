@@ -41,20 +41,24 @@ struct GradProblem {
 //      of the state leaving chunk c (transposed like S)
 //   r  [B*H][2][T] floats: r_t = <dC_t, C_t> - <dB_t, B_t> of every token
 //   anchor [B*H*nc][2] doubles: <R_c, S_out(c)>, S_out(c) the state leaving chunk c
+//   dA_part [B*H*nc][2] doubles: each chunk's share of dA
 struct GradWorkspace {
     float* R;
     float* r;
     double* anchor;
+    double* dA_part;
 };
 
 // Backward kernels (exact fp32, SIMT).
-__global__ void ssdc_bwd_chunk_adjoint(GradProblem g, Workspace ws, GradWorkspace gw);
-__global__ void ssdc_adjoint_pass(GradProblem g, Workspace ws, GradWorkspace gw);
+__global__ void ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw);
+__global__ void ssdc_bwd_passes(GradProblem g, Workspace ws, GradWorkspace gw);
 __global__ void ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw);
 __global__ void ssdc_bwd_dt(GradProblem g, Workspace ws, GradWorkspace gw);
-size_t bwd_adjoint_smem();
+__global__ void ssdc_bwd_dA(GradProblem g, Workspace ws, GradWorkspace gw);
+size_t bwd_states_smem();
 size_t bwd_chunk_smem();
 constexpr int kBwdDtThreads = 256;
+constexpr int kBwdChunkThreads = 512;  // threads of ssdc_bwd_chunk
 
 // SIMT (exact fp32) kernels.
 __global__ void ssdc_simt_chunk_state(Problem p, Workspace ws);

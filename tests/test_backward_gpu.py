@@ -169,7 +169,7 @@ def test_backward_repeated_calls_are_bitwise_identical():
     g2 = run_bwd(inp, og, 64, backward=b)
     for k in g1:
         assert np.array_equal(g1[k], g2[k]), k
-    assert ssdc.last_launch_count() == 6
+    assert ssdc.last_launch_count() == 5
 
 
 def test_backward_single_layer_matches_oracle():
