@@ -166,13 +166,15 @@ struct StatesSmem {
     CTile a, b;  // x and dec o B; then dY and C'
 };
 
+template <int kN, int kD>
 __global__ void __launch_bounds__(kBwdThreads)
 ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     StatesSmem& sm = *reinterpret_cast<StatesSmem*>(smem_raw);
     const Problem& p = g.f;
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int Q = p.Q, N = p.N, D = p.D, H = p.H;
+    const int Q = p.Q, H = p.H;
+    const int N = kN > 0 ? kN : p.N, D = kD > 0 ? kD : p.D;  // compile-time at the production shape
     const int64_t t0 = (int64_t)c * Q;
     const int valid = chunk_valid(p, t0);
     const int tid = threadIdx.x;
@@ -214,6 +216,7 @@ ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw) {
                 }
             }
             __syncthreads();
+#pragma unroll 4
             for (int l = 0; l < rows; ++l) {
                 float2 u[4], w[4];
 #pragma unroll
@@ -373,13 +376,15 @@ struct BwdSmem {
     double anc[kChunkWarps][2];       // per-warp partial sums of <R_c, S_out(c)>
 };
 
+template <int kN, int kD>
 __global__ void __launch_bounds__(kChunkThreads)
 ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
     constexpr int NT = kChunkThreads;
     const Problem& p = g.f;
-    const int Q = p.Q, N = p.N, D = p.D, H = p.H;
+    const int Q = p.Q, H = p.H;
+    const int N = kN > 0 ? kN : p.N, D = kD > 0 ? kD : p.D;  // compile-time at the production shape
     const int nb = (Q + kRows - 1) / kRows;
     const bool single = nb == 1;
     const int c = blockIdx.x / nb, ib = blockIdx.x % nb;
@@ -436,7 +441,9 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) G[i][j] = make_float2(0.0f, 0.0f);
-            for (int n = 0; n < N; ++n) {
+#pragma unroll 8
+    #pragma unroll 8
+        for (int n = 0; n < N; ++n) {
                 float2 a[4], q[2];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) a[i] = sm.str1.v[rb + i][n];
@@ -456,6 +463,7 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
         // dX[l][d] += sum_t conj(P[t][l]) dY[t][d]; on the diagonal pair P[t][l] = 0 for t < l,
         // so a warp starts at its first row
         const int t_lo = jb == ib ? rb : 0;
+#pragma unroll 4
         for (int t = t_lo; t < trows; ++t) {
             float2 a[4], y[2];
 #pragma unroll
@@ -475,7 +483,9 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) W[i][j] = make_float2(0.0f, 0.0f);
-            for (int d = 0; d < D; ++d) {
+#pragma unroll 8
+    #pragma unroll 8
+        for (int d = 0; d < D; ++d) {
                 float2 y[4], q[2];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) y[i] = sm.str2.v[rb + i][d];
@@ -493,6 +503,7 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
         }
         __syncthreads();
         // dB[l][n] += sum_t V[t][l] conj(C[t][n])  (V[t][l] = 0 for t < l, as P)
+#pragma unroll 4
         for (int t = t_lo; t < trows; ++t) {
             float2 v[4], cc[2];
 #pragma unroll
@@ -521,6 +532,7 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+#pragma unroll 8
         for (int n = 0; n < N; ++n) {
             float2 q[4], r[2];
 #pragma unroll
@@ -541,6 +553,7 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
                 dx[i][j].y += v.y;
                 acc[i][j] = make_float2(0.0f, 0.0f);
             }
+#pragma unroll 8
         for (int d = 0; d < D; ++d) {
             float2 q[4], r[2];
 #pragma unroll
@@ -661,7 +674,9 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) W[i][j] = make_float2(0.0f, 0.0f);
-            for (int d = 0; d < D; ++d) {
+#pragma unroll 8
+    #pragma unroll 8
+        for (int d = 0; d < D; ++d) {
                 float2 y[4], q[2];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) y[i] = sm.own2.v[rb + i][d];
@@ -687,6 +702,7 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
         // dC[t][n] += sum_l V[t][l] conj(B[l][n]); on the diagonal pair V[t][l] = 0 for l > t,
         // so a warp stops after its last row
         const int l_hi = jb == ib ? min(lrows, rb + 4) : lrows;
+#pragma unroll 4
         for (int l = 0; l < l_hi; ++l) {
             float2 v[4], q[2];
 #pragma unroll
@@ -707,6 +723,7 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+#pragma unroll 8
         for (int d = 0; d < D; ++d) {
             float2 y[4], sv[2];
 #pragma unroll
@@ -866,7 +883,36 @@ ssdc_bwd_dA(GradProblem g, Workspace ws, GradWorkspace gw) {
     }
 }
 
-size_t bwd_states_smem() { return sizeof(StatesSmem); }
-size_t bwd_chunk_smem() { return sizeof(BwdSmem); }
+// Host side of the two templated kernels: N = D = 64 (the production shape)
+// takes the instantiation with compile-time loop bounds.
+
+cudaError_t bwd_set_smem_attrs() {
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(ssdc_bwd_chunk_states<0, 0>, a, (int)sizeof(StatesSmem));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ssdc_bwd_chunk_states<64, 64>, a, (int)sizeof(StatesSmem));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ssdc_bwd_chunk<0, 0>, a, (int)sizeof(BwdSmem));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ssdc_bwd_chunk<64, 64>, a, (int)sizeof(BwdSmem));
+    return e;
+}
+
+void bwd_launch_chunk_states(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw,
+                             cudaStream_t stream) {
+    const Problem& p = g.f;
+    const dim3 grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
+    if (p.N == 64 && p.D == 64)
+        ssdc_bwd_chunk_states<64, 64><<<grid, kBwdThreads, sizeof(StatesSmem), stream>>>(g, ws, gw);
+    else
+        ssdc_bwd_chunk_states<0, 0><<<grid, kBwdThreads, sizeof(StatesSmem), stream>>>(g, ws, gw);
+}
+
+void bwd_launch_chunk(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw, cudaStream_t stream) {
+    const Problem& p = g.f;
+    const int nb = (p.Q + kRows - 1) / kRows;
+    const dim3 grid((unsigned)(p.nc * nb), (unsigned)p.H, (unsigned)p.B);
+    if (p.N == 64 && p.D == 64)
+        ssdc_bwd_chunk<64, 64><<<grid, kChunkThreads, sizeof(BwdSmem), stream>>>(g, ws, gw);
+    else
+        ssdc_bwd_chunk<0, 0><<<grid, kChunkThreads, sizeof(BwdSmem), stream>>>(g, ws, gw);
+}
 
 }  // namespace ssdc

@@ -115,12 +115,7 @@ int setup_device_attrs() {
     if (cudaFuncSetAttribute(ssdc::ssdc_simt_chunk_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)ssdc::simt_scan_smem()) != cudaSuccess)
         return SSDC_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssdc::ssdc_bwd_chunk_states, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssdc::bwd_states_smem()) != cudaSuccess)
-        return SSDC_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssdc::ssdc_bwd_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssdc::bwd_chunk_smem()) != cudaSuccess)
-        return SSDC_ERR_CUDA;
+    if (ssdc::bwd_set_smem_attrs() != cudaSuccess) return SSDC_ERR_CUDA;
     g_attr_done[dev].store(1, std::memory_order_release);
     return SSDC_OK;
 }
@@ -476,17 +471,14 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     (void)cudaGetLastError();  // clear a stale error from unrelated work
     int launches = 0;
     if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
-    const dim3 chunk_grid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
-    ssdc::ssdc_bwd_chunk_states<<<chunk_grid, 256, ssdc::bwd_states_smem(), stream>>>(g, w, gw);
+    ssdc::bwd_launch_chunk_states(g, w, gw, stream);
     record_event(++launches, stream);
     const dim3 passes_grid(2 * pass_grid.x, pass_grid.y);  // forward and backward chains side by side
     ssdc::ssdc_bwd_passes<<<passes_grid, ssdc::kPassThreads, 0, stream>>>(g, w, gw);
     record_event(++launches, stream);
-    const int nb = (p.Q + 63) / 64;
-    const dim3 bgrid((unsigned)(p.nc * nb), (unsigned)p.H, (unsigned)p.B);
-    ssdc::ssdc_bwd_chunk<<<bgrid, ssdc::kBwdChunkThreads, ssdc::bwd_chunk_smem(), stream>>>(g, w, gw);
+    ssdc::bwd_launch_chunk(g, w, gw, stream);
     record_event(++launches, stream);
     const int64_t dt_blocks = ssdc::ceil_div64((int64_t)p.B * p.H * p.nc, ssdc::kBwdDtThreads / 32);
     ssdc::ssdc_bwd_dt<<<(unsigned)dt_blocks, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);

@@ -50,15 +50,18 @@ struct GradWorkspace {
 };
 
 // Backward kernels (exact fp32, SIMT).
-__global__ void ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw);
+// The chunk-state/adjoint kernel and the chunk-gradient kernel are templates
+// (compile-time N = D = 64, or sizes from the problem); these enqueue the
+// right instantiation and set their shared-memory limits.
+cudaError_t bwd_set_smem_attrs();
+void bwd_launch_chunk_states(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw,
+                             cudaStream_t stream);
+void bwd_launch_chunk(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw, cudaStream_t stream);
 __global__ void ssdc_bwd_passes(GradProblem g, Workspace ws, GradWorkspace gw);
-__global__ void ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw);
 __global__ void ssdc_bwd_dt(GradProblem g, Workspace ws, GradWorkspace gw);
 __global__ void ssdc_bwd_dA(GradProblem g, Workspace ws, GradWorkspace gw);
-size_t bwd_states_smem();
-size_t bwd_chunk_smem();
 constexpr int kBwdDtThreads = 256;
-constexpr int kBwdChunkThreads = 512;  // threads of ssdc_bwd_chunk
+constexpr int kBwdChunkThreads = 512;  // threads of the chunk-gradient kernel
 
 // SIMT (exact fp32) kernels.
 __global__ void ssdc_simt_chunk_state(Problem p, Workspace ws);
