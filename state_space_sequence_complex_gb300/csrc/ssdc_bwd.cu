@@ -359,9 +359,10 @@ ssdc_bwd_passes(GradProblem g, Workspace ws, GradWorkspace gw) {
 //          term, and r_t.
 // A chunk of one block (Q <= 64) has a single block pair: part 2 then reuses
 // part 1's tiles (C, dY, B) and V instead of loading and forming them again.
-// 512 threads: warp w owns the 4 rows 4w .. 4w+3 of every 64 x 64 result and
-// lane c its columns c and c + 32, so on the diagonal block pair, where P and
-// V vanish above the diagonal, a warp's row sums start (or stop) at its rows.
+// 512 threads: each warp owns a strip of 4 consecutive rows of every 64 x 64
+// result and lane c its columns c and c + 32, so on the diagonal block pair,
+// where P and V vanish above the diagonal, a warp's row sums start (or stop)
+// at its rows.
 
 constexpr int kChunkThreads = kBwdChunkThreads;
 constexpr int kChunkWarps = kChunkThreads / 32;
@@ -396,8 +397,14 @@ ssdc_bwd_chunk(GradProblem g, Workspace ws, GradWorkspace gw) {
     const int tid = threadIdx.x;
     const int64_t bt0 = (int64_t)b * p.T + t0;
     const int64_t chunk = ((int64_t)b * H + h) * p.nc + c;
-    // micro-tile: rows rb + i (i < 4), cols cg + 32 j (j < 2)
-    const int warp = tid >> 5, cg = tid & 31, rb = 4 * warp;
+    // micro-tile: rows rb + i (i < 4), cols cg + 32 j (j < 2). Warp w owns row strip
+    // s(w); the causal loops' length grows (or shrinks) with s, and the strips are
+    // dealt so that the four warps w, w+4, w+8, w+12 that share a scheduler
+    // (w mod 4) get strips k, 7-k, 8+k, 15-k: equal work per scheduler.
+    const int warp = tid >> 5, cg = tid & 31;
+    const int wk = warp & 3, wm = warp >> 2;
+    const int strip = wm == 0 ? wk : wm == 1 ? 7 - wk : wm == 2 ? 8 + wk : 15 - wk;
+    const int rb = 4 * strip;
 
     if (tid < 32)
         chunk_cumsum_warp(p.dt + bt0 * H + h, H, valid, Q, p.A_re[h], p.A_im[h], sm.acs);
