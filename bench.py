@@ -273,6 +273,20 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+def reduce_param_grads(dA_re, dA_im):
+    """Data-parallel backward: every rank holds the gradients of its own batch rows;
+    dA, the gradient of the per-head parameter A, sums over all rows, so its two
+    planes are summed over the ranks (one all-reduce). Identity on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return
+    buf = torch.cat([dA_re.reshape(-1), dA_im.reshape(-1)])
+    dist.all_reduce(buf, op=dist.ReduceOp.SUM)
+    dA_re.copy_(buf[:dA_re.numel()].view_as(dA_re))
+    dA_im.copy_(buf[dA_re.numel():].view_as(dA_im))
+
+
 def device_layer_inputs(w, layer, dev, g):
     """The inputs of one layer of `w` drawn on the device (torch generator seeded with
     seed + layer) from the distributions of `inputs`: x, A, B_t, C_t planes and dt."""
@@ -293,11 +307,18 @@ def backward_workload(args, w):
     """Measurement mode for the backward pass: one step = ssd_complex_bwd over every layer
     of the workload (inputs and output gradients drawn on the device), L2 flushed before
     each step. With --real-x the model's case: x real, a loss of Re(y) alone (dy.im null)
-    and no final-state gradient."""
+    and no final-state gradient. Under torchrun each rank runs its own batch (data
+    parallel, weak scaling) and every step all-reduces dA over the ranks."""
     import torch
     from state_space_sequence_complex_gb300 import build, ssdc
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if dist.is_nccl_available() else "gloo")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     build.build()
     ssdc.load()
     Q = args.chunk or w.Q
@@ -305,14 +326,18 @@ def backward_workload(args, w):
     s = math.sqrt(0.5)
     layers = []
     for i in range(w.layers):
-        L = device_layer_inputs(w, i, dev, g)
+        L = device_layer_inputs(w, i + 1000 * rank_layer(rank), dev, g)
         dy = [torch.randn(w.B, w.T, w.H, w.D, device=dev, generator=g) * s for _ in range(2)]
         dfs = [torch.randn(w.B, w.H, w.N, w.D, device=dev, generator=g) * s for _ in range(2)]
         if args.real_x:
             L[1], dy[1], dfs = None, None, [None, None]
         layers.append(L + dy + dfs)
     b = ssdc.Backward(w.B, w.T, w.H, w.N, w.D, Q, "fp32", device=dev)
-    run = lambda: [b(*L) for L in layers]
+
+    def run():
+        for L in layers:
+            b(*L)
+            reduce_param_grads(b.grads["dA_re"], b.grads["dA_im"])
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     for i in range(max(args.warmup, 3)):
@@ -320,6 +345,9 @@ def backward_workload(args, w):
         run()
     torch.cuda.synchronize()
     sampler = ClockSampler(dev.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.1)
     ev = []
@@ -332,10 +360,13 @@ def backward_workload(args, w):
         ev.append((e0, e1))
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
     st = ssdc.ssd_complex_status(b.workspace)
     if st != ssdc.SSDC_OK:
         raise SystemExit(f"device status after timed steps: {ssdc.strerror(st)}")
     ms = sum(a.elapsed_time(e) for a, e in ev) / len(ev)
+    ms = max_over_ranks([ms], device=dev)[0]
     ssdc.timing_enable(True)
     per_kernel = []
     for k in range(min(args.steps, 50)):
@@ -357,24 +388,28 @@ def backward_workload(args, w):
     # dC_t (8 N each), dt and ddt (4 each)
     xb = 4.0 if args.real_x else 8.0
     bytes_unit = 3 * xb * w.D + 32.0 * w.N + 8.0
-    units = w.token_heads * w.layers
+    units = w.token_heads * w.layers * world
+    if rank != 0:
+        return
     cpu = None
-    if w.name == inputs.LAYER.name and Q == w.Q and not args.no_cpu_baseline and not args.real_x:
+    if (world == 1 and w.name == inputs.LAYER.name and Q == w.Q and not args.no_cpu_baseline
+            and not args.real_x):
         cpu = run_oracle_grad_baseline(w)
     line = {
         "metric": "complex-SSD bwd token·heads/s (exact fp32 gradients of every input)",
-        "value": units / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "value": units / (ms / 1000.0), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic, drawn on the device per layer",
         "config": {"workload": f"{w.name} Q{Q} backward" + (", real x, Re(y) loss" if args.real_x else ""),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N, "chunk_size": Q,
                    "layers": w.layers, "real_x": bool(args.real_x), "precision": "fp32",
-                   "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)"},
+                   "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"data parallel: {world} batch(es), dA all-reduced each step"},
         "roofline": {"bound": "alu", "kernel": names[top], "achieved": tf, "peak": alu_peak,
                      "peak_kind": alu_kind, "unit": "TFLOP/s", "frac": tf / alu_peak, "traffic": None,
                      "algorithmic_flops_per_launch": fl,
-                     "step_alu_frac": sum(fl_unit.values()) * units / (ms / 1000.0) / 1e12 / alu_peak,
-                     "hbm_step_frac": bytes_unit * units / (ms / 1000.0) / 1e9 / peaks()[0],
+                     "step_alu_frac": sum(fl_unit.values()) * units / world / (ms / 1000.0) / 1e12 / alu_peak,
+                     "hbm_step_frac": bytes_unit * units / world / (ms / 1000.0) / 1e9 / peaks()[0],
                      "kernel_ms": {n: m for n, m in zip(names, kmeans)}},
         "cpu_baseline": cpu,
         "e2e": None,
@@ -519,8 +554,8 @@ def other_workload(args, w):
 def main():
     args = parse()
     if args.backward:
-        if args.impl == "reference" or args.gpus != 1 or args.segments > 1:
-            raise SystemExit("the backward measurement runs on one GPU with --impl ours, unsegmented")
+        if args.impl == "reference" or args.segments > 1:
+            raise SystemExit("the backward measurement runs with --impl ours, unsegmented")
         backward_workload(args, inputs.ALL[args.workload])
         return
     if args.workload != "layer" or args.segments > 1 or args.real_x:

@@ -226,3 +226,16 @@ def test_scan_autograd_real_x_loss_of_re_y():
            "dB": n(leaves["B_re"]) + 1j * n(leaves["B_im"]),
            "dC": n(leaves["C_re"]) + 1j * n(leaves["C_im"]), "ddt": n(leaves["dt"])}
     check(got, ref, inp, "autograd, real x")
+
+
+@pytest.mark.parametrize("Q", [64, 256])
+def test_backward_long_sequence(Q):
+    """The long-memory workload's length (T = 65536: 1024 chunks at Q = 64) with its
+    slow decays, at N = D = 8 so that the oracle's stored states stay small: both chunk
+    recurrences run the full length, and dz is anchored in every chunk."""
+    Bn, T, H, D, N = 1, 65536, 2, 8, 8
+    inp = inputs.custom(Bn, T, H, D, N, seed=860 + Q, dt_mean=-2.0, dt_std=0.5,
+                        re_lo=-0.1, re_hi=-0.01)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=861)
+    s0 = state(inp, 862)
+    check(run_bwd(inp, og, Q, s0=s0), oracle_grads(inp, og, s0=s0), inp, f"long sequence Q{Q}")
