@@ -109,12 +109,7 @@ int setup_device_attrs() {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return SSDC_ERR_CUDA;
     if (major != 10 || minor != 3) return SSDC_ERR_DEVICE;
-    if (cudaFuncSetAttribute(ssdc::ssdc_simt_chunk_state, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssdc::simt_state_smem()) != cudaSuccess)
-        return SSDC_ERR_CUDA;
-    if (cudaFuncSetAttribute(ssdc::ssdc_simt_chunk_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ssdc::simt_scan_smem()) != cudaSuccess)
-        return SSDC_ERR_CUDA;
+    if (ssdc::simt_set_smem_attrs() != cudaSuccess) return SSDC_ERR_CUDA;
     if (ssdc::bwd_set_smem_attrs() != cudaSuccess) return SSDC_ERR_CUDA;
     g_attr_done[dev].store(1, std::memory_order_release);
     return SSDC_OK;
@@ -231,14 +226,11 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
     if (dims.precision == SSDC_PREC_FP32) {
-        const dim3 sgrid((unsigned)p.nc, (unsigned)p.H, (unsigned)p.B);
-        ssdc::ssdc_simt_chunk_state<<<sgrid, 256, ssdc::simt_state_smem(), stream>>>(p, w);
+        ssdc::simt_launch_chunk_state(p, w, stream);
         record_event(++launches, stream);
         ssdc::ssdc_state_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(p, w);
         record_event(++launches, stream);
-        const int lblocks = (p.Q + 63) / 64;
-        const dim3 cgrid((unsigned)(p.nc * lblocks), (unsigned)p.H, (unsigned)p.B);
-        ssdc::ssdc_simt_chunk_scan<<<cgrid, 256, ssdc::simt_scan_smem(), stream>>>(p, w);
+        ssdc::simt_launch_chunk_scan(p, w, stream);
         record_event(++launches, stream);
     } else if (use_fused(dims, chunk_size)) {
         const char* env = getenv("SSDC_FUSED_CLUSTER");

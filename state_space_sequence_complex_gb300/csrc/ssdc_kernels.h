@@ -64,10 +64,12 @@ constexpr int kBwdDtThreads = 256;
 constexpr int kBwdChunkThreads = 512;  // threads of the chunk-gradient kernel
 
 // SIMT (exact fp32) kernels.
-__global__ void ssdc_simt_chunk_state(Problem p, Workspace ws);
-__global__ void ssdc_simt_chunk_scan(Problem p, Workspace ws);
-size_t simt_state_smem();
-size_t simt_scan_smem();
+// SIMT kernels are templates (compile-time N = D = 64, or sizes from the
+// problem); these enqueue the right instantiation and set their shared-memory
+// limits.
+cudaError_t simt_set_smem_attrs();
+void simt_launch_chunk_state(const Problem& p, const Workspace& ws, cudaStream_t stream);
+void simt_launch_chunk_scan(const Problem& p, const Workspace& ws, cudaStream_t stream);
 
 // Inter-chunk state pass (fp32, both precisions).
 __global__ void ssdc_state_pass(Problem p, Workspace ws);
