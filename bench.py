@@ -147,7 +147,9 @@ def profiled_traffic(kernel: str):
     None if the kernel source changed since that capture."""
     import hashlib
     files = {"fused_kernel": ("profiles/fused_kernel_single_layer.md",
-                              "state_space_sequence_complex_gb300/csrc/ssdc_fused.cu")}
+                              "state_space_sequence_complex_gb300/csrc/ssdc_fused.cu"),
+             "bwd_chunk": ("profiles/bwd_chunk_single_layer.md",
+                           "state_space_sequence_complex_gb300/csrc/ssdc_bwd.cu")}
     if kernel not in files:
         return None
     prof, src = (os.path.join(ROOT, f) for f in files[kernel])
@@ -406,7 +408,9 @@ def backward_workload(args, w):
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
                    "parallelism": f"data parallel: {world} batch(es), dA all-reduced each step"},
         "roofline": {"bound": "alu", "kernel": names[top], "achieved": tf, "peak": alu_peak,
-                     "peak_kind": alu_kind, "unit": "TFLOP/s", "frac": tf / alu_peak, "traffic": None,
+                     "peak_kind": alu_kind, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                     "traffic": profiled_traffic(names[top]) if w.name == inputs.LAYER.name and Q == w.Q
+                     and not args.real_x else None,
                      "algorithmic_flops_per_launch": fl,
                      "step_alu_frac": sum(fl_unit.values()) * units / world / (ms / 1000.0) / 1e12 / alu_peak,
                      "hbm_step_frac": bytes_unit * units / world / (ms / 1000.0) / 1e9 / peaks()[0],

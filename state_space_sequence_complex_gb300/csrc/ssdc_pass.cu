@@ -18,7 +18,8 @@ namespace ssdc {
 
 constexpr int kPassAhead = 8;
 
-__global__ void __launch_bounds__(kPassThreads)
+// Capped at 128 registers so that two blocks fit on an SM (130 without the cap).
+__global__ void __launch_bounds__(kPassThreads, 2)
 ssdc_state_pass(Problem p, Workspace ws) {
     const int64_t bh = blockIdx.y;
     const int ND = p.N * p.D;
