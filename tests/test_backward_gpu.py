@@ -239,3 +239,17 @@ def test_backward_long_sequence(Q):
     og = inputs.output_grads(Bn, T, H, D, N, seed=861)
     s0 = state(inp, 862)
     check(run_bwd(inp, og, Q, s0=s0), oracle_grads(inp, og, s0=s0), inp, f"long sequence Q{Q}")
+
+
+def test_backward_dt_zero_and_growing_states():
+    """dt = 0 everywhere (A_bar = 2^A at every token) and Re(A) > 0 (the pages' Skill-2
+    example draws Re(A) around -1 with a tail above zero: the states grow), the latter on
+    a short sequence, where growth stays within fp32 range."""
+    Bn, T, H, D, N, Q = 2, 200, 2, 16, 16, 32
+    inp = inputs.custom(Bn, T, H, D, N, seed=870, dt_mode="zero")
+    og = inputs.output_grads(Bn, T, H, D, N, seed=871)
+    check(run_bwd(inp, og, Q), oracle_grads(inp, og), inp, "dt = 0")
+    Bn, T = 1, 48
+    inp = inputs.custom(Bn, T, H, D, N, seed=872, re_lo=0.01, re_hi=0.1)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=873)
+    check(run_bwd(inp, og, 16), oracle_grads(inp, og), inp, "Re(A) > 0")
