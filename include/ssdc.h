@@ -260,10 +260,13 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
  *   ddt_t = Re(dz_t conj(A)) sigmoid(dt_t),  dA = sum_{b,t} softplus(dt_t) dz_t
  *   d_initial_state = conj(A_bar_0) g_0
  * The library computes it chunk by chunk: it recomputes the chunk states
- * S_in[c], runs the adjoint state recurrence backwards over the chunks, forms
- * dx, dB_t and dC_t per chunk, and obtains dz_t from the identity
- *   dz_t = <d_final_state, final_state> + sum_{t' >= t} (<dC_t', C_t'> - <dB_t', B_t'>)
- * with <u, v> = sum u conj(v) (accumulated in fp64).
+ * S_in[c], runs the adjoint state recurrence backwards over the chunks (R_c,
+ * the gradient of the state leaving chunk c), forms dx, dB_t and dC_t per
+ * chunk, and obtains dz_t for token t of chunk c from the identity
+ *   dz_t = <R_c, S_out(c)> + sum_{t' >= t in chunk c} (<dC_t', C_t'> - <dB_t', B_t'>)
+ * with <u, v> = sum u conj(v), S_out(c) the state leaving chunk c, and the
+ * sums accumulated in fp64. dA is summed over b and t in a fixed order, so
+ * repeated calls give bit-identical results.
  *
  *   x, A, B_t, C_t, dt, initial_state   the forward pass's inputs, as for
  *                        ssd_complex_fwd_init (initial_state: both planes null
