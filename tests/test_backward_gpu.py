@@ -253,3 +253,50 @@ def test_backward_dt_zero_and_growing_states():
     inp = inputs.custom(Bn, T, H, D, N, seed=872, re_lo=0.01, re_hi=0.1)
     og = inputs.output_grads(Bn, T, H, D, N, seed=873)
     check(run_bwd(inp, og, 16), oracle_grads(inp, og), inp, "Re(A) > 0")
+
+
+def test_scan_autograd_through_segments():
+    """Two segments chained through the carried state (the second starts from the first's
+    final state), A shared between them: autograd through both calls gives the whole
+    sequence's gradients; dA accumulates over the two calls."""
+    Bn, T, H, D, N, Q, T1 = 1, 256, 2, 16, 16, 32, 128
+    inp = inputs.custom(Bn, T, H, D, N, seed=880)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=881)
+    arrs = inp.arrays()
+    A_re = cuda(arrs["A_re"]).requires_grad_(True)
+    A_im = cuda(arrs["A_im"]).requires_grad_(True)
+    seg = lambda a, b: {k: cuda(v[:, a:b]).requires_grad_(True) for k, v in arrs.items() if v.ndim > 1}
+    s1, s2 = seg(0, T1), seg(T1, T)
+    args = lambda s: (s["x_re"], s["x_im"], A_re, A_im, s["B_re"], s["B_im"], s["C_re"], s["C_im"], s["dt"])
+    y1r, y1i, f1r, f1i = ssdc.ssd_complex_scan(*args(s1), Q, precision="fp32")
+    y2r, y2i, f2r, f2i = ssdc.ssd_complex_scan(*args(s2), Q, s0_re=f1r, s0_im=f1i, precision="fp32")
+    gy_re, gy_im = cuda(og.dy_re), cuda(og.dy_im)
+    loss = ((y1r * gy_re[:, :T1]).sum() + (y1i * gy_im[:, :T1]).sum() + (y2r * gy_re[:, T1:]).sum()
+            + (y2i * gy_im[:, T1:]).sum() + (f2r * cuda(og.dfs_re)).sum() + (f2i * cuda(og.dfs_im)).sum())
+    loss.backward()
+    ref = oracle_grads(inp, og)
+    n = lambda t: t.grad.double().cpu().numpy()
+    cat = lambda k: np.concatenate([n(s1[k]), n(s2[k])], axis=1)
+    got = {"dx": cat("x_re") + 1j * cat("x_im"), "dB": cat("B_re") + 1j * cat("B_im"),
+           "dC": cat("C_re") + 1j * cat("C_im"), "ddt": cat("dt"), "dA": n(A_re) + 1j * n(A_im)}
+    check(got, ref, inp, "autograd through two segments")
+
+
+def test_scan_autograd_staged_forward():
+    """The staged TF32 forward (Q = 128) under autograd: the exact backward does not depend
+    on the forward's precision."""
+    Bn, T, H, D, N, Q = 1, 300, 2, 64, 64, 128
+    inp = inputs.custom(Bn, T, H, D, N, seed=890)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=891)
+    leaves = {k: cuda(v).requires_grad_(True) for k, v in inp.arrays().items()}
+    y_re, y_im, fs_re, fs_im = ssdc.ssd_complex_scan(*[leaves[k] for k in ORDER], Q, precision="tf32")
+    loss = ((y_re * cuda(og.dy_re)).sum() + (y_im * cuda(og.dy_im)).sum()
+            + (fs_re * cuda(og.dfs_re)).sum() + (fs_im * cuda(og.dfs_im)).sum())
+    loss.backward()
+    ref = oracle_grads(inp, og)
+    n = lambda t: t.grad.double().cpu().numpy()
+    got = {"dx": n(leaves["x_re"]) + 1j * n(leaves["x_im"]),
+           "dA": n(leaves["A_re"]) + 1j * n(leaves["A_im"]),
+           "dB": n(leaves["B_re"]) + 1j * n(leaves["B_im"]),
+           "dC": n(leaves["C_re"]) + 1j * n(leaves["C_im"]), "ddt": n(leaves["dt"])}
+    check(got, ref, inp, "autograd, staged TF32 forward")
