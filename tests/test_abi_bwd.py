@@ -142,3 +142,30 @@ def test_optional_nulls_pass_host_checks(lib):
                dfs_im=None, ds0_re=None, ds0_im=None)
     assert call(lib, opt, d, Q=32, ws=end) in PASSED_HOST_CHECKS
     assert call(lib, p, d, Q=32, ws=end) in PASSED_HOST_CHECKS
+
+
+def test_binding_rejects_unsupported_backward_before_allocating(lib):
+    """ssdc.Backward raises (no silent fallback) for a precision or size the backward
+    does not take, before any device memory is requested."""
+    with pytest.raises(ssdc.SSDCError):
+        ssdc.Backward(1, 128, 2, 64, 64, 64, precision="tf32", device="cpu")
+    with pytest.raises(ssdc.SSDCError):
+        ssdc.Backward(1, 128, 2, 64, 64, 48, device="cpu")
+    with pytest.raises(ssdc.SSDCError):
+        ssdc.Backward(1, 128, 2, 72, 64, 64, device="cpu")
+
+
+def test_header_documents_every_backward_output():
+    """Each output of ssd_complex_bwd is described in the header, with its shape."""
+    import os
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                             "include", "ssdc.h")).read()
+    start = text.index("Backward pass:")
+    doc = text[start:text.index("size_t ssd_complex_bwd_workspace_bytes")]
+    import re
+    for name, shape in (("dx", "(B,T,H,D)"), ("dA", "(H)"), ("dB_t, dC_t", "(B,T,H,N)"),
+                        ("ddt", "(B,T,H)"), ("d_initial_state", "(B,H,N,D)")):
+        # the argument lines: " *   <name>   output <shape> ..."
+        pat = re.compile(r"^\s*\*\s+" + re.escape(name) + r"\s{2,}output")
+        line = next(l for l in doc.splitlines() if pat.match(l))
+        assert shape in line, (name, line)
