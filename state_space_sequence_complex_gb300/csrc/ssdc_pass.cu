@@ -18,8 +18,7 @@ namespace ssdc {
 
 constexpr int kPassAhead = 8;
 
-// Capped at 128 registers so that two blocks fit on an SM (130 without the cap).
-__global__ void __launch_bounds__(kPassThreads, 2)
+__global__ void __launch_bounds__(kPassThreads)
 ssdc_state_pass(Problem p, Workspace ws) {
     const int64_t bh = blockIdx.y;
     const int ND = p.N * p.D;
