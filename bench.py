@@ -143,8 +143,16 @@ def fp32_alu_peak_tflops(dev_index: int):
 
 
 def profiled_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary of `kernel`, or
-    None if the kernel source changed since that capture."""
+    """DRAM bytes per launch (read + write) from the committed ncu summary of
+    `kernel`, or None if the kernel source changed since that capture."""
+    d = profiled_dram(kernel)
+    return None if d is None else d["traffic"]
+
+
+def profiled_dram(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`:
+    {"traffic", "read", "write"} (read and write None where the summary gives
+    only their sum), or None if the kernel source changed since that capture."""
     import hashlib
     files = {"fused_kernel": ("profiles/fused_kernel_single_layer.md",
                               "state_space_sequence_complex_gb300/csrc/ssdc_fused.cu"),
@@ -153,13 +161,17 @@ def profiled_traffic(kernel: str):
     if kernel not in files:
         return None
     prof, src = (os.path.join(ROOT, f) for f in files[kernel])
+    keys = ("traffic_bytes_per_launch", "dram_read_bytes_per_launch", "dram_write_bytes_per_launch",
+            "source_sha256_16")
     try:
         fields = dict(line.split(": ", 1) for line in open(prof).read().splitlines() if ": " in line
-                      and line.split(": ", 1)[0] in ("traffic_bytes_per_launch", "source_sha256_16"))
+                      and line.split(": ", 1)[0] in keys)
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if fields.get("source_sha256_16", "").strip() != digest:
             return None
-        return float(fields["traffic_bytes_per_launch"])
+        get = lambda k: float(fields[k]) if k in fields else None
+        return {"traffic": get("traffic_bytes_per_launch"), "read": get("dram_read_bytes_per_launch"),
+                "write": get("dram_write_bytes_per_launch")}
     except Exception:
         return None
 
@@ -643,6 +655,23 @@ def main():
         per_kernel.append(ssdc.timing_read())
     ssdc.timing_enable(False)
 
+    # ---- back to back without the L2 flush (consecutive layers of a model): host time
+    # per call (argument checks, cached launch set-up, the launch) against device time
+    # per call; the GPU never waits for the host while the host time is the smaller ----
+    b2b_calls = 200
+    torch.cuda.synchronize()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    t0 = time.perf_counter()
+    for _ in range(b2b_calls):
+        call()
+    host_s = time.perf_counter() - t0
+    b1.record(stream)
+    torch.cuda.synchronize()
+    back_to_back = {"calls": b2b_calls, "host_us_per_call": 1e6 * host_s / b2b_calls,
+                    "device_us_per_call": 1000.0 * b0.elapsed_time(b1) / b2b_calls,
+                    "l2": "not flushed between calls"}
+
     # ---- end to end through the C ABI with host buffers (ssd_complex_fwd_host): every
     # step copies its inputs from pinned host memory, runs the scan and copies y and the
     # final state back; the call returns when they are in host memory ----
@@ -687,12 +716,20 @@ def main():
     achieved = bytes_per_launch / (kmeans[top] / 1000.0) / 1e9
     step_achieved = bytes_per_launch / (ms / 1000.0) / 1e9 / 1.0
 
+    dram = profiled_dram(names[top])
     roofline = {"bound": "hbm", "kernel": names[top], "achieved": achieved, "peak": peak,
                 "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(names[top]),
+                "frac": achieved / peak, "traffic": None if dram is None else dram["traffic"],
                 "algorithmic_bytes_per_launch": bytes_per_launch,
                 "kernel_ms": {n: m for n, m in zip(names, kmeans)},
                 "step_frac": step_achieved / peak}
+    if dram is not None and dram["read"] is not None:
+        # the write count of one captured launch misses the part of y still in L2 when the
+        # kernel ends (written back later): reads are the comparable figure
+        roofline["traffic_read"] = dram["read"]
+        roofline["traffic_write"] = dram["write"]
+        roofline["traffic_note"] = ("ncu DRAM bytes of one launch; y lines still dirty in L2 at kernel "
+                                    "end are written back after it, so write < y bytes")
     if precision == "tf32" and len(kmeans) == 1:
         # context: the same launch against the TF32 tensor peak (the file's BF16 peak times the
         # nominal TF32 / BF16 ratio), with the algorithmic (causal) flops
@@ -730,6 +767,7 @@ def main():
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "back_to_back": back_to_back,
     }
     print(json.dumps(line), flush=True)
 

@@ -182,6 +182,26 @@ int ssd_complex_timing_enable(int enable);
 int ssd_complex_timing_read(float *ms, int n);
 
 /*
+ * Process-wide options (tuning and tests; normal use needs none of them).
+ * Each call sets one option for every later forward call, from any thread;
+ * returns SSDC_OK, or SSDC_ERR_INVALID for an unknown option or value. The
+ * library reads no environment variables.
+ *
+ *   SSDC_OPT_FUSED_CLUSTER        cluster size of the fused TF32 kernel:
+ *                                 0 = chosen per call (default), or 1, 2, 4, 8
+ *   SSDC_OPT_FUSED_PLANE_MAPS     1 (default): one tensor map fetches both planes
+ *                                 of a tensor where it can; 0: one map per plane
+ *   SSDC_OPT_TEST_DROP_STATE_CHUNK  test hook, -1 = off (default): the fused
+ *                                 kernel does not send the state of this chunk
+ *                                 index to the next CTA, whose bounded wait then
+ *                                 gives up and records SSDC_ERR_TIMEOUT
+ */
+#define SSDC_OPT_FUSED_CLUSTER 1
+#define SSDC_OPT_FUSED_PLANE_MAPS 2
+#define SSDC_OPT_TEST_DROP_STATE_CHUNK 3
+int ssd_complex_set_option(int option, int64_t value);
+
+/*
  * Forward pass that allocates nothing, for callers that cannot allocate
  * device memory when they run the scan (code running inside a memory-pool or
  * allocator hook, latency-critical paths that forbid allocator calls, or
@@ -198,16 +218,29 @@ int ssd_complex_timing_read(float *ms, int n);
  * routine.
  *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it for the life of the process; make that
+ * first call before any stream capture, and do not use the library across a
+ * device reset (cudaDeviceReset), which would leave that address stale.
  * All calls share the one array and leave their chunk states in it: calls
  * whose work may overlap on the GPU (different streams, or threads without
  * ordering) race on it and must be serialised by the caller. The array needs
- * no clearing between calls.
+ * no clearing between calls: each call clears the status word at its start,
+ * and every chunk state is written before it is read.
+ *
+ * A device-side error (a bounded wait that gave up) is recorded in the
+ * array's status word; ssd_complex_noalloc_status() reads it.
  */
 #define SSDC_NOALLOC_SCRATCH_BYTES ((size_t)32 * 1024 * 1024 + (size_t)64 * 1024)
 int ssd_complex_fwd_noalloc(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
                             const float *dt, ssdc_dims dims, int chunk_size,
                             ssdc_cout y, ssdc_cout final_state, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns the device status the last
+ * ssd_complex_fwd_noalloc call on the current device recorded (SSDC_OK or
+ * SSDC_ERR_TIMEOUT), or SSDC_ERR_CUDA if the stream reports an error. It
+ * allocates nothing: the status word is read from the static array with
+ * cudaMemcpyFromSymbol. */
+int ssd_complex_noalloc_status(cudaStream_t stream);
 
 /*
  * Forward pass on HOST buffers: the library copies the inputs to the device,

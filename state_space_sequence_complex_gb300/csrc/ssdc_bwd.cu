@@ -70,7 +70,6 @@ ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw) {
     const int tid = threadIdx.x;
     const int64_t bt0 = (int64_t)b * p.T + t0;
     const int64_t chunk = ((int64_t)b * H + h) * p.nc + c;
-    if (c == 0 && h == 0 && b == 0 && tid == 0) *ws.status = SSDC_OK;
 
     if (tid < 32)
         chunk_cumsum_warp(p.dt + bt0 * H + h, H, valid, Q, p.A_re[h], p.A_im[h], sm.acs);

@@ -45,6 +45,7 @@
 // from the workers; warp 17 issues the TMA loads of the next chunk into the
 // other stage of a two-stage ring and computes its cumulative log-decay.
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -288,10 +289,9 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     const uint32_t CL = items.cl, rank = items.rank;
     const uint32_t succ = (rank + 1) % CL, pred = (rank + CL - 1) % CL;
 
-    if (tid == 0 && blockIdx.x == 0) *ws.status = SSDC_OK;
     // the swizzled tiles need a 1024-byte aligned base (uniform across the grid)
     if (ptx::smem_addr(smem_raw) & 1023u) {
-        if (tid == 0) atomicExch(ws.status, SSDC_ERR_CUDA);
+        if (tid == 0) atomicCAS(ws.status, SSDC_OK, SSDC_ERR_CUDA);
         return;
     }
     if (tid == 0) {
@@ -826,14 +826,91 @@ int set_attrs(int dev) {
 
 }  // namespace
 
+namespace {
+
+// Per-call host work is kept off the launch path: the cluster choice is cached
+// per (device, sequences, chunks), and the tensor maps per (pointers, sizes).
+struct ClusterKey {
+    int dev;
+    int64_t nseq, nc;
+};
+struct ClusterChoice {
+    ClusterKey key;
+    int cl, nclusters;
+};
+struct MapKey {
+    const void* ptr[7];
+    int64_t T;
+    int B, H;
+    bool fast;
+};
+struct MapEntry {
+    MapKey key;
+    FusedMaps maps;
+};
+constexpr int kCacheSlots = 16;
+std::mutex g_cache_mu;
+ClusterChoice g_cluster_cache[kCacheSlots];
+int g_cluster_used = 0, g_cluster_next = 0;
+MapEntry g_map_cache[kCacheSlots];
+int g_map_used = 0, g_map_next = 0;
+
+bool same_map_key(const MapKey& a, const MapKey& b) {
+    for (int i = 0; i < 7; ++i)
+        if (a.ptr[i] != b.ptr[i]) return false;
+    return a.T == b.T && a.B == b.B && a.H == b.H && a.fast == b.fast;
+}
+
+// The launch's tensor maps, encoded once per pointer set and size.
+int cached_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
+    MapKey k;
+    memset(&k, 0, sizeof(k));
+    const void* ptrs[7] = {p.x_re, p.x_im, p.B_re, p.B_im, p.C_re, p.C_im, nullptr};
+    for (int i = 0; i < 7; ++i) k.ptr[i] = ptrs[i];
+    k.T = p.T;
+    k.B = p.B;
+    k.H = p.H;
+    k.fast = allow_fast;
+    {
+        std::lock_guard<std::mutex> g(g_cache_mu);
+        for (int i = 0; i < g_map_used; ++i)
+            if (same_map_key(g_map_cache[i].key, k)) {
+                *fm = g_map_cache[i].maps;
+                return SSDC_OK;
+            }
+    }
+    const int rc = make_fused_maps(p, allow_fast, fm);
+    if (rc != SSDC_OK) return rc;
+    std::lock_guard<std::mutex> g(g_cache_mu);
+    MapEntry& e = g_map_cache[g_map_next];
+    e.key = k;
+    e.maps = *fm;
+    g_map_next = (g_map_next + 1) % kCacheSlots;
+    if (g_map_used < kCacheSlots) ++g_map_used;
+    return SSDC_OK;
+}
+
+}  // namespace
+
 // Choose the cluster size: the one that minimises (waves of clusters) x
 // (chunks per CTA, or the serial state chain if that is longer).
 int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSDC_ERR_CUDA;
+    const int64_t nseq = (int64_t)p.B * p.H;
+    {
+        std::lock_guard<std::mutex> g(g_cache_mu);
+        for (int i = 0; i < g_cluster_used; ++i) {
+            const ClusterChoice& c = g_cluster_cache[i];
+            if (c.key.dev == dev && c.key.nseq == nseq && c.key.nc == p.nc) {
+                *cl_out = c.cl;
+                *nclusters_out = c.nclusters;
+                return SSDC_OK;
+            }
+        }
+    }
     const int arc = set_attrs(dev);
     if (arc != SSDC_OK) return arc;
-    const int64_t nseq = (int64_t)p.B * p.H;
     double best = 1e300;
     int best_cl = 1, best_n = 1;
     for (int cl = 1; cl <= 8; cl *= 2) {
@@ -868,6 +945,10 @@ int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
     }
     *cl_out = best_cl;
     *nclusters_out = best_n;
+    std::lock_guard<std::mutex> g(g_cache_mu);
+    g_cluster_cache[g_cluster_next] = ClusterChoice{ClusterKey{dev, nseq, p.nc}, best_cl, best_n};
+    g_cluster_next = (g_cluster_next + 1) % kCacheSlots;
+    if (g_cluster_used < kCacheSlots) ++g_cluster_used;
     return SSDC_OK;
 }
 
@@ -890,7 +971,7 @@ int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int
         nclusters = (int)(nseq < fit ? nseq : fit);
     }
     fused::FusedMaps fm;
-    rc = fused::make_fused_maps(p, plane_maps, &fm);
+    rc = fused::cached_maps(p, plane_maps, &fm);
     if (rc != SSDC_OK) return rc;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

@@ -20,6 +20,11 @@ namespace {
 
 thread_local int g_last_launches = 0;
 
+// Process-wide options (ssd_complex_set_option); read on every call, set rarely.
+std::atomic<int> g_opt_cluster{0};           // SSDC_OPT_FUSED_CLUSTER: 0 = chosen per call
+std::atomic<int> g_opt_plane_maps{1};        // SSDC_OPT_FUSED_PLANE_MAPS
+std::atomic<int64_t> g_opt_drop_state_chunk{-1};  // SSDC_OPT_TEST_DROP_STATE_CHUNK: -1 = off
+
 // Instrumentation events (see ssd_complex_timing_enable).
 constexpr int kMaxTimed = 8;
 bool g_timing = false;
@@ -214,15 +219,14 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     p.T = dims.T; p.B = (int)dims.B; p.H = (int)dims.H; p.N = (int)dims.N; p.D = (int)dims.D;
     p.Q = chunk_size;
     p.nc = ssdc::ceil_div64(dims.T, chunk_size);
-    {
-        const char* drop = getenv("SSDC_TEST_DROP_STATE_CHUNK");
-        p.drop_send_chunk = drop ? atoll(drop) : -1;
-    }
+    p.drop_send_chunk = g_opt_drop_state_chunk.load(std::memory_order_relaxed);
     ssdc::Workspace w = carve(workspace, dims, chunk_size);
 
     (void)cudaGetLastError();  // clear a stale error from unrelated work
     int launches = 0;
     if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
+    // the status word starts at SSDC_OK; a kernel's failed wait records the first error
+    if (cudaMemsetAsync(w.status, 0, sizeof(int), stream) != cudaSuccess) return SSDC_ERR_CUDA;
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
     if (dims.precision == SSDC_PREC_FP32) {
@@ -233,13 +237,8 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
         ssdc::simt_launch_chunk_scan(p, w, stream);
         record_event(++launches, stream);
     } else if (use_fused(dims, chunk_size)) {
-        const char* env = getenv("SSDC_FUSED_CLUSTER");
-        const int force = env ? atoi(env) : 0;
-        if (force != 0 && force != 1 && force != 2 && force != 4 && force != 8) return SSDC_ERR_INVALID;
-        // SSDC_FUSED_PLANE_MAPS=0 makes the kernel fetch each plane with its own copies (the
-        // path taken when the two planes of a tensor cannot share one tensor map)
-        const char* pm = getenv("SSDC_FUSED_PLANE_MAPS");
-        const bool plane_maps = !(pm && pm[0] == '0' && pm[1] == 0);
+        const int force = g_opt_cluster.load(std::memory_order_relaxed);
+        const bool plane_maps = g_opt_plane_maps.load(std::memory_order_relaxed) != 0;
         const int n = ssdc::fused_launch(p, w, stream, force, plane_maps);
         if (n < 0) return n;
         launches += n;
@@ -304,6 +303,24 @@ const char* ssd_complex_strerror(int status) {
 }
 
 int ssd_complex_last_launch_count(void) { return g_last_launches; }
+
+int ssd_complex_set_option(int option, int64_t value) {
+    switch (option) {
+        case SSDC_OPT_FUSED_CLUSTER:
+            if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return SSDC_ERR_INVALID;
+            g_opt_cluster.store((int)value);
+            return SSDC_OK;
+        case SSDC_OPT_FUSED_PLANE_MAPS:
+            if (value != 0 && value != 1) return SSDC_ERR_INVALID;
+            g_opt_plane_maps.store((int)value);
+            return SSDC_OK;
+        case SSDC_OPT_TEST_DROP_STATE_CHUNK:
+            if (value < -1) return SSDC_ERR_INVALID;
+            g_opt_drop_state_chunk.store(value);
+            return SSDC_OK;
+        default: return SSDC_ERR_INVALID;
+    }
+}
 
 int ssd_complex_timing_enable(int enable) {
     if (enable && !g_events_made) {
@@ -463,6 +480,7 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     (void)cudaGetLastError();  // clear a stale error from unrelated work
     int launches = 0;
     if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
+    if (cudaMemsetAsync(w.status, 0, sizeof(int), stream) != cudaSuccess) return SSDC_ERR_CUDA;
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
     ssdc::bwd_launch_chunk_states(g, w, gw, stream);

@@ -55,6 +55,16 @@ extern "C" int ssd_complex_fwd_noalloc(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssd
     const int arc = scratch_address(&ws);
     if (arc != SSDC_OK) return arc;
     // The staged paths need no zeroed workspace: every chunk state is written
-    // before it is read, and the first kernel resets the status word.
+    // before it is read, and the call clears the status word on the stream.
     return ssd_complex_fwd_ws(x, A, B_t, C_t, dt, dims, chunk_size, y, final_state, ws, kScratchBytes, stream);
+}
+
+// The status word is the first int of the array (the workspace layout of the
+// staged paths); it is copied out by symbol, with no allocation.
+extern "C" int ssd_complex_noalloc_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SSDC_ERR_CUDA;
+    int status = SSDC_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&status, g_scratch, sizeof(int), 0, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SSDC_ERR_CUDA;
+    return status;
 }

@@ -43,7 +43,6 @@ ssdc_simt_chunk_state(Problem p, Workspace ws) {
     const int valid = chunk_valid(p, t0);
     const int tid = threadIdx.x;
     const int64_t bt0 = (int64_t)b * p.T + t0;
-    if (c == 0 && h == 0 && b == 0 && tid == 0) *ws.status = SSDC_OK;
 
     if (tid < 32)
         chunk_cumsum_warp(p.dt + bt0 * H + h, H, valid, Q, p.A_re[h], p.A_im[h], sm.acs);

@@ -67,7 +67,6 @@ tc_chunk_state(Problem p, Workspace ws, const __grid_constant__ TcMaps maps) {
     const int Q = p.Q, H = p.H;
     const int64_t t0 = (int64_t)c * Q;
     const int nvalid = (int)(p.T - t0 < (int64_t)Q ? p.T - t0 : (int64_t)Q);
-    if (c == 0 && h == 0 && b == 0 && tid == 0) *ws.status = SSDC_OK;
 
     if (tid == 0) {
         ptx::mbar_init(&sm.bar_in, 1);

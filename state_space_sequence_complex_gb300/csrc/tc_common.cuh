@@ -81,7 +81,9 @@ __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
     return tmem + (((uint32_t)(warp & 3) * 32u) << 16);
 }
 
-__device__ __forceinline__ void fail(int* status) { atomicExch(status, SSDC_ERR_TIMEOUT); }
+// Record a wait that gave up. The status word is cleared on the stream before a
+// call's first launch; the first error recorded sticks.
+__device__ __forceinline__ void fail(int* status) { atomicCAS(status, SSDC_OK, SSDC_ERR_TIMEOUT); }
 
 template <int kCols>
 __device__ __forceinline__ void tmem_store(uint32_t taddr, const float* v) {

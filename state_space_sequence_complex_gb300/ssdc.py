@@ -30,7 +30,13 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
            "ssd_complex_fwd", "ssd_complex_status", "ssd_complex_strerror",
            "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read",
            "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host",
-           "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd")
+           "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd",
+           "ssd_complex_set_option", "ssd_complex_noalloc_status")
+
+# ssd_complex_set_option keys
+OPT_FUSED_CLUSTER = 1
+OPT_FUSED_PLANE_MAPS = 2
+OPT_TEST_DROP_STATE_CHUNK = 3
 
 
 class ssdc_dims(ctypes.Structure):
@@ -96,6 +102,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_timing_enable.restype = ctypes.c_int
     lib.ssd_complex_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int]
     lib.ssd_complex_timing_read.restype = ctypes.c_int
+    lib.ssd_complex_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
+    lib.ssd_complex_set_option.restype = ctypes.c_int
+    lib.ssd_complex_noalloc_status.argtypes = [vp]
+    lib.ssd_complex_noalloc_status.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -375,6 +385,39 @@ def ssd_complex_status(workspace, stream=None) -> int:
 
     s = torch.cuda.current_stream() if stream is None else stream
     return load().ssd_complex_status(_ptr(workspace), ctypes.c_void_p(s.cuda_stream))
+
+
+def ssd_complex_noalloc_status(stream=None) -> int:
+    """Device status of the last ssd_complex_fwd_noalloc call (syncs the stream)."""
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return load().ssd_complex_noalloc_status(ctypes.c_void_p(s.cuda_stream))
+
+
+def set_option(option: int, value: int) -> None:
+    """Set a process-wide option of the library (ssd_complex_set_option)."""
+    rc = load().ssd_complex_set_option(int(option), int(value))
+    if rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_set_option")
+
+
+class option:
+    """Context manager: set an option for the duration of a block, then restore
+    `restore` (the option's default)."""
+
+    DEFAULTS = {OPT_FUSED_CLUSTER: 0, OPT_FUSED_PLANE_MAPS: 1, OPT_TEST_DROP_STATE_CHUNK: -1}
+
+    def __init__(self, key: int, value: int):
+        self.key, self.value = key, value
+
+    def __enter__(self):
+        set_option(self.key, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        set_option(self.key, self.DEFAULTS[self.key])
+        return False
 
 
 def last_launch_count() -> int:

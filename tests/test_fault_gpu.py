@@ -20,16 +20,16 @@ def built():
     ssdc.load()
 
 
-def test_dropped_state_times_out_then_recovers(monkeypatch):
+def test_dropped_state_times_out_then_recovers(lib_option):
     import torch
-    monkeypatch.setenv("SSDC_FUSED_CLUSTER", "2")
+    lib_option(ssdc.OPT_FUSED_CLUSTER, 2)
     inp = inputs.custom(1, 128, 1, 64, 64, seed=5)  # two chunks on a 2-CTA cluster
     dev = to_device(inp)
     f = ssdc.Forward(*inp.dims, 64, "tf32")
-    monkeypatch.setenv("SSDC_TEST_DROP_STATE_CHUNK", "0")
+    lib_option(ssdc.OPT_TEST_DROP_STATE_CHUNK, 0)
     f(*[dev[k] for k in ORDER])
     torch.cuda.synchronize()
     assert f.status() == ssdc.SSDC_ERR_TIMEOUT
-    monkeypatch.delenv("SSDC_TEST_DROP_STATE_CHUNK")
+    lib_option(ssdc.OPT_TEST_DROP_STATE_CHUNK, -1)
     y, s, _ = run_library(inp, 64, "tf32", dev=dev, forward=f)
     assert_close(y, s, *naive_scan_inputs(inp), "tf32", "after a timed-out call")

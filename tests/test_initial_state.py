@@ -74,10 +74,10 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}T{}H{}D{}N{}Q{}-{}-CL{}".format(*c))
-def test_initial_state_matches_oracle(case, monkeypatch):
+def test_initial_state_matches_oracle(case, lib_option):
     Bn, T, H, D, N, Q, precision, cl = case
     if cl:
-        monkeypatch.setenv("SSDC_FUSED_CLUSTER", str(cl))
+        lib_option(ssdc.OPT_FUSED_CLUSTER, cl)
     inp = inputs.custom(Bn, T, H, D, N, seed=400 + T + H)
     s0 = random_state(inp, seed=T)
     y_ref, s_ref = oracle(inp, s0)
@@ -94,11 +94,11 @@ def test_zero_initial_state_is_the_plain_scan(precision):
 
 
 @pytest.mark.parametrize("precision,cl", [("fp32", 0), ("tf32", 1), ("tf32", 4)])
-def test_segments_continue_in_place(precision, cl, monkeypatch):
+def test_segments_continue_in_place(precision, cl, lib_option):
     """[0, T1) then [T1, T) started from the carried final state (the Forward's own
     final-state tensors passed back as the initial state) equals the whole scan."""
     if cl:
-        monkeypatch.setenv("SSDC_FUSED_CLUSTER", str(cl))
+        lib_option(ssdc.OPT_FUSED_CLUSTER, cl)
     Bn, T, H, D, N, Q = 2, 768, 3, 64, 64, 64
     T1 = 320
     inp = inputs.custom(Bn, T, H, D, N, seed=441)

@@ -103,15 +103,15 @@ def test_staged_tf32_path(T, Q):
 
 
 @pytest.mark.parametrize("cluster", [1, 2, 4, 8])
-def test_fused_cluster_sizes(cluster, monkeypatch):
+def test_fused_cluster_sizes(cluster, lib_option):
     # several sequences per cluster, a partial last chunk, more chunks than CTAs
-    monkeypatch.setenv("SSDC_FUSED_CLUSTER", str(cluster))
+    lib_option(ssdc.OPT_FUSED_CLUSTER, cluster)
     inp = inputs.custom(2, 64 * 9 + 13, 3, 64, 64, seed=3000 + cluster)
     check(inp, 64, "tf32", f"fused cluster {cluster}")
 
 
-def test_fused_fewer_chunks_than_cluster(monkeypatch):
-    monkeypatch.setenv("SSDC_FUSED_CLUSTER", "8")
+def test_fused_fewer_chunks_than_cluster(lib_option):
+    lib_option(ssdc.OPT_FUSED_CLUSTER, 8)
     inp = inputs.custom(1, 130, 2, 64, 64, seed=31)   # 3 chunks on an 8-CTA cluster
     check(inp, 64, "tf32", "3 chunks, cluster 8")
 
@@ -137,11 +137,11 @@ def _planes_in_order(t, name, imag_first):
 
 @pytest.mark.parametrize("plane_maps", ["1", "0"])
 @pytest.mark.parametrize("order", ["re_first", "im_first", "mixed"])
-def test_fused_tensor_map_paths(order, plane_maps, monkeypatch):
+def test_fused_tensor_map_paths(order, plane_maps, lib_option):
     # T a multiple of 8 (the interleaved C map applies) with a partial last chunk; each
     # tensor's planes either in one map (in either address order) or in one map per plane
-    monkeypatch.setenv("SSDC_FUSED_CLUSTER", "2")
-    monkeypatch.setenv("SSDC_FUSED_PLANE_MAPS", plane_maps)
+    lib_option(ssdc.OPT_FUSED_CLUSTER, 2)
+    lib_option(ssdc.OPT_FUSED_PLANE_MAPS, int(plane_maps))
     inp = inputs.custom(2, 64 * 5 + 24, 3, 64, 64, seed=3100)
     y_ref, s_ref = naive_scan_inputs(inp)
     t = to_device(inp)

@@ -55,10 +55,10 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}T{}H{}D{}N{}Q{}-{}-CL{}".format(*c))
-def test_real_x_matches_oracle_and_zero_plane(case, monkeypatch):
+def test_real_x_matches_oracle_and_zero_plane(case, lib_option):
     Bn, T, H, D, N, Q, precision, cl = case
     if cl:
-        monkeypatch.setenv("SSDC_FUSED_CLUSTER", str(cl))
+        lib_option(ssdc.OPT_FUSED_CLUSTER, cl)
     inp = inputs.custom(Bn, T, H, D, N, seed=500 + T + H)
     y_ref, s_ref = oracle_real(inp)
     y, s = run(inp, Q, precision)
