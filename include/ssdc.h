@@ -191,6 +191,9 @@ int ssd_complex_timing_read(float *ms, int n);
  *                                 0 = chosen per call (default), or 1, 2, 4, 8
  *   SSDC_OPT_FUSED_PLANE_MAPS     1 (default): one tensor map fetches both planes
  *                                 of a tensor where it can; 0: one map per plane
+ *   SSDC_OPT_FUSED_KERNEL         fused TF32 kernel: 0 = chosen per call
+ *                                 (default), 1 = the cluster kernel, 2 = the
+ *                                 kernel with the state in tensor memory
  *   SSDC_OPT_TEST_DROP_STATE_CHUNK  test hook, -1 = off (default): the fused
  *                                 kernel does not send the state of this chunk
  *                                 index to the next CTA, whose bounded wait then
@@ -199,6 +202,7 @@ int ssd_complex_timing_read(float *ms, int n);
 #define SSDC_OPT_FUSED_CLUSTER 1
 #define SSDC_OPT_FUSED_PLANE_MAPS 2
 #define SSDC_OPT_TEST_DROP_STATE_CHUNK 3
+#define SSDC_OPT_FUSED_KERNEL 4
 int ssd_complex_set_option(int option, int64_t value);
 
 /*

@@ -24,6 +24,7 @@ thread_local int g_last_launches = 0;
 std::atomic<int> g_opt_cluster{0};           // SSDC_OPT_FUSED_CLUSTER: 0 = chosen per call
 std::atomic<int> g_opt_plane_maps{1};        // SSDC_OPT_FUSED_PLANE_MAPS
 std::atomic<int64_t> g_opt_drop_state_chunk{-1};  // SSDC_OPT_TEST_DROP_STATE_CHUNK: -1 = off
+std::atomic<int> g_opt_kernel{0};            // SSDC_OPT_FUSED_KERNEL: 0 = chosen per call
 
 // Instrumentation events (see ssd_complex_timing_enable).
 constexpr int kMaxTimed = 8;
@@ -64,14 +65,19 @@ int check_sizes(const ssdc_dims& d, int Q) {
     if (d.precision == SSDC_PREC_FP32) {
         if (!is_pow2_in(Q, 16, 256)) return SSDC_ERR_UNSUPPORTED;
         if (d.N % 8 || d.D % 8 || d.N > 64 || d.D > 64) return SSDC_ERR_UNSUPPORTED;
-    } else {
+    } else if (d.precision == SSDC_PREC_TF32_STAGED) {
         if (!ssdc::tc_supported((int)d.N, (int)d.D, Q)) return SSDC_ERR_UNSUPPORTED;
+    } else {
+        if (!ssdc::tc_supported((int)d.N, (int)d.D, Q) && !ssdc::fused2_supported((int)d.N, (int)d.D, Q))
+            return SSDC_ERR_UNSUPPORTED;
     }
     return SSDC_OK;
 }
 
+// TF32 sizes that one of the two fused kernels runs (the others take the staged path).
 bool use_fused(const ssdc_dims& d, int Q) {
-    return d.precision == SSDC_PREC_TF32 && ssdc::fused_supported((int)d.N, (int)d.D, Q);
+    return d.precision == SSDC_PREC_TF32 &&
+           (ssdc::fused_supported((int)d.N, (int)d.D, Q) || ssdc::fused2_supported((int)d.N, (int)d.D, Q));
 }
 
 size_t ws_bytes_for(const ssdc_dims& d, int Q) {
@@ -239,7 +245,26 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     } else if (use_fused(dims, chunk_size)) {
         const int force = g_opt_cluster.load(std::memory_order_relaxed);
         const bool plane_maps = g_opt_plane_maps.load(std::memory_order_relaxed) != 0;
-        const int n = ssdc::fused_launch(p, w, stream, force, plane_maps);
+        // the cluster kernel takes Q = N = D = 64 only; there it runs when a forced cluster size
+        // asks for it, or when the sequences are too few to fill the GPU one CTA each (it splits
+        // them over cluster CTAs); otherwise the kernel with the state in tensor memory runs
+        int kernel = g_opt_kernel.load(std::memory_order_relaxed);
+        const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q);
+        if (kernel == 0) {
+            if (!cluster_ok) {
+                kernel = 2;
+            } else if (force > 0) {
+                kernel = 1;
+            } else {
+                int cl = 1;
+                rc = ssdc::fused_cluster_choice(p, &cl);
+                if (rc != SSDC_OK) return rc;
+                kernel = cl > 1 ? 1 : 2;
+            }
+        }
+        if (kernel == 1 && !cluster_ok) return SSDC_ERR_UNSUPPORTED;
+        const int n = kernel == 2 ? ssdc::fused2_launch(p, w, stream, plane_maps)
+                                  : ssdc::fused_launch(p, w, stream, force, plane_maps);
         if (n < 0) return n;
         launches += n;
         record_event(launches, stream);
@@ -313,6 +338,10 @@ int ssd_complex_set_option(int option, int64_t value) {
         case SSDC_OPT_FUSED_PLANE_MAPS:
             if (value != 0 && value != 1) return SSDC_ERR_INVALID;
             g_opt_plane_maps.store((int)value);
+            return SSDC_OK;
+        case SSDC_OPT_FUSED_KERNEL:
+            if (value < 0 || value > 2) return SSDC_ERR_INVALID;
+            g_opt_kernel.store((int)value);
             return SSDC_OK;
         case SSDC_OPT_TEST_DROP_STATE_CHUNK:
             if (value < -1) return SSDC_ERR_INVALID;

@@ -86,7 +86,15 @@ bool tc_supported(int N, int D, int Q);
 // size; 1, 2, 4 or 8 forces it. plane_maps = false fetches every plane with
 // its own tensor map even where one map could fetch both.
 bool fused_supported(int N, int D, int Q);
+// The cluster size the cluster kernel would choose for this problem (1: one CTA
+// per sequence fills the GPU).
+int fused_cluster_choice(const Problem& p, int* cl);
 int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster, bool plane_maps);
+
+// Fused TF32 kernel with the chunk state in tensor memory: one CTA per SM walks
+// whole sequences. Q in {16, 32, 64}; N, D multiples of 8 up to 64.
+bool fused2_supported(int N, int D, int Q);
+int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bool plane_maps);
 
 // Launch count reported by ssd_complex_last_launch_count() for the calling thread.
 void set_last_launch_count(int n);

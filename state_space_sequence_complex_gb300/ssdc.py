@@ -37,6 +37,7 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
 OPT_FUSED_CLUSTER = 1
 OPT_FUSED_PLANE_MAPS = 2
 OPT_TEST_DROP_STATE_CHUNK = 3
+OPT_FUSED_KERNEL = 4
 
 
 class ssdc_dims(ctypes.Structure):
@@ -406,7 +407,7 @@ class option:
     """Context manager: set an option for the duration of a block, then restore
     `restore` (the option's default)."""
 
-    DEFAULTS = {OPT_FUSED_CLUSTER: 0, OPT_FUSED_PLANE_MAPS: 1, OPT_TEST_DROP_STATE_CHUNK: -1}
+    DEFAULTS = {OPT_FUSED_CLUSTER: 0, OPT_FUSED_PLANE_MAPS: 1, OPT_TEST_DROP_STATE_CHUNK: -1, OPT_FUSED_KERNEL: 0}
 
     def __init__(self, key: int, value: int):
         self.key, self.value = key, value

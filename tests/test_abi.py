@@ -45,7 +45,15 @@ def test_supported_sets(lib):
     assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == 0
     assert ok(ssdc.dims(2, 2048, 16, 64, 64, "fp32"), 64) == 0
     assert ok(ssdc.dims(1, 128, 2, 8, 8, "fp32"), 16) == 0
-    assert ok(ssdc.dims(1, 128, 2, 8, 8, "tf32"), 16) == ssdc.SSDC_ERR_UNSUPPORTED
+    # TF32: Q = 16 / 32 / 64 with N, D multiples of 8 up to 64 (the fused kernels), and
+    # Q = 128 / 256 with N = D = 64 (the staged path)
+    assert ok(ssdc.dims(1, 128, 2, 8, 8, "tf32"), 16) == 0
+    assert ok(ssdc.dims(1, 128, 2, 8, 24, "tf32"), 32) == 0
+    assert ok(ssdc.dims(1, 128, 2, 12, 64, "tf32"), 64) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 72, 64, "tf32"), 64) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 32, 64, "tf32"), 128) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 64, 64, "tf32"), 256) == 0
+    assert ok(ssdc.dims(1, 128, 2, 8, 8, "tf32_staged"), 16) == ssdc.SSDC_ERR_UNSUPPORTED
     assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 48) == ssdc.SSDC_ERR_UNSUPPORTED
     assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 512) == ssdc.SSDC_ERR_UNSUPPORTED
     assert ok(ssdc.dims(1, 128, 2, 72, 64, "fp32"), 64) == ssdc.SSDC_ERR_UNSUPPORTED
@@ -68,7 +76,9 @@ def test_workspace_bytes(lib):
         assert nb >= chunks * 2 * 64 * 64 * 4 + chunks * 8 + 4
     # the fused tensor-core path keeps the chunk states on chip: status word only
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == 256
-    # at other chunk sizes the TF32 path stages the states
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(1, 128, 2, 8, 8, "tf32"), 16) == 256
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 32) == 256
+    # at Q = 128 and 256 the TF32 path stages the states
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 128) > 256
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 48) == 0
     # uneven T rounds the chunk count up
@@ -156,7 +166,7 @@ def test_rejects_overlapping_outputs(lib):
 
 
 def test_rejects_unsupported_before_launch(lib):
-    d = ssdc.dims(1, 128, 2, 64, 64, "tf32")
+    d = ssdc.dims(1, 128, 2, 64, 64, "tf32_staged")
     ptrs, end = fake_ptrs(d)
     assert _call(lib, ptrs, d, Q=16, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
     d = ssdc.dims(1, 128, 2, 64, 64, 3)

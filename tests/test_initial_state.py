@@ -55,7 +55,7 @@ def oracle(inp, s0):
     return naive_scan_inputs(inp, s0=s0_32)
 
 
-# (B, T, H, D, N, Q, precision, cluster): T not a multiple of Q in several; 40 sequences
+# (B, T, H, D, N, Q, precision, cluster; -1: the tensor-memory kernel): T not a multiple of Q in several; 40 sequences
 # at clusters of 4 and 8 give clusters that own two sequences (a state from the last CTA
 # of the cluster follows an initial state in the first CTA's buffer).
 CASES = [
@@ -70,14 +70,21 @@ CASES = [
     (5, 640, 8, 64, 64, 64, "tf32", 4),
     (5, 640, 8, 64, 64, 64, "tf32", 8),
     (5, 136, 8, 64, 64, 64, "tf32", 4),
+    (1, 200, 2, 16, 16, 32, "tf32", 0),
+    (2, 130, 3, 8, 24, 16, "tf32", 0),
+    (2, 330, 3, 64, 64, 64, "tf32", -1),
+    (20, 200, 8, 64, 64, 64, "tf32", -1),
+    (20, 136, 8, 64, 64, 32, "tf32", -1),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}T{}H{}D{}N{}Q{}-{}-CL{}".format(*c))
 def test_initial_state_matches_oracle(case, lib_option):
     Bn, T, H, D, N, Q, precision, cl = case
-    if cl:
+    if cl > 0:
         lib_option(ssdc.OPT_FUSED_CLUSTER, cl)
+    elif cl < 0:  # the fused kernel with the state in tensor memory
+        lib_option(ssdc.OPT_FUSED_KERNEL, 2)
     inp = inputs.custom(Bn, T, H, D, N, seed=400 + T + H)
     s0 = random_state(inp, seed=T)
     y_ref, s_ref = oracle(inp, s0)
@@ -93,12 +100,14 @@ def test_zero_initial_state_is_the_plain_scan(precision):
     assert np.array_equal(y0, y1) and np.array_equal(s0, s1)
 
 
-@pytest.mark.parametrize("precision,cl", [("fp32", 0), ("tf32", 1), ("tf32", 4)])
+@pytest.mark.parametrize("precision,cl", [("fp32", 0), ("tf32", 1), ("tf32", 4), ("tf32", -1)])
 def test_segments_continue_in_place(precision, cl, lib_option):
     """[0, T1) then [T1, T) started from the carried final state (the Forward's own
     final-state tensors passed back as the initial state) equals the whole scan."""
-    if cl:
+    if cl > 0:
         lib_option(ssdc.OPT_FUSED_CLUSTER, cl)
+    elif cl < 0:  # the fused kernel with the state in tensor memory
+        lib_option(ssdc.OPT_FUSED_KERNEL, 2)
     Bn, T, H, D, N, Q = 2, 768, 3, 64, 64, 64
     T1 = 320
     inp = inputs.custom(Bn, T, H, D, N, seed=441)

@@ -47,10 +47,46 @@ def test_uneven_and_edge_lengths(T, Q, precision):
     check(inp, Q, precision, f"T={T} Q={Q}")
 
 
+@pytest.mark.parametrize("precision", PRECISIONS)
 @pytest.mark.parametrize("N,D", [(8, 8), (16, 64), (64, 8), (32, 24), (56, 40)])
-def test_state_and_head_sizes_fp32(N, D):
+def test_state_and_head_sizes(N, D, precision):
     inp = inputs.custom(2, 200, 3, D, N, seed=N * 100 + D)
-    check(inp, 64, "fp32", f"N={N} D={D}")
+    check(inp, 64, precision, f"N={N} D={D}")
+
+
+# The fused kernel with the state in tensor memory, forced: every chunk size it takes,
+# feature sizes below the tile (zero columns), ragged tails, T < Q, T = Q.
+@pytest.mark.parametrize("N,D,Q,T", [(8, 8, 16, 128), (8, 8, 16, 90), (16, 64, 32, 257), (64, 8, 64, 200),
+                                     (32, 24, 16, 333), (56, 40, 32, 1000), (64, 64, 16, 300), (64, 64, 32, 1000),
+                                     (64, 64, 64, 64 * 9 + 13), (24, 48, 32, 20), (64, 64, 64, 64), (8, 16, 16, 1)])
+def test_tensor_memory_kernel(N, D, Q, T, lib_option):
+    lib_option(ssdc.OPT_FUSED_KERNEL, 2)
+    inp = inputs.custom(2, T, 3, D, N, seed=5000 + N + D + Q + T)
+    check(inp, Q, "tf32", f"tensor-memory kernel N={N} D={D} Q={Q} T={T}")
+
+
+@pytest.mark.parametrize("Q", [32, 64])
+def test_tensor_memory_kernel_several_sequences_per_cta(Q, lib_option):
+    # 160 sequences on at most 152 CTAs: some CTAs walk two sequences
+    lib_option(ssdc.OPT_FUSED_KERNEL, 2)
+    inp = inputs.custom(20, 200, 8, 64, 64, seed=5100 + Q)
+    check(inp, Q, "tf32", f"160 sequences Q={Q}")
+
+
+def test_both_fused_kernels_on_one_problem(lib_option):
+    # the same inputs through the cluster kernel (forced 2-CTA clusters) and the
+    # tensor-memory kernel: each against the oracle
+    inp = inputs.custom(3, 64 * 7 + 5, 5, 64, 64, seed=5200)
+    ref = naive_scan_inputs(inp)
+    out = {}
+    for kernel in (1, 2):
+        lib_option(ssdc.OPT_FUSED_KERNEL, kernel)
+        if kernel == 1:
+            lib_option(ssdc.OPT_FUSED_CLUSTER, 2)
+        y, s, _ = run_library(inp, 64, "tf32")
+        assert_close(y, s, *ref, "tf32", f"fused kernel {kernel}")
+        out[kernel] = (y, s)
+    assert rel_fro(out[1][0], out[2][0]) <= TOL["tf32"]
 
 
 @pytest.mark.parametrize("precision", PRECISIONS)
@@ -135,12 +171,16 @@ def _planes_in_order(t, name, imag_first):
     t[name + "_re"], t[name + "_im"] = (buf[1], buf[0]) if imag_first else (buf[0], buf[1])
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("plane_maps", ["1", "0"])
 @pytest.mark.parametrize("order", ["re_first", "im_first", "mixed"])
-def test_fused_tensor_map_paths(order, plane_maps, lib_option):
+def test_fused_tensor_map_paths(order, plane_maps, kernel, lib_option):
     # T a multiple of 8 (the interleaved C map applies) with a partial last chunk; each
-    # tensor's planes either in one map (in either address order) or in one map per plane
-    lib_option(ssdc.OPT_FUSED_CLUSTER, 2)
+    # tensor's planes either in one map (in either address order) or in one map per plane;
+    # the cluster kernel (2-CTA clusters) and the tensor-memory kernel
+    lib_option(ssdc.OPT_FUSED_KERNEL, kernel)
+    if kernel == 1:
+        lib_option(ssdc.OPT_FUSED_CLUSTER, 2)
     lib_option(ssdc.OPT_FUSED_PLANE_MAPS, int(plane_maps))
     inp = inputs.custom(2, 64 * 5 + 24, 3, 64, 64, seed=3100)
     y_ref, s_ref = naive_scan_inputs(inp)

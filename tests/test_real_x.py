@@ -51,14 +51,19 @@ CASES = [
     (2, 330, 3, 64, 64, 64, "tf32", 2),
     (2, 640, 3, 64, 64, 64, "tf32", 4),
     (1, 640, 2, 64, 64, 64, "tf32", 8),
+    (1, 200, 2, 16, 16, 32, "tf32", 0),
+    (2, 330, 3, 64, 64, 64, "tf32", -1),
+    (20, 200, 8, 64, 64, 64, "tf32", -1),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}T{}H{}D{}N{}Q{}-{}-CL{}".format(*c))
 def test_real_x_matches_oracle_and_zero_plane(case, lib_option):
     Bn, T, H, D, N, Q, precision, cl = case
-    if cl:
+    if cl > 0:
         lib_option(ssdc.OPT_FUSED_CLUSTER, cl)
+    elif cl < 0:  # the fused kernel with the state in tensor memory
+        lib_option(ssdc.OPT_FUSED_KERNEL, 2)
     inp = inputs.custom(Bn, T, H, D, N, seed=500 + T + H)
     y_ref, s_ref = oracle_real(inp)
     y, s = run(inp, Q, precision)
