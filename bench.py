@@ -156,6 +156,8 @@ def profiled_dram(kernel: str):
     import hashlib
     files = {"fused_kernel": ("profiles/fused_kernel_single_layer.md",
                               "state_space_sequence_complex_gb300/csrc/ssdc_fused.cu"),
+             "fused_tmem_kernel": ("profiles/fused_tmem_kernel_training_batch.md",
+                                   "state_space_sequence_complex_gb300/csrc/ssdc_fused2.cu"),
              "bwd_chunk": ("profiles/bwd_chunk_single_layer.md",
                            "state_space_sequence_complex_gb300/csrc/ssdc_bwd.cu")}
     if kernel not in files:
@@ -534,7 +536,9 @@ def other_workload(args, w):
     ssdc.timing_enable(False)
     nk = min(len(p) for p in per_kernel)
     kmeans = [sum(p[i] for p in per_kernel) / len(per_kernel) for i in range(nk)]
-    names = {1: ["fused_kernel"], 3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
+    path = ssdc.last_path()
+    names = {1: ["fused_tmem_kernel" if path == "fused_tmem" else "fused_kernel"],
+             3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
         nk, [f"launch{i}" for i in range(nk)])
     top = int(np.argmax(kmeans))
     peak, peak_kind = peaks()
@@ -553,6 +557,7 @@ def other_workload(args, w):
                    + (", real x" if args.real_x else ""), "real_x": bool(args.real_x),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
                    "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
+                   "path": path,
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)"},
         "roofline": {"bound": "hbm", "kernel": names[top], "achieved": bytes_per_launch / (launch_ms / 1000.0) / 1e9,
                      "peak": peak, "peak_kind": f"{peak_kind} HBM copy GB/s (burst)", "unit": "GB/s",
@@ -708,7 +713,9 @@ def main():
     # dominant kernel: the launch with the largest mean device time
     nk = min(len(p) for p in per_kernel)
     kmeans = [sum(p[i] for p in per_kernel) / len(per_kernel) for i in range(nk)]
-    names = {1: ["fused_kernel"], 3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
+    path = ssdc.last_path()
+    names = {1: ["fused_tmem_kernel" if path == "fused_tmem" else "fused_kernel"],
+             3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
         nk, [f"launch{i}" for i in range(nk)])
     top = int(np.argmax(kmeans))
     peak, peak_kind = peaks()
@@ -758,7 +765,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
-                   "chunk_size": w.Q, "seed": w.seed, "precision": precision,
+                   "chunk_size": w.Q, "seed": w.seed, "precision": precision, "path": path,
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
                    "parallelism": f"weak: {world} independent batch(es), no collective"},
         "roofline": roofline,

@@ -170,6 +170,25 @@ const char *ssd_complex_strerror(int status);
  * stream (from the calling thread). */
 int ssd_complex_last_launch_count(void);
 
+/* The path the last successful forward call took (from the calling thread),
+ * or -1 before the first:
+ *   SSDC_PATH_STAGED_FP32    exact fp32: chunk states, state pass, chunk outputs
+ *   SSDC_PATH_STAGED_TF32    the same three launches on the tensor cores
+ *   SSDC_PATH_FUSED_CLUSTER  one launch; each sequence's chunks dealt over the
+ *                            CTAs of a thread-block cluster, chunk states passed
+ *                            through distributed shared memory (Q = N = D = 64)
+ *   SSDC_PATH_FUSED_TMEM     one launch; one CTA per SM walks whole sequences,
+ *                            the chunk state held in tensor memory (Q = 16, 32,
+ *                            64; N, D multiples of 8 up to 64)
+ * SSDC_PREC_TF32 takes SSDC_PATH_FUSED_TMEM wherever the sequences fill the GPU
+ * one CTA each, SSDC_PATH_FUSED_CLUSTER for fewer sequences at Q = N = D = 64,
+ * and the staged path for Q = 128 and 256. */
+#define SSDC_PATH_STAGED_FP32 0
+#define SSDC_PATH_STAGED_TF32 1
+#define SSDC_PATH_FUSED_CLUSTER 2
+#define SSDC_PATH_FUSED_TMEM 3
+int ssd_complex_last_path(void);
+
 /*
  * Per-kernel timing (instrumentation for benchmarks). While enabled, every
  * forward call records a CUDA event on its stream before its first launch and

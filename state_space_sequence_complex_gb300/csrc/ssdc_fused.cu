@@ -686,6 +686,7 @@ struct ClusterKey {
 struct ClusterChoice {
     ClusterKey key;
     int cl, nclusters;
+    double cost;
 };
 constexpr int kCacheSlots = 16;
 std::mutex g_cache_mu;
@@ -694,8 +695,9 @@ int g_cluster_used = 0, g_cluster_next = 0;
 }  // namespace
 
 // Choose the cluster size: the one that minimises (waves of clusters) x
-// (chunks per CTA, or the serial state chain if that is longer).
-int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
+// (chunks per CTA, or the serial state chain if that is longer). *cost_out is
+// that minimum, in units of one CTA's time for one chunk.
+int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out, double* cost_out = nullptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSDC_ERR_CUDA;
     const int64_t nseq = (int64_t)p.B * p.H;
@@ -706,6 +708,7 @@ int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
             if (c.key.dev == dev && c.key.nseq == nseq && c.key.nc == p.nc) {
                 *cl_out = c.cl;
                 *nclusters_out = c.nclusters;
+                if (cost_out) *cost_out = c.cost;
                 return SSDC_OK;
             }
         }
@@ -746,8 +749,9 @@ int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
     }
     *cl_out = best_cl;
     *nclusters_out = best_n;
+    if (cost_out) *cost_out = best;
     std::lock_guard<std::mutex> g(g_cache_mu);
-    g_cluster_cache[g_cluster_next] = ClusterChoice{ClusterKey{dev, nseq, p.nc}, best_cl, best_n};
+    g_cluster_cache[g_cluster_next] = ClusterChoice{ClusterKey{dev, nseq, p.nc}, best_cl, best_n, best};
     g_cluster_next = (g_cluster_next + 1) % kCacheSlots;
     if (g_cluster_used < kCacheSlots) ++g_cluster_used;
     return SSDC_OK;
@@ -757,9 +761,9 @@ int pick_cluster(const Problem& p, int* cl_out, int* nclusters_out) {
 
 bool fused_supported(int N, int D, int Q) { return N == 64 && D == 64 && Q == 64; }
 
-int fused_cluster_choice(const Problem& p, int* cl) {
+int fused_cluster_choice(const Problem& p, int* cl, double* cost) {
     int n = 1;
-    return fused::pick_cluster(p, cl, &n);
+    return fused::pick_cluster(p, cl, &n, cost);
 }
 
 int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster, bool plane_maps) {

@@ -19,6 +19,7 @@
 namespace {
 
 thread_local int g_last_launches = 0;
+thread_local int g_last_path = -1;
 
 // Process-wide options (ssd_complex_set_option); read on every call, set rarely.
 std::atomic<int> g_opt_cluster{0};           // SSDC_OPT_FUSED_CLUSTER: 0 = chosen per call
@@ -235,6 +236,7 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     if (cudaMemsetAsync(w.status, 0, sizeof(int), stream) != cudaSuccess) return SSDC_ERR_CUDA;
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
+    int path = SSDC_PATH_STAGED_FP32;
     if (dims.precision == SSDC_PREC_FP32) {
         ssdc::simt_launch_chunk_state(p, w, stream);
         record_event(++launches, stream);
@@ -245,9 +247,12 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     } else if (use_fused(dims, chunk_size)) {
         const int force = g_opt_cluster.load(std::memory_order_relaxed);
         const bool plane_maps = g_opt_plane_maps.load(std::memory_order_relaxed) != 0;
-        // the cluster kernel takes Q = N = D = 64 only; there it runs when a forced cluster size
-        // asks for it, or when the sequences are too few to fill the GPU one CTA each (it splits
-        // them over cluster CTAs); otherwise the kernel with the state in tensor memory runs
+        // The cluster kernel takes Q = N = D = 64 only; there it runs when a forced cluster size
+        // asks for it, or when its estimated time is the shorter. Estimates, from per-chunk
+        // times measured on a GB300 at full occupancy: the tensor-memory kernel walks
+        // ceil(sequences / SMs) x chunks at about 3.7 us a chunk; the cluster kernel, its chosen
+        // cost at about 4.1 us a chunk with one CTA per sequence and 5.2 us with the state
+        // handed between CTAs.
         int kernel = g_opt_kernel.load(std::memory_order_relaxed);
         const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q);
         if (kernel == 0) {
@@ -256,19 +261,28 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
             } else if (force > 0) {
                 kernel = 1;
             } else {
-                int cl = 1;
-                rc = ssdc::fused_cluster_choice(p, &cl);
+                int cl = 1, dev = 0, sms = 0;
+                double cost = 0.0;
+                rc = ssdc::fused_cluster_choice(p, &cl, &cost);
                 if (rc != SSDC_OK) return rc;
-                kernel = cl > 1 ? 1 : 2;
+                if (cudaGetDevice(&dev) != cudaSuccess ||
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+                    return SSDC_ERR_CUDA;
+                const int64_t nseq = (int64_t)p.B * p.H;
+                const double t_tmem = 3.7 * (double)((nseq + sms - 1) / sms) * (double)p.nc;
+                const double t_cluster = (cl > 1 ? 5.2 : 4.1) * cost;
+                kernel = t_tmem <= t_cluster ? 2 : 1;
             }
         }
         if (kernel == 1 && !cluster_ok) return SSDC_ERR_UNSUPPORTED;
         const int n = kernel == 2 ? ssdc::fused2_launch(p, w, stream, plane_maps)
                                   : ssdc::fused_launch(p, w, stream, force, plane_maps);
         if (n < 0) return n;
+        path = kernel == 2 ? SSDC_PATH_FUSED_TMEM : SSDC_PATH_FUSED_CLUSTER;
         launches += n;
         record_event(launches, stream);
     } else {
+        path = SSDC_PATH_STAGED_TF32;
         int n = ssdc::tc_launch_chunk_state(p, w, stream);
         if (n < 0) return n;
         launches += n;
@@ -282,6 +296,7 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     }
     if (cudaGetLastError() != cudaSuccess) return SSDC_ERR_CUDA;
     g_last_launches = launches;
+    g_last_path = path;
     if (g_timing) g_timed_launches = launches;
     return SSDC_OK;
 }
@@ -289,6 +304,8 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
 }  // namespace
 
 extern "C" {
+
+int ssd_complex_last_path(void) { return g_last_path; }
 
 int ssd_complex_fwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt,
                     ssdc_dims dims, int chunk_size, ssdc_cout y, ssdc_cout final_state,

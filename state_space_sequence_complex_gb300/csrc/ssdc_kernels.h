@@ -86,9 +86,10 @@ bool tc_supported(int N, int D, int Q);
 // size; 1, 2, 4 or 8 forces it. plane_maps = false fetches every plane with
 // its own tensor map even where one map could fetch both.
 bool fused_supported(int N, int D, int Q);
-// The cluster size the cluster kernel would choose for this problem (1: one CTA
-// per sequence fills the GPU).
-int fused_cluster_choice(const Problem& p, int* cl);
+// The cluster size the cluster kernel would choose for this problem, and its
+// estimated length in chunk-times of one CTA (waves x the longer of a CTA's
+// chunks and the state chain).
+int fused_cluster_choice(const Problem& p, int* cl, double* cost);
 int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster, bool plane_maps);
 
 // Fused TF32 kernel with the chunk state in tensor memory: one CTA per SM walks

@@ -31,7 +31,9 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
            "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read",
            "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host",
            "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd",
-           "ssd_complex_set_option", "ssd_complex_noalloc_status")
+           "ssd_complex_set_option", "ssd_complex_noalloc_status", "ssd_complex_last_path")
+
+PATHS = {0: "staged_fp32", 1: "staged_tf32", 2: "fused_cluster", 3: "fused_tmem"}
 
 # ssd_complex_set_option keys
 OPT_FUSED_CLUSTER = 1
@@ -105,6 +107,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_timing_read.restype = ctypes.c_int
     lib.ssd_complex_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
     lib.ssd_complex_set_option.restype = ctypes.c_int
+    lib.ssd_complex_last_path.argtypes = []
+    lib.ssd_complex_last_path.restype = ctypes.c_int
     lib.ssd_complex_noalloc_status.argtypes = [vp]
     lib.ssd_complex_noalloc_status.restype = ctypes.c_int
     _lib = lib
@@ -423,6 +427,11 @@ class option:
 
 def last_launch_count() -> int:
     return load().ssd_complex_last_launch_count()
+
+
+def last_path() -> str:
+    """Name of the path the calling thread's last forward call took (ssd_complex_last_path)."""
+    return PATHS.get(load().ssd_complex_last_path(), "none")
 
 
 def timing_enable(on: bool = True) -> None:
