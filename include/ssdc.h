@@ -150,6 +150,36 @@ int ssd_complex_fwd_init(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
                          void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Joining segments of a sequence split in time (across ranks or calls). The
+ * state pass between chunks (landing page "03 Chunkwise SSD", the STATE line:
+ * a state carried forward is multiplied by the exponential of the accumulated
+ * log-decay) applied to whole segments: a segment with total decay a_seg and
+ * end state S_seg (scanned from a zero state) takes the incoming state S_in to
+ * a_seg S_in + S_seg, and consecutive segments compose as
+ *   (a2, S2) o (a1, S1) = (a2 a1, a2 S1 + S2).
+ * A rank that holds segment r of T therefore scans it from zero, gathers the
+ * (a_seg, S_seg) of the segments before it, combines them in order into its
+ * incoming state, and scans its segment again from that state
+ * (ssd_complex_fwd_init) for its rows of y and its final state.
+ *
+ * ssd_complex_segment_decay: a_seg[b,h] = exp(sum_t softplus(dt[b,t,h]) A[h])
+ * over the T tokens of dt (B,T,H); the sum and the exponential in fp64.
+ *   A       (H) complex;  dt (B,T,H);  a_seg  output (B,H) complex
+ * Uses dims.B, T, H; pointers 16-byte aligned device pointers; one launch on
+ * `stream`. Errors as for ssd_complex_fwd_ws.
+ *
+ * ssd_complex_state_combine: s_out = a s_in + s_add, per (b, h) with a[b,h]:
+ *   a       (B,H) complex;  s_in, s_add, s_out (B,H,N,D) complex
+ *   s_in    both planes NULL for a zero incoming state (s_out = s_add)
+ * s_out may be s_in or s_add (element-wise, in place). Uses dims.B, H, N, D;
+ * one launch on `stream`.
+ */
+int ssd_complex_segment_decay(ssdc_cin A, const float *dt, ssdc_dims dims,
+                              ssdc_cout a_seg, cudaStream_t stream);
+int ssd_complex_state_combine(ssdc_cin a, ssdc_cin s_in, ssdc_cin s_add, ssdc_dims dims,
+                              ssdc_cout s_out, cudaStream_t stream);
+
+/*
  * Forward pass that allocates its workspace on `stream` (cudaMallocAsync /
  * cudaFreeAsync, stream-ordered). A device-side error cannot be queried after
  * it returns; use the _ws form with ssd_complex_status() to read one.

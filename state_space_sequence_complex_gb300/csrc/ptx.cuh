@@ -358,6 +358,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// A float rounded to TF32 (10 explicit mantissa bits), to nearest with ties
+// away from zero: half a TF32 ulp added to the magnitude bits, then the 13 low
+// bits cleared (a carry moves into the exponent, as rounding up should; +-Inf
+// stay infinite). The TF32 MMA itself drops the low 13 bits of an fp32 operand
+// (truncation, measured): operands the threads write are rounded here first,
+// which roughly halves their rounding error. Two integer operations, where the
+// conversion instruction runs on a slower pipe.
+__device__ __forceinline__ float to_tf32(float v) {
+    return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
+}
+
 // ------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor for tcgen05 (64 bit):
 //   [0,14)  start address >> 4        [16,30) leading byte offset >> 4

@@ -466,8 +466,12 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 
             // ---- B: x^T (interleaved rows d) in place of x; C' = C o exp(Acs[l]) rows into TMEM
             {
-                const float4 o[4] = {make_float4(xv[0].x, xv[1].x, xv[2].x, xv[3].x), make_float4(xv[0].y, xv[1].y, xv[2].y, xv[3].y),
-                                     make_float4(xv[0].z, xv[1].z, xv[2].z, xv[3].z), make_float4(xv[0].w, xv[1].w, xv[2].w, xv[3].w)};
+                using ptx::to_tf32;
+                const float4 o[4] = {
+                    make_float4(to_tf32(xv[0].x), to_tf32(xv[1].x), to_tf32(xv[2].x), to_tf32(xv[3].x)),
+                    make_float4(to_tf32(xv[0].y), to_tf32(xv[1].y), to_tf32(xv[2].y), to_tf32(xv[3].y)),
+                    make_float4(to_tf32(xv[0].z), to_tf32(xv[1].z), to_tf32(xv[2].z), to_tf32(xv[3].z)),
+                    make_float4(to_tf32(xv[0].w), to_tf32(xv[1].w), to_tf32(xv[2].w), to_tf32(xv[3].w))};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int mm = inter_m(4 * xdb + j, xp);
@@ -486,10 +490,10 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 for (int j = 0; j < 4; ++j) {
                     const float2 cr = *reinterpret_cast<const float2*>(cbase + pair_off(kh, cre, 8 * j + 2 * lq));
                     const float2 ci = *reinterpret_cast<const float2*>(cbase + pair_off(kh, cim, 8 * j + 2 * lq));
-                    w[4 * j + 0] = cr.x * e.x - ci.x * e.y;
-                    w[4 * j + 1] = cr.y * e.x - ci.y * e.y;
-                    w[4 * j + 2] = cr.x * e.y + ci.x * e.x;
-                    w[4 * j + 3] = cr.y * e.y + ci.y * e.x;
+                    w[4 * j + 0] = ptx::to_tf32(cr.x * e.x - ci.x * e.y);
+                    w[4 * j + 1] = ptx::to_tf32(cr.y * e.x - ci.y * e.y);
+                    w[4 * j + 2] = ptx::to_tf32(cr.x * e.y + ci.x * e.x);
+                    w[4 * j + 3] = ptx::to_tf32(cr.y * e.y + ci.y * e.x);
                 }
                 ptx::tmem_st_16x256b_x4(tl + kCwin + 32 * kh, w);
             }
@@ -531,8 +535,8 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const float2 v = cmul(dv[i], j ? make_float2(bv[0][i].y, bv[1][i].y) : make_float2(bv[0][i].x, bv[1][i].x));
-                        ore[i] = v.x;
-                        oim[i] = v.y;
+                        ore[i] = ptx::to_tf32(v.x);
+                        oim[i] = ptx::to_tf32(v.y);
                     }
                     *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 0, nr) + chunk16(bsb & 7, nr)) =
                         make_float4(ore[0], ore[1], ore[2], ore[3]);
@@ -573,10 +577,10 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     const float2 g1 = make_float2(ga[4 * j + kRr + 1] - gb[4 * j + kRi + 1],
                                                   gb[4 * j + kRr + 1] + ga[4 * j + kRi + 1]);
                     const float2 p0 = cmul(g0, L0), p1 = cmul(g1, L1);
-                    w[4 * j + 0] = p0.x;
-                    w[4 * j + 1] = p1.x;
-                    w[4 * j + 2] = p0.y;
-                    w[4 * j + 3] = p1.y;
+                    w[4 * j + 0] = ptx::to_tf32(p0.x);
+                    w[4 * j + 1] = ptx::to_tf32(p1.x);
+                    w[4 * j + 2] = ptx::to_tf32(p0.y);
+                    w[4 * j + 3] = ptx::to_tf32(p1.y);
                 }
                 ptx::tmem_st_16x256b_x4(tl + kPwin + 32 * kh, w);
                 // P and C' rows of this warp are in TMEM

@@ -400,7 +400,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                         r[k] = *reinterpret_cast<const float*>(rowbase + sr * 128 + chunk16(cq, sr));
                     }
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = xp ? r[k ^ 4] : r[k];
+                    for (int k = 0; k < 16; ++k) v[k] = ptx::to_tf32(xp ? r[k ^ 4] : r[k]);
                 }
                 ptx::tmem_st16(lane_base(tmem, warp) + kXwin + 16 * cg, v);
             }
@@ -438,8 +438,8 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const float2 v = cmul(dv[i], j ? make_float2(bv[0][i].y, bv[1][i].y) : make_float2(bv[0][i].x, bv[1][i].x));
-                        ore[i] = v.x;
-                        oim[i] = v.y;
+                        ore[i] = ptx::to_tf32(v.x);
+                        oim[i] = ptx::to_tf32(v.y);
                     }
                     *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 0, nr) + chunk16(bsb & 7, nr)) =
                         make_float4(ore[0], ore[1], ore[2], ore[3]);
@@ -467,10 +467,13 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     const float2 e = sm.eacs[s][8 * g + i];
                     const float4 v0 = *reinterpret_cast<const float4*>(r0), v1 = *reinterpret_cast<const float4*>(r1);
                     const float4 cr = kSwapC ? v1 : v0, ci = kSwapC ? v0 : v1;
-                    *reinterpret_cast<float4*>(r0) = make_float4(cr.x * e.x - ci.x * e.y, cr.y * e.x - ci.y * e.y,
-                                                                 cr.z * e.x - ci.z * e.y, cr.w * e.x - ci.w * e.y);
-                    *reinterpret_cast<float4*>(r1) = make_float4(cr.x * e.y + ci.x * e.x, cr.y * e.y + ci.y * e.x,
-                                                                 cr.z * e.y + ci.z * e.x, cr.w * e.y + ci.w * e.x);
+                    using ptx::to_tf32;
+                    *reinterpret_cast<float4*>(r0) =
+                        make_float4(to_tf32(cr.x * e.x - ci.x * e.y), to_tf32(cr.y * e.x - ci.y * e.y),
+                                    to_tf32(cr.z * e.x - ci.z * e.y), to_tf32(cr.w * e.x - ci.w * e.y));
+                    *reinterpret_cast<float4*>(r1) =
+                        make_float4(to_tf32(cr.x * e.y + ci.x * e.x), to_tf32(cr.y * e.y + ci.y * e.x),
+                                    to_tf32(cr.z * e.y + ci.z * e.x), to_tf32(cr.w * e.y + ci.w * e.x));
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::tc_fence_before();  // the y loads of D precede the Y_off MMA
@@ -512,8 +515,10 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 const int mre = inter_m(rr, 0), mim = inter_m(rr, 1);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    *reinterpret_cast<float2*>(bbase + pair_off(kh, mre, 8 * j + 2 * lq)) = make_float2(pv[j][0].x, pv[j][1].x);
-                    *reinterpret_cast<float2*>(bbase + pair_off(kh, mim, 8 * j + 2 * lq)) = make_float2(pv[j][0].y, pv[j][1].y);
+                    *reinterpret_cast<float2*>(bbase + pair_off(kh, mre, 8 * j + 2 * lq)) =
+                        make_float2(ptx::to_tf32(pv[j][0].x), ptx::to_tf32(pv[j][1].x));
+                    *reinterpret_cast<float2*>(bbase + pair_off(kh, mim, 8 * j + 2 * lq)) =
+                        make_float2(ptx::to_tf32(pv[j][0].y), ptx::to_tf32(pv[j][1].y));
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::tc_fence_before();  // the C B^T loads precede the next C B^T MMA

@@ -66,8 +66,11 @@ __device__ __forceinline__ void transpose_tile(const float* src, float* dst, int
             const int r = 4 * rb + i;
             v[i] = *reinterpret_cast<const float4*>(sp + r * 128 + (((cb & 7) ^ (r & 7)) << 4));
         }
-        const float4 o[4] = {make_float4(v[0].x, v[1].x, v[2].x, v[3].x), make_float4(v[0].y, v[1].y, v[2].y, v[3].y),
-                             make_float4(v[0].z, v[1].z, v[2].z, v[3].z), make_float4(v[0].w, v[1].w, v[2].w, v[3].w)};
+        using ptx::to_tf32;  // the tile is an MMA operand: rounded to nearest TF32
+        const float4 o[4] = {make_float4(to_tf32(v[0].x), to_tf32(v[1].x), to_tf32(v[2].x), to_tf32(v[3].x)),
+                             make_float4(to_tf32(v[0].y), to_tf32(v[1].y), to_tf32(v[2].y), to_tf32(v[3].y)),
+                             make_float4(to_tf32(v[0].z), to_tf32(v[1].z), to_tf32(v[2].z), to_tf32(v[3].z)),
+                             make_float4(to_tf32(v[0].w), to_tf32(v[1].w), to_tf32(v[2].w), to_tf32(v[3].w))};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int r = 4 * cb + j;
@@ -85,10 +88,16 @@ __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
 // call's first launch; the first error recorded sticks.
 __device__ __forceinline__ void fail(int* status) { atomicCAS(status, SSDC_OK, SSDC_ERR_TIMEOUT); }
 
+// Store an MMA A window: every value rounded to nearest TF32 first.
 template <int kCols>
 __device__ __forceinline__ void tmem_store(uint32_t taddr, const float* v) {
 #pragma unroll
-    for (int q = 0; q < kCols / 16; ++q) ptx::tmem_st16(taddr + 16 * q, v + 16 * q);
+    for (int q = 0; q < kCols / 16; ++q) {
+        float r[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = ptx::to_tf32(v[16 * q + i]);
+        ptx::tmem_st16(taddr + 16 * q, r);
+    }
 }
 
 template <int kCols>

@@ -31,7 +31,8 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
            "ssd_complex_last_launch_count", "ssd_complex_timing_enable", "ssd_complex_timing_read",
            "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host",
            "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd",
-           "ssd_complex_set_option", "ssd_complex_noalloc_status", "ssd_complex_last_path")
+           "ssd_complex_set_option", "ssd_complex_noalloc_status", "ssd_complex_last_path",
+           "ssd_complex_segment_decay", "ssd_complex_state_combine")
 
 PATHS = {0: "staged_fp32", 1: "staged_tf32", 2: "fused_cluster", 3: "fused_tmem"}
 
@@ -107,6 +108,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_timing_read.restype = ctypes.c_int
     lib.ssd_complex_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
     lib.ssd_complex_set_option.restype = ctypes.c_int
+    lib.ssd_complex_segment_decay.argtypes = [ssdc_cin, vp, ssdc_dims, ssdc_cout, vp]
+    lib.ssd_complex_segment_decay.restype = ctypes.c_int
+    lib.ssd_complex_state_combine.argtypes = [ssdc_cin, ssdc_cin, ssdc_cin, ssdc_dims, ssdc_cout, vp]
+    lib.ssd_complex_state_combine.restype = ctypes.c_int
     lib.ssd_complex_last_path.argtypes = []
     lib.ssd_complex_last_path.restype = ctypes.c_int
     lib.ssd_complex_noalloc_status.argtypes = [vp]
@@ -390,6 +395,30 @@ def ssd_complex_status(workspace, stream=None) -> int:
 
     s = torch.cuda.current_stream() if stream is None else stream
     return load().ssd_complex_status(_ptr(workspace), ctypes.c_void_p(s.cuda_stream))
+
+
+def ssd_complex_segment_decay(A_re, A_im, dt, *, a_re, a_im, stream=None) -> None:
+    """a_seg[b,h] = exp(sum_t softplus(dt[b,t,h]) A[h]) into (a_re, a_im) (B,H)."""
+    import torch
+    Bn, T, H = dt.shape
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_segment_decay(_cin(A_re, A_im), _ptr(dt), dims(Bn, T, H, 1, 1, "fp32"),
+                                          _cout(a_re, a_im), ctypes.c_void_p(s.cuda_stream))
+    if rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_segment_decay")
+
+
+def ssd_complex_state_combine(a_re, a_im, s_in_re, s_in_im, s_add_re, s_add_im, *, out_re, out_im,
+                              stream=None) -> None:
+    """s_out = a s_in + s_add per (b, h); s_in may be (None, None) for zero."""
+    import torch
+    Bn, H, N, D = s_add_re.shape
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_state_combine(_cin(a_re, a_im), _opt_in(s_in_re, s_in_im), _cin(s_add_re, s_add_im),
+                                          dims(Bn, 1, H, N, D, "fp32"), _cout(out_re, out_im),
+                                          ctypes.c_void_p(s.cuda_stream))
+    if rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_state_combine")
 
 
 def ssd_complex_noalloc_status(stream=None) -> int:

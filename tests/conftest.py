@@ -23,6 +23,26 @@ def lib_option():
         ssdc.set_option(k, ssdc.option.DEFAULTS[k])
 
 
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Every parity comparison's relative Frobenius errors, and the largest per
+    precision (the margin against the tolerance)."""
+    try:
+        from tests.gpu_util import RECORDED, TOL
+    except Exception:
+        return
+    if not RECORDED:
+        return
+    tr = terminalreporter
+    tr.section("parity errors (relative Frobenius, y and final state)")
+    for test, precision, what, ey, es in RECORDED:
+        tr.write_line(f"{precision:12s} y {ey:.3e}  state {es:.3e}  {test} {what}")
+    for precision in sorted({r[1] for r in RECORDED}):
+        rows = [r for r in RECORDED if r[1] == precision]
+        my, ms = max(r[3] for r in rows), max(r[4] for r in rows)
+        tr.write_line(f"max {precision}: y {my:.3e}  state {ms:.3e}  over {len(rows)} comparisons "
+                      f"(tolerance {TOL[precision]:g})")
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300) and the built libssdc.so")
     config.addinivalue_line("markers", "slow: full-size workloads (minutes)")

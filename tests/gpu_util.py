@@ -1,8 +1,14 @@
 """Helpers of the GPU parity tests: run the library through the C ABI on the
 seeded inputs and compare with the oracle by relative Frobenius error."""
+import os
+
 import numpy as np
 
 from state_space_sequence_complex_gb300 import ssdc
+
+# (test, precision, what, rel_fro y, rel_fro state) of every comparison made
+# through assert_close; conftest prints them at the end of the session.
+RECORDED = []
 
 # Tolerances on relative Frobenius error, y and final state (exact fp32 SIMT
 # path and TF32 tensor-core path).
@@ -37,6 +43,8 @@ def run_library(inp, Q, precision, dev=None, forward=None):
 def assert_close(y, s, y_ref, s_ref, precision, what=""):
     assert np.all(np.isfinite(y)) and np.all(np.isfinite(s)), f"non-finite output {what}"
     ey, es = rel_fro(y, y_ref), rel_fro(s, s_ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    RECORDED.append((test, precision, what, ey, es))
     tol = TOL[precision]
     assert ey <= tol and es <= tol, f"{what} {precision}: rel_fro y {ey:.3e} state {es:.3e} > {tol}"
     return ey, es
