@@ -48,6 +48,9 @@ def parse():
                     help="layer: the headline single-layer workload; the others are measurement modes "
                          "with device-generated inputs (no CPU baseline, no end-to-end figure)")
     ap.add_argument("--chunk", type=int, default=0, help="chunk size Q (default: the workload's)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="measurement mode: run this many of the workload's layers (default: all), e.g. one "
+                         "training-batch layer for a profiler capture")
     ap.add_argument("--segments", type=int, default=1,
                     help="measurement mode: process T in this many segments, each started from the "
                          "previous segment's final state (the initial-state entry point)")
@@ -554,6 +557,7 @@ def other_workload(args, w):
         "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32",
         "data": "synthetic, drawn on the device per layer",
         "config": {"workload": f"{w.name} Q{Q}" + (f" in {K} segments of T={Ts}, state carried" if K > 1 else "")
+                   + (f", {w.layers} layer(s) run" if args.layers > 0 else "")
                    + (", real x" if args.real_x else ""), "real_x": bool(args.real_x),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
                    "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
@@ -582,7 +586,8 @@ def main():
     if args.workload != "layer" or args.segments > 1 or args.real_x:
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
-        other_workload(args, inputs.ALL[args.workload])
+        w = inputs.ALL[args.workload]
+        other_workload(args, w.with_(layers=args.layers) if args.layers > 0 else w)
         return
     w = inputs.LAYER
     if args.impl == "reference":
