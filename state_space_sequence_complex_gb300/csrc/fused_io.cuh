@@ -142,13 +142,13 @@ bool make_pair_map(CUtensorMap* m, const float* re, const float* im, int F, cons
     const cuuint64_t row = (cuuint64_t)F * 4;
     const cuuint64_t dims[5] = {(cuuint64_t)F, (cuuint64_t)p.H, (cuuint64_t)p.T, 2, (cuuint64_t)p.B};
     const cuuint64_t strides[4] = {row, row * p.H, ps, row * p.H * (cuuint64_t)p.T};
-    const cuuint32_t box[5] = {32, 1, (cuuint32_t)p.Q, 2, 1};
+    const cuuint32_t box[5] = {32, 1, (cuuint32_t)(p.Q < kQ ? p.Q : kQ), 2, 1};
     return tc::encode_tiled_f32(m, base, 5, dims, strides, box);
 }
 
 // Both planes of C, time split into 8-row groups (T a multiple of 8, so that
-// batch and group merge into one dimension), boxes (32, 1, 8, 2, Q / 8): the
-// interleaved layout, row 16g + 8p + i.
+// batch and group merge into one dimension), boxes (32, 1, 8, 2, rows / 8), rows
+// = min(Q, 64): the interleaved layout, row 16g + 8p + i.
 bool make_interleaved_map(CUtensorMap* m, const Problem& p, bool* swap) {
     if (p.T % 8 != 0 || p.Q % 8 != 0 || (int64_t)p.B * p.T / 8 >= (int64_t(1) << 31)) return false;
     const float* base;
@@ -157,7 +157,7 @@ bool make_interleaved_map(CUtensorMap* m, const Problem& p, bool* swap) {
     const cuuint64_t row = (cuuint64_t)p.N * 4;
     const cuuint64_t dims[5] = {(cuuint64_t)p.N, (cuuint64_t)p.H, 8, 2, (cuuint64_t)p.B * (cuuint64_t)p.T / 8};
     const cuuint64_t strides[4] = {row, row * p.H, ps, 8 * row * p.H};
-    const cuuint32_t box[5] = {32, 1, 8, 2, (cuuint32_t)(p.Q / 8)};
+    const cuuint32_t box[5] = {32, 1, 8, 2, (cuuint32_t)((p.Q < kQ ? p.Q : kQ) / 8)};
     return tc::encode_tiled_f32(m, base, 5, dims, strides, box);
 }
 
@@ -165,25 +165,28 @@ int make_fused_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
     memset(fm, 0, sizeof(*fm));
     fm->real_x = p.x_im == nullptr;
     bool sw = false;
-    // a two-plane box puts its second plane right after its Q rows: it lands in the stacked
-    // layout (planes 64 rows apart) only for Q = 64; smaller chunks take one map per plane
-    const bool pair_ok = allow_fast && p.Q == kQ;
+    // Tiles are 64 rows: a chunk of Q >= 64 tokens is Q / 64 tiles, a smaller chunk fills the
+    // first Q rows of one. A two-plane box puts its second plane right after its rows: it lands
+    // in the stacked layout (planes 64 rows apart) only for 64-row boxes; smaller chunks take one
+    // map per plane.
+    const int rows = p.Q < kQ ? p.Q : kQ;
+    const bool pair_ok = allow_fast && rows == kQ;
     if (pair_ok && !fm->real_x && make_pair_map(&fm->x2, p.x_re, p.x_im, p.D, p, &sw))
         fm->fast |= 1, fm->swap |= sw ? 1 : 0;
     if (pair_ok && make_pair_map(&fm->B2, p.B_re, p.B_im, p.N, p, &sw)) fm->fast |= 2, fm->swap |= sw ? 2 : 0;
     if (allow_fast && make_interleaved_map(&fm->C2, p, &sw)) fm->fast |= 4, fm->swap |= sw ? 4 : 0;
     bool ok = true;
     if (!(fm->fast & 1))
-        ok = ok && tc::encode_feature_map(&fm->x_re, p.x_re, p.D, p.H, p.T, p.B, p.Q) &&
-             (fm->real_x || tc::encode_feature_map(&fm->x_im, p.x_im, p.D, p.H, p.T, p.B, p.Q));
+        ok = ok && tc::encode_feature_map(&fm->x_re, p.x_re, p.D, p.H, p.T, p.B, rows) &&
+             (fm->real_x || tc::encode_feature_map(&fm->x_im, p.x_im, p.D, p.H, p.T, p.B, rows));
     if (!(fm->fast & 2))
-        ok = ok && tc::encode_feature_map(&fm->B_re, p.B_re, p.N, p.H, p.T, p.B, p.Q) &&
-             tc::encode_feature_map(&fm->B_im, p.B_im, p.N, p.H, p.T, p.B, p.Q);
+        ok = ok && tc::encode_feature_map(&fm->B_re, p.B_re, p.N, p.H, p.T, p.B, rows) &&
+             tc::encode_feature_map(&fm->B_im, p.B_im, p.N, p.H, p.T, p.B, rows);
     if (!(fm->fast & 4))
         ok = ok && tc::encode_feature_map(&fm->c8_re, p.C_re, p.N, p.H, p.T, p.B, 8) &&
              tc::encode_feature_map(&fm->c8_im, p.C_im, p.N, p.H, p.T, p.B, 8);
-    ok = ok && tc::encode_feature_map(&fm->y_re, p.y_re, p.D, p.H, p.T, p.B, p.Q) &&
-         tc::encode_feature_map(&fm->y_im, p.y_im, p.D, p.H, p.T, p.B, p.Q);
+    ok = ok && tc::encode_feature_map(&fm->y_re, p.y_re, p.D, p.H, p.T, p.B, rows) &&
+         tc::encode_feature_map(&fm->y_im, p.y_im, p.D, p.H, p.T, p.B, rows);
     return ok ? SSDC_OK : SSDC_ERR_CUDA;
 }
 

@@ -497,12 +497,9 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 }
                 ptx::tmem_st_16x256b_x4(tl + kCwin + 32 * kh, w);
             }
-            if (self_fill) {
-                // S_in[0] = the given initial state (N, D) of this sequence, into the incoming
-                // state tile: directly with CL = 1; otherwise staged in the C buffer (C' has been
-                // read) and copied by the quadrant's leader like a state from a predecessor, so
-                // that its arrival is counted on the same barrier
-                float vr[8], vi[8];
+            // S_in[0] = the given initial state (N, D) of this sequence, this thread's values in
+            // the state layout
+            auto load_s0 = [&](float* vr, float* vi) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const int n = 32 * kh + 8 * (k >> 1) + 2 * lq + (k & 1);
@@ -510,16 +507,12 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     vr[k] = p.s0_re[o];
                     vi[k] = p.s0_im[o];
                 }
-                for_pairs(CL > 1 ? cbase : reinterpret_cast<char*>(sm.sin), vr, vi, true);
+            };
+            if (self_fill && CL == 1) {  // straight into the incoming state tile (read by Y_off after p_ready)
+                float vr[8], vi[8];
+                load_s0(vr, vi);
+                for_pairs(reinterpret_cast<char*>(sm.sin), vr, vi, true);
                 ptx::fence_proxy_async_smem();
-                if (CL > 1) {
-                    ptx::named_sync(1 + qd, 128);
-                    if (leader) {
-                        const uint32_t off = (uint32_t)qd * kQuarterBytes;
-                        ptx::bulk_copy_to_cluster(self_sin + off, cs + off, kQuarterBytes, self_sin_full);
-                        ptx::bulk_commit();
-                    }
-                }
             }
             wait_mma(0, it);  // C B^T has read B
 
@@ -605,6 +598,23 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     const int j = k >> 1, e = k & 1;
                     outr[k] = sa[4 * j + e] - sb[4 * j + 2 + e];
                     outi[k] = sb[4 * j + e] + sa[4 * j + 2 + e];
+                }
+            }
+            if (self_fill && CL > 1) {
+                // With CL > 1 the initial state is staged in the C buffer and copied by the
+                // quadrant's leader like a state from a predecessor, so that its arrival is counted
+                // on the same barrier. Not before now: a quadrant's 8 KB of the staging buffer holds
+                // C rows of other quadrants, and the C B^T MMA reads the whole tile; the S_loc MMA
+                // just waited for was issued after C B^T and after every worker had read its C' rows.
+                float vr[8], vi[8];
+                load_s0(vr, vi);
+                for_pairs(cbase, vr, vi, true);
+                ptx::fence_proxy_async_smem();
+                ptx::named_sync(1 + qd, 128);
+                if (leader) {
+                    const uint32_t off = (uint32_t)qd * kQuarterBytes;
+                    ptx::bulk_copy_to_cluster(self_sin + off, cs + off, kQuarterBytes, self_sin_full);
+                    ptx::bulk_commit();
                 }
             }
             if (has_in) {

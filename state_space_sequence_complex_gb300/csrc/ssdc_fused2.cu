@@ -1,11 +1,9 @@
 // Fused single-pass forward of the chunkwise complex SSD scan on the TF32
-// tensor cores with the chunk state held in tensor memory (Q = 16, 32 or 64;
-// N and D multiples of 8 up to 64).
-// One CTA per SM walks whole (b, h) sequences chunk by chunk; every step of
-// the chunked decomposition (landing page, "03 Chunkwise SSD": L, Y_diag =
-// (C B^T o L) X, the per-chunk state, the pass between chunks, Y_off) runs in
-// this one launch, inputs are read from HBM once and y and the final state
-// written once.
+// tensor cores with the chunk state held in tensor memory (Q = 16, 32, 64, 128
+// or 256; N and D multiples of 8 up to 64). One CTA per SM walks whole (b, h)
+// sequences chunk by chunk; every step of the chunked decomposition (landing
+// page, "03 Chunkwise SSD": L, Y_diag = (C B^T o L) X, the per-chunk state,
+// the pass between chunks, Y_off) runs in this one launch.
 //
 // Transposed output. The kernel accumulates y^T instead of y:
 //     Y^T = X^T P^T + S_in^T C'^T,   P = (C B^T) o L,   C' = C o exp(Acs)
@@ -27,12 +25,25 @@
 // thread. Y_off does not wait for anything of its own chunk but C': its state
 // was formed at the end of the previous chunk.
 //
-// Threads: 16 worker warps (phases below), warp 16 issues every MMA in chunk
-// order on mbarrier hand-offs, warp 17 issues the TMA loads of the chunk after
-// next into the other stage and computes its cumulative log-decay. Each of
-// the three tiles of a stage is released as soon as its last reader is done
-// (x after its columns are read, C after Y_off, B after Y_diag), so the loads
-// of chunk c+2 start during chunk c.
+// Blocks. Tiles are 64 tokens. A chunk of Q >= 64 tokens is R = Q / 64 row
+// tiles r, and its quadratic part the lower-triangular blocks (r, j), j <= r:
+//     Y_r^T = sum_{j <= r} X_j^T P_rj^T + S_in^T C'_r^T,
+//     P_rj[l, s] = (C_r B_j^T)[l, s] exp(Acs[64 r + l] - Acs[64 j + s])
+// (causal inside the diagonal block only), each block a C B^T, a P and a
+// Y_diag MMA, with C_r, B_j and x_j loaded for it (the tiles of earlier
+// blocks come again from L2). Y_r accumulates over its row's blocks in TMEM;
+// the diagonal block also adds its column's share of the chunk state (the
+// (dec o B)^T MMA, accumulated over the rows) and row r's Y_off, and the last
+// one forms the state leaving the chunk. The items of a CTA are the blocks in
+// this order, row by row; for Q <= 64 a chunk is one diagonal block.
+//
+// Threads: 16 worker warps (phases below), warp 16 issues every MMA in block
+// order on mbarrier hand-offs, warp 17 issues the TMA loads of the block after
+// next into the other stage and computes each chunk's cumulative log-decay.
+// Each of the three tiles of a stage is released as soon as its last reader
+// is done (x after its columns are read and the y staged in it is stored, C
+// after C B^T or Y_off, B after Y_diag), so the loads of block k+2 start
+// during block k.
 //
 // Smaller shapes run on the same 64-row, 64-column tiles. Feature columns past
 // N or D are read as zeros by the tensor maps (and never stored), so they add
@@ -42,13 +53,14 @@
 // dec[s] is zero for s >= Q, P is causal, and y rows past Q are not stored
 // (the TMA store boxes are Q rows high).
 //
-// Worker phases of chunk c (stage s):
-//   A  decay tables; X^T window from the x tile; (B rows into registers)
-//   B  (dec o B)^T in place of B          -> S^T MMA
-//   D  y of chunk c-1 from the Y^T accumulator to global memory
-//   C  C' in place of C                   -> Y_off MMA (S_in^T window)
-//   E  P = (C B^T) o L into the B tile    -> Y_diag MMA
-//   F  S_out^T = a_c S_in^T + S_loc^T into the S window (or the final state)
+// Worker phases of block (r, j) (stage s):
+//   A  the chunk's decay tables (first block); X^T window of x_j; (B_j rows)
+//   B  diagonal: (dec o B_j)^T in place of B    -> state MMA
+//   D  first block of a row: y of the previous row, staged in this x tile
+//   C  diagonal: C'_r in place of C             -> Y_off MMA (S_in^T window)
+//   E  P_rj = (C_r B_j^T) o L into the B tile   -> Y_diag MMA
+//   F  last block of the chunk: S_out^T = a_c S_in^T + S_loc^T into the S
+//      window (or the final state)
 #include <mutex>
 
 #include "fused_io.cuh"
@@ -67,6 +79,7 @@ constexpr int kProducer = kWorkerWarps + 1;  // warp 17: TMA loads and decays
 constexpr int kThreads = kWorkers + 64;
 constexpr uint32_t kWorkerBar = 1;  // named barrier of the worker warps
 constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxQc = 256;  // the largest chunk
 // TMEM columns: three 128-column accumulators (C B^T; Y^T; S_loc^T) and two
 // 64-column A windows (X^T; S_in^T).
 constexpr uint32_t kAccG = 0, kAccY = 128, kAccS = 256, kXwin = 384, kSwin = 448;
@@ -74,47 +87,52 @@ constexpr uint32_t kAccG = 0, kAccY = 128, kAccS = 256, kXwin = 384, kSwin = 448
 struct Smem {
     float c[2][64 * 128];  // [stage] C (interleaved, A of C B^T), then C' in place (B of Y_off)
     float b[2][64 * 128];  // [stage] B (stacked), then (dec o B)^T (stacked, rows n), then P (interleaved)
-    float x[2][64 * 128];  // [stage] x (stacked): read into the X^T window
-    float2 acs[2][kQ];     // [stage] in-chunk cumulative log-decay
-    float2 dec[2][kQ];     // [stage] exp(Acs[Q-1] - Acs[s])
-    float2 eacs[2][kQ];    // [stage] exp(Acs[l])
-    float2 step[2][kQ];    // [stage] exp(Acs[s] - Acs[s-1]) (s >= 1)
-    float2 a_c[2];         // [stage] exp(Acs[Q-1])
-    uint64_t full[2];                       // stage loaded (tiles and decays)
+    float x[2][64 * 128];  // [stage] x (stacked): read into the X^T window; then y staging
+    float2 acs[2][kMaxQc];   // [chunk parity] in-chunk cumulative log-decay
+    float2 dec[2][kMaxQc];   // [chunk parity] exp(Acs[Q-1] - Acs[s]), zero past Q
+    float2 eacs[2][kMaxQc];  // [chunk parity] exp(Acs[l])
+    float2 step[2][kMaxQc];  // [chunk parity] exp(Acs[s] - Acs[s-1]) (s >= 1)
+    float2 a_c[2];           // [chunk parity] exp(Acs[Q-1])
+    uint64_t full[2];                          // stage loaded (tiles, and a chunk's decays)
     uint64_t free_x[2], free_b[2], free_c[2];  // stage tiles released
     uint64_t xt_ready, bt_ready, c_ready, p_ready, sin_ready;  // worker hand-offs (one arrival per warp)
-    uint64_t mma_g, mma_s, mma_yo, mma_y;   // MMA completions, one phase per chunk
+    uint64_t mma_g, mma_s, mma_yo, mma_y;      // MMA completions
     uint32_t tmem;
 };
 
 static_assert(sizeof(Smem) <= 232448, "shared-memory plan exceeds the 227 KB a CTA can have");
 
-// Chunk `c` of sequence `q` = b H + h.
-struct Pos {
-    int q, c, b, h;
+// Block (r, j) of chunk c of sequence q = b H + h.
+struct Item {
+    int q, c, r, j;
 };
 
-__device__ __forceinline__ Pos pos_at(int q, int c, int H) {
-    Pos p;
-    p.q = q;
-    p.c = c;
-    p.b = (int)((uint32_t)q / (uint32_t)H);
-    p.h = q - p.b * H;
-    return p;
+__device__ __forceinline__ Item item_at(int q, int c, int r, int j) {
+    Item it;
+    it.q = q;
+    it.c = c;
+    it.r = r;
+    it.j = j;
+    return it;
 }
 
-// The items of this CTA, in order: every chunk of sequences blockIdx.x,
-// blockIdx.x + gridDim.x, ...
-__device__ __forceinline__ Pos pos_next(const Pos& p, int nc, int H) {
-    return p.c + 1 < nc ? pos_at(p.q, p.c + 1, H) : pos_at(p.q + (int)gridDim.x, 0, H);
+// The items of this CTA, in order: the blocks of every chunk of sequences
+// blockIdx.x, blockIdx.x + gridDim.x, ..., row by row. (Without kBlocks every
+// chunk is one block, r = j = 0, and the compiler drops the block logic.)
+template <bool kBlocks>
+__device__ __forceinline__ Item item_next(const Item& p, int R, int nc) {
+    if (kBlocks && p.j < p.r) return item_at(p.q, p.c, p.r, p.j + 1);
+    if (kBlocks && p.r + 1 < R) return item_at(p.q, p.c, p.r + 1, 0);
+    if (p.c + 1 < nc) return item_at(p.q, p.c + 1, 0, 0);
+    return item_at(p.q + (int)gridDim.x, 0, 0, 0);
 }
 
-// Producer: TMA of one chunk's x (stacked; only the real plane for a real x),
-// C (interleaved) or B (stacked) into stage buffers, counted on `bar`.
-// A box of Q rows of one 32-column half of one plane is Q x 128 bytes.
-__device__ __forceinline__ void load_x(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int Q,
+// Producer: TMA of one block's x (stacked; only the real plane for a real x),
+// C (interleaved) or B (stacked) into stage buffers, counted on `bar`. A box
+// of `rows` rows of one 32-column half of one plane is rows x 128 bytes.
+__device__ __forceinline__ void load_x(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int rows,
                                        int lane) {
-    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(Q * 128 * (fm.real_x ? 2 : 4)));
+    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * (fm.real_x ? 2 : 4)));
     __syncwarp();
     if (fm.fast & 1) {
         if (lane < 2) ptx::tma_load_5d(dst + stk_row(lane, 0, 0), &fm.x2, bar, 32 * lane, h, t0, 0, b);
@@ -127,9 +145,9 @@ __device__ __forceinline__ void load_x(char* dst, const FusedMaps& fm, uint64_t*
     }
 }
 
-__device__ __forceinline__ void load_b(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int Q,
+__device__ __forceinline__ void load_b(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int rows,
                                        int lane) {
-    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(Q * 128 * 4));
+    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * 4));
     __syncwarp();
     if ((fm.fast >> 1) & 1) {
         if (lane < 2) ptx::tma_load_5d(dst + stk_row(lane, 0, 0), &fm.B2, bar, 32 * lane, h, t0, 0, b);
@@ -140,14 +158,14 @@ __device__ __forceinline__ void load_b(char* dst, const FusedMaps& fm, uint64_t*
 }
 
 __device__ __forceinline__ void load_c(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int64_t T,
-                                       int Q, int lane) {
-    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(Q * 128 * 4));
+                                       int rows, int lane) {
+    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * 4));
     __syncwarp();
     if ((fm.fast >> 2) & 1) {
         if (lane < 2)
             ptx::tma_load_5d(dst + inter_row(lane, 0), &fm.C2, bar, 32 * lane, h, 0, 0, (int)(((int64_t)b * T + t0) >> 3));
-    } else {  // rows 8g .. 8g+7 of plane pl, per 32-column half (Q / 8 groups)
-        const int ng = Q >> 3;
+    } else {  // rows 8g .. 8g+7 of plane pl, per 32-column half (rows / 8 groups)
+        const int ng = rows >> 3;
         if (lane < 4 * ng) {
             const int half = lane / (2 * ng), g = (lane >> 1) % ng, pl = lane & 1;
             ptx::tma_load_4d(dst + inter_row(half, 16 * g + 8 * pl), pl ? &fm.c8_im : &fm.c8_re, bar, 32 * half, h,
@@ -156,16 +174,60 @@ __device__ __forceinline__ void load_c(char* dst, const FusedMaps& fm, uint64_t*
     }
 }
 
-template <bool kSwapC>
+// Producer: the cumulative log-decay of a chunk of Q = 128 or 256 tokens (Q / 32
+// consecutive tokens per lane, a warp scan of the lane sums), tokens past T with
+// zero log-decay. The sum is fp32: its rounding (about 1e-7 of |Acs|, so about
+// 1e-5 relative on a decay factor) is far below TF32's. (Chunks of up to 64
+// tokens take the cluster kernel's loader, two tokens a lane, which also gives
+// the rows of a tile past Q zero log-decay.)
+__device__ __forceinline__ void chunk_acs(const Problem& p, int b, int h, int64_t t0, int Q, int lane, float2* acs) {
+    const int per = Q / 32;
+    const float Ar = p.A_re[h], Ai = p.A_im[h];
+    float lr[kMaxQc / 32], li[kMaxQc / 32];
+    float sr = 0.0f, si = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kMaxQc / 32; ++k) {
+        const int64_t tok = t0 + lane * per + k;
+        float ar = 0.0f, ai = 0.0f;
+        if (k < per && tok < p.T) {
+            const float sp = softplus_f(p.dt[((int64_t)b * p.T + tok) * p.H + h]);
+            ar = sp * Ar;
+            ai = sp * Ai;
+        }
+        sr += ar;
+        si += ai;
+        lr[k] = sr;
+        li[k] = si;
+    }
+    float cr = sr, ci = si;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float ur = __shfl_up_sync(0xffffffffu, cr, off);
+        const float ui = __shfl_up_sync(0xffffffffu, ci, off);
+        if (lane >= off) {
+            cr += ur;
+            ci += ui;
+        }
+    }
+    const float er = cr - sr, ei = ci - si;  // exclusive prefix of this lane's tokens
+#pragma unroll
+    for (int k = 0; k < kMaxQc / 32; ++k)
+        if (k < per) acs[lane * per + k] = make_float2(er + lr[k], ei + li[k]);
+}
+
+// kBlocks: chunks of Q = 128 or 256 tokens, several 64 x 64 blocks each.
+template <bool kSwapC, bool kBlocks>
 __global__ void __launch_bounds__(kThreads, 1)
 fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H, nc = (int)p.nc, Q = p.Q, N = p.N, D = p.D;
+    const int rows = Q < kQ ? Q : kQ;  // tile rows holding tokens
+    const int R = kBlocks ? Q / kQ : 1;  // row tiles per chunk
     const int nseq = p.B * H;
     const int nseq_cta = (int)blockIdx.x < nseq ? (nseq - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int nitems = nseq_cta * nc;
+    const int nitems = nseq_cta * nc * (R * (R + 1) / 2);
 
     // the swizzled tiles need a 1024-byte aligned base (uniform across the grid)
     if (ptx::smem_addr(smem_raw) & 1023u) {
@@ -216,26 +278,42 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             }
             __syncwarp();
         };
-        Pos ld = pos_at((int)blockIdx.x, 0, H);
+        Item ld = item_at((int)blockIdx.x, 0, 0, 0);
+        int chunks = 0;  // chunks begun by this CTA
+        // single-block chunks: the next chunk's dt is read ahead, while this one's tiles load
         Alog al = {};
-        if (nitems > 0) al = load_alog(p, ld.b, ld.h, (int64_t)ld.c * Q, lane, Q);
-        for (int j = 0; j < nitems; ++j) {  // item j into stage j & 1
-            const int st = j & 1;
-            const uint32_t ph = (uint32_t)((j - 2) >> 1) & 1u;
-            const int t0 = ld.c * Q;
-            if (j >= 2) wait(&sm.free_x[st], ph);
-            load_x(reinterpret_cast<char*>(sm.x[st]), fm, &sm.full[st], ld.h, t0, ld.b, Q, lane);
-            if (j >= 2) wait(&sm.free_c[st], ph);
-            load_c(reinterpret_cast<char*>(sm.c[st]), fm, &sm.full[st], ld.h, t0, ld.b, p.T, Q, lane);
-            if (j >= 2) wait(&sm.free_b[st], ph);
-            load_b(reinterpret_cast<char*>(sm.b[st]), fm, &sm.full[st], ld.h, t0, ld.b, Q, lane);
-            const Alog now = al;
-            ld = pos_next(ld, nc, H);
-            if (j + 1 < nitems) al = load_alog(p, ld.b, ld.h, (int64_t)ld.c * Q, lane, Q);
-            store_acs(sm.acs[st], &sm.full[st], now, lane);
+        if (!kBlocks && nitems > 0) al = load_alog(p, ld.q / H, ld.q % H, 0, lane, Q);
+        for (int k = 0; k < nitems; ++k) {  // item k into stage k & 1
+            const int st = k & 1;
+            const uint32_t ph = (uint32_t)((k - 2) >> 1) & 1u;
+            const int tc0 = ld.c * Q, tr = tc0 + kQ * ld.r, tj = tc0 + kQ * ld.j;
+            const int bb = ld.q / H, hh = ld.q - bb * H;
+            if (k >= 2) wait(&sm.free_x[st], ph);
+            load_x(reinterpret_cast<char*>(sm.x[st]), fm, &sm.full[st], hh, tj, bb, rows, lane);
+            if (k >= 2) wait(&sm.free_c[st], ph);
+            load_c(reinterpret_cast<char*>(sm.c[st]), fm, &sm.full[st], hh, tr, bb, p.T, rows, lane);
+            if (k >= 2) wait(&sm.free_b[st], ph);
+            load_b(reinterpret_cast<char*>(sm.b[st]), fm, &sm.full[st], hh, tj, bb, rows, lane);
+            const Item nx = item_next<kBlocks>(ld, R, nc);
+            if (!kBlocks) {  // every block is a chunk and carries its decays
+                const Alog now = al;
+                if (k + 1 < nitems) {
+                    const int nb = nx.q / H;
+                    al = load_alog(p, nb, nx.q - nb * H, (int64_t)nx.c * Q, lane, Q);
+                }
+                store_acs(sm.acs[st], &sm.full[st], now, lane);
+            } else {
+                if (ld.r == 0 && ld.j == 0) {
+                    chunk_acs(p, bb, hh, tc0, Q, lane, sm.acs[chunks & 1]);
+                    ++chunks;
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sm.full[st]);
+            }
+            ld = nx;
         }
     } else if (warp == kIssuer) {
-        // ============ MMA warp: lane 0 issues every MMA in chunk order ============
+        // ============ MMA warp: lane 0 issues every MMA in block order ============
         bool ok = true;
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             if (ok && !ptx::mbar_wait(bar, parity, kWaitIters)) {
@@ -243,33 +321,46 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 ok = false;
             }
         };
-        Pos cur = pos_at((int)blockIdx.x, 0, H);
-        for (int it = 0; it < nitems && lane == 0; ++it) {
-            const int s = it & 1;
-            const uint32_t ph = (uint32_t)it & 1u;
+        Item cur = item_at((int)blockIdx.x, 0, 0, 0);
+        int ndiag = 0, nchunk = 0;  // diagonal blocks and chunks issued
+        bool row_acc = false;       // the row's Y^T accumulator holds a product already
+        for (int k = 0; k < nitems && lane == 0; ++k) {
+            const int s = k & 1;
+            const uint32_t ph = (uint32_t)k & 1u, pd = (uint32_t)ndiag & 1u;
+            const bool diag = cur.j == cur.r;
             const bool has_in = cur.c > 0 || p.s0_re != nullptr;
             const uint32_t cs = ptx::smem_addr(sm.c[s]), bs = ptx::smem_addr(sm.b[s]);
-            wait(&sm.full[s], (uint32_t)((it >> 1) & 1));
+            if (cur.j == 0) row_acc = false;
+            wait(&sm.full[s], (uint32_t)((k >> 1) & 1));
             ptx::tc_fence_after();
-            issue_ss128(tmem + kAccG, desc128(cs), desc128(bs));  // C [B_0 | B_1]^T
+            issue_ss128(tmem + kAccG, desc128(cs), desc128(bs));  // C_r [B_j0 | B_j1]^T
             ptx::mma_commit(&sm.mma_g);
+            if (!diag) ptx::mma_commit(&sm.free_c[s]);  // C is read by C B^T only
             wait(&sm.xt_ready, ph);
-            wait(&sm.bt_ready, ph);
-            ptx::tc_fence_after();
-            issue_ts128(tmem + kAccS, tmem + kXwin, desc128(bs), false);  // X^T (dec o B)
-            ptx::mma_commit(&sm.mma_s);
-            wait(&sm.c_ready, ph);
-            wait(&sm.sin_ready, ph);
-            ptx::tc_fence_after();
-            if (has_in) issue_ts128(tmem + kAccY, tmem + kSwin, desc128(cs), false);  // S_in^T C'^T
-            ptx::mma_commit(&sm.mma_yo);
-            ptx::mma_commit(&sm.free_c[s]);
+            if (diag) {
+                wait(&sm.bt_ready, pd);
+                ptx::tc_fence_after();
+                issue_ts128(tmem + kAccS, tmem + kXwin, desc128(bs), cur.r > 0);  // + X_j^T (dec o B_j)
+                ptx::mma_commit(&sm.mma_s);
+                wait(&sm.c_ready, pd);
+                if (cur.r == 0) wait(&sm.sin_ready, (uint32_t)nchunk & 1u);  // the chunk's incoming state
+                ptx::tc_fence_after();
+                if (has_in) {
+                    issue_ts128(tmem + kAccY, tmem + kSwin, desc128(cs), row_acc);  // S_in^T C'_r^T
+                    row_acc = true;
+                }
+                ptx::mma_commit(&sm.mma_yo);
+                ptx::mma_commit(&sm.free_c[s]);
+            }
             wait(&sm.p_ready, ph);
             ptx::tc_fence_after();
-            issue_ts128(tmem + kAccY, tmem + kXwin, desc128(bs), has_in);  // + X^T P^T
+            issue_ts128(tmem + kAccY, tmem + kXwin, desc128(bs), row_acc);  // + X_j^T P_rj^T
+            row_acc = true;
             ptx::mma_commit(&sm.mma_y);
             ptx::mma_commit(&sm.free_b[s]);
-            cur = pos_next(cur, nc, H);
+            if (diag) ++ndiag;
+            if (diag && cur.r == R - 1) ++nchunk;
+            cur = item_next<kBlocks>(cur, R, nc);
         }
         __syncwarp();
     } else {
@@ -307,13 +398,13 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             }
             ptx::tmem_st_16x256b_x4(tl + kSwin + 32 * kh, w);
         };
-        // y rows of chunk `pos` from the Y^T accumulator (lanes (d, plane of X), columns
+        // y rows of the row tile `row` from the Y^T accumulator (lanes (d, plane of X), columns
         // 16g + 8p + i = plane p of token 8g + i of P and of C') into the staging tile `buf`
         // (two stacked planes, rows l, the 128-byte swizzle of the TMA boxes; the four rows and
         // eight columns of a warp's store fall on distinct 16-byte positions), then, once every
         // worker has written its part, one thread stores the tile with four TMA copies (rows
         // past T are not written) and commits them as one bulk group.
-        auto stage_y = [&](char* buf, const Pos& pos) {
+        auto stage_y = [&](char* buf, const Item& row) {
             float v[32];
             ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh, v);
             ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh + 32, v + 16);
@@ -337,18 +428,18 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             ptx::fence_proxy_async_smem();
             ptx::named_sync(kWorkerBar, kWorkers);
             if (tid == 0) {
-                const int t0 = pos.c * Q;
+                const int t0 = row.c * Q + kQ * row.r, yb = row.q / H, yh = row.q - yb * H;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, pos.h, t0, pos.b);
-                    ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, pos.h, t0, pos.b);
+                    ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, yh, t0, yb);
+                    ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
                 }
                 ptx::bulk_commit();
             }
         };
 
-        Pos cur = pos_at((int)blockIdx.x, 0, H), prev = cur;
-        // the S window of the first item: its initial state, if any
+        Item cur = item_at((int)blockIdx.x, 0, 0, 0);
+        // the S window of the first chunk: its initial state, if any
         if (nitems > 0 && p.s0_re != nullptr) {
             store_s0(cur.q);
             ptx::tmem_wait_st();
@@ -357,29 +448,41 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm.sin_ready);
 
+        int ndiag = 0, nchunk = 0;  // diagonal blocks and chunks begun
         for (int it = 0; it < nitems; ++it) {
             const int s = it & 1;
-            const uint32_t ph = (uint32_t)it & 1u;
+            const uint32_t ph = (uint32_t)it & 1u, pd = (uint32_t)ndiag & 1u;
+            const bool diag = cur.j == cur.r;
+            const bool chunk_first = cur.r == 0 && cur.j == 0, chunk_last = diag && cur.r == R - 1;
+            const bool staged = it > 0 && cur.j == 0;  // the previous row's y goes out through this x tile
             const bool has_in = cur.c > 0 || p.s0_re != nullptr;
-            const bool last = cur.c == nc - 1;
+            const int cp = kBlocks ? (chunk_first ? nchunk : nchunk - 1) & 1 : s;  // the chunk's table parity
+            const int orow = kQ * cur.r, ocol = kQ * cur.j;          // token offsets in the chunk
             char* xbase = reinterpret_cast<char*>(sm.x[s]);
             char* bbase = reinterpret_cast<char*>(sm.b[s]);
             char* cbase = reinterpret_cast<char*>(sm.c[s]);
+            if (chunk_first) ++nchunk;
             wait(&sm.full[s], (uint32_t)((it >> 1) & 1));
-            // the previous chunk's MMAs are complete: its X^T window and Y^T accumulator are free
+            // the previous block's MMAs are complete: the X^T window and the Y^T accumulator are free
             if (it > 0) wait(&sm.mma_y, ph ^ 1u);
             ptx::tc_fence_after();
 
-            // ---- A: decay tables; X^T window; B rows into registers
-            if (tid < kQ) {  // zero past the chunk's Q tokens (rows holding no token of it)
-                sm.dec[s][tid] = tid < Q ? cexp_fast(cdiff(sm.acs[s][kQ - 1], sm.acs[s][tid])) : make_float2(0.0f, 0.0f);
-            } else if (tid < 2 * kQ) {
-                sm.eacs[s][tid - kQ] = cexp_fast(sm.acs[s][tid - kQ]);
-            } else if (tid == 2 * kQ) {
-                sm.a_c[s] = cexp_fast(sm.acs[s][kQ - 1]);
-            } else if (tid < 3 * kQ) {
-                const int t = tid - 2 * kQ;  // 1 .. Q-1
-                sm.step[s][t] = cexp_fast(cdiff(sm.acs[s][t], sm.acs[s][t - 1]));
+            // ---- A: the chunk's decay tables; X^T window; B rows into registers
+            if (chunk_first) {
+                // over the rows of the chunk's tiles (Q, or 64 for a shorter chunk)
+                const float2 last_acs = sm.acs[cp][Q - 1];
+                const int Qe = kBlocks ? Q : kQ;
+                for (int i = tid; i < 3 * Qe; i += kWorkers) {
+                    const int which = i >= 2 * Qe ? 2 : (i >= Qe ? 1 : 0), t = i - which * Qe;
+                    if (which == 0) {  // zero past the chunk's Q tokens (rows holding no token of it)
+                        sm.dec[cp][t] = t < Q ? cexp_fast(cdiff(last_acs, sm.acs[cp][t])) : make_float2(0.0f, 0.0f);
+                    } else if (which == 1) {
+                        sm.eacs[cp][t] = cexp_fast(sm.acs[cp][t]);
+                    } else if (t >= 1) {
+                        sm.step[cp][t] = cexp_fast(cdiff(sm.acs[cp][t], sm.acs[cp][t - 1]));
+                    }
+                }
+                if (tid == 0) sm.a_c[cp] = cexp_fast(last_acs);
             }
             {
                 // X^T rows: TMEM lane 32 qd + lane = plane xp of column xd; columns s of group cg.
@@ -409,28 +512,30 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             const int bjh = L1;
             const int bsb = L2 + 2 * (warp >> 1), bnb = L0 + 2 * L3 + 4 * L4 + 8 * (warp & 1);
             float2 bv[2][4];
+            if (diag) {
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp)
+                for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int sr = 4 * bsb + i;
-                    bv[pp][i] = *reinterpret_cast<const float2*>(bbase + stk_row(bnb >> 3, pp ^ swb, sr) +
-                                                                 chunk16(bnb & 7, sr) + 8 * bjh);
-                }
+                    for (int i = 0; i < 4; ++i) {
+                        const int sr = 4 * bsb + i;
+                        bv[pp][i] = *reinterpret_cast<const float2*>(bbase + stk_row(bnb >> 3, pp ^ swb, sr) +
+                                                                     chunk16(bnb & 7, sr) + 8 * bjh);
+                    }
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::named_sync(kWorkerBar, kWorkers);
-            // every worker has read x; the tile is free at once on the first item, and otherwise
-            // once the previous chunk's y, staged in it below, has been read by its TMA stores
-            if (tid == 0 && it == 0) ptx::mbar_arrive(&sm.free_x[s]);
+            // every worker has read x; the tile is free at once, unless the previous row's y is
+            // staged in it below (then once its TMA stores have read it)
+            if (tid == 0 && !staged) ptx::mbar_arrive(&sm.free_x[s]);
             if (lane == 0) ptx::mbar_arrive(&sm.xt_ready);
 
-            // ---- B: (dec o B)^T in place of B (after C B^T has read it)
+            // ---- B: (dec o B_j)^T in place of B (after C B^T has read it)
             wait(&sm.mma_g, ph);
-            {
+            if (diag) {
                 float2 dv[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dv[i] = sm.dec[s][4 * bsb + i];
+                for (int i = 0; i < 4; ++i) dv[i] = sm.dec[cp][ocol + 4 * bsb + i];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {  // column n of B -> row n of the output
                     const int nr = 4 * bnb + 2 * bjh + j;
@@ -451,20 +556,30 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 if (lane == 0) ptx::mbar_arrive(&sm.bt_ready);
             }
 
-            // ---- D: the previous chunk's y, staged in this chunk's x tile
-            if (it > 0) stage_y(xbase, prev);
+            // ---- D: the previous row's y, staged in this block's x tile
+            if (staged) {  // the row before this one in the CTA's order
+                Item row = cur;
+                if (cur.r > 0) {
+                    row.r = cur.r - 1;
+                } else {
+                    row.r = R - 1;
+                    row.c = cur.c > 0 ? cur.c - 1 : nc - 1;
+                    if (cur.c == 0) row.q = cur.q - (int)gridDim.x;
+                }
+                stage_y(xbase, row);
+            }
 
-            // ---- C: C' = C o exp(Acs[l]) in place, plane 0 real. Unit: physical 16-byte chunk j
-            // of rows 16g + i (plane 0) and 16g + 8 + i (plane 1) of one half (token l = 8g + i);
+            // ---- C: C'_r = C_r o exp(Acs[l]) in place, plane 0 real. Unit: physical 16-byte chunk
+            // j of rows 16g + i (plane 0) and 16g + 8 + i (plane 1) of one half (token l = 8g + i);
             // eight lanes cover the eight chunks of a row.
-            {
+            if (diag) {
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int u = tid + kWorkers * k;
                     const int j = u & 7, i = (u >> 3) & 7, g = (u >> 6) & 7, half = u >> 9;
                     char* r0 = cbase + inter_row(half, 16 * g + i) + 16 * j;
                     char* r1 = r0 + 8 * 128;
-                    const float2 e = sm.eacs[s][8 * g + i];
+                    const float2 e = sm.eacs[cp][orow + 8 * g + i];
                     const float4 v0 = *reinterpret_cast<const float4*>(r0), v1 = *reinterpret_cast<const float4*>(r1);
                     const float4 cr = kSwapC ? v1 : v0, ci = kSwapC ? v0 : v1;
                     using ptx::to_tf32;
@@ -479,39 +594,42 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 ptx::tc_fence_before();  // the y loads of D precede the Y_off MMA
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&sm.c_ready);
+            } else if (staged) {
+                ptx::tc_fence_before();  // the y loads of D precede the next Y^T MMA (after p_ready)
             }
 
-            // ---- E: P = (C B^T) o L on row rr, columns col, col + 1 (col = 32 kh + 8 j + 2 lq),
-            // into the B tile once the S^T MMA has read (dec o B)^T. In the accumulator, one 64-column
-            // half holds the products with B_r, the other with B_i; lane plane 0 / 1 of the row holds
-            // the products of C's plane 0 / 1 (C_r first unless kSwapC).
+            // ---- E: P_rj = (C_r B_j^T) o L on row rr, columns col, col + 1 (col = 32 kh + 8 j + 2 lq),
+            // into the B tile once the state MMA has read (dec o B)^T (or C B^T has read B). In the
+            // accumulator, one 64-column half holds the products with B_r, the other with B_i; lane
+            // plane 0 / 1 of the row holds the products of C's plane 0 / 1 (C_r first unless kSwapC).
             {
                 float ga[16], gb[16];
                 ptx::tmem_ld_16x256b_x4(tl + gbr + 32 * kh, ga);
                 ptx::tmem_ld_16x256b_x4(tl + gbi + 32 * kh, gb);
                 ptx::tmem_wait_ld();
-                const float2 acs_l = sm.acs[s][rr];
+                const float2 acs_l = sm.acs[cp][orow + rr];
                 float2 pv[4][2];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    // L[rr, col + 1] from one exponential, L[rr, col] = L[rr, col + 1] exp(-dA[col + 1])
+                    // L[rr, col + 1] from one exponential, L[rr, col] = L[rr, col + 1] exp(-dA[col + 1]);
+                    // causal inside the diagonal block, every pair below it
                     const int col = 32 * kh + 8 * j + 2 * lq;
                     // Re G = Cr Br - Ci Bi, Im G = Cr Bi + Ci Br
                     const float2 g0 = make_float2(ga[4 * j + kRr] - gb[4 * j + kRi], gb[4 * j + kRr] + ga[4 * j + kRi]);
                     const float2 g1 = make_float2(ga[4 * j + kRr + 1] - gb[4 * j + kRi + 1],
                                                   gb[4 * j + kRr + 1] + ga[4 * j + kRi + 1]);
                     float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
-                    if (col + 1 <= rr) {
-                        const float2 L1v = cexp_fast(cdiff(acs_l, sm.acs[s][col + 1]));
+                    if (!diag || col + 1 <= rr) {
+                        const float2 L1v = cexp_fast(cdiff(acs_l, sm.acs[cp][ocol + col + 1]));
                         p1 = cmul(g1, L1v);
-                        p0 = cmul(g0, cmul(L1v, sm.step[s][col + 1]));
+                        p0 = cmul(g0, cmul(L1v, sm.step[cp][ocol + col + 1]));
                     } else if (col == rr) {
                         p0 = g0;
                     }
                     pv[j][0] = p0;
                     pv[j][1] = p1;
                 }
-                wait(&sm.mma_s, ph);
+                if (diag) wait(&sm.mma_s, pd);
                 const int mre = inter_m(rr, 0), mim = inter_m(rr, 1);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -527,14 +645,14 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             }
 
             // ---- F: S_out^T = a_c S_in^T + S_loc^T on column d = rr, state rows n = 32 kh + 8 j + 2 lq + e
-            {
+            if (chunk_last) {
                 float sa[16], sb[16];
                 ptx::tmem_ld_16x256b_x4(tl + kAccS + 32 * kh, sa);       // products with (dec o B)_r
                 ptx::tmem_ld_16x256b_x4(tl + kAccS + 64 + 32 * kh, sb);  // products with (dec o B)_i
                 float w[16];
                 if (has_in) ptx::tmem_ld_16x256b_x4(tl + kSwin + 32 * kh, w);
                 ptx::tmem_wait_ld();
-                const float2 a = sm.a_c[s];
+                const float2 a = sm.a_c[cp];
                 float outr[8], outi[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -548,11 +666,11 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                         outi[k] += a.x * si + a.y * sr;
                     }
                 }
-                // Y_off of this chunk has read the window
-                wait(&sm.mma_yo, ph);
+                // the last Y_off of this chunk has read the window
+                wait(&sm.mma_yo, pd);
                 ptx::tc_fence_after();
-                const Pos nxt = pos_next(cur, nc, H);
-                if (last) {
+                const Item nxt = item_next<kBlocks>(cur, R, nc);
+                if (cur.c == nc - 1) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const int n = 32 * kh + 8 * (k >> 1) + 2 * lq + (k & 1);
@@ -577,19 +695,21 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&sm.sin_ready);
             }
-            if (tid == 0 && it > 0) {  // the y stores have read the x tile
+            if (tid == 0 && staged) {  // the y stores have read the x tile
                 ptx::bulk_wait_read_all();
                 ptx::mbar_arrive(&sm.free_x[s]);
             }
-            prev = cur;
-            cur = pos_next(cur, nc, H);
+            if (diag) ++ndiag;
+            cur = item_next<kBlocks>(cur, R, nc);
         }
         if (nitems > 0) {
-            // the last chunk's y, staged in its x tile (read by the last stores, see above)
+            // the last row's y, staged in the last block's x tile (read by its last stores, above)
             wait(&sm.mma_y, (uint32_t)(nitems - 1) & 1u);
             ptx::tc_fence_after();
             ptx::named_sync(kWorkerBar, kWorkers);
-            stage_y(reinterpret_cast<char*>(sm.x[(nitems - 1) & 1]), prev);
+            // the last block of the CTA's last chunk: its last row
+            const int qlast = (int)blockIdx.x + (nseq_cta - 1) * (int)gridDim.x;
+            stage_y(reinterpret_cast<char*>(sm.x[(nitems - 1) & 1]), item_at(qlast, nc - 1, R - 1, R - 1));
             if (tid == 0) ptx::bulk_wait_all();
         }
     }
@@ -605,11 +725,11 @@ std::mutex g_mu;
 int set_attrs(int dev) {
     std::lock_guard<std::mutex> g(g_mu);
     if (g_attr_set[dev]) return SSDC_OK;
-    if (cudaFuncSetAttribute(fused2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(fused2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
-        return SSDC_ERR_CUDA;
+    const void* kernels[4] = {(const void*)fused2_kernel<false, false>, (const void*)fused2_kernel<true, false>,
+                              (const void*)fused2_kernel<false, true>, (const void*)fused2_kernel<true, true>};
+    for (const void* k : kernels)
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+            return SSDC_ERR_CUDA;
     g_attr_set[dev] = true;
     return SSDC_OK;
 }
@@ -618,7 +738,8 @@ int set_attrs(int dev) {
 }  // namespace fused2
 
 bool fused2_supported(int N, int D, int Q) {
-    return (Q == 16 || Q == 32 || Q == 64) && N >= 8 && N <= 64 && N % 8 == 0 && D >= 8 && D <= 64 && D % 8 == 0;
+    return (Q == 16 || Q == 32 || Q == 64 || Q == 128 || Q == 256) && N >= 8 && N <= 64 && N % 8 == 0 && D >= 8 &&
+           D <= 64 && D % 8 == 0;
 }
 
 int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bool plane_maps) {
@@ -634,10 +755,18 @@ int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bo
     const int64_t nseq = (int64_t)p.B * p.H;
     const int grid = (int)(nseq < sms ? nseq : sms);
     const dim3 g((unsigned)grid), b(fused2::kThreads);
-    if (fm.swap & 4)
-        fused2::fused2_kernel<true><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
-    else
-        fused2::fused2_kernel<false><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+    const bool swap_c = (fm.swap & 4) != 0, blocks = p.Q > fused2::kQ;
+    if (blocks) {
+        if (swap_c)
+            fused2::fused2_kernel<true, true><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+        else
+            fused2::fused2_kernel<false, true><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+    } else {
+        if (swap_c)
+            fused2::fused2_kernel<true, false><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+        else
+            fused2::fused2_kernel<false, false><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+    }
     return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
 }
 

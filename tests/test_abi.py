@@ -45,13 +45,16 @@ def test_supported_sets(lib):
     assert ok(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == 0
     assert ok(ssdc.dims(2, 2048, 16, 64, 64, "fp32"), 64) == 0
     assert ok(ssdc.dims(1, 128, 2, 8, 8, "fp32"), 16) == 0
-    # TF32: Q = 16 / 32 / 64 with N, D multiples of 8 up to 64 (the fused kernels), and
-    # Q = 128 / 256 with N = D = 64 (the staged path)
+    # TF32: Q = 16 / 32 / 64 / 128 / 256 with N, D multiples of 8 up to 64 (the fused
+    # kernels); the staged TF32 path takes N = D = 64 and Q >= 32 only
     assert ok(ssdc.dims(1, 128, 2, 8, 8, "tf32"), 16) == 0
     assert ok(ssdc.dims(1, 128, 2, 8, 24, "tf32"), 32) == 0
     assert ok(ssdc.dims(1, 128, 2, 12, 64, "tf32"), 64) == ssdc.SSDC_ERR_UNSUPPORTED
     assert ok(ssdc.dims(1, 128, 2, 72, 64, "tf32"), 64) == ssdc.SSDC_ERR_UNSUPPORTED
-    assert ok(ssdc.dims(1, 128, 2, 32, 64, "tf32"), 128) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 32, 64, "tf32"), 128) == 0
+    assert ok(ssdc.dims(1, 128, 2, 8, 40, "tf32"), 256) == 0
+    assert ok(ssdc.dims(1, 128, 2, 32, 64, "tf32_staged"), 128) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert ok(ssdc.dims(1, 128, 2, 64, 64, "tf32"), 512) == ssdc.SSDC_ERR_UNSUPPORTED
     assert ok(ssdc.dims(1, 128, 2, 64, 64, "tf32"), 256) == 0
     assert ok(ssdc.dims(1, 128, 2, 8, 8, "tf32_staged"), 16) == ssdc.SSDC_ERR_UNSUPPORTED
     assert ok(ssdc.dims(1, 128, 2, 64, 64, "fp32"), 48) == ssdc.SSDC_ERR_UNSUPPORTED
@@ -78,8 +81,10 @@ def test_workspace_bytes(lib):
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == 256
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(1, 128, 2, 8, 8, "tf32"), 16) == 256
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 32) == 256
-    # at Q = 128 and 256 the TF32 path stages the states
-    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 128) > 256
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 128) == 256
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 256) == 256
+    # the staged TF32 path keeps the chunk states in the workspace
+    assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 128) > 256
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 48) == 0
     # uneven T rounds the chunk count up
     assert ssdc.ssd_complex_fwd_workspace_bytes(ssdc.dims(1, 65, 1, 64, 64, "fp32"), 64) > \

@@ -75,6 +75,9 @@ CASES = [
     (2, 330, 3, 64, 64, 64, "tf32", -1),
     (20, 200, 8, 64, 64, 64, "tf32", -1),
     (20, 136, 8, 64, 64, 32, "tf32", -1),
+    (20, 300, 8, 64, 64, 128, "tf32", -1),
+    (2, 600, 3, 64, 64, 256, "tf32", -1),
+    (2, 130, 3, 8, 24, 128, "tf32", -1),
 ]
 
 

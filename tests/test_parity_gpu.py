@@ -54,18 +54,23 @@ def test_state_and_head_sizes(N, D, precision):
     check(inp, 64, precision, f"N={N} D={D}")
 
 
-# The fused kernel with the state in tensor memory, forced: every chunk size it takes,
-# feature sizes below the tile (zero columns), ragged tails, T < Q, T = Q.
+# The fused kernel with the state in tensor memory, forced: every chunk size it takes
+# (chunks of 128 and 256 tokens as 3 and 10 blocks of 64 x 64), feature sizes below the
+# tile (zero columns), ragged tails (inside the last block, and whole blocks past T),
+# T < Q, T = Q.
 @pytest.mark.parametrize("N,D,Q,T", [(8, 8, 16, 128), (8, 8, 16, 90), (16, 64, 32, 257), (64, 8, 64, 200),
                                      (32, 24, 16, 333), (56, 40, 32, 1000), (64, 64, 16, 300), (64, 64, 32, 1000),
-                                     (64, 64, 64, 64 * 9 + 13), (24, 48, 32, 20), (64, 64, 64, 64), (8, 16, 16, 1)])
+                                     (64, 64, 64, 64 * 9 + 13), (24, 48, 32, 20), (64, 64, 64, 64), (8, 16, 16, 1),
+                                     (64, 64, 128, 300), (64, 64, 128, 3 * 128), (16, 40, 128, 1000),
+                                     (8, 8, 128, 129), (64, 64, 256, 511), (64, 64, 256, 256), (32, 64, 256, 700),
+                                     (64, 64, 256, 70), (48, 16, 256, 1030)])
 def test_tensor_memory_kernel(N, D, Q, T, lib_option):
     lib_option(ssdc.OPT_FUSED_KERNEL, 2)
     inp = inputs.custom(2, T, 3, D, N, seed=5000 + N + D + Q + T)
     check(inp, Q, "tf32", f"tensor-memory kernel N={N} D={D} Q={Q} T={T}")
 
 
-@pytest.mark.parametrize("Q", [32, 64])
+@pytest.mark.parametrize("Q", [32, 64, 128, 256])
 def test_tensor_memory_kernel_several_sequences_per_cta(Q, lib_option):
     # 160 sequences on at most 152 CTAs: some CTAs walk two sequences
     lib_option(ssdc.OPT_FUSED_KERNEL, 2)
@@ -190,3 +195,19 @@ def test_fused_tensor_map_paths(order, plane_maps, kernel, lib_option):
         _planes_in_order(t, name, flip)
     y, s, _ = run_library(inp, 64, "tf32", dev=t)
     assert_close(y, s, y_ref, s_ref, "tf32", f"planes {order}, plane maps {plane_maps}")
+
+
+@pytest.mark.parametrize("Q", [128, 256])
+@pytest.mark.parametrize("plane_maps", ["1", "0"])
+def test_tensor_memory_kernel_map_paths_long_chunks(Q, plane_maps, lib_option):
+    # chunks of several 64-token blocks through each tensor-map form (T a multiple of 8:
+    # the interleaved C map applies), planes in mixed address order
+    lib_option(ssdc.OPT_FUSED_PLANE_MAPS, int(plane_maps))
+    inp = inputs.custom(2, 2 * Q + 72, 3, 64, 64, seed=3200 + Q)
+    y_ref, s_ref = naive_scan_inputs(inp)
+    t = to_device(inp)
+    for name, flip in zip(["x", "B", "C"], (True, False, True)):
+        _planes_in_order(t, name, flip)
+    y, s, _ = run_library(inp, Q, "tf32", dev=t)
+    assert ssdc.last_path() == "fused_tmem"
+    assert_close(y, s, y_ref, s_ref, "tf32", f"Q={Q}, plane maps {plane_maps}")

@@ -54,6 +54,8 @@ CASES = [
     (1, 200, 2, 16, 16, 32, "tf32", 0),
     (2, 330, 3, 64, 64, 64, "tf32", -1),
     (20, 200, 8, 64, 64, 64, "tf32", -1),
+    (20, 300, 8, 64, 64, 128, "tf32", -1),
+    (2, 600, 3, 64, 64, 256, "tf32", -1),
 ]
 
 
