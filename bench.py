@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="measurement mode: run this many of the workload's layers (default: all), e.g. one "
                          "training-batch layer for a profiler capture")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="measurement mode: override the workload's batch size B (e.g. a smaller case of "
+                         "the same shape for a profiler capture)")
     ap.add_argument("--segments", type=int, default=1,
                     help="measurement mode: process T in this many segments, each started from the "
                          "previous segment's final state (the initial-state entry point)")
@@ -558,6 +561,7 @@ def other_workload(args, w):
         "data": "synthetic, drawn on the device per layer",
         "config": {"workload": f"{w.name} Q{Q}" + (f" in {K} segments of T={Ts}, state carried" if K > 1 else "")
                    + (f", {w.layers} layer(s) run" if args.layers > 0 else "")
+                   + (f", batch {w.B}" if args.batch > 0 else "")
                    + (", real x" if args.real_x else ""), "real_x": bool(args.real_x),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
                    "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
@@ -583,11 +587,15 @@ def main():
             raise SystemExit("the backward measurement runs with --impl ours, unsegmented")
         backward_workload(args, inputs.ALL[args.workload])
         return
-    if args.workload != "layer" or args.segments > 1 or args.real_x:
+    if args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0:
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
         w = inputs.ALL[args.workload]
-        other_workload(args, w.with_(layers=args.layers) if args.layers > 0 else w)
+        if args.layers > 0:
+            w = w.with_(layers=args.layers)
+        if args.batch > 0:
+            w = w.with_(B=args.batch)
+        other_workload(args, w)
         return
     w = inputs.LAYER
     if args.impl == "reference":

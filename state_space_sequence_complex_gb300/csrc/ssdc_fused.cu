@@ -382,20 +382,32 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh + 32, yv + 16);
             ptx::tmem_wait_ld();
             const int64_t t = (int64_t)pos.c * kQ + rr;
-            if (t < p.T) {
-                const int64_t row = (((int64_t)pos.b * p.T + t) * H + pos.h) * 64;
+            const int64_t row = (((int64_t)pos.b * p.T + (t < p.T ? t : 0)) * H + pos.h) * 64;
+            const bool odd = lq & 1;
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < 2; ++u) {
+                // this thread's column pairs d0 = 32 kh + 16 u + 2 lq (block dd = 0) and d0 + 8 (dd = 1);
+                // Re y = (P_r x_r)[p0] - (P_i x_i)[p1], Im y = (P_r x_i)[p0] + (P_i x_r)[p1]
+                float2 re[2], im[2];
 #pragma unroll
-                    for (int dd = 0; dd < 2; ++dd) {
-                        const int jr = 16 * u + 8 * dd, ji = jr + 4;  // register blocks of planes x_r, x_i
-                        const int d = 32 * kh + 16 * u + 8 * dd + 2 * lq;
-                        // Re y = (P_r x_r)[p0] - (P_i x_i)[p1], Im y = (P_r x_i)[p0] + (P_i x_r)[p1]
-                        *reinterpret_cast<float2*>(p.y_re + row + d) =
-                            make_float2(yv[jr + 0] - yv[ji + 2], yv[jr + 1] - yv[ji + 3]);
-                        *reinterpret_cast<float2*>(p.y_im + row + d) =
-                            make_float2(yv[ji + 0] + yv[jr + 2], yv[ji + 1] + yv[jr + 3]);
-                    }
+                for (int dd = 0; dd < 2; ++dd) {
+                    const int jr = 16 * u + 8 * dd, ji = jr + 4;  // register blocks of planes x_r, x_i
+                    re[dd] = make_float2(yv[jr + 0] - yv[ji + 2], yv[jr + 1] - yv[ji + 3]);
+                    im[dd] = make_float2(yv[ji + 0] + yv[jr + 2], yv[ji + 1] + yv[jr + 3]);
+                }
+                // lanes lq and lq ^ 1 swap one pair each, so that every lane stores 16 bytes: an even
+                // lane columns d0 .. d0 + 3 of block 0, an odd lane d0 + 6 .. d0 + 9 of block 1 (its
+                // partner's pair, then its own); the four lanes of a row cover 64 contiguous bytes
+                const float2 sre = odd ? re[0] : re[1], sim = odd ? im[0] : im[1];
+                const float2 rre = make_float2(__shfl_xor_sync(0xffffffffu, sre.x, 1), __shfl_xor_sync(0xffffffffu, sre.y, 1));
+                const float2 rim = make_float2(__shfl_xor_sync(0xffffffffu, sim.x, 1), __shfl_xor_sync(0xffffffffu, sim.y, 1));
+                const int d = 32 * kh + 16 * u + 2 * lq + (odd ? 6 : 0);
+                if (t < p.T) {
+                    *reinterpret_cast<float4*>(p.y_re + row + d) =
+                        odd ? make_float4(rre.x, rre.y, re[1].x, re[1].y) : make_float4(re[0].x, re[0].y, rre.x, rre.y);
+                    *reinterpret_cast<float4*>(p.y_im + row + d) =
+                        odd ? make_float4(rim.x, rim.y, im[1].x, im[1].y) : make_float4(im[0].x, im[0].y, rim.x, rim.y);
+                }
             }
         };
 
