@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--segments", type=int, default=1,
                     help="measurement mode: process T in this many segments, each started from the "
                          "previous segment's final state (the initial-state entry point)")
+    ap.add_argument("--bf16", action="store_true",
+                    help="measurement mode: x, B_t and C_t in bfloat16 (ssd_complex_fwd_bf16), the rest fp32")
     ap.add_argument("--real-x", action="store_true",
                     help="measurement mode: x real (x.im = NULL, only x.re is read), as in the model")
     ap.add_argument("--backward", action="store_true",
@@ -489,6 +491,11 @@ def other_workload(args, w):
         return [[t if t.dim() == 1 else t[:, k * Ts:(k + 1) * Ts].contiguous() for t in L] for k in range(K)]
 
     layers = [split(layer_inputs(i)) for i in range(w.layers)]
+    if args.bf16:  # bfloat16 activations: x, B_t, C_t (the draws rounded to nearest even)
+        for L in layers:
+            for seg in L:
+                for i in (0, 1, 4, 5, 6, 7):
+                    seg[i] = seg[i].to(torch.bfloat16)
     if args.real_x:  # no imaginary plane for x
         for L in layers:
             for seg in L:
@@ -496,7 +503,9 @@ def other_workload(args, w):
     precision = args.precision
     if precision == "auto":
         precision = "tf32" if ssdc.ssd_complex_fwd_supported(ssdc.dims(w.B, Ts, w.H, w.N, w.D, "tf32"), Q) == 0 else "fp32"
-    f = ssdc.Forward(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev)
+    if args.bf16 and precision != "tf32":
+        raise SystemExit("--bf16 runs on the TF32 path only")
+    f = ssdc.Forward(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev, bf16_inputs=args.bf16)
 
     def run_layer(L, timed=False):
         for k, seg in enumerate(L):
@@ -550,19 +559,24 @@ def other_workload(args, w):
     peak, peak_kind = peaks()
     wq = w.with_(Q=Q, T=Ts)
     # per launch; a segment after the first also reads its initial state (8 N D bytes per sequence)
-    bytes_per_launch = ((algorithmic_bytes_per_unit(wq) - (4.0 * w.D if args.real_x else 0.0)) * wq.token_heads
+    # (bfloat16 x, B_t, C_t: 2 bytes a plane element instead of 4; a real x: one plane)
+    in_bytes = (8.0 * w.D + 8.0 * w.N) if args.bf16 else 0.0
+    x_im_bytes = (2.0 if args.bf16 else 4.0) * w.D if args.real_x else 0.0
+    bytes_per_launch = ((algorithmic_bytes_per_unit(wq) - in_bytes - x_im_bytes) * wq.token_heads
                         + 8.0 * w.N * w.D * w.B * w.H * (K - 1) / K)
     launch_ms = sum(kmeans)
     units = w.token_heads * w.layers
     line = {
         "metric": METRIC, "value": units / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32",
+        "vs_baseline": None,
+        "dtype": ("bf16 inputs, tf32" if args.bf16 else "tf32") if precision == "tf32" else "f32",
         "data": "synthetic, drawn on the device per layer",
         "config": {"workload": f"{w.name} Q{Q}" + (f" in {K} segments of T={Ts}, state carried" if K > 1 else "")
                    + (f", {w.layers} layer(s) run" if args.layers > 0 else "")
                    + (f", batch {w.B}" if args.batch > 0 else "")
-                   + (", real x" if args.real_x else ""), "real_x": bool(args.real_x),
+                   + (", real x" if args.real_x else "") + (", bf16 x/B/C" if args.bf16 else ""),
+                   "real_x": bool(args.real_x), "bf16_inputs": bool(args.bf16),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
                    "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
                    "path": path,
@@ -587,7 +601,7 @@ def main():
             raise SystemExit("the backward measurement runs with --impl ours, unsegmented")
         backward_workload(args, inputs.ALL[args.workload])
         return
-    if args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0:
+    if args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0 or args.bf16:
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
         w = inputs.ALL[args.workload]

@@ -98,10 +98,10 @@ typedef struct {
 
 /*
  * Supported sizes.
- *   SSDC_PREC_FP32: chunk_size in {16, 32, 64, 128, 256};
- *                   N and D multiples of 8 in [8, 64].
- *   SSDC_PREC_TF32, SSDC_PREC_TF32_STAGED: chunk_size in {32, 64, 128, 256};
- *                   N = D = 64.
+ *   SSDC_PREC_FP32:        chunk_size in {16, 32, 64, 128, 256};
+ *                          N and D multiples of 8 in [8, 64].
+ *   SSDC_PREC_TF32:        the same sets.
+ *   SSDC_PREC_TF32_STAGED: chunk_size in {32, 64, 128, 256}; N = D = 64.
  * T need not be a multiple of chunk_size: the last chunk is partial.
  */
 int ssd_complex_fwd_supported(ssdc_dims dims, int chunk_size);
@@ -145,6 +145,32 @@ int ssd_complex_fwd_ws(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
  * of ssd_complex_fwd_ws; one null plane is SSDC_ERR_INVALID.
  */
 int ssd_complex_fwd_init(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
+                         const float *dt, ssdc_cin initial_state, ssdc_dims dims,
+                         int chunk_size, ssdc_cout y, ssdc_cout final_state,
+                         void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Forward pass with bfloat16 activations: x, B_t and C_t are planar bfloat16
+ * arrays (the layouts of ssd_complex_fwd_ws, 2 bytes an element); A, dt, the
+ * initial and final states and y stay fp32, and so does every sum and the state
+ * (the pages train with BF16 activations around a complex64 state). 1282 bytes
+ * per token-head instead of 2068. The scan is the same operation on the inputs'
+ * values: C B^T multiplies the bfloat16 values as they are (tensor-core BF16
+ * products, exact, fp32 sums); every other product takes them as exact fp32
+ * (TF32) values, as the TF32 path does its fp32 inputs.
+ *
+ *   x, B_t, C_t     planar bfloat16, 16-byte aligned; x.im may be null (a real x)
+ *   initial_state   as for ssd_complex_fwd_init (both planes null: zero)
+ *   dims.precision  must be SSDC_PREC_TF32; N, D multiples of 8 in [8, 64],
+ *                   chunk_size in {16, 32, 64, 128, 256} (else SSDC_ERR_UNSUPPORTED)
+ * The other arguments, the workspace (ssd_complex_fwd_workspace_bytes), the
+ * overlap rules and the errors are those of ssd_complex_fwd_ws. One launch, the
+ * fused kernel with the state in tensor memory.
+ */
+typedef struct {
+    const uint16_t *re, *im;
+} ssdc_cin_bf16;
+int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_cin_bf16 C_t,
                          const float *dt, ssdc_cin initial_state, ssdc_dims dims,
                          int chunk_size, ssdc_cout y, ssdc_cout final_state,
                          void *workspace, size_t ws_bytes, cudaStream_t stream);

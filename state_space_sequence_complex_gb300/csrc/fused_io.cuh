@@ -164,6 +164,20 @@ bool make_interleaved_map(CUtensorMap* m, const Problem& p, bool* swap) {
 int make_fused_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
     memset(fm, 0, sizeof(*fm));
     fm->real_x = p.x_im == nullptr;
+    if (p.in_bf16) {
+        // bfloat16 x, B_t, C_t: one map per plane, boxes of 64 features (one 128-byte row);
+        // C in 8-row boxes that land in the interleaved layout
+        const int rows16 = p.Q < kQ ? p.Q : kQ;
+        bool ok = tc::encode_feature_map_bf16(&fm->x_re, p.x_re, p.D, p.H, p.T, p.B, rows16) &&
+                  (fm->real_x || tc::encode_feature_map_bf16(&fm->x_im, p.x_im, p.D, p.H, p.T, p.B, rows16)) &&
+                  tc::encode_feature_map_bf16(&fm->B_re, p.B_re, p.N, p.H, p.T, p.B, rows16) &&
+                  tc::encode_feature_map_bf16(&fm->B_im, p.B_im, p.N, p.H, p.T, p.B, rows16) &&
+                  tc::encode_feature_map_bf16(&fm->c8_re, p.C_re, p.N, p.H, p.T, p.B, 8) &&
+                  tc::encode_feature_map_bf16(&fm->c8_im, p.C_im, p.N, p.H, p.T, p.B, 8) &&
+                  tc::encode_feature_map(&fm->y_re, p.y_re, p.D, p.H, p.T, p.B, rows16) &&
+                  tc::encode_feature_map(&fm->y_im, p.y_im, p.D, p.H, p.T, p.B, rows16);
+        return ok ? SSDC_OK : SSDC_ERR_CUDA;
+    }
     bool sw = false;
     // Tiles are 64 rows: a chunk of Q >= 64 tokens is Q / 64 tiles, a smaller chunk fills the
     // first Q rows of one. A two-plane box puts its second plane right after its rows: it lands
@@ -196,7 +210,7 @@ struct MapKey {
     const void* ptr[8];
     int64_t T;
     int B, H, N, D, Q;
-    bool fast;
+    bool fast, bf16;
 };
 struct MapEntry {
     MapKey key;
@@ -210,7 +224,8 @@ int g_map_used = 0, g_map_next = 0;
 bool same_map_key(const MapKey& a, const MapKey& b) {
     for (int i = 0; i < 8; ++i)
         if (a.ptr[i] != b.ptr[i]) return false;
-    return a.T == b.T && a.B == b.B && a.H == b.H && a.N == b.N && a.D == b.D && a.Q == b.Q && a.fast == b.fast;
+    return a.T == b.T && a.B == b.B && a.H == b.H && a.N == b.N && a.D == b.D && a.Q == b.Q && a.fast == b.fast &&
+           a.bf16 == b.bf16;
 }
 
 int cached_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
@@ -225,6 +240,7 @@ int cached_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
     k.D = p.D;
     k.Q = p.Q;
     k.fast = allow_fast;
+    k.bf16 = p.in_bf16 != 0;
     {
         std::lock_guard<std::mutex> g(g_map_mu);
         for (int i = 0; i < g_map_used; ++i)

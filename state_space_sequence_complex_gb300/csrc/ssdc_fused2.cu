@@ -83,11 +83,11 @@ constexpr int kMaxQc = 256;  // the largest chunk
 // TMEM columns: three 128-column accumulators (C B^T; Y^T; S_loc^T) and two
 // 64-column A windows (X^T; S_in^T).
 constexpr uint32_t kAccG = 0, kAccY = 128, kAccS = 256, kXwin = 384, kSwin = 448;
+constexpr int kPlane16 = 64 * 128;  // bytes of one 64-row plane of a bfloat16 tile
+constexpr uint32_t kIdescBf16 = ptx::idesc_bf16(128, 128);
 
-struct Smem {
-    float c[2][64 * 128];  // [stage] C (interleaved, A of C B^T), then C' in place (B of Y_off)
-    float b[2][64 * 128];  // [stage] B (stacked), then (dec o B)^T (stacked, rows n), then P (interleaved)
-    float x[2][64 * 128];  // [stage] x (stacked): read into the X^T window; then y staging
+// Decay tables, barriers and the TMEM address: the part common to both input types.
+struct Tail {
     float2 acs[2][kMaxQc];   // [chunk parity] in-chunk cumulative log-decay
     float2 dec[2][kMaxQc];   // [chunk parity] exp(Acs[Q-1] - Acs[s]), zero past Q
     float2 eacs[2][kMaxQc];  // [chunk parity] exp(Acs[l])
@@ -100,7 +100,30 @@ struct Smem {
     uint32_t tmem;
 };
 
-static_assert(sizeof(Smem) <= 232448, "shared-memory plan exceeds the 227 KB a CTA can have");
+template <bool kBf16>
+struct Smem;
+// fp32 inputs: the stage tiles are also the tiles the threads rewrite.
+template <>
+struct Smem<false> : Tail {
+    alignas(1024) float c[2][64 * 128];  // [stage] C (interleaved, A of C B^T), then C' in place (B of Y_off)
+    float b[2][64 * 128];  // [stage] B (stacked), then (dec o B)^T (stacked, rows n), then P (interleaved)
+    float x[2][64 * 128];  // [stage] x (stacked): read into the X^T window; then y staging
+};
+// bfloat16 inputs: 16 KB stage tiles (a 128-byte row of 64 features per token and plane, the
+// same row orders as above), read by C B^T and by the threads; what the threads compute goes to
+// fp32 work tiles in the fp32 layouts.
+template <>
+struct Smem<true> : Tail {
+    alignas(1024) uint16_t c[2][64 * 128];  // [stage] C (interleaved), A of C B^T
+    uint16_t b[2][64 * 128];                // [stage] B (stacked), B of C B^T
+    uint16_t x[2][64 * 128];                // [stage] x (stacked)
+    alignas(1024) float cw[64 * 128];       // C' (interleaved), B of Y_off
+    float bw[64 * 128];                     // (dec o B)^T (stacked, rows n), then P (interleaved)
+    float yw[64 * 128];                     // y staging (stacked)
+};
+
+static_assert(sizeof(Smem<false>) <= 232448 && sizeof(Smem<true>) <= 232448,
+              "shared-memory plan exceeds the 227 KB a CTA can have");
 
 // Block (r, j) of chunk c of sequence q = b H + h.
 struct Item {
@@ -174,6 +197,45 @@ __device__ __forceinline__ void load_c(char* dst, const FusedMaps& fm, uint64_t*
     }
 }
 
+// The same for bfloat16 inputs: one box of 64 features (one 128-byte row) per
+// token and plane; the per-plane maps only.
+__device__ __forceinline__ void load_x16(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int rows,
+                                         int lane) {
+    const int n = fm.real_x ? 1 : 2;
+    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * n));
+    __syncwarp();
+    if (lane < n) ptx::tma_load_4d(dst + lane * kPlane16, lane ? &fm.x_im : &fm.x_re, bar, 0, h, t0, b);
+}
+
+__device__ __forceinline__ void load_b16(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int rows,
+                                         int lane) {
+    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * 2));
+    __syncwarp();
+    if (lane < 2) ptx::tma_load_4d(dst + lane * kPlane16, lane ? &fm.B_im : &fm.B_re, bar, 0, h, t0, b);
+}
+
+__device__ __forceinline__ void load_c16(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int rows,
+                                         int lane) {
+    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * 2));
+    __syncwarp();
+    if (lane < 2 * (rows >> 3)) {  // rows 8g .. 8g+7 of plane pl land at rows 16g + 8pl
+        const int g = lane >> 1, pl = lane & 1;
+        ptx::tma_load_4d(dst + (16 * g + 8 * pl) * 128, pl ? &fm.c8_im : &fm.c8_re, bar, 0, h, t0 + 8 * g, b);
+    }
+}
+
+// C_r [B_j]^T from the bfloat16 tiles: 4 MMAs of K = 16 (32 bytes of each 128-byte row).
+__device__ __forceinline__ void issue_g16(uint32_t d, uint32_t a_base, uint32_t b_base) {
+    const uint64_t da = desc128(a_base), db = desc128(b_base);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ptx::mma_f16_ss(d, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), kIdescBf16, k > 0 ? 1u : 0u);
+}
+
+// Offset of the bfloat16 element (row r, feature f) in a 128-byte swizzled row of a 16-bit tile.
+__device__ __forceinline__ uint32_t off16(int r, int f) {
+    return (uint32_t)(r * 128) + chunk16(f >> 3, r) + (uint32_t)((f & 7) << 1);
+}
+
 // Producer: the cumulative log-decay of a chunk of Q = 128 or 256 tokens (Q / 32
 // consecutive tokens per lane, a warp scan of the lane sums), tokens past T with
 // zero log-decay. The sum is fp32: its rounding (about 1e-7 of |Acs|, so about
@@ -216,11 +278,14 @@ __device__ __forceinline__ void chunk_acs(const Problem& p, int b, int h, int64_
 }
 
 // kBlocks: chunks of Q = 128 or 256 tokens, several 64 x 64 blocks each.
-template <bool kSwapC, bool kBlocks>
+// kBf16: x, B_t and C_t in bfloat16. C B^T then multiplies them as they are
+// (kind::f16, exact products); x enters the X^T window and B and C the
+// threads' products as exact fp32 values, the rest is as for fp32 inputs.
+template <bool kSwapC, bool kBlocks, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
 fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    Smem<kBf16>& sm = *reinterpret_cast<Smem<kBf16>*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H, nc = (int)p.nc, Q = p.Q, N = p.N, D = p.D;
     const int rows = Q < kQ ? Q : kQ;  // tile rows holding tokens
@@ -259,7 +324,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     if (Q < kQ) {
         // rows past Q are never loaded: give them finite contents
         float4* z = reinterpret_cast<float4*>(sm.c);
-        constexpr int kVecs = 3 * 2 * 64 * 128 / 4;  // the c, b and x tiles of both stages
+        constexpr int kVecs = (int)(3 * sizeof(sm.c) / 16);  // the c, b and x tiles of both stages
         for (int i = tid; i < kVecs; i += kThreads) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         ptx::fence_proxy_async_smem();
     }
@@ -288,12 +353,18 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             const uint32_t ph = (uint32_t)((k - 2) >> 1) & 1u;
             const int tc0 = ld.c * Q, tr = tc0 + kQ * ld.r, tj = tc0 + kQ * ld.j;
             const int bb = ld.q / H, hh = ld.q - bb * H;
+            char* xd = reinterpret_cast<char*>(sm.x[st]);
+            char* cd = reinterpret_cast<char*>(sm.c[st]);
+            char* bd = reinterpret_cast<char*>(sm.b[st]);
             if (k >= 2) wait(&sm.free_x[st], ph);
-            load_x(reinterpret_cast<char*>(sm.x[st]), fm, &sm.full[st], hh, tj, bb, rows, lane);
+            if constexpr (kBf16) load_x16(xd, fm, &sm.full[st], hh, tj, bb, rows, lane);
+            else load_x(xd, fm, &sm.full[st], hh, tj, bb, rows, lane);
             if (k >= 2) wait(&sm.free_c[st], ph);
-            load_c(reinterpret_cast<char*>(sm.c[st]), fm, &sm.full[st], hh, tr, bb, p.T, rows, lane);
+            if constexpr (kBf16) load_c16(cd, fm, &sm.full[st], hh, tr, bb, rows, lane);
+            else load_c(cd, fm, &sm.full[st], hh, tr, bb, p.T, rows, lane);
             if (k >= 2) wait(&sm.free_b[st], ph);
-            load_b(reinterpret_cast<char*>(sm.b[st]), fm, &sm.full[st], hh, tj, bb, rows, lane);
+            if constexpr (kBf16) load_b16(bd, fm, &sm.full[st], hh, tj, bb, rows, lane);
+            else load_b(bd, fm, &sm.full[st], hh, tj, bb, rows, lane);
             const Item nx = item_next<kBlocks>(ld, R, nc);
             if (!kBlocks) {  // every block is a chunk and carries its decays
                 const Alog now = al;
@@ -330,23 +401,29 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             const bool diag = cur.j == cur.r;
             const bool has_in = cur.c > 0 || p.s0_re != nullptr;
             const uint32_t cs = ptx::smem_addr(sm.c[s]), bs = ptx::smem_addr(sm.b[s]);
+            uint32_t cw = cs, bw = bs;  // the tiles the threads write: C'; (dec o B)^T and P
+            if constexpr (kBf16) {
+                cw = ptx::smem_addr(sm.cw);
+                bw = ptx::smem_addr(sm.bw);
+            }
             if (cur.j == 0) row_acc = false;
             wait(&sm.full[s], (uint32_t)((k >> 1) & 1));
             ptx::tc_fence_after();
-            issue_ss128(tmem + kAccG, desc128(cs), desc128(bs));  // C_r [B_j0 | B_j1]^T
+            if constexpr (kBf16) issue_g16(tmem + kAccG, cs, bs);  // C_r [B_j0 | B_j1]^T
+            else issue_ss128(tmem + kAccG, desc128(cs), desc128(bs));
             ptx::mma_commit(&sm.mma_g);
             if (!diag) ptx::mma_commit(&sm.free_c[s]);  // C is read by C B^T only
             wait(&sm.xt_ready, ph);
             if (diag) {
                 wait(&sm.bt_ready, pd);
                 ptx::tc_fence_after();
-                issue_ts128(tmem + kAccS, tmem + kXwin, desc128(bs), cur.r > 0);  // + X_j^T (dec o B_j)
+                issue_ts128(tmem + kAccS, tmem + kXwin, desc128(bw), cur.r > 0);  // + X_j^T (dec o B_j)
                 ptx::mma_commit(&sm.mma_s);
                 wait(&sm.c_ready, pd);
                 if (cur.r == 0) wait(&sm.sin_ready, (uint32_t)nchunk & 1u);  // the chunk's incoming state
                 ptx::tc_fence_after();
                 if (has_in) {
-                    issue_ts128(tmem + kAccY, tmem + kSwin, desc128(cs), row_acc);  // S_in^T C'_r^T
+                    issue_ts128(tmem + kAccY, tmem + kSwin, desc128(cw), row_acc);  // S_in^T C'_r^T
                     row_acc = true;
                 }
                 ptx::mma_commit(&sm.mma_yo);
@@ -354,7 +431,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             }
             wait(&sm.p_ready, ph);
             ptx::tc_fence_after();
-            issue_ts128(tmem + kAccY, tmem + kXwin, desc128(bs), row_acc);  // + X_j^T P_rj^T
+            issue_ts128(tmem + kAccY, tmem + kXwin, desc128(bw), row_acc);  // + X_j^T P_rj^T
             row_acc = true;
             ptx::mma_commit(&sm.mma_y);
             ptx::mma_commit(&sm.free_b[s]);
@@ -461,6 +538,15 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             char* xbase = reinterpret_cast<char*>(sm.x[s]);
             char* bbase = reinterpret_cast<char*>(sm.b[s]);
             char* cbase = reinterpret_cast<char*>(sm.c[s]);
+            // where the threads write C', (dec o B)^T and P, and stage y
+            char* cwork = cbase;
+            char* bwork = bbase;
+            char* ystage = xbase;
+            if constexpr (kBf16) {
+                cwork = reinterpret_cast<char*>(sm.cw);
+                bwork = reinterpret_cast<char*>(sm.bw);
+                ystage = reinterpret_cast<char*>(sm.yw);
+            }
             if (chunk_first) ++nchunk;
             wait(&sm.full[s], (uint32_t)((it >> 1) & 1));
             // the previous block's MMAs are complete: the X^T window and the Y^T accumulator are free
@@ -493,6 +579,16 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 if (xp == 1 && fm.real_x) {
 #pragma unroll
                     for (int k = 0; k < 16; ++k) v[k] = 0.0f;
+                } else if constexpr (kBf16) {  // exact in TF32: no rounding
+                    const char* planebase = xbase + xp * kPlane16;
+                    float r[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int sr = 16 * cg + (k ^ (4 * xp));
+                        r[k] = ptx::bf16_lo(*reinterpret_cast<const uint16_t*>(planebase + off16(sr, xd)));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = xp ? r[k ^ 4] : r[k];
                 } else {
                     const char* rowbase = xbase + stk_row(xd >> 5, xp ^ swx, 0) + 4 * (xd & 3);
                     const int cq = (xd & 31) >> 2;
@@ -518,8 +614,14 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int sr = 4 * bsb + i;
-                        bv[pp][i] = *reinterpret_cast<const float2*>(bbase + stk_row(bnb >> 3, pp ^ swb, sr) +
-                                                                     chunk16(bnb & 7, sr) + 8 * bjh);
+                        if constexpr (kBf16) {
+                            const uint32_t two = *reinterpret_cast<const uint32_t*>(
+                                bbase + pp * kPlane16 + off16(sr, 4 * bnb + 2 * bjh));
+                            bv[pp][i] = make_float2(ptx::bf16_lo(two), ptx::bf16_hi(two));
+                        } else {
+                            bv[pp][i] = *reinterpret_cast<const float2*>(bbase + stk_row(bnb >> 3, pp ^ swb, sr) +
+                                                                         chunk16(bnb & 7, sr) + 8 * bjh);
+                        }
                     }
             }
             ptx::tmem_wait_st();
@@ -527,7 +629,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             ptx::named_sync(kWorkerBar, kWorkers);
             // every worker has read x; the tile is free at once, unless the previous row's y is
             // staged in it below (then once its TMA stores have read it)
-            if (tid == 0 && !staged) ptx::mbar_arrive(&sm.free_x[s]);
+            if (tid == 0 && (kBf16 || !staged)) ptx::mbar_arrive(&sm.free_x[s]);
             if (lane == 0) ptx::mbar_arrive(&sm.xt_ready);
 
             // ---- B: (dec o B_j)^T in place of B (after C B^T has read it)
@@ -546,9 +648,9 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                         ore[i] = ptx::to_tf32(v.x);
                         oim[i] = ptx::to_tf32(v.y);
                     }
-                    *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 0, nr) + chunk16(bsb & 7, nr)) =
+                    *reinterpret_cast<float4*>(bwork + stk_row(bsb >> 3, 0, nr) + chunk16(bsb & 7, nr)) =
                         make_float4(ore[0], ore[1], ore[2], ore[3]);
-                    *reinterpret_cast<float4*>(bbase + stk_row(bsb >> 3, 1, nr) + chunk16(bsb & 7, nr)) =
+                    *reinterpret_cast<float4*>(bwork + stk_row(bsb >> 3, 1, nr) + chunk16(bsb & 7, nr)) =
                         make_float4(oim[0], oim[1], oim[2], oim[3]);
                 }
                 ptx::fence_proxy_async_smem();
@@ -566,7 +668,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     row.c = cur.c > 0 ? cur.c - 1 : nc - 1;
                     if (cur.c == 0) row.q = cur.q - (int)gridDim.x;
                 }
-                stage_y(xbase, row);
+                stage_y(ystage, row);
             }
 
             // ---- C: C'_r = C_r o exp(Acs[l]) in place, plane 0 real. Unit: physical 16-byte chunk
@@ -577,10 +679,21 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 for (int k = 0; k < 2; ++k) {
                     const int u = tid + kWorkers * k;
                     const int j = u & 7, i = (u >> 3) & 7, g = (u >> 6) & 7, half = u >> 9;
-                    char* r0 = cbase + inter_row(half, 16 * g + i) + 16 * j;
+                    char* r0 = cwork + inter_row(half, 16 * g + i) + 16 * j;
                     char* r1 = r0 + 8 * 128;
                     const float2 e = sm.eacs[cp][orow + 8 * g + i];
-                    const float4 v0 = *reinterpret_cast<const float4*>(r0), v1 = *reinterpret_cast<const float4*>(r1);
+                    float4 v0, v1;
+                    if constexpr (kBf16) {
+                        // physical chunk j of row m holds features 32 half + 4 (j ^ (m % 8)) .. + 3
+                        const int f = 32 * half + 4 * (j ^ i);
+                        const uint2 w0 = *reinterpret_cast<const uint2*>(cbase + off16(16 * g + i, f));
+                        const uint2 w1 = *reinterpret_cast<const uint2*>(cbase + off16(16 * g + 8 + i, f));
+                        v0 = make_float4(ptx::bf16_lo(w0.x), ptx::bf16_hi(w0.x), ptx::bf16_lo(w0.y), ptx::bf16_hi(w0.y));
+                        v1 = make_float4(ptx::bf16_lo(w1.x), ptx::bf16_hi(w1.x), ptx::bf16_lo(w1.y), ptx::bf16_hi(w1.y));
+                    } else {
+                        v0 = *reinterpret_cast<const float4*>(r0);
+                        v1 = *reinterpret_cast<const float4*>(r1);
+                    }
                     const float4 cr = kSwapC ? v1 : v0, ci = kSwapC ? v0 : v1;
                     using ptx::to_tf32;
                     *reinterpret_cast<float4*>(r0) =
@@ -633,9 +746,9 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 const int mre = inter_m(rr, 0), mim = inter_m(rr, 1);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    *reinterpret_cast<float2*>(bbase + pair_off(kh, mre, 8 * j + 2 * lq)) =
+                    *reinterpret_cast<float2*>(bwork + pair_off(kh, mre, 8 * j + 2 * lq)) =
                         make_float2(ptx::to_tf32(pv[j][0].x), ptx::to_tf32(pv[j][1].x));
-                    *reinterpret_cast<float2*>(bbase + pair_off(kh, mim, 8 * j + 2 * lq)) =
+                    *reinterpret_cast<float2*>(bwork + pair_off(kh, mim, 8 * j + 2 * lq)) =
                         make_float2(ptx::to_tf32(pv[j][0].y), ptx::to_tf32(pv[j][1].y));
                 }
                 ptx::fence_proxy_async_smem();
@@ -695,9 +808,9 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&sm.sin_ready);
             }
-            if (tid == 0 && staged) {  // the y stores have read the x tile
+            if (tid == 0 && staged) {  // the y stores have read the staging tile
                 ptx::bulk_wait_read_all();
-                ptx::mbar_arrive(&sm.free_x[s]);
+                if (!kBf16) ptx::mbar_arrive(&sm.free_x[s]);
             }
             if (diag) ++ndiag;
             cur = item_next<kBlocks>(cur, R, nc);
@@ -709,7 +822,9 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             ptx::named_sync(kWorkerBar, kWorkers);
             // the last block of the CTA's last chunk: its last row
             const int qlast = (int)blockIdx.x + (nseq_cta - 1) * (int)gridDim.x;
-            stage_y(reinterpret_cast<char*>(sm.x[(nitems - 1) & 1]), item_at(qlast, nc - 1, R - 1, R - 1));
+            char* buf = reinterpret_cast<char*>(sm.x[(nitems - 1) & 1]);
+            if constexpr (kBf16) buf = reinterpret_cast<char*>(sm.yw);
+            stage_y(buf, item_at(qlast, nc - 1, R - 1, R - 1));
             if (tid == 0) ptx::bulk_wait_all();
         }
     }
@@ -718,15 +833,17 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
-constexpr size_t kSmemBytes = sizeof(Smem);
+constexpr size_t kSmemBytes = sizeof(Smem<false>) > sizeof(Smem<true>) ? sizeof(Smem<false>) : sizeof(Smem<true>);
 bool g_attr_set[64] = {};
 std::mutex g_mu;
 
 int set_attrs(int dev) {
     std::lock_guard<std::mutex> g(g_mu);
     if (g_attr_set[dev]) return SSDC_OK;
-    const void* kernels[4] = {(const void*)fused2_kernel<false, false>, (const void*)fused2_kernel<true, false>,
-                              (const void*)fused2_kernel<false, true>, (const void*)fused2_kernel<true, true>};
+    const void* kernels[6] = {
+        (const void*)fused2_kernel<false, false, false>, (const void*)fused2_kernel<true, false, false>,
+        (const void*)fused2_kernel<false, true, false>,  (const void*)fused2_kernel<true, true, false>,
+        (const void*)fused2_kernel<false, false, true>,  (const void*)fused2_kernel<false, true, true>};
     for (const void* k : kernels)
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
             return SSDC_ERR_CUDA;
@@ -756,16 +873,22 @@ int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bo
     const int grid = (int)(nseq < sms ? nseq : sms);
     const dim3 g((unsigned)grid), b(fused2::kThreads);
     const bool swap_c = (fm.swap & 4) != 0, blocks = p.Q > fused2::kQ;
-    if (blocks) {
-        if (swap_c)
-            fused2::fused2_kernel<true, true><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+    const size_t sb = fused2::kSmemBytes;
+    if (p.in_bf16) {  // bfloat16 inputs take the per-plane maps: never swapped
+        if (blocks)
+            fused2::fused2_kernel<false, true, true><<<g, b, sb, stream>>>(p, ws, fm);
         else
-            fused2::fused2_kernel<false, true><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+            fused2::fused2_kernel<false, false, true><<<g, b, sb, stream>>>(p, ws, fm);
+    } else if (blocks) {
+        if (swap_c)
+            fused2::fused2_kernel<true, true, false><<<g, b, sb, stream>>>(p, ws, fm);
+        else
+            fused2::fused2_kernel<false, true, false><<<g, b, sb, stream>>>(p, ws, fm);
     } else {
         if (swap_c)
-            fused2::fused2_kernel<true, false><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+            fused2::fused2_kernel<true, false, false><<<g, b, sb, stream>>>(p, ws, fm);
         else
-            fused2::fused2_kernel<false, false><<<g, b, fused2::kSmemBytes, stream>>>(p, ws, fm);
+            fused2::fused2_kernel<false, false, false><<<g, b, sb, stream>>>(p, ws, fm);
     }
     return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
 }

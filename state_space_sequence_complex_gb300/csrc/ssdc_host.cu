@@ -127,11 +127,12 @@ int setup_device_attrs() {
     return SSDC_OK;
 }
 
-// The forward pass behind ssd_complex_fwd_ws and ssd_complex_fwd_init: s0 = the
-// initial state's planes, or both null for a zero initial state.
+// The forward pass behind ssd_complex_fwd_ws, ssd_complex_fwd_init and
+// ssd_complex_fwd_bf16: s0 = the initial state's planes, or both null for a zero
+// initial state; in_bf16: x, B_t and C_t point to bfloat16 planes.
 int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt, ssdc_cin s0, ssdc_dims dims,
              int chunk_size, ssdc_cout y, ssdc_cout final_state, void* workspace, size_t ws_bytes,
-             cudaStream_t stream);
+             cudaStream_t stream, bool in_bf16 = false);
 
 }  // namespace
 
@@ -158,15 +159,29 @@ int ssd_complex_fwd_init(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, con
                     stream);
 }
 
+int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_cin_bf16 C_t, const float* dt,
+                         ssdc_cin initial_state, ssdc_dims dims, int chunk_size, ssdc_cout y,
+                         ssdc_cout final_state, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    auto as_cin = [](ssdc_cin_bf16 v) {
+        return ssdc_cin{reinterpret_cast<const float*>(v.re), reinterpret_cast<const float*>(v.im)};
+    };
+    return fwd_impl(as_cin(x), A, as_cin(B_t), as_cin(C_t), dt, initial_state, dims, chunk_size, y, final_state,
+                    workspace, ws_bytes, stream, true);
+}
+
 }  // extern "C"
 
 namespace {
 
 int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt, ssdc_cin s0, ssdc_dims dims,
              int chunk_size, ssdc_cout y, ssdc_cout final_state, void* workspace, size_t ws_bytes,
-             cudaStream_t stream) {
+             cudaStream_t stream, bool in_bf16) {
     int rc = check_sizes(dims, chunk_size);
     if (rc != SSDC_OK) return rc;
+    // bfloat16 inputs run on the tensor-memory kernel only
+    if (in_bf16 && (dims.precision != SSDC_PREC_TF32 ||
+                    !ssdc::fused2_supported((int)dims.N, (int)dims.D, chunk_size)))
+        return SSDC_ERR_UNSUPPORTED;
     // x.im may be null: a real x (its imaginary plane is zero and is not read)
     const void* ptrs[] = {x.re, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt,
                           y.re, y.im, final_state.re, final_state.im};
@@ -185,13 +200,14 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
 
     // outputs must not overlap inputs, the workspace or each other
     const int64_t BTH = dims.B * dims.T * dims.H;
-    auto rng = [](const void* p, int64_t n) {
+    auto rng = [](const void* p, int64_t n, size_t elem = sizeof(float)) {
         const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-        return Range{lo, p == nullptr ? lo : lo + (uintptr_t)n * sizeof(float)};  // null: empty
+        return Range{lo, p == nullptr ? lo : lo + (uintptr_t)n * elem};  // null: empty
     };
-    const Range in[] = {rng(x.re, BTH * dims.D), rng(x.im, BTH * dims.D), rng(A.re, dims.H),
-                        rng(A.im, dims.H), rng(B_t.re, BTH * dims.N), rng(B_t.im, BTH * dims.N),
-                        rng(C_t.re, BTH * dims.N), rng(C_t.im, BTH * dims.N), rng(dt, BTH),
+    const size_t ie = in_bf16 ? 2 : sizeof(float);  // bytes of an x, B_t or C_t element
+    const Range in[] = {rng(x.re, BTH * dims.D, ie), rng(x.im, BTH * dims.D, ie), rng(A.re, dims.H),
+                        rng(A.im, dims.H), rng(B_t.re, BTH * dims.N, ie), rng(B_t.im, BTH * dims.N, ie),
+                        rng(C_t.re, BTH * dims.N, ie), rng(C_t.im, BTH * dims.N, ie), rng(dt, BTH),
                         Range{reinterpret_cast<uintptr_t>(workspace),
                               reinterpret_cast<uintptr_t>(workspace) + ws_bytes}};
     const int64_t fsn = dims.B * dims.H * dims.N * dims.D;
@@ -227,6 +243,7 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     p.Q = chunk_size;
     p.nc = ssdc::ceil_div64(dims.T, chunk_size);
     p.drop_send_chunk = g_opt_drop_state_chunk.load(std::memory_order_relaxed);
+    p.in_bf16 = in_bf16 ? 1 : 0;
     ssdc::Workspace w = carve(workspace, dims, chunk_size);
 
     (void)cudaGetLastError();  // clear a stale error from unrelated work
@@ -253,8 +270,8 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
         // ceil(sequences / SMs) x chunks at about 3.7 us a chunk; the cluster kernel, its chosen
         // cost at about 4.1 us a chunk with one CTA per sequence and 5.2 us with the state
         // handed between CTAs.
-        int kernel = g_opt_kernel.load(std::memory_order_relaxed);
-        const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q);
+        int kernel = in_bf16 ? 2 : g_opt_kernel.load(std::memory_order_relaxed);
+        const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q) && !in_bf16;
         if (kernel == 0) {
             if (!cluster_ok) {
                 kernel = 2;

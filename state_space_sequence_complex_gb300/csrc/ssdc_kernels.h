@@ -17,6 +17,9 @@ struct Problem {
     int64_t T;
     int B, H, N, D, Q;
     int64_t nc;  // chunks per sequence, ceil(T / Q)
+    // x, B_t and C_t hold bfloat16 planes (the pointers above are their
+    // addresses, read only through tensor maps); 0: fp32
+    int in_bf16 = 0;
     // Test hook of the fused kernel: the CTA of this chunk index does not send
     // the state it computes (-1 = off), so that its successor's bounded wait
     // gives up and reports SSDC_ERR_TIMEOUT.

@@ -400,6 +400,19 @@ bool encode_feature_map(CUtensorMap* m, const float* base, int F, int H, int64_t
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// (F, H, T, B) bfloat16 plane, box (64, 1, rows, 1): one 128-byte swizzled row
+// of 64 features per token, zero fill past F and T.
+bool encode_feature_map_bf16(CUtensorMap* m, const void* base, int F, int H, int64_t T, int B, int rows) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)F, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)F * 2, (cuuint64_t)F * H * 2, (cuuint64_t)F * H * 2 * (cuuint64_t)T};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tiled_f32(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                       const cuuint32_t* box) {
     if (!get_encoder() || rank < 1 || rank > 5) return false;

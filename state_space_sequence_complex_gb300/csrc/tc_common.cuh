@@ -128,6 +128,8 @@ struct TcMaps {
 int make_maps(const Problem& p, const float* ws_S, TcMaps* m);
 // Host: one (F, H, T, B) fp32 plane with boxes of (32, 1, rows, 1).
 bool encode_feature_map(CUtensorMap* m, const float* base, int F, int H, int64_t T, int B, int rows);
+// Host: one (F, H, T, B) bfloat16 plane with boxes of (64, 1, rows, 1).
+bool encode_feature_map_bf16(CUtensorMap* m, const void* base, int F, int H, int64_t T, int B, int rows);
 // Host: an fp32 map of any rank (up to 5) with 128-byte swizzle and zero fill;
 // strides[i] is the byte stride of dimension i + 1.
 bool encode_tiled_f32(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,

@@ -32,7 +32,7 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
            "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host",
            "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd",
            "ssd_complex_set_option", "ssd_complex_noalloc_status", "ssd_complex_last_path",
-           "ssd_complex_segment_decay", "ssd_complex_state_combine")
+           "ssd_complex_segment_decay", "ssd_complex_state_combine", "ssd_complex_fwd_bf16")
 
 PATHS = {0: "staged_fp32", 1: "staged_tf32", 2: "fused_cluster", 3: "fused_tmem"}
 
@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_fwd_ws.restype = ctypes.c_int
     lib.ssd_complex_fwd_init.argtypes = common[:5] + [ssdc_cin] + common[5:] + [vp, sz, vp]
     lib.ssd_complex_fwd_init.restype = ctypes.c_int
+    lib.ssd_complex_fwd_bf16.argtypes = common[:5] + [ssdc_cin] + common[5:] + [vp, sz, vp]
+    lib.ssd_complex_fwd_bf16.restype = ctypes.c_int
     lib.ssd_complex_fwd.argtypes = common + [vp]
     lib.ssd_complex_fwd.restype = ctypes.c_int
     lib.ssd_complex_status.argtypes = [vp, vp]
@@ -201,6 +203,29 @@ def ssd_complex_fwd_init(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, s0_
         int(workspace.numel()), ctypes.c_void_p(s.cuda_stream))
     if check and rc != SSDC_OK:
         raise SSDCError(rc, "ssd_complex_fwd_init")
+    return rc
+
+
+def ssd_complex_fwd_bf16(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *, s0_re=None,
+                         s0_im=None, y_re, y_im, fs_re, fs_im, workspace, stream=None, check=True) -> int:
+    """Call ``ssd_complex_fwd_bf16`` on torch CUDA tensors: x, B, C planar
+    ``torch.bfloat16`` (``x_im`` may be None for a real x); A, dt, the optional
+    initial state (s0_re, s0_im) and the outputs float32. Returns the status."""
+    import torch
+
+    for t in (x_re, x_im, B_re, B_im, C_re, C_im):
+        if t is not None and t.dtype != torch.bfloat16:
+            raise TypeError("x, B and C must be torch.bfloat16")
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    d = dims(Bn, T, H, N, D, "tf32")
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_fwd_bf16(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt), _opt_in(s0_re, s0_im),
+        d, int(chunk_size), _cout(y_re, y_im), _cout(fs_re, fs_im), _ptr(workspace), int(workspace.numel()),
+        ctypes.c_void_p(s.cuda_stream))
+    if check and rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_fwd_bf16")
     return rc
 
 
@@ -484,12 +509,17 @@ class Forward:
     tensors and returns ``(y_re, y_im, final_state_re, final_state_im)``;
     ``y_re`` is Re(y)."""
 
-    def __init__(self, Bn, T, H, N, D, chunk_size, precision="tf32", device="cuda"):
+    def __init__(self, Bn, T, H, N, D, chunk_size, precision="tf32", device="cuda", bf16_inputs=False):
+        """``bf16_inputs``: x, B and C are passed as torch.bfloat16 tensors
+        (``ssd_complex_fwd_bf16``; the TF32 precision only)."""
         import torch
 
         self.shape = (Bn, T, H, N, D)
         self.chunk_size = int(chunk_size)
         self.precision = precision
+        self.bf16_inputs = bool(bf16_inputs)
+        if self.bf16_inputs and precision != "tf32":
+            raise SSDCError(SSDC_ERR_UNSUPPORTED, "bfloat16 inputs run on the TF32 path only")
         d = dims(Bn, T, H, N, D, precision)
         rc = ssd_complex_fwd_supported(d, chunk_size)
         if rc != SSDC_OK:
@@ -506,7 +536,11 @@ class Forward:
                  s0_re=None, s0_im=None):
         """``s0_re, s0_im``: an optional initial state (B,H,N,D); passing this
         object's own ``fs_re, fs_im`` continues the previous call in place."""
-        if s0_re is None and s0_im is None:
+        if self.bf16_inputs:
+            ssd_complex_fwd_bf16(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, self.chunk_size,
+                                 s0_re=s0_re, s0_im=s0_im, y_re=self.y_re, y_im=self.y_im, fs_re=self.fs_re,
+                                 fs_im=self.fs_im, workspace=self.workspace, stream=stream)
+        elif s0_re is None and s0_im is None:
             ssd_complex_fwd_ws(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, self.chunk_size,
                                precision=self.precision, y_re=self.y_re, y_im=self.y_im,
                                fs_re=self.fs_re, fs_im=self.fs_im, workspace=self.workspace,

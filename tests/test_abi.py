@@ -271,3 +271,35 @@ def test_set_option_rejects_bad_values(lib):
     assert lib.ssd_complex_set_option(99, 0) == ssdc.SSDC_ERR_INVALID
     for key, default in ssdc.option.DEFAULTS.items():  # defaults are accepted (and left set)
         assert lib.ssd_complex_set_option(key, default) == ssdc.SSDC_OK
+
+
+def _call_bf16(lib, ptrs, d, Q=64, ws=None, ws_bytes=1 << 30):
+    p = ptrs
+    cin = lambda a, b: ssdc.ssdc_cin(a, b)
+    cout = lambda a, b: ssdc.ssdc_cout(a, b)
+    return lib.ssd_complex_fwd_bf16(cin(p[0], p[1]), cin(p[2], p[3]), cin(p[4], p[5]), cin(p[6], p[7]),
+                                    p[8], cin(None, None), d, Q, cout(p[9], p[10]), cout(p[11], p[12]),
+                                    ws, ws_bytes, None)
+
+
+def test_bf16_entry_checks_before_launch(lib):
+    """The bfloat16-input entry point takes the TF32 precision and the tensor-memory
+    kernel's sizes only; its pointer and overlap checks count 2-byte elements for x, B, C."""
+    for prec, N, Q in (("fp32", 64, 64), ("tf32_staged", 64, 64), ("tf32", 12, 64), ("tf32", 64, 48)):
+        d = ssdc.dims(1, 128, 2, N, 64, prec)
+        ptrs, end = fake_ptrs(d)
+        assert _call_bf16(lib, ptrs, d, Q=Q, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
+    d = ssdc.dims(1, 128, 2, 64, 64, "tf32")
+    ptrs, end = fake_ptrs(d)
+    for i in (0, 2, 4, 8, 9, 12):
+        bad = list(ptrs)
+        bad[i] = None
+        assert _call_bf16(lib, bad, d, ws=end) == ssdc.SSDC_ERR_INVALID
+    bad = list(ptrs)
+    bad[4] += 8
+    assert _call_bf16(lib, bad, d, ws=end) == ssdc.SSDC_ERR_ALIGN
+    # y.re starting inside the bfloat16 x.re (its last 16 bytes) is an overlap
+    BTH = d.B * d.T * d.H
+    inside = list(ptrs)
+    inside[9] = ptrs[0] + BTH * d.D * 2 - 16
+    assert _call_bf16(lib, inside, d, ws=end) == ssdc.SSDC_ERR_INVALID
