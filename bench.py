@@ -356,7 +356,9 @@ def backward_workload(args, w):
         if args.real_x:
             L[1], dy[1], dfs = None, None, [None, None]
         layers.append(L + dy + dfs)
-    b = ssdc.Backward(w.B, w.T, w.H, w.N, w.D, Q, "fp32", device=dev)
+    # --precision tf32: the chunk gradients on the TF32 tensor cores (Q <= 64)
+    precision = "tf32" if args.precision == "tf32" else "fp32"
+    b = ssdc.Backward(w.B, w.T, w.H, w.N, w.D, Q, precision, device=dev)
 
     def run():
         for L in layers:
@@ -407,6 +409,11 @@ def backward_workload(args, w):
     fl_unit = bwd_flops_per_unit(wq)
     fl = fl_unit.get(names[top], 0.0) * w.token_heads
     alu_peak, alu_kind = fp32_alu_peak_tflops(dev.index)
+    bound, kind_top = "alu", alu_kind
+    top_peak = alu_peak
+    if precision == "tf32" and names[top] == "bwd_chunk":  # a tensor-core kernel
+        bound, top_peak = "tensor", bf16_peak_tflops() * 1.1 / 2.25
+        kind_top = "measured cuBLAS bf16 TFLOP/s x the nominal TF32 / BF16 ratio 1.1 / 2.25"
     tf = fl / (kmeans[top] / 1000.0) / 1e12
     # minimum HBM bytes per token-head: x, dy, dx (8 D each, 4 D when real), B_t, C_t, dB_t,
     # dC_t (8 N each), dt and ddt (4 each)
@@ -419,20 +426,23 @@ def backward_workload(args, w):
     if (world == 1 and w.name == inputs.LAYER.name and Q == w.Q and not args.no_cpu_baseline
             and not args.real_x):
         cpu = run_oracle_grad_baseline(w)
+    # the FP32 ALU fraction of the whole step (SIMT kernels) is reported either way
     line = {
-        "metric": "complex-SSD bwd token·heads/s (exact fp32 gradients of every input)",
+        "metric": "complex-SSD bwd token·heads/s (" + ("TF32 chunk gradients" if precision == "tf32"
+                                                       else "exact fp32 gradients") + " of every input)",
         "value": units / (ms / 1000.0), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic, drawn on the device per layer",
+        "vs_baseline": None, "dtype": "tf32" if precision == "tf32" else "f32",
+        "data": "synthetic, drawn on the device per layer",
         "config": {"workload": f"{w.name} Q{Q} backward" + (", real x, Re(y) loss" if args.real_x else ""),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N, "chunk_size": Q,
-                   "layers": w.layers, "real_x": bool(args.real_x), "precision": "fp32",
+                   "layers": w.layers, "real_x": bool(args.real_x), "precision": precision,
                    "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MiB write)",
                    "parallelism": f"data parallel: {world} batch(es), dA all-reduced each step"},
-        "roofline": {"bound": "alu", "kernel": names[top], "achieved": tf, "peak": alu_peak,
-                     "peak_kind": alu_kind, "unit": "TFLOP/s", "frac": tf / alu_peak,
+        "roofline": {"bound": bound, "kernel": names[top], "achieved": tf, "peak": top_peak,
+                     "peak_kind": kind_top, "unit": "TFLOP/s", "frac": tf / top_peak,
                      "traffic": profiled_traffic(names[top]) if w.name == inputs.LAYER.name and Q == w.Q
-                     and not args.real_x else None,
+                     and not args.real_x and precision == "fp32" else None,
                      "algorithmic_flops_per_launch": fl,
                      "step_alu_frac": sum(fl_unit.values()) * units / world / (ms / 1000.0) / 1e12 / alu_peak,
                      "hbm_step_frac": bytes_unit * units / world / (ms / 1000.0) / 1e9 / peaks()[0],

@@ -401,9 +401,12 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
  * each other, an input or the workspace. One null plane of a pair that must
  * be given together is SSDC_ERR_INVALID.
  *
- * Precision: SSDC_PREC_FP32 only (exact fp32 on the SIMT cores, every decay
- * with the accurate expf / sincosf); the other precisions return
- * SSDC_ERR_UNSUPPORTED. Sizes as for SSDC_PREC_FP32 in the forward pass.
+ * Precision: SSDC_PREC_FP32 is exact fp32 on the SIMT cores (every decay with
+ * the accurate expf / sincosf), for the sizes of SSDC_PREC_FP32 in the forward
+ * pass. SSDC_PREC_TF32 computes the per-chunk gradient products (dx, dB_t,
+ * dC_t) on the TF32 tensor cores, with chunk_size 16, 32 or 64 and N, D
+ * multiples of 8 up to 64; the chunk recurrences and the step-size gradients
+ * stay exact fp32. SSDC_PREC_TF32_STAGED returns SSDC_ERR_UNSUPPORTED.
  * Errors, streams and ownership as for ssd_complex_fwd_ws.
  */
 size_t ssd_complex_bwd_workspace_bytes(ssdc_dims dims, int chunk_size);

@@ -1,0 +1,681 @@
+// Chunk gradients of the backward pass on the TF32 tensor cores (tcgen05,
+// operands staged by TMA, accumulators in tensor memory), for chunks of Q =
+// 16, 32 or 64 tokens and N, D multiples of 8 up to 64. The same adjoint as
+// the exact kernel of ssdc_bwd.cu (page "Extending -- SSM variants & Triton
+// kernels", Step 3: the backward recomputes the forward, seeded with the true
+// output gradients; landing page, "03 Chunkwise SSD", for the chunked form):
+// with P = (C B^T) o L, W = dY x^H, V = W o conj(L) and R_c the gradient of the
+// state leaving the chunk,
+//   dX^T = dY^T conj(P) + R_c^T conj(dec o B)^T
+//   dB^T = conj(C)^T V + R_c conj(dec o x)^T
+//   dC   = V conj(B) + conj(exp(Acs)) o (dY conj(S_in)^T)
+// written so that each is a sum of plain products: every conjugation and
+// every per-row decay is applied to an operand when it is written (P, V and
+// the transposed B as the threads form them; B, x and dY scaled in place once
+// the products that read them as loaded are done; the windows as they are
+// filled), never in the combine. Then r_t = <dC_t, C_t> - <dB_t, B_t> and the
+// chunk's anchor <R_c, S_out(c)>, as in the exact kernel.
+//
+// One CTA per chunk; 16 worker warps, one warp issuing the MMAs, one loading.
+// Complex products are M = 128, N = 128 real MMAs: the A rows interleave the
+// planes in groups of eight (row 16g + 8p + i = plane p of row 8g + i: the C
+// and dY tiles as loaded, and the TMEM windows), the B rows are stacked
+// (64 rows of plane 0, then plane 1: the B and x tiles as loaded, and the
+// tiles the threads write). One accumulator then holds all four real
+// products of each complex product, in TMEM lanes m and m + 8 and columns c
+// and 64 + c, which the 16x256b access shape hands to one thread.
+//
+// TMEM: acc0 (C B^T, then dX^T), acc1 (dY x^T, then dB^T), acc2 (dC), and
+// two 64-column A windows filled three times. Stages, each ended by a
+// hand-off to the MMA warp:
+//   loads   C, dY (interleaved), B, x (stacked); the R_c^T window (global)
+//   MMA 1   acc0 = C B^T, acc1 = dY x^T
+//   P       P from acc0 -> conj(P)^T tile; BT = conj(B)^T; B' = conj(dec o B)
+//           in place; the dY^T window
+//   MMA 2   acc0 = dY^T conj(P) + R_c^T B'^T                         (dX^T)
+//   V       dX staged and stored (TMA); V from acc1 -> V^T tile (over
+//           conj(P)^T); x'' = conj(dec o x) in place; dY'' = conj(exp(Acs))
+//           o dY in place; windows conj(C)^T and R_c
+//   MMA 3   acc1 = conj(C)^T V + R_c x''^T                            (dB^T)
+//   W       the V window (from the V^T tile); conj(S_in) tile (over V^T);
+//           dB staged and stored, -<dB_l, B_l>
+//   MMA 4   acc2 = V BT^T + dY'' conj(S_in)^T                          (dC)
+//   C       dC stored, r_t
+// Every barrier completes once, so every wait is on phase 0, and every wait
+// is bounded (a wait that gives up records SSDC_ERR_TIMEOUT and the later
+// waits are skipped).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "fused_io.cuh"
+
+namespace ssdc {
+namespace bwdtc {
+namespace {
+
+using namespace tc;
+using namespace fused;
+
+constexpr int kWorkers = 512;
+constexpr int kWorkerWarps = kWorkers / 32;
+constexpr int kIssuer = kWorkerWarps;
+constexpr int kProducer = kWorkerWarps + 1;
+constexpr int kThreads = kWorkers + 64;
+constexpr uint32_t kWorkerBar = 1;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcc0 = 0, kAcc1 = 128, kAcc2 = 256, kWa = 384, kWb = 448;
+
+struct Smem {
+    float c[64 * 128];   // C, interleaved rows (t, plane)
+    float y[64 * 128];   // dY, interleaved rows (t, plane); then dY'' in place
+    float b[64 * 128];   // B, stacked rows (l, plane); then B' in place; then the dX staging (rows l)
+    float x[64 * 128];   // x, stacked rows (l, plane); then x'' in place; then the dB staging (rows l)
+    float bt[64 * 128];  // conj(B)^T, stacked rows (n, plane), K = l
+    float pv[64 * 128];  // conj(P)^T, then V^T (stacked rows (l, plane), K = t); then conj(S_in) (rows n, K = d)
+    float2 acs[64], dec[64], eacs[64], step[64];
+    float2 nbb[64];       // -<dB_l, B_l>
+    float2 dct[2][64];    // <dC_t, C_t>, per 32-column half
+    double anc[kWorkerWarps][2];
+    uint64_t full, mma1, mma2, mma3, mma4, p_ready, v_ready, w_ready;
+    uint32_t tmem;
+};
+
+static_assert(sizeof(Smem) <= 232448, "shared-memory plan exceeds the 227 KB a CTA can have");
+
+// Tensor maps of one call: C and dY in 8-row boxes (the interleaved layout),
+// B and x in boxes of `rows` rows (stacked), dX and dB for the TMA stores.
+struct BwdMaps {
+    CUtensorMap c_re, c_im, y_re, y_im, b_re, b_im, x_re, x_im, dx_re, dx_im, db_re, db_im;
+    int real_x, real_dy, dx_im_out;
+};
+
+// Element (r, k) of a 64-row plane of a stacked or interleaved tile: 32-column
+// half k / 32, row r, the 128-byte swizzle.
+__device__ __forceinline__ uint32_t elem(int r, int k) {
+    return (uint32_t)((k >> 5) * kIntHalf + r * 128) + chunk16((k & 31) >> 2, r) + (uint32_t)(4 * (k & 3));
+}
+// Stacked: plane p of row r at rows 64 p + r of each half; interleaved: row 16 (r / 8) + 8 p + r % 8.
+__device__ __forceinline__ uint32_t stk(int p, int r, int k) { return elem(r, k) + (uint32_t)(p * kHalfBytes); }
+__device__ __forceinline__ uint32_t itl(int p, int r, int k) { return elem(inter_m(r, p), k); }
+__device__ __forceinline__ float ld(const char* base, uint32_t o) { return *reinterpret_cast<const float*>(base + o); }
+__device__ __forceinline__ void st(char* base, uint32_t o, float v) { *reinterpret_cast<float*>(base + o) = v; }
+
+// D (+)= A * B over K = 64, both operands in shared memory.
+__device__ __forceinline__ void issue_ss(uint32_t d, uint32_t a, uint32_t b, bool accumulate) {
+    const uint64_t da = desc128(a), db = desc128(b);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        ptx::mma_tf32_ss(d, desc_k(da, k), desc_k(db, k), kIdesc128, (accumulate || k > 0) ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_chunk_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_constant__ BwdMaps bm) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    const Problem& p = g.f;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H, N = p.N, D = p.D, Q = p.Q;
+    const int64_t nc = p.nc;
+    const int64_t chunk = blockIdx.x;  // (b H + h) nc + c
+    const int c = (int)(chunk % nc);
+    const int64_t bh = chunk / nc;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    const int64_t t0 = (int64_t)c * Q;
+    const int valid = (int)(p.T - t0 < (int64_t)Q ? p.T - t0 : (int64_t)Q);
+    const int rows = Q < kQ ? Q : kQ;
+
+    if (ptx::smem_addr(smem_raw) & 1023u) {
+        if (tid == 0) atomicCAS(ws.status, SSDC_OK, SSDC_ERR_CUDA);
+        return;
+    }
+    if (tid == 0) {
+        uint64_t* one[] = {&sm.full, &sm.mma1, &sm.mma2, &sm.mma3, &sm.mma4};
+        for (uint64_t* bar : one) ptx::mbar_init(bar, 1);
+        ptx::mbar_init(&sm.p_ready, kWorkerWarps);
+        ptx::mbar_init(&sm.v_ready, kWorkerWarps);
+        ptx::mbar_init(&sm.w_ready, kWorkerWarps);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(&sm.tmem, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (Q < kQ || bm.real_x || bm.real_dy) {
+        // rows past Q and the planes of a real x or dY are never loaded: zeros
+        float4* z = reinterpret_cast<float4*>(sm.c);
+        constexpr int kVecs = 4 * 64 * 128 / 4;  // the c, y, b and x tiles
+        for (int i = tid; i < kVecs; i += kThreads) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+
+    if (warp == kProducer) {
+        // ===================== loads and the cumulative log-decay =====================
+        const Alog al = load_alog(p, b, h, t0, lane, rows);
+        if (lane == 0) {
+            const uint32_t planes = 2u + 2u + 2u + (bm.real_x ? 1u : 2u) - (bm.real_dy ? 1u : 0u);
+            ptx::mbar_expect_tx(&sm.full, (uint32_t)rows * 256u * planes);
+        }
+        __syncwarp();
+        const int ng = rows >> 3;
+        // C and dY: 8-row boxes per plane and half (rows 16 g + 8 pl); B and x: one box per plane and half
+        for (int op = lane; op < 8 * ng + 8; op += 32) {
+            if (op < 8 * ng) {
+                const int which = op / (4 * ng), k = op % (4 * ng);
+                const int half = k / (2 * ng), gg = (k >> 1) % ng, pl = k & 1;
+                if (which == 1 && pl == 1 && bm.real_dy) continue;
+                char* dst = reinterpret_cast<char*>(which ? sm.y : sm.c) + half * kIntHalf + (16 * gg + 8 * pl) * 128;
+                const CUtensorMap* m = which ? (pl ? &bm.y_im : &bm.y_re) : (pl ? &bm.c_im : &bm.c_re);
+                ptx::tma_load_4d(dst, m, &sm.full, 32 * half, h, (int)t0 + 8 * gg, b);
+            } else {
+                const int k = op - 8 * ng, which = k >> 2, half = (k >> 1) & 1, pl = k & 1;
+                if (which == 1 && pl == 1 && bm.real_x) continue;
+                char* dst = reinterpret_cast<char*>(which ? sm.x : sm.b) + half * kIntHalf + pl * kHalfBytes;
+                const CUtensorMap* m = which ? (pl ? &bm.x_im : &bm.x_re) : (pl ? &bm.b_im : &bm.b_re);
+                ptx::tma_load_4d(dst, m, &sm.full, 32 * half, h, (int)t0, b);
+            }
+        }
+        store_acs(sm.acs, &sm.full, al, lane);
+    } else if (warp == kIssuer) {
+        // ===================== MMA issue =====================
+        bool ok = true;
+        auto wait = [&](uint64_t* bar) {
+            if (ok && !ptx::mbar_wait(bar, 0u, kWaitIters)) {
+                fail(ws.status);
+                ok = false;
+            }
+        };
+        if (lane == 0) {
+            const uint32_t cs = ptx::smem_addr(sm.c), ys = ptx::smem_addr(sm.y), bs = ptx::smem_addr(sm.b);
+            const uint32_t xs = ptx::smem_addr(sm.x), bts = ptx::smem_addr(sm.bt), pvs = ptx::smem_addr(sm.pv);
+            wait(&sm.full);
+            ptx::tc_fence_after();
+            issue_ss(tmem + kAcc0, cs, bs, false);  // C B^T
+            issue_ss(tmem + kAcc1, ys, xs, false);  // dY x^T
+            ptx::mma_commit(&sm.mma1);
+            wait(&sm.p_ready);
+            ptx::tc_fence_after();
+            issue_ts128(tmem + kAcc0, tmem + kWa, desc128(pvs), false);  // dY^T conj(P)
+            issue_ts128(tmem + kAcc0, tmem + kWb, desc128(bs), true);    // + R_c^T B'^T
+            ptx::mma_commit(&sm.mma2);
+            wait(&sm.v_ready);
+            ptx::tc_fence_after();
+            issue_ts128(tmem + kAcc1, tmem + kWa, desc128(pvs), false);  // conj(C)^T V
+            issue_ts128(tmem + kAcc1, tmem + kWb, desc128(xs), true);    // + R_c x''^T
+            ptx::mma_commit(&sm.mma3);
+            wait(&sm.w_ready);
+            ptx::tc_fence_after();
+            issue_ts128(tmem + kAcc2, tmem + kWa, desc128(bts), false);  // V conj(B)
+            issue_ss(tmem + kAcc2, ys, pvs, true);                       // + dY'' conj(S_in)^T
+            ptx::mma_commit(&sm.mma4);
+        }
+        __syncwarp();
+    } else {
+        // ===================== 16 worker warps =====================
+        // 16x256b fragment: TMEM lane quadrant qd, 16-lane block blk, 32-column half kh; lane i4
+        // holds plane 0 and lane i4 + 8 plane 1 of A row rr; columns c = 32 kh + 8 j + 2 lq + e of
+        // the B operand's plane 0 (first 64 columns) and plane 1 (next 64).
+        const int qd = warp & 3, blk = (warp >> 2) & 1, kh = warp >> 3;
+        const int i4 = lane >> 2, lq = lane & 3;
+        const int rr = 16 * qd + 8 * blk + i4;
+        const uint32_t tl = lane_base(tmem, warp) + ((uint32_t)(16 * blk) << 16);
+        // window fill: this lane writes TMEM lane 32 qd + lane = plane wp of row wr, columns 16 wc ..
+        const int wr = 16 * qd + 8 * (lane >> 4) + (lane & 7), wp = (lane >> 3) & 1, wc = warp >> 2;
+        const uint32_t wl = lane_base(tmem, warp);
+        char* cb = reinterpret_cast<char*>(sm.c);
+        char* yb = reinterpret_cast<char*>(sm.y);
+        char* bb = reinterpret_cast<char*>(sm.b);
+        char* xb = reinterpret_cast<char*>(sm.x);
+        char* btb = reinterpret_cast<char*>(sm.bt);
+        char* pvb = reinterpret_cast<char*>(sm.pv);
+        const float* R = gw.R + chunk * 2 * (int64_t)D * N;     // R_c^T [plane][d][n]
+        const float* Sin = ws.S + chunk * 2 * (int64_t)D * N;   // S_in^T [plane][d][n]
+        bool ok = true;
+        auto wait = [&](uint64_t* bar) {
+            if (ok && !ptx::mbar_wait(bar, 0u, kWaitIters)) {
+                fail(ws.status);
+                ok = false;
+            }
+        };
+        // (values v[k], k < 16, of window columns 16 wc + k) -> TMEM, rounded to TF32
+        auto put_window = [&](uint32_t col0, const float* v) {
+            float r[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = ptx::to_tf32(v[k]);
+            ptx::tmem_st16(wl + col0 + 16 * wc, r);
+        };
+        // Window of a transposed interleaved tile: row wr, column k = plane wp of T[k][wr], T with
+        // rows k interleaved (C or dY); plane-1 lanes read row k ^ 4 (rows 8 apart share banks)
+        auto window_from_itl = [&](const char* src, float sign1, float* v) {
+            float r[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = ld(src, itl(wp, 16 * wc + (k ^ (4 * wp)), wr));
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = (wp ? sign1 : 1.0f) * (wp ? r[k ^ 4] : r[k]);
+        };
+        // The same from a stacked tile with rows k (V^T)
+        auto window_from_stk = [&](const char* src, float* v) {
+            float r[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = ld(src, stk(wp, 16 * wc + (k ^ (4 * wp)), wr));
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = wp ? r[k ^ 4] : r[k];
+        };
+        // Stage an accumulator whose A rows are features f (lanes) and B rows tokens l (stacked
+        // columns) as rows l of a TMA store tile: Re = A0 B0 - A1 B1, Im = A0 B1 + A1 B0.
+        auto stage_t = [&](uint32_t acc, char* buf) {
+            float v0[16], v1[16];
+            ptx::tmem_ld_16x256b_x4(tl + acc + 32 * kh, v0);       // products with B's plane 0
+            ptx::tmem_ld_16x256b_x4(tl + acc + 64 + 32 * kh, v1);  // and with its plane 1
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int l = 32 * kh + 8 * j + 2 * lq + e;
+                    st(buf, stk(0, l, rr), v0[4 * j + e] - v1[4 * j + 2 + e]);
+                    st(buf, stk(1, l, rr), v1[4 * j + e] + v0[4 * j + 2 + e]);
+                }
+        };
+        auto store_t = [&](const CUtensorMap* re, const CUtensorMap* im, const char* buf) {
+            if (tid == 0) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    ptx::tma_store_4d(re, buf + half * kIntHalf, 32 * half, h, (int)t0, b);
+                    if (im != nullptr) ptx::tma_store_4d(im, buf + half * kIntHalf + kHalfBytes, 32 * half, h, (int)t0, b);
+                }
+                ptx::bulk_commit();
+            }
+        };
+
+        // ---- while the tiles load: the R_c^T window (rows d, K = n) and the anchor <R_c, S_out(c)>
+        {
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int n = 16 * wc + k;
+                v[k] = (wr < D && n < N) ? __ldg(R + ((int64_t)wp * D + wr) * N + n) : 0.0f;
+            }
+            put_window(kWb, v);
+        }
+        {
+            const bool last_chunk = c == nc - 1;
+            const float* nxt = ws.S + (chunk + 1) * 2 * (int64_t)D * N;
+            // D N <= 4096: at most 8 elements a thread, all loads issued before the sums
+            float lr[8], li[8], lsr[8], lsi[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int e = tid + kWorkers * k;
+                lr[k] = li[k] = lsr[k] = lsi[k] = 0.0f;
+                if (e < D * N) {
+                    if (last_chunk) {
+                        const int d = e / N, n = e - (e / N) * N;
+                        const int64_t o = (bh * N + n) * D + d;
+                        lsr[k] = p.fs_re[o];
+                        lsi[k] = p.fs_im[o];
+                    } else {
+                        lsr[k] = __ldg(nxt + e);
+                        lsi[k] = __ldg(nxt + (int64_t)D * N + e);
+                    }
+                    lr[k] = __ldg(R + e);
+                    li[k] = __ldg(R + (int64_t)D * N + e);
+                }
+            }
+            float ar = 0.0f, ai = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                ar += lr[k] * lsr[k] + li[k] * lsi[k];  // R conj(S_out)
+                ai += li[k] * lsr[k] - lr[k] * lsi[k];
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                ar += __shfl_xor_sync(0xffffffffu, ar, off);
+                ai += __shfl_xor_sync(0xffffffffu, ai, off);
+            }
+            if (lane == 0) {
+                sm.anc[warp][0] = ar;
+                sm.anc[warp][1] = ai;
+            }
+        }
+        wait(&sm.full);
+        ptx::tc_fence_after();
+        // decay tables
+        if (tid < 3 * kQ) {
+            const int t = tid % kQ, which = tid / kQ;
+            if (which == 0) sm.dec[t] = t < Q ? cexp_fast(cdiff(sm.acs[Q - 1], sm.acs[t])) : make_float2(0.0f, 0.0f);
+            else if (which == 1) sm.eacs[t] = cexp_fast(sm.acs[t]);
+            else if (t >= 1) sm.step[t] = cexp_fast(cdiff(sm.acs[t], sm.acs[t - 1]));
+        }
+        ptx::named_sync(kWorkerBar, kWorkers);
+        if (tid == 0) {
+            double sr = 0.0, si = 0.0;
+            for (int w = 0; w < kWorkerWarps; ++w) {
+                sr += sm.anc[w][0];
+                si += sm.anc[w][1];
+            }
+            gw.anchor[2 * chunk] = sr;
+            gw.anchor[2 * chunk + 1] = si;
+        }
+
+        // decay L[rr, col] of a causal pair (t = rr >= l = col), from one exponential per column pair
+        auto decay_pair = [&](int col, float2* L0, float2* L1) {
+            *L0 = make_float2(0.0f, 0.0f);
+            *L1 = make_float2(0.0f, 0.0f);
+            if (col + 1 <= rr) {
+                *L1 = cexp_fast(cdiff(sm.acs[rr], sm.acs[col + 1]));
+                *L0 = cmul(*L1, sm.step[col + 1]);
+            } else if (col == rr) {
+                *L0 = make_float2(1.0f, 0.0f);
+            }
+        };
+
+        // ---- stage P (after C B^T and dY x^T)
+        wait(&sm.mma1);
+        ptx::tc_fence_after();
+        {
+            float ga[16], gb[16];
+            ptx::tmem_ld_16x256b_x4(tl + kAcc0 + 32 * kh, ga);
+            ptx::tmem_ld_16x256b_x4(tl + kAcc0 + 64 + 32 * kh, gb);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = 32 * kh + 8 * j + 2 * lq;
+                float2 L0, L1;
+                decay_pair(col, &L0, &L1);
+                // G = C B^T: Re = Cr Br - Ci Bi, Im = Cr Bi + Ci Br
+                const float2 g0 = make_float2(ga[4 * j] - gb[4 * j + 2], gb[4 * j] + ga[4 * j + 2]);
+                const float2 g1 = make_float2(ga[4 * j + 1] - gb[4 * j + 3], gb[4 * j + 1] + ga[4 * j + 3]);
+                const float2 p0 = cmul(g0, L0), p1 = cmul(g1, L1);
+                // conj(P)^T: row l = col (+1), column t = rr
+                st(pvb, stk(0, col, rr), ptx::to_tf32(p0.x));
+                st(pvb, stk(1, col, rr), ptx::to_tf32(-p0.y));
+                st(pvb, stk(0, col + 1, rr), ptx::to_tf32(p1.x));
+                st(pvb, stk(1, col + 1, rr), ptx::to_tf32(-p1.y));
+            }
+        }
+        {
+            // BT = conj(B)^T, then B' = conj(dec o B) in place. Blocks: rows l = 4 bsb + i, columns
+            // n = 4 bnb + 2 bjh + {0, 1}; each thread rewrites exactly the B elements it read.
+            const int L0b = lane & 1, L1b = (lane >> 1) & 1, L2b = (lane >> 2) & 1, L3b = (lane >> 3) & 1, L4b = lane >> 4;
+            const int bjh = L1b, bsb = L2b + 2 * (warp >> 1), bnb = L0b + 2 * L3b + 4 * L4b + 8 * (warp & 1);
+            float2 bv[2][4];
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int l = 4 * bsb + i, n = 4 * bnb + 2 * bjh;
+                    bv[pp][i] = make_float2(ld(bb, stk(pp, l, n)), ld(bb, stk(pp, l, n + 1)));
+                }
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn) {
+                const int n = 4 * bnb + 2 * bjh + jn;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int l = 4 * bsb + i;
+                    const float br = jn ? bv[0][i].y : bv[0][i].x, bi = jn ? bv[1][i].y : bv[1][i].x;
+                    st(btb, stk(0, n, l), ptx::to_tf32(br));
+                    st(btb, stk(1, n, l), ptx::to_tf32(-bi));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int l = 4 * bsb + i, n = 4 * bnb + 2 * bjh;
+                const float2 dv = sm.dec[l];
+                // conj(dec B): Re = dr br - di bi, Im = -(dr bi + di br)
+                const float2 w0 = make_float2(dv.x * bv[0][i].x - dv.y * bv[1][i].x, dv.x * bv[0][i].y - dv.y * bv[1][i].y);
+                const float2 w1 = make_float2(-(dv.x * bv[1][i].x + dv.y * bv[0][i].x),
+                                              -(dv.x * bv[1][i].y + dv.y * bv[0][i].y));
+                st(bb, stk(0, l, n), ptx::to_tf32(w0.x));
+                st(bb, stk(0, l, n + 1), ptx::to_tf32(w0.y));
+                st(bb, stk(1, l, n), ptx::to_tf32(w1.x));
+                st(bb, stk(1, l, n + 1), ptx::to_tf32(w1.y));
+            }
+        }
+        {
+            float v[16];
+            window_from_itl(yb, 1.0f, v);  // dY^T
+            put_window(kWa, v);
+        }
+        ptx::tmem_wait_st();
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.p_ready);
+
+        // ---- stage V (after dX^T). The R_c window's loads are issued before the wait.
+        float rwin[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {  // R_c: rows n, K = d
+            const int d = 16 * wc + k;
+            rwin[k] = (wr < N && d < D) ? __ldg(R + ((int64_t)wp * D + d) * N + wr) : 0.0f;
+        }
+        wait(&sm.mma2);
+        ptx::tc_fence_after();
+        put_window(kWb, rwin);
+        ptx::named_sync(kWorkerBar, kWorkers);  // every worker is past its B and dY reads
+        stage_t(kAcc0, bb);                     // dX (B' is consumed)
+        {
+            float ga[16], gb[16];
+            ptx::tmem_ld_16x256b_x4(tl + kAcc1 + 32 * kh, ga);
+            ptx::tmem_ld_16x256b_x4(tl + kAcc1 + 64 + 32 * kh, gb);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = 32 * kh + 8 * j + 2 * lq;
+                float2 L0, L1;
+                decay_pair(col, &L0, &L1);
+                // W = dY conj(x): Re = Yr xr + Yi xi, Im = Yi xr - Yr xi
+                const float2 w0 = make_float2(ga[4 * j] + gb[4 * j + 2], ga[4 * j + 2] - gb[4 * j]);
+                const float2 w1 = make_float2(ga[4 * j + 1] + gb[4 * j + 3], ga[4 * j + 3] - gb[4 * j + 1]);
+                const float2 v0 = cmul(w0, make_float2(L0.x, -L0.y)), v1 = cmul(w1, make_float2(L1.x, -L1.y));
+                st(pvb, stk(0, col, rr), ptx::to_tf32(v0.x));  // V^T
+                st(pvb, stk(1, col, rr), ptx::to_tf32(v0.y));
+                st(pvb, stk(0, col + 1, rr), ptx::to_tf32(v1.x));
+                st(pvb, stk(1, col + 1, rr), ptx::to_tf32(v1.y));
+            }
+        }
+        {
+            // x'' = conj(dec o x) in place: same blocks as B (rows l, columns d)
+            const int L0b = lane & 1, L1b = (lane >> 1) & 1, L2b = (lane >> 2) & 1, L3b = (lane >> 3) & 1, L4b = lane >> 4;
+            const int bjh = L1b, bsb = L2b + 2 * (warp >> 1), bnb = L0b + 2 * L3b + 4 * L4b + 8 * (warp & 1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int l = 4 * bsb + i, d = 4 * bnb + 2 * bjh;
+                const float2 dv = sm.dec[l];
+                const float2 xr = make_float2(ld(xb, stk(0, l, d)), ld(xb, stk(0, l, d + 1)));
+                const float2 xi = make_float2(ld(xb, stk(1, l, d)), ld(xb, stk(1, l, d + 1)));
+                st(xb, stk(0, l, d), ptx::to_tf32(dv.x * xr.x - dv.y * xi.x));
+                st(xb, stk(0, l, d + 1), ptx::to_tf32(dv.x * xr.y - dv.y * xi.y));
+                st(xb, stk(1, l, d), ptx::to_tf32(-(dv.x * xi.x + dv.y * xr.x)));
+                st(xb, stk(1, l, d + 1), ptx::to_tf32(-(dv.x * xi.y + dv.y * xr.y)));
+            }
+        }
+        {
+            // dY'' = conj(exp(Acs[t])) dY in place: rows t = 8 gq + i (planes at rows 16 gq + i, + 8),
+            // columns 4 jq .. 4 jq + 3 of half hq; physical 16-byte chunks, the factor per row
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int u = tid + kWorkers * k;
+                const int jq = u & 7, i = (u >> 3) & 7, gq = (u >> 6) & 7, hq = u >> 9;
+                char* r0 = yb + hq * kIntHalf + (16 * gq + i) * 128 + 16 * jq;
+                char* r1 = r0 + 8 * 128;
+                const float2 e = sm.eacs[8 * gq + i];
+                const float4 a = *reinterpret_cast<const float4*>(r0), q = *reinterpret_cast<const float4*>(r1);
+                using ptx::to_tf32;
+                // (er - i ei)(yr + i yi) = er yr + ei yi + i (er yi - ei yr)
+                *reinterpret_cast<float4*>(r0) =
+                    make_float4(to_tf32(e.x * a.x + e.y * q.x), to_tf32(e.x * a.y + e.y * q.y),
+                                to_tf32(e.x * a.z + e.y * q.z), to_tf32(e.x * a.w + e.y * q.w));
+                *reinterpret_cast<float4*>(r1) =
+                    make_float4(to_tf32(e.x * q.x - e.y * a.x), to_tf32(e.x * q.y - e.y * a.y),
+                                to_tf32(e.x * q.z - e.y * a.z), to_tf32(e.x * q.w - e.y * a.w));
+            }
+        }
+        {
+            float v[16];
+            window_from_itl(cb, -1.0f, v);  // conj(C)^T
+            put_window(kWa, v);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_sync(kWorkerBar, kWorkers);  // the dX staging is written
+        store_t(&bm.dx_re, bm.dx_im_out ? &bm.dx_im : nullptr, bb);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.v_ready);
+
+        // ---- stage W (after dB^T). The S_in loads (8 elements a thread) are issued before the wait.
+        float sinr[8], sini[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int e = tid + kWorkers * k, d = e >> 6, n = e & 63;
+            const bool in = d < D && n < N;
+            sinr[k] = in ? __ldg(Sin + (int64_t)d * N + n) : 0.0f;
+            sini[k] = in ? __ldg(Sin + (int64_t)D * N + (int64_t)d * N + n) : 0.0f;
+        }
+        wait(&sm.mma3);
+        ptx::tc_fence_after();
+        {
+            float v[16];
+            window_from_stk(pvb, v);  // V: rows t, K = l, from V^T
+            put_window(kWa, v);
+        }
+        ptx::named_sync(kWorkerBar, kWorkers);  // every V^T read is done
+        {
+            // conj(S_in): rows n, K = d, from S_in^T [plane][d][n]
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int e = tid + kWorkers * k, d = e >> 6, n = e & 63;
+                st(pvb, stk(0, n, d), ptx::to_tf32(sinr[k]));
+                st(pvb, stk(1, n, d), ptx::to_tf32(-sini[k]));
+            }
+        }
+        stage_t(kAcc1, xb);  // dB (x'' is consumed)
+        ptx::fence_proxy_async_smem();
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::named_sync(kWorkerBar, kWorkers);
+        if (lane == 0) ptx::mbar_arrive(&sm.w_ready);
+        store_t(&bm.db_re, &bm.db_im, xb);
+        {
+            // -<dB_l, B_l> = -sum_n dB[l, n] conj(B[l, n]), conj(B[l, n]) = BT[n][l]: 8 threads a row
+            const int l = tid >> 3, s8 = tid & 7;
+            float sr = 0.0f, si = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int n = 8 * s8 + k;
+                const float dr = ld(xb, stk(0, l, n)), di = ld(xb, stk(1, l, n));
+                const float br = ld(btb, stk(0, n, l)), bi = ld(btb, stk(1, n, l));
+                sr += dr * br - di * bi;
+                si += dr * bi + di * br;
+            }
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                sr += __shfl_xor_sync(0xffffffffu, sr, off);
+                si += __shfl_xor_sync(0xffffffffu, si, off);
+            }
+            if (s8 == 0) sm.nbb[l] = make_float2(-sr, -si);
+        }
+
+        // ---- stage C (after dC)
+        wait(&sm.mma4);
+        ptx::tc_fence_after();
+        {
+            float ga[16], gb[16];
+            ptx::tmem_ld_16x256b_x4(tl + kAcc2 + 32 * kh, ga);
+            ptx::tmem_ld_16x256b_x4(tl + kAcc2 + 64 + 32 * kh, gb);
+            ptx::tmem_wait_ld();
+            const bool row_ok = rr < valid;
+            const int64_t tok = ((int64_t)b * p.T + t0 + rr) * H + h;
+            float sr = 0.0f, si = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = 32 * kh + 8 * j + 2 * lq;
+                const float2 d0 = make_float2(ga[4 * j] - gb[4 * j + 2], gb[4 * j] + ga[4 * j + 2]);
+                const float2 d1 = make_float2(ga[4 * j + 1] - gb[4 * j + 3], gb[4 * j + 1] + ga[4 * j + 3]);
+                if (row_ok && n < N) {  // N is a multiple of 8: n + 1 < N too
+                    *reinterpret_cast<float2*>(g.dC_re + tok * N + n) = make_float2(d0.x, d1.x);
+                    *reinterpret_cast<float2*>(g.dC_im + tok * N + n) = make_float2(d0.y, d1.y);
+                }
+                // <dC_t, C_t> = sum dC conj(C)
+                const float c0r = ld(cb, itl(0, rr, n)), c0i = ld(cb, itl(1, rr, n));
+                const float c1r = ld(cb, itl(0, rr, n + 1)), c1i = ld(cb, itl(1, rr, n + 1));
+                sr += d0.x * c0r + d0.y * c0i + d1.x * c1r + d1.y * c1i;
+                si += d0.y * c0r - d0.x * c0i + d1.y * c1r - d1.x * c1i;
+            }
+            sr += __shfl_xor_sync(0xffffffffu, sr, 1);
+            si += __shfl_xor_sync(0xffffffffu, si, 1);
+            sr += __shfl_xor_sync(0xffffffffu, sr, 2);
+            si += __shfl_xor_sync(0xffffffffu, si, 2);
+            if (lq == 0) sm.dct[kh][rr] = make_float2(sr, si);
+        }
+        ptx::named_sync(kWorkerBar, kWorkers);
+        if (tid < 64 && tid < valid) {
+            const float2 a = sm.dct[0][tid], q = sm.dct[1][tid], nb = sm.nbb[tid];
+            float* rre = gw.r + bh * 2 * p.T;
+            rre[t0 + tid] = a.x + q.x + nb.x;
+            rre[p.T + t0 + tid] = a.y + q.y + nb.y;
+        }
+        if (tid == 0) ptx::bulk_wait_all();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+constexpr size_t kSmemBytes = sizeof(Smem);
+bool g_attr_set[64] = {};
+
+int make_maps(const GradProblem& g, BwdMaps* m) {
+    const Problem& p = g.f;
+    memset(m, 0, sizeof(*m));
+    m->real_x = p.x_im == nullptr;
+    m->real_dy = g.dy_im == nullptr;
+    m->dx_im_out = g.dx_im != nullptr;
+    const int rows = p.Q < kQ ? p.Q : kQ;
+    bool ok = encode_feature_map(&m->c_re, p.C_re, p.N, p.H, p.T, p.B, 8) &&
+              encode_feature_map(&m->c_im, p.C_im, p.N, p.H, p.T, p.B, 8) &&
+              encode_feature_map(&m->y_re, g.dy_re, p.D, p.H, p.T, p.B, 8) &&
+              (m->real_dy || encode_feature_map(&m->y_im, g.dy_im, p.D, p.H, p.T, p.B, 8)) &&
+              encode_feature_map(&m->b_re, p.B_re, p.N, p.H, p.T, p.B, rows) &&
+              encode_feature_map(&m->b_im, p.B_im, p.N, p.H, p.T, p.B, rows) &&
+              encode_feature_map(&m->x_re, p.x_re, p.D, p.H, p.T, p.B, rows) &&
+              (m->real_x || encode_feature_map(&m->x_im, p.x_im, p.D, p.H, p.T, p.B, rows)) &&
+              encode_feature_map(&m->dx_re, g.dx_re, p.D, p.H, p.T, p.B, rows) &&
+              (!m->dx_im_out || encode_feature_map(&m->dx_im, g.dx_im, p.D, p.H, p.T, p.B, rows)) &&
+              encode_feature_map(&m->db_re, g.dB_re, p.N, p.H, p.T, p.B, rows) &&
+              encode_feature_map(&m->db_im, g.dB_im, p.N, p.H, p.T, p.B, rows);
+    return ok ? SSDC_OK : SSDC_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace bwdtc
+
+bool bwd_tc_supported(int N, int D, int Q) {
+    return (Q == 16 || Q == 32 || Q == 64) && N >= 8 && N <= 64 && N % 8 == 0 && D >= 8 && D <= 64 && D % 8 == 0;
+}
+
+int bwd_tc_launch_chunk(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw, cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSDC_ERR_CUDA;
+    if (!bwdtc::g_attr_set[dev]) {
+        if (cudaFuncSetAttribute(bwdtc::bwd_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bwdtc::kSmemBytes) != cudaSuccess)
+            return SSDC_ERR_CUDA;
+        bwdtc::g_attr_set[dev] = true;
+    }
+    bwdtc::BwdMaps m;
+    const int rc = bwdtc::make_maps(g, &m);
+    if (rc != SSDC_OK) return rc;
+    const Problem& p = g.f;
+    const int64_t chunks = (int64_t)p.B * p.H * p.nc;
+    bwdtc::bwd_chunk_tc<<<(unsigned)chunks, bwdtc::kThreads, bwdtc::kSmemBytes, stream>>>(g, ws, gw, m);
+    return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
+}
+
+}  // namespace ssdc

@@ -437,10 +437,15 @@ BwdLayout bwd_layout(const ssdc_dims& d, int Q) {
     return l;
 }
 
+// The exact fp32 backward takes every size the forward does; the TF32 one
+// (chunk gradients on the tensor cores) Q = 16, 32, 64 with N, D multiples of
+// 8 up to 64.
 int check_bwd_sizes(const ssdc_dims& d, int Q) {
     const int rc = check_sizes(d, Q);
     if (rc != SSDC_OK) return rc;
-    return d.precision == SSDC_PREC_FP32 ? SSDC_OK : SSDC_ERR_UNSUPPORTED;
+    if (d.precision == SSDC_PREC_FP32) return SSDC_OK;
+    if (d.precision == SSDC_PREC_TF32 && ssdc::bwd_tc_supported((int)d.N, (int)d.D, Q)) return SSDC_OK;
+    return SSDC_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -551,7 +556,12 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     const dim3 passes_grid(2 * pass_grid.x, pass_grid.y);  // forward and backward chains side by side
     ssdc::ssdc_bwd_passes<<<passes_grid, ssdc::kPassThreads, 0, stream>>>(g, w, gw);
     record_event(++launches, stream);
-    ssdc::bwd_launch_chunk(g, w, gw, stream);
+    if (dims.precision == SSDC_PREC_TF32) {
+        const int n = ssdc::bwd_tc_launch_chunk(g, w, gw, stream);
+        if (n < 0) return n;
+    } else {
+        ssdc::bwd_launch_chunk(g, w, gw, stream);
+    }
     record_event(++launches, stream);
     const int64_t dt_blocks = ssdc::ceil_div64((int64_t)p.B * p.H * p.nc, ssdc::kBwdDtThreads / 32);
     ssdc::ssdc_bwd_dt<<<(unsigned)dt_blocks, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);

@@ -56,6 +56,10 @@ struct GradWorkspace {
 // The chunk-state/adjoint kernel and the chunk-gradient kernel are templates
 // (compile-time N = D = 64, or sizes from the problem); these enqueue the
 // right instantiation and set their shared-memory limits.
+// The chunk-gradient kernel on the TF32 tensor cores (ssdc_bwd_tc.cu): Q = 16,
+// 32 or 64, N and D multiples of 8 up to 64; returns launches or an error.
+bool bwd_tc_supported(int N, int D, int Q);
+int bwd_tc_launch_chunk(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw, cudaStream_t stream);
 cudaError_t bwd_set_smem_attrs();
 void bwd_launch_chunk_states(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw,
                              cudaStream_t stream);

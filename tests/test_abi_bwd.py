@@ -69,18 +69,26 @@ def test_workspace_bytes(lib):
     nb = ssdc.ssd_complex_bwd_workspace_bytes(d, 64)
     # chunk states, their gradients, decays, the final state and r_t per token
     assert nb >= 2 * chunks * 2 * 64 * 64 * 4 + chunks * 8 + 2 * 16 * 64 * 64 * 8 + 2 * 2048 * 16 * 8
-    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == 0
+    # the TF32 backward (Q <= 64) has the same workspace as the exact one
+    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == nb
+    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 128) == 0
     assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 64) == 0
     assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "fp32"), 48) == 0
     assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(1, 65, 1, 64, 64, "fp32"), 64) > \
         ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(1, 64, 1, 64, 64, "fp32"), 64)
 
 
-def test_precision_other_than_fp32_is_unsupported(lib):
-    for prec in ("tf32", "tf32_staged"):
-        d = ssdc.dims(1, 128, 2, 64, 64, prec)
-        p, end = fake_ptrs(d)
-        assert call(lib, p, d, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
+def test_precisions_the_backward_takes(lib):
+    """exact fp32 at every size; TF32 at Q <= 64 (the tensor-core chunk gradients); never
+    the staged TF32 precision."""
+    d = ssdc.dims(1, 128, 2, 64, 64, "tf32_staged")
+    p, end = fake_ptrs(d)
+    assert call(lib, p, d, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
+    d = ssdc.dims(1, 128, 2, 64, 64, "tf32")
+    p, end = fake_ptrs(d)
+    assert call(lib, p, d, Q=128, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
+    for Q in (16, 32, 64):
+        assert call(lib, p, d, Q=Q, ws=end) in PASSED_HOST_CHECKS
 
 
 def test_rejects_null_required_pointer(lib):
@@ -148,7 +156,9 @@ def test_binding_rejects_unsupported_backward_before_allocating(lib):
     """ssdc.Backward raises (no silent fallback) for a precision or size the backward
     does not take, before any device memory is requested."""
     with pytest.raises(ssdc.SSDCError):
-        ssdc.Backward(1, 128, 2, 64, 64, 64, precision="tf32", device="cpu")
+        ssdc.Backward(1, 128, 2, 64, 64, 64, precision="tf32_staged", device="cpu")
+    with pytest.raises(ssdc.SSDCError):
+        ssdc.Backward(1, 128, 2, 64, 64, 128, precision="tf32", device="cpu")
     with pytest.raises(ssdc.SSDCError):
         ssdc.Backward(1, 128, 2, 64, 64, 48, device="cpu")
     with pytest.raises(ssdc.SSDCError):

@@ -1,0 +1,101 @@
+"""Parity of the TF32 backward pass (ssd_complex_bwd with SSDC_PREC_TF32: the
+per-chunk gradient products on the tensor cores) with the gradient oracle.
+The bar is the TF32 forward's, 2e-3: relative Frobenius error for dx, dB_t,
+dC_t and d_initial_state, and, for ddt and dA, error relative to the size of
+the per-token terms their sums cancel (the scales of the exact backward's
+tests). Cases: the single-layer size, every chunk size the kernel takes, N
+and D below 64, ragged tails, T = 1, an initial state, no final-state
+gradient, a real x with a loss of Re(y) alone."""
+import numpy as np
+import pytest
+
+from state_space_sequence_complex_gb300 import inputs, ssdc
+from tests.gpu_util import RECORDED, rel_fro
+from tests.test_backward_gpu import oracle_grads, run_bwd, state, term_scale
+
+pytestmark = pytest.mark.gpu
+
+TOL_TF32 = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from state_space_sequence_complex_gb300 import build
+    build.build()
+    ssdc.load()
+
+
+def check_tf32(got, ref, inp, what):
+    errs = {}
+    for k, v in got.items():
+        assert np.all(np.isfinite(v)), f"{what}: non-finite {k}"
+        if k not in ("ddt", "dA"):
+            errs[k] = rel_fro(v, ref[k])
+    m = term_scale(inp, ref)
+    dt = inp.dt.astype(np.float64)
+    A = np.abs(inp.complex()["A"])
+    scale = np.linalg.norm((A * m / (1.0 + np.exp(-dt))).ravel())
+    errs["ddt"] = float(np.linalg.norm((got["ddt"] - ref["ddt"]).ravel()) / scale)
+    scale = (np.logaddexp(0.0, dt) * m).sum(axis=(0, 1))
+    errs["dA"] = float(np.max(np.abs(got["dA"] - ref["dA"]) / scale))
+    RECORDED.append((what, "tf32 bwd", ", ".join(f"{k} {e:.1e}" for k, e in sorted(errs.items())),
+                     max(errs.get("dx", 0), errs.get("dB", 0), errs.get("dC", 0)),
+                     max(errs["ddt"], errs["dA"])))
+    bad = {k: e for k, e in errs.items() if e > TOL_TF32}
+    assert not bad, f"{what}: errors {errs}"
+    return errs
+
+
+def run_tf32(inp, og, Q, **kw):
+    b = ssdc.Backward(*inp.dims, Q, precision="tf32")
+    return run_bwd(inp, og, Q, backward=b, **kw)
+
+
+# (B, T, H, D, N, Q)
+CASES = [
+    (2, 2048, 16, 64, 64, 64),
+    (2, 200, 3, 64, 64, 64),
+    (2, 257, 3, 64, 64, 32),
+    (1, 130, 2, 8, 8, 16),
+    (2, 333, 3, 40, 16, 64),
+    (1, 1, 2, 64, 64, 64),
+    (3, 100, 2, 24, 56, 32),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}T{}H{}D{}N{}Q{}".format(*c))
+def test_tf32_backward_matches_gradient_oracle(case):
+    Bn, T, H, D, N, Q = case
+    inp = inputs.custom(Bn, T, H, D, N, seed=8000 + T + Q)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=8100 + T)
+    got = run_tf32(inp, og, Q)
+    check_tf32(got, oracle_grads(inp, og), inp, f"tf32 backward {case}")
+
+
+def test_tf32_backward_initial_state_no_final_gradient():
+    inp = inputs.custom(2, 300, 3, 64, 64, seed=8200)
+    og = inputs.output_grads(2, 300, 3, 64, 64, seed=8201)
+    s0 = state(inp, 8202)
+    got = run_tf32(inp, og, 64, s0=s0, with_dfs=False)
+    check_tf32(got, oracle_grads(inp, og, s0=s0, with_dfs=False), inp, "tf32 backward, initial state")
+
+
+def test_tf32_backward_real_x_and_real_loss():
+    inp = inputs.custom(2, 256, 4, 64, 64, seed=8300)
+    og = inputs.output_grads(2, 256, 4, 64, 64, seed=8301)
+    got = run_tf32(inp, og, 64, real_x=True, dy_imag=False, with_dfs=False)
+    ref = oracle_grads(inp, og, real_x=True, dy_imag=False, with_dfs=False)
+    check_tf32(got, ref, inp, "tf32 backward, real x, Re(y) loss")
+
+
+def test_tf32_backward_agrees_with_exact_backward():
+    # the same call at both precisions: within the TF32 bar of each other, and bit-identical
+    # when repeated
+    inp = inputs.custom(2, 640, 8, 64, 64, seed=8400)
+    og = inputs.output_grads(2, 640, 8, 64, 64, seed=8401)
+    g32 = run_bwd(inp, og, 64)
+    gtf = run_tf32(inp, og, 64)
+    gtf2 = run_tf32(inp, og, 64)
+    for k in ("dx", "dB", "dC"):
+        assert rel_fro(gtf[k], g32[k]) <= TOL_TF32
+        assert np.array_equal(gtf[k], gtf2[k])
