@@ -1,4 +1,4 @@
-// Chunk gradients of the backward pass on the TF32 tensor cores (tcgen05,
+// The backward pass's per-chunk products on the TF32 tensor cores (tcgen05,
 // operands staged by TMA, accumulators in tensor memory), for chunks of Q =
 // 16, 32 or 64 tokens and N, D multiples of 8 up to 64. The same adjoint as
 // the exact kernel of ssdc_bwd.cu (page "Extending -- SSM variants & Triton
@@ -653,6 +653,235 @@ int make_maps(const GradProblem& g, BwdMaps* m) {
     return ok ? SSDC_OK : SSDC_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Per chunk, on the tensor cores: the forward's local state and the adjoint's
+// input of the chunk,
+//   S_loc^T = x^T (dec o B)          -> ws.S slot of the chunk, [plane][d][n]
+//   U^T     = dY^T conj(C')          -> gw.R slot, C' = exp(Acs) o C
+// and a_c = exp(Acs[Q-1]) (the exact kernel's outputs, in the same layouts).
+// A operands are TMEM windows (x^T, dY^T) read from the stacked tiles by
+// column; B operands are the B and C tiles transposed in place (rows n, K =
+// the token), the decay and the conjugation applied as they are written.
+
+struct StatesSmem {
+    float x[64 * 128];  // x, stacked (rows s)
+    float b[64 * 128];  // B, stacked; then (dec o B)^T in place (rows n, K = s)
+    float y[64 * 128];  // dY, stacked (rows l)
+    float c[64 * 128];  // C, stacked; then conj(C')^T in place (rows n, K = l)
+    float2 acs[64], dec[64], eacs[64];
+    uint64_t full, ready, done;
+    uint32_t tmem;
+};
+
+static_assert(sizeof(StatesSmem) <= 232448, "shared-memory plan exceeds the 227 KB a CTA can have");
+
+struct StatesMaps {
+    CUtensorMap x_re, x_im, b_re, b_im, y_re, y_im, c_re, c_im;  // boxes (32, 1, rows, 1)
+    int real_x, real_dy;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_states_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_constant__ StatesMaps sm_maps) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    StatesSmem& sm = *reinterpret_cast<StatesSmem*>(smem_raw);
+    const StatesMaps& mp = sm_maps;
+    const Problem& p = g.f;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H, N = p.N, D = p.D, Q = p.Q;
+    const int64_t nc = p.nc;
+    const int64_t chunk = blockIdx.x;  // (b H + h) nc + c
+    const int c = (int)(chunk % nc);
+    const int64_t bh = chunk / nc;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    const int64_t t0 = (int64_t)c * Q;
+    const int rows = Q < kQ ? Q : kQ;
+    constexpr uint32_t kS = 0, kU = 128, kWx = 256, kWy = 320;
+
+    if (ptx::smem_addr(smem_raw) & 1023u) {
+        if (tid == 0) atomicCAS(ws.status, SSDC_OK, SSDC_ERR_CUDA);
+        return;
+    }
+    if (tid == 0) {
+        ptx::mbar_init(&sm.full, 1);
+        ptx::mbar_init(&sm.ready, kWorkerWarps);
+        ptx::mbar_init(&sm.done, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(&sm.tmem, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (Q < kQ || mp.real_x || mp.real_dy) {
+        float4* z = reinterpret_cast<float4*>(sm.x);
+        constexpr int kVecs = 4 * 64 * 128 / 4;  // the four tiles
+        for (int i = tid; i < kVecs; i += kThreads) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sm.tmem;
+
+    if (warp == kProducer) {
+        const Alog al = load_alog(p, b, h, t0, lane, rows);
+        if (lane == 0) {
+            const uint32_t planes = 8u - (mp.real_x ? 1u : 0u) - (mp.real_dy ? 1u : 0u);
+            ptx::mbar_expect_tx(&sm.full, (uint32_t)rows * 256u * planes);
+        }
+        __syncwarp();
+        if (lane < 16) {  // tensor (x, B, dY, C), 32-column half, plane
+            const int which = lane >> 2, half = (lane >> 1) & 1, pl = lane & 1;
+            const bool skip = pl == 1 && ((which == 0 && mp.real_x) || (which == 2 && mp.real_dy));
+            if (!skip) {
+                float* tiles[4] = {sm.x, sm.b, sm.y, sm.c};
+                const CUtensorMap* maps[4][2] = {{&mp.x_re, &mp.x_im}, {&mp.b_re, &mp.b_im},
+                                                 {&mp.y_re, &mp.y_im}, {&mp.c_re, &mp.c_im}};
+                char* dst = reinterpret_cast<char*>(tiles[which]) + half * kIntHalf + pl * kHalfBytes;
+                ptx::tma_load_4d(dst, maps[which][pl], &sm.full, 32 * half, h, (int)t0, b);
+            }
+        }
+        store_acs(sm.acs, &sm.full, al, lane);
+    } else if (warp == kIssuer) {
+        if (lane == 0) {
+            bool ok = true;
+            if (!ptx::mbar_wait(&sm.ready, 0u, kWaitIters)) {
+                fail(ws.status);
+                ok = false;
+            }
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_ts128(tmem + kS, tmem + kWx, desc128(ptx::smem_addr(sm.b)), false);  // x^T (dec o B)
+                issue_ts128(tmem + kU, tmem + kWy, desc128(ptx::smem_addr(sm.c)), false);  // dY^T conj(C')
+            }
+            ptx::mma_commit(&sm.done);
+        }
+        __syncwarp();
+    } else {
+        const int qd = warp & 3, blk = (warp >> 2) & 1, kh = warp >> 3;
+        const int i4 = lane >> 2, lq = lane & 3;
+        const int rr = 16 * qd + 8 * blk + i4;
+        const uint32_t tl = lane_base(tmem, warp) + ((uint32_t)(16 * blk) << 16);
+        const int wr = 16 * qd + 8 * (lane >> 4) + (lane & 7), wp = (lane >> 3) & 1, wc = warp >> 2;
+        const uint32_t wl = lane_base(tmem, warp);
+        char* xb = reinterpret_cast<char*>(sm.x);
+        char* bb = reinterpret_cast<char*>(sm.b);
+        char* yb = reinterpret_cast<char*>(sm.y);
+        char* cb = reinterpret_cast<char*>(sm.c);
+        bool ok = true;
+        if (!ptx::mbar_wait(&sm.full, 0u, kWaitIters)) {
+            fail(ws.status);
+            ok = false;
+        }
+        if (tid < 2 * kQ) {
+            const int t = tid % kQ;
+            if (tid < kQ) sm.dec[t] = t < Q ? cexp_fast(cdiff(sm.acs[Q - 1], sm.acs[t])) : make_float2(0.0f, 0.0f);
+            else sm.eacs[t] = cexp_fast(sm.acs[t]);
+        }
+        // windows x^T and dY^T: row wr (d), column k (token) = plane wp of T[k][wr] from a stacked
+        // tile; plane-1 lanes read row k ^ 4 (the planes' rows share banks)
+        auto window = [&](const char* src, uint32_t col0) {
+            float r[16], v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = ld(src, stk(wp, 16 * wc + (k ^ (4 * wp)), wr));
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = ptx::to_tf32(wp ? r[k ^ 4] : r[k]);
+            ptx::tmem_st16(wl + col0 + 16 * wc, v);
+        };
+        window(xb, kWx);
+        window(yb, kWy);
+        // B and C blocks: rows s = 4 bsb + i, columns n = 4 bnb + 2 bjh + {0, 1}, both planes
+        const int L0 = lane & 1, L1 = (lane >> 1) & 1, L2 = (lane >> 2) & 1, L3 = (lane >> 3) & 1, L4 = lane >> 4;
+        const int bjh = L1, bsb = L2 + 2 * (warp >> 1), bnb = L0 + 2 * L3 + 4 * L4 + 8 * (warp & 1);
+        float2 bv[2][4], cv[2][4];
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int sr = 4 * bsb + i, n = 4 * bnb + 2 * bjh;
+                bv[pp][i] = make_float2(ld(bb, stk(pp, sr, n)), ld(bb, stk(pp, sr, n + 1)));
+                cv[pp][i] = make_float2(ld(cb, stk(pp, sr, n)), ld(cb, stk(pp, sr, n + 1)));
+            }
+        ptx::named_sync(kWorkerBar, kWorkers);  // every B and C read is done; the tables are written
+#pragma unroll
+        for (int jn = 0; jn < 2; ++jn) {  // column n -> row n of the transposed tiles
+            const int nr = 4 * bnb + 2 * bjh + jn;
+            float br[4], bi[4], cr[4], ci[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int sr = 4 * bsb + i;
+                const float2 bvv = jn ? make_float2(bv[0][i].y, bv[1][i].y) : make_float2(bv[0][i].x, bv[1][i].x);
+                const float2 cvv = jn ? make_float2(cv[0][i].y, cv[1][i].y) : make_float2(cv[0][i].x, cv[1][i].x);
+                const float2 db = cmul(sm.dec[sr], bvv);   // dec o B
+                const float2 ce = cmul(sm.eacs[sr], cvv);  // C' = exp(Acs) o C, conjugated below
+                br[i] = ptx::to_tf32(db.x);
+                bi[i] = ptx::to_tf32(db.y);
+                cr[i] = ptx::to_tf32(ce.x);
+                ci[i] = ptx::to_tf32(-ce.y);
+            }
+            *reinterpret_cast<float4*>(bb + stk(0, nr, 4 * bsb)) = make_float4(br[0], br[1], br[2], br[3]);
+            *reinterpret_cast<float4*>(bb + stk(1, nr, 4 * bsb)) = make_float4(bi[0], bi[1], bi[2], bi[3]);
+            *reinterpret_cast<float4*>(cb + stk(0, nr, 4 * bsb)) = make_float4(cr[0], cr[1], cr[2], cr[3]);
+            *reinterpret_cast<float4*>(cb + stk(1, nr, 4 * bsb)) = make_float4(ci[0], ci[1], ci[2], ci[3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.ready);
+        if (ok && !ptx::mbar_wait(&sm.done, 0u, kWaitIters)) fail(ws.status);
+        ptx::tc_fence_after();
+        // S_loc^T and U^T rows d = rr: Re = A0 B0 - A1 B1, Im = A0 B1 + A1 B0
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            float ga[16], gb[16];
+            ptx::tmem_ld_16x256b_x4(tl + (which ? kU : kS) + 32 * kh, ga);
+            ptx::tmem_ld_16x256b_x4(tl + (which ? kU : kS) + 64 + 32 * kh, gb);
+            ptx::tmem_wait_ld();
+            float* out = (which ? gw.R : ws.S) + chunk * 2 * (int64_t)D * N;
+            if (rr < D) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int n = 32 * kh + 8 * j + 2 * lq;
+                    if (n < N) {  // N is a multiple of 8: n + 1 < N too
+                        *reinterpret_cast<float2*>(out + rr * N + n) =
+                            make_float2(ga[4 * j] - gb[4 * j + 2], ga[4 * j + 1] - gb[4 * j + 3]);
+                        *reinterpret_cast<float2*>(out + (int64_t)D * N + rr * N + n) =
+                            make_float2(gb[4 * j] + ga[4 * j + 2], gb[4 * j + 1] + ga[4 * j + 3]);
+                    }
+                }
+            }
+        }
+        if (tid == 0) {
+            const float2 a = sm.eacs[Q - 1];
+            ws.a[2 * chunk] = a.x;
+            ws.a[2 * chunk + 1] = a.y;
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+constexpr size_t kStatesSmemBytes = sizeof(StatesSmem);
+bool g_states_attr_set[64] = {};
+
+int make_states_maps(const GradProblem& g, StatesMaps* m) {
+    const Problem& p = g.f;
+    memset(m, 0, sizeof(*m));
+    m->real_x = p.x_im == nullptr;
+    m->real_dy = g.dy_im == nullptr;
+    const int rows = p.Q < kQ ? p.Q : kQ;
+    bool ok = encode_feature_map(&m->x_re, p.x_re, p.D, p.H, p.T, p.B, rows) &&
+              (m->real_x || encode_feature_map(&m->x_im, p.x_im, p.D, p.H, p.T, p.B, rows)) &&
+              encode_feature_map(&m->b_re, p.B_re, p.N, p.H, p.T, p.B, rows) &&
+              encode_feature_map(&m->b_im, p.B_im, p.N, p.H, p.T, p.B, rows) &&
+              encode_feature_map(&m->y_re, g.dy_re, p.D, p.H, p.T, p.B, rows) &&
+              (m->real_dy || encode_feature_map(&m->y_im, g.dy_im, p.D, p.H, p.T, p.B, rows)) &&
+              encode_feature_map(&m->c_re, p.C_re, p.N, p.H, p.T, p.B, rows) &&
+              encode_feature_map(&m->c_im, p.C_im, p.N, p.H, p.T, p.B, rows);
+    return ok ? SSDC_OK : SSDC_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace bwdtc
 
@@ -675,6 +904,25 @@ int bwd_tc_launch_chunk(const GradProblem& g, const Workspace& ws, const GradWor
     const Problem& p = g.f;
     const int64_t chunks = (int64_t)p.B * p.H * p.nc;
     bwdtc::bwd_chunk_tc<<<(unsigned)chunks, bwdtc::kThreads, bwdtc::kSmemBytes, stream>>>(g, ws, gw, m);
+    return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
+}
+
+int bwd_tc_launch_chunk_states(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw,
+                               cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSDC_ERR_CUDA;
+    if (!bwdtc::g_states_attr_set[dev]) {
+        if (cudaFuncSetAttribute(bwdtc::bwd_states_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bwdtc::kStatesSmemBytes) != cudaSuccess)
+            return SSDC_ERR_CUDA;
+        bwdtc::g_states_attr_set[dev] = true;
+    }
+    bwdtc::StatesMaps m;
+    const int rc = bwdtc::make_states_maps(g, &m);
+    if (rc != SSDC_OK) return rc;
+    const Problem& p = g.f;
+    const int64_t chunks = (int64_t)p.B * p.H * p.nc;
+    bwdtc::bwd_states_tc<<<(unsigned)chunks, bwdtc::kThreads, bwdtc::kStatesSmemBytes, stream>>>(g, ws, gw, m);
     return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
 }
 

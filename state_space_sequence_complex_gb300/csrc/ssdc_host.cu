@@ -551,7 +551,12 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     if (cudaMemsetAsync(w.status, 0, sizeof(int), stream) != cudaSuccess) return SSDC_ERR_CUDA;
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
-    ssdc::bwd_launch_chunk_states(g, w, gw, stream);
+    if (dims.precision == SSDC_PREC_TF32) {
+        const int n = ssdc::bwd_tc_launch_chunk_states(g, w, gw, stream);
+        if (n < 0) return n;
+    } else {
+        ssdc::bwd_launch_chunk_states(g, w, gw, stream);
+    }
     record_event(++launches, stream);
     const dim3 passes_grid(2 * pass_grid.x, pass_grid.y);  // forward and backward chains side by side
     ssdc::ssdc_bwd_passes<<<passes_grid, ssdc::kPassThreads, 0, stream>>>(g, w, gw);

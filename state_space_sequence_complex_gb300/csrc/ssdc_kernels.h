@@ -60,6 +60,9 @@ struct GradWorkspace {
 // 32 or 64, N and D multiples of 8 up to 64; returns launches or an error.
 bool bwd_tc_supported(int N, int D, int Q);
 int bwd_tc_launch_chunk(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw, cudaStream_t stream);
+// Its chunk-state kernel (S_loc, U_c and a_c per chunk, the outputs of the exact one).
+int bwd_tc_launch_chunk_states(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw,
+                               cudaStream_t stream);
 cudaError_t bwd_set_smem_attrs();
 void bwd_launch_chunk_states(const GradProblem& g, const Workspace& ws, const GradWorkspace& gw,
                              cudaStream_t stream);

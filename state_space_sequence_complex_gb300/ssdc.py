@@ -362,14 +362,15 @@ def _scan_function():
         passes None), returning a gradient for every tensor input."""
 
         @staticmethod
-        def forward(ctx, chunk_size, precision, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt,
-                    s0_re, s0_im):
+        def forward(ctx, chunk_size, precision, bwd_precision, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im,
+                    dt, s0_re, s0_im):
             Bn, T, H, D = x_re.shape
             N = B_re.shape[-1]
             f = Forward(Bn, T, H, N, D, chunk_size, precision, device=x_re.device)
             y_re, y_im, fs_re, fs_im = f(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt,
                                          s0_re=s0_re, s0_im=s0_im)
             ctx.chunk_size = chunk_size
+            ctx.bwd_precision = bwd_precision
             ctx.real_x = x_im is None
             ctx.with_s0 = s0_re is not None
             ctx.save_for_backward(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, s0_re, s0_im)
@@ -388,10 +389,10 @@ def _scan_function():
             else:
                 gfs = (z((Bn, H, N, D)) if gfs_re is None else gfs_re.contiguous(),
                        z((Bn, H, N, D)) if gfs_im is None else gfs_im.contiguous())
-            b = Backward(Bn, T, H, N, D, ctx.chunk_size, "fp32", device=x_re.device)
+            b = Backward(Bn, T, H, N, D, ctx.chunk_size, ctx.bwd_precision, device=x_re.device)
             g = b(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, gy_re, gy_im, *gfs,
                   s0_re=s0_re if ctx.with_s0 else None, s0_im=s0_im if ctx.with_s0 else None)
-            return (None, None, g["dx_re"], None if ctx.real_x else g["dx_im"], g["dA_re"],
+            return (None, None, None, g["dx_re"], None if ctx.real_x else g["dx_im"], g["dA_re"],
                     g["dA_im"], g["dB_re"], g["dB_im"], g["dC_re"], g["dC_im"], g["ddt"],
                     g["ds0_re"] if ctx.with_s0 else None, g["ds0_im"] if ctx.with_s0 else None)
 
@@ -402,17 +403,18 @@ _SCAN_FN = None
 
 
 def ssd_complex_scan(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
-                     s0_re=None, s0_im=None, precision="tf32"):
+                     s0_re=None, s0_im=None, precision="tf32", bwd_precision="fp32"):
     """Differentiable complex SSD scan on planar float32 CUDA tensors: returns
     ``(y_re, y_im, final_state_re, final_state_im)``; ``y_re`` is Re(y). The
-    forward runs at ``precision``; the backward is the library's exact-fp32
-    backward pass. ``x_im`` may be None (a real x); the initial state
-    ``(s0_re, s0_im)`` is optional."""
+    forward runs at ``precision``; the backward is the library's backward pass
+    at ``bwd_precision`` ("fp32": exact; "tf32": the chunk gradients on the
+    tensor cores, chunk sizes up to 64). ``x_im`` may be None (a real x); the
+    initial state ``(s0_re, s0_im)`` is optional."""
     global _SCAN_FN
     if _SCAN_FN is None:
         _SCAN_FN = _scan_function()
-    return _SCAN_FN.apply(int(chunk_size), precision, x_re, x_im, A_re, A_im, B_re, B_im, C_re,
-                          C_im, dt, s0_re, s0_im)
+    return _SCAN_FN.apply(int(chunk_size), precision, bwd_precision, x_re, x_im, A_re, A_im, B_re, B_im,
+                          C_re, C_im, dt, s0_re, s0_im)
 
 
 def ssd_complex_status(workspace, stream=None) -> int:

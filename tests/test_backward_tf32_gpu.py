@@ -99,3 +99,26 @@ def test_tf32_backward_agrees_with_exact_backward():
     for k in ("dx", "dB", "dC"):
         assert rel_fro(gtf[k], g32[k]) <= TOL_TF32
         assert np.array_equal(gtf[k], gtf2[k])
+
+
+def test_scan_autograd_with_tf32_backward():
+    """ssd_complex_scan with the TF32 forward and the TF32 backward under autograd: a
+    loss with random output gradients and an initial state; every input gets its
+    gradient, within the TF32 bar of the gradient oracle."""
+    from tests.test_backward_gpu import ORDER, cuda
+    Bn, T, H, D, N, Q = 2, 170, 2, 16, 32, 32
+    inp = inputs.custom(Bn, T, H, D, N, seed=8500)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=8501)
+    s0 = state(inp, 8502)
+    leaves = {k: cuda(v).requires_grad_(True) for k, v in inp.arrays().items()}
+    s0_re, s0_im = cuda(s0.real).requires_grad_(True), cuda(s0.imag).requires_grad_(True)
+    y_re, y_im, fs_re, fs_im = ssdc.ssd_complex_scan(*[leaves[k] for k in ORDER], Q, s0_re=s0_re, s0_im=s0_im,
+                                                     precision="tf32", bwd_precision="tf32")
+    loss = ((y_re * cuda(og.dy_re)).sum() + (y_im * cuda(og.dy_im)).sum()
+            + (fs_re * cuda(og.dfs_re)).sum() + (fs_im * cuda(og.dfs_im)).sum())
+    loss.backward()
+    n = lambda t: t.grad.double().cpu().numpy()
+    got = {"dx": n(leaves["x_re"]) + 1j * n(leaves["x_im"]), "dA": n(leaves["A_re"]) + 1j * n(leaves["A_im"]),
+           "dB": n(leaves["B_re"]) + 1j * n(leaves["B_im"]), "dC": n(leaves["C_re"]) + 1j * n(leaves["C_im"]),
+           "ddt": n(leaves["dt"]), "ds0": n(s0_re) + 1j * n(s0_im)}
+    check_tf32(got, oracle_grads(inp, og, s0=s0), inp, "tf32 backward through autograd")
