@@ -407,33 +407,31 @@ bwd_chunk_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_constan
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int l = 4 * bsb + i, n = 4 * bnb + 2 * bjh;
-                    bv[pp][i] = make_float2(ld(bb, stk(pp, l, n)), ld(bb, stk(pp, l, n + 1)));
-                }
+                for (int i = 0; i < 4; ++i)
+                    bv[pp][i] = *reinterpret_cast<const float2*>(bb + stk(pp, 4 * bsb + i, 4 * bnb + 2 * bjh));
+            using ptx::to_tf32;
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn) {
+            for (int jn = 0; jn < 2; ++jn) {  // 16-byte rows of BT: row n, columns l = 4 bsb .. + 3
                 const int n = 4 * bnb + 2 * bjh + jn;
+                float r4[4], i4v[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int l = 4 * bsb + i;
-                    const float br = jn ? bv[0][i].y : bv[0][i].x, bi = jn ? bv[1][i].y : bv[1][i].x;
-                    st(btb, stk(0, n, l), ptx::to_tf32(br));
-                    st(btb, stk(1, n, l), ptx::to_tf32(-bi));
+                    r4[i] = to_tf32(jn ? bv[0][i].y : bv[0][i].x);
+                    i4v[i] = to_tf32(-(jn ? bv[1][i].y : bv[1][i].x));
                 }
+                *reinterpret_cast<float4*>(btb + stk(0, n, 4 * bsb)) = make_float4(r4[0], r4[1], r4[2], r4[3]);
+                *reinterpret_cast<float4*>(btb + stk(1, n, 4 * bsb)) = make_float4(i4v[0], i4v[1], i4v[2], i4v[3]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int l = 4 * bsb + i, n = 4 * bnb + 2 * bjh;
                 const float2 dv = sm.dec[l];
                 // conj(dec B): Re = dr br - di bi, Im = -(dr bi + di br)
-                const float2 w0 = make_float2(dv.x * bv[0][i].x - dv.y * bv[1][i].x, dv.x * bv[0][i].y - dv.y * bv[1][i].y);
-                const float2 w1 = make_float2(-(dv.x * bv[1][i].x + dv.y * bv[0][i].x),
-                                              -(dv.x * bv[1][i].y + dv.y * bv[0][i].y));
-                st(bb, stk(0, l, n), ptx::to_tf32(w0.x));
-                st(bb, stk(0, l, n + 1), ptx::to_tf32(w0.y));
-                st(bb, stk(1, l, n), ptx::to_tf32(w1.x));
-                st(bb, stk(1, l, n + 1), ptx::to_tf32(w1.y));
+                *reinterpret_cast<float2*>(bb + stk(0, l, n)) =
+                    make_float2(to_tf32(dv.x * bv[0][i].x - dv.y * bv[1][i].x), to_tf32(dv.x * bv[0][i].y - dv.y * bv[1][i].y));
+                *reinterpret_cast<float2*>(bb + stk(1, l, n)) =
+                    make_float2(to_tf32(-(dv.x * bv[1][i].x + dv.y * bv[0][i].x)),
+                                to_tf32(-(dv.x * bv[1][i].y + dv.y * bv[0][i].y)));
             }
         }
         {
@@ -487,12 +485,12 @@ bwd_chunk_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_constan
             for (int i = 0; i < 4; ++i) {
                 const int l = 4 * bsb + i, d = 4 * bnb + 2 * bjh;
                 const float2 dv = sm.dec[l];
-                const float2 xr = make_float2(ld(xb, stk(0, l, d)), ld(xb, stk(0, l, d + 1)));
-                const float2 xi = make_float2(ld(xb, stk(1, l, d)), ld(xb, stk(1, l, d + 1)));
-                st(xb, stk(0, l, d), ptx::to_tf32(dv.x * xr.x - dv.y * xi.x));
-                st(xb, stk(0, l, d + 1), ptx::to_tf32(dv.x * xr.y - dv.y * xi.y));
-                st(xb, stk(1, l, d), ptx::to_tf32(-(dv.x * xi.x + dv.y * xr.x)));
-                st(xb, stk(1, l, d + 1), ptx::to_tf32(-(dv.x * xi.y + dv.y * xr.y)));
+                float2* p0 = reinterpret_cast<float2*>(xb + stk(0, l, d));
+                float2* p1 = reinterpret_cast<float2*>(xb + stk(1, l, d));
+                const float2 xr = *p0, xi = *p1;
+                using ptx::to_tf32;
+                *p0 = make_float2(to_tf32(dv.x * xr.x - dv.y * xi.x), to_tf32(dv.x * xr.y - dv.y * xi.y));
+                *p1 = make_float2(to_tf32(-(dv.x * xi.x + dv.y * xr.x)), to_tf32(-(dv.x * xi.y + dv.y * xr.y)));
             }
         }
         {
@@ -568,7 +566,7 @@ bwd_chunk_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_constan
             float sr = 0.0f, si = 0.0f;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int n = 8 * s8 + k;
+                const int n = 8 * s8 + ((k + s8) & 7);  // rotated: the eight lanes of a row read BT rows of distinct swizzles
                 const float dr = ld(xb, stk(0, l, n)), di = ld(xb, stk(1, l, n));
                 const float br = ld(btb, stk(0, n, l)), bi = ld(btb, stk(1, n, l));
                 sr += dr * br - di * bi;
