@@ -569,8 +569,9 @@ def other_workload(args, w):
     peak, peak_kind = peaks()
     wq = w.with_(Q=Q, T=Ts)
     # per launch; a segment after the first also reads its initial state (8 N D bytes per sequence)
-    # (bfloat16 x, B_t, C_t: 2 bytes a plane element instead of 4; a real x: one plane)
-    in_bytes = (8.0 * w.D + 8.0 * w.N) if args.bf16 else 0.0
+    # (bfloat16 x, B_t, C_t: 2 bytes a plane element instead of 4, so 4 D + 8 N fewer; a real
+    # x: one plane)
+    in_bytes = (4.0 * w.D + 8.0 * w.N) if args.bf16 else 0.0
     x_im_bytes = (2.0 if args.bf16 else 4.0) * w.D if args.real_x else 0.0
     bytes_per_launch = ((algorithmic_bytes_per_unit(wq) - in_bytes - x_im_bytes) * wq.token_heads
                         + 8.0 * w.N * w.D * w.B * w.H * (K - 1) / K)

@@ -153,8 +153,9 @@ int ssd_complex_fwd_init(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
  * Forward pass with bfloat16 activations: x, B_t and C_t are planar bfloat16
  * arrays (the layouts of ssd_complex_fwd_ws, 2 bytes an element); A, dt, the
  * initial and final states and y stay fp32, and so does every sum and the state
- * (the pages train with BF16 activations around a complex64 state). 1282 bytes
- * per token-head instead of 2068. The scan is the same operation on the inputs'
+ * (the pages train with BF16 activations around a complex64 state): x, B_t
+ * and C_t take 768 bytes per token-head instead of 1536 (1300 in all, instead
+ * of 2068, at N = D = 64 and T = 2048). The scan is the same operation on the inputs'
  * values: C B^T multiplies the bfloat16 values as they are (tensor-core BF16
  * products, exact, fp32 sums); every other product takes them as exact fp32
  * (TF32) values, as the TF32 path does its fp32 inputs.
