@@ -192,6 +192,17 @@ def algorithmic_bytes_per_unit(w) -> float:
     return 16 * w.D + 16 * w.N + 4 + 8 * w.N * w.D / w.T
 
 
+def input_bytes_per_unit(w, bf16=False, real_x=False) -> float:
+    """algorithmic_bytes_per_unit with x, B_t, C_t in bfloat16 (2 bytes a plane element
+    instead of 4: 4 D + 8 N fewer) and / or a real x (no imaginary plane)."""
+    b = algorithmic_bytes_per_unit(w)
+    if bf16:
+        b -= 4.0 * w.D + 8.0 * w.N
+    if real_x:
+        b -= (2.0 if bf16 else 4.0) * w.D
+    return b
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
 
@@ -569,11 +580,7 @@ def other_workload(args, w):
     peak, peak_kind = peaks()
     wq = w.with_(Q=Q, T=Ts)
     # per launch; a segment after the first also reads its initial state (8 N D bytes per sequence)
-    # (bfloat16 x, B_t, C_t: 2 bytes a plane element instead of 4, so 4 D + 8 N fewer; a real
-    # x: one plane)
-    in_bytes = (4.0 * w.D + 8.0 * w.N) if args.bf16 else 0.0
-    x_im_bytes = (2.0 if args.bf16 else 4.0) * w.D if args.real_x else 0.0
-    bytes_per_launch = ((algorithmic_bytes_per_unit(wq) - in_bytes - x_im_bytes) * wq.token_heads
+    bytes_per_launch = (input_bytes_per_unit(wq, bf16=args.bf16, real_x=args.real_x) * wq.token_heads
                         + 8.0 * w.N * w.D * w.B * w.H * (K - 1) / K)
     launch_ms = sum(kmeans)
     units = w.token_heads * w.layers

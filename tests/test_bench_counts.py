@@ -12,6 +12,15 @@ def test_forward_bytes_per_token_head():
     assert bench.algorithmic_bytes_per_unit(w) == 16 * 64 + 16 * 64 + 4 + 8 * 64 * 64 / 2048 == 2068
 
 
+def test_forward_bytes_bf16_and_real_x():
+    w = inputs.LAYER
+    # bfloat16 x, B_t, C_t: 768 bytes instead of 1536; a real x drops its imaginary plane
+    assert bench.input_bytes_per_unit(w, bf16=True) == 2068 - 768 == 1300
+    assert bench.input_bytes_per_unit(w, real_x=True) == 2068 - 256
+    assert bench.input_bytes_per_unit(w, bf16=True, real_x=True) == 1300 - 128
+    assert bench.input_bytes_per_unit(w) == 2068
+
+
 def test_forward_flops_per_token_head():
     f = bench.fp32_flops_per_unit(inputs.LAYER)
     # chunk state 8ND, state pass 8ND/Q, chunk scan over the causal triangle 4(Q+1)(N+D) + 8ND
