@@ -173,3 +173,16 @@ def naive_scan_inputs(inp, **kw):
     """``naive_scan`` on an ``inputs.Inputs`` bundle."""
     return naive_scan(inp.x_re, inp.x_im, inp.A_re, inp.A_im, inp.B_re, inp.B_im,
                       inp.C_re, inp.C_im, inp.dt, **kw)
+
+
+def head_mix(y, W):
+    """The MIMO head mixer on Re(y) (landing page, "02 MIMO Mixer": a fully
+    connected 16 x 16 mixer across the SSM heads, 1024 -> 1024 features = 16
+    heads x 64, identity-initialised). Output head g of token t is
+        out[b, t, g, d] = sum_h W[g, h] Re(y)[b, t, h, d],
+    the same H x H matrix for every feature d. y (B,T,H,D) complex or real,
+    W (H,H); returns float64 (B,T,H,D)."""
+    y = np.asarray(y)
+    W = np.asarray(W, dtype=np.float64)
+    return np.einsum("gh,bthd->btgd", W, np.real(y).astype(np.float64))
+
