@@ -177,6 +177,34 @@ int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_ci
                          void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Forward pass with the MIMO head mixer fused into its epilogue (landing page,
+ * "02 MIMO Mixer": a fully connected mixer across the H SSM heads, H x H,
+ * identity-initialised, applied to the Re(y) the block consumes):
+ *   out[b, t, g, d] = sum_h mix[g * H + h] Re(y)[b, t, h, d],
+ * the same matrix for every feature d. Only the mixed Re(y) is written (no
+ * y.im, no separate Re(y)), so y does not make a round trip through memory
+ * before the mixer. The tiles of Re(y) of one batch row and 64-token tile from
+ * all H heads meet in `out`; the CTA that stores the last of them mixes them
+ * in place (no CTA waits for another).
+ *
+ *   mix             (H, H) fp32 device array, row g = output head g; required
+ *   out             (B, T, H, D) fp32 device array, 16-byte aligned
+ *   initial_state   as for ssd_complex_fwd_init (both planes null: zero)
+ *   dims.precision  SSDC_PREC_TF32; H <= 16; N, D multiples of 8 in [8, 64];
+ *                   chunk_size 16, 32 or 64 (else SSDC_ERR_UNSUPPORTED)
+ *   workspace       ssd_complex_fwd_mimo_workspace_bytes() bytes (a status word
+ *                   and one counter per batch row and 64-token tile)
+ * The other arguments, the overlap rules and the errors are those of
+ * ssd_complex_fwd_ws. One launch, the fused kernel with the state in tensor
+ * memory.
+ */
+size_t ssd_complex_fwd_mimo_workspace_bytes(ssdc_dims dims, int chunk_size);
+int ssd_complex_fwd_mimo(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float *dt,
+                         const float *mix, ssdc_cin initial_state, ssdc_dims dims, int chunk_size,
+                         float *out, ssdc_cout final_state, void *workspace, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/*
  * Joining segments of a sequence split in time (across ranks or calls). The
  * state pass between chunks (landing page "03 Chunkwise SSD", the STATE line:
  * a state carried forward is multiplied by the exponential of the accumulated

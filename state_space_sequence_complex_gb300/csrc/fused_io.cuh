@@ -76,6 +76,7 @@ struct FusedMaps {
     int fast;                            // bit 0: x2, bit 1: B2, bit 2: C2 in use
     int swap;                            // bit k: the fast map's plane 0 is the imaginary plane (0 x, 1 B, 2 C)
     int real_x;                          // x has no imaginary plane (x_re only)
+    int y_im_out;                        // y_im is written (not with the fused head mixer)
 };
 
 // Loader warp: dt of one chunk's tokens (two per lane over a 64-row tile; rows
@@ -175,7 +176,8 @@ int make_fused_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
                   tc::encode_feature_map_bf16(&fm->c8_re, p.C_re, p.N, p.H, p.T, p.B, 8) &&
                   tc::encode_feature_map_bf16(&fm->c8_im, p.C_im, p.N, p.H, p.T, p.B, 8) &&
                   tc::encode_feature_map(&fm->y_re, p.y_re, p.D, p.H, p.T, p.B, rows16) &&
-                  tc::encode_feature_map(&fm->y_im, p.y_im, p.D, p.H, p.T, p.B, rows16);
+                  (p.y_im == nullptr || tc::encode_feature_map(&fm->y_im, p.y_im, p.D, p.H, p.T, p.B, rows16));
+        fm->y_im_out = p.y_im != nullptr;
         return ok ? SSDC_OK : SSDC_ERR_CUDA;
     }
     bool sw = false;
@@ -200,7 +202,8 @@ int make_fused_maps(const Problem& p, bool allow_fast, FusedMaps* fm) {
         ok = ok && tc::encode_feature_map(&fm->c8_re, p.C_re, p.N, p.H, p.T, p.B, 8) &&
              tc::encode_feature_map(&fm->c8_im, p.C_im, p.N, p.H, p.T, p.B, 8);
     ok = ok && tc::encode_feature_map(&fm->y_re, p.y_re, p.D, p.H, p.T, p.B, rows) &&
-         tc::encode_feature_map(&fm->y_im, p.y_im, p.D, p.H, p.T, p.B, rows);
+         (p.y_im == nullptr || tc::encode_feature_map(&fm->y_im, p.y_im, p.D, p.H, p.T, p.B, rows));
+    fm->y_im_out = p.y_im != nullptr;
     return ok ? SSDC_OK : SSDC_ERR_CUDA;
 }
 

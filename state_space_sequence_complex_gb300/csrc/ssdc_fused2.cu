@@ -98,6 +98,8 @@ struct Tail {
     uint64_t xt_ready, bt_ready, c_ready, p_ready, sin_ready;  // worker hand-offs (one arrival per warp)
     uint64_t mma_g, mma_s, mma_yo, mma_y;      // MMA completions
     uint32_t tmem;
+    int mix_task;            // fused head mixer: the tile this CTA mixes now, or -1
+    float wmix[16 * 16];     // fused head mixer: W, zero past H
 };
 
 template <bool kBf16>
@@ -281,7 +283,8 @@ __device__ __forceinline__ void chunk_acs(const Problem& p, int b, int h, int64_
 // kBf16: x, B_t and C_t in bfloat16. C B^T then multiplies them as they are
 // (kind::f16, exact products); x enters the X^T window and B and C the
 // threads' products as exact fp32 values, the rest is as for fp32 inputs.
-template <bool kSwapC, bool kBlocks, bool kBf16>
+// kMix: the head mixer fused into the epilogue (single-block chunks only).
+template <bool kSwapC, bool kBlocks, bool kBf16, bool kMix = false>
 __global__ void __launch_bounds__(kThreads, 1)
 fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -321,6 +324,9 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         ptx::tmem_alloc(&sm.tmem, kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (kMix)
+        for (int i = tid; i < 16 * 16; i += kThreads)
+            sm.wmix[i] = ((i >> 4) < H && (i & 15) < H) ? p.mix_w[(i >> 4) * H + (i & 15)] : 0.0f;
     if (Q < kQ) {
         // rows past Q are never loaded: give them finite contents
         float4* z = reinterpret_cast<float4*>(sm.c);
@@ -509,9 +515,51 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, yh, t0, yb);
-                    ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
+                    if (fm.y_im_out) ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
                 }
                 ptx::bulk_commit();
+            }
+        };
+
+        // Fused head mixer (p.mix_w): a row tile's Re(y) of every head of batch row b goes to
+        // y_re by the staged stores; the CTA whose store completes the count of its (b, tile)
+        // (one per head) then mixes the tile in place, out[t, g, :] = sum_h W[g, h] Re(y)[t, h, :].
+        // Nothing waits for another CTA: the last to arrive does the work.
+        const int ntiles = (int)((p.T + rows - 1) / rows);
+        auto tile_slot = [&](const Item& row) {
+            const int yb = row.q / H;
+            return yb * ntiles + (row.c * Q + kQ * row.r) / rows;
+        };
+        auto mix_after_store = [&](int slot) {
+            if (tid == 0) {
+                ptx::bulk_wait_all();  // the tile's Re(y) is in global memory
+                ptx::fence_proxy_async_global();
+                __threadfence();
+                const int old = atomicAdd(p.mix_count + slot, 1);
+                __threadfence();
+                sm.mix_task = old == H - 1 ? slot : -1;
+            }
+            ptx::named_sync(kWorkerBar, kWorkers);
+            const int task = sm.mix_task;
+            if (task < 0) return;
+            const int mb = task / ntiles;
+            const int64_t mt0 = (int64_t)(task - mb * ntiles) * rows;
+            const int nt = (int)(p.T - mt0 < (int64_t)rows ? p.T - mt0 : (int64_t)rows);
+            for (int e = tid; e < nt * D; e += kWorkers) {
+                const int tt = e / D, d = e - tt * D;
+                float* col = p.y_re + (((int64_t)mb * p.T + mt0 + tt) * H) * D + d;
+                float v[16];
+#pragma unroll
+                for (int hh = 0; hh < 16; ++hh) v[hh] = hh < H ? __ldcg(col + (int64_t)hh * D) : 0.0f;
+#pragma unroll
+                for (int g = 0; g < 16; ++g) {
+                    if (g < H) {
+                        float o = 0.0f;
+#pragma unroll
+                        for (int hh = 0; hh < 16; ++hh) o = fmaf(sm.wmix[g * 16 + hh], v[hh], o);
+                        col[(int64_t)g * D] = o;
+                    }
+                }
             }
         };
 
@@ -527,6 +575,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 
         int ndiag = 0, nchunk = 0;  // diagonal blocks and chunks begun
         for (int it = 0; it < nitems; ++it) {
+            int mix_slot = -1;  // the row tile staged in this item (fused head mixer)
             const int s = it & 1;
             const uint32_t ph = (uint32_t)it & 1u, pd = (uint32_t)ndiag & 1u;
             const bool diag = cur.j == cur.r;
@@ -669,6 +718,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     if (cur.c == 0) row.q = cur.q - (int)gridDim.x;
                 }
                 stage_y(ystage, row);
+                mix_slot = tile_slot(row);
             }
 
             // ---- C: C'_r = C_r o exp(Acs[l]) in place, plane 0 real. Unit: physical 16-byte chunk
@@ -808,7 +858,14 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&sm.sin_ready);
             }
-            if (tid == 0 && staged) {  // the y stores have read the staging tile
+            if (kMix && staged) {
+                // the stores have completed (and read the staging tile): release x, count, mix
+                if (tid == 0) {
+                    ptx::bulk_wait_all();
+                    if (!kBf16) ptx::mbar_arrive(&sm.free_x[s]);
+                }
+                mix_after_store(mix_slot);
+            } else if (tid == 0 && staged) {  // the y stores have read the staging tile
                 ptx::bulk_wait_read_all();
                 if (!kBf16) ptx::mbar_arrive(&sm.free_x[s]);
             }
@@ -825,7 +882,8 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             char* buf = reinterpret_cast<char*>(sm.x[(nitems - 1) & 1]);
             if constexpr (kBf16) buf = reinterpret_cast<char*>(sm.yw);
             stage_y(buf, item_at(qlast, nc - 1, R - 1, R - 1));
-            if (tid == 0) ptx::bulk_wait_all();
+            if (kMix) mix_after_store(tile_slot(item_at(qlast, nc - 1, R - 1, R - 1)));
+            else if (tid == 0) ptx::bulk_wait_all();
         }
     }
     ptx::tc_fence_before();
@@ -840,10 +898,11 @@ std::mutex g_mu;
 int set_attrs(int dev) {
     std::lock_guard<std::mutex> g(g_mu);
     if (g_attr_set[dev]) return SSDC_OK;
-    const void* kernels[6] = {
-        (const void*)fused2_kernel<false, false, false>, (const void*)fused2_kernel<true, false, false>,
-        (const void*)fused2_kernel<false, true, false>,  (const void*)fused2_kernel<true, true, false>,
-        (const void*)fused2_kernel<false, false, true>,  (const void*)fused2_kernel<false, true, true>};
+    const void* kernels[8] = {
+        (const void*)fused2_kernel<false, false, false>,       (const void*)fused2_kernel<true, false, false>,
+        (const void*)fused2_kernel<false, true, false>,        (const void*)fused2_kernel<true, true, false>,
+        (const void*)fused2_kernel<false, false, true>,        (const void*)fused2_kernel<false, true, true>,
+        (const void*)fused2_kernel<false, false, false, true>, (const void*)fused2_kernel<false, false, true, true>};
     for (const void* k : kernels)
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
             return SSDC_ERR_CUDA;
@@ -874,7 +933,13 @@ int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bo
     const dim3 g((unsigned)grid), b(fused2::kThreads);
     const bool swap_c = (fm.swap & 4) != 0, blocks = p.Q > fused2::kQ;
     const size_t sb = fused2::kSmemBytes;
-    if (p.in_bf16) {  // bfloat16 inputs take the per-plane maps: never swapped
+    if (p.mix_w != nullptr) {  // the fused head mixer: Q <= 64, per-plane maps (never swapped)
+        if (blocks || swap_c) return SSDC_ERR_UNSUPPORTED;
+        if (p.in_bf16)
+            fused2::fused2_kernel<false, false, true, true><<<g, b, sb, stream>>>(p, ws, fm);
+        else
+            fused2::fused2_kernel<false, false, false, true><<<g, b, sb, stream>>>(p, ws, fm);
+    } else if (p.in_bf16) {  // bfloat16 inputs take the per-plane maps: never swapped
         if (blocks)
             fused2::fused2_kernel<false, true, true><<<g, b, sb, stream>>>(p, ws, fm);
         else

@@ -81,6 +81,12 @@ bool use_fused(const ssdc_dims& d, int Q) {
            (ssdc::fused_supported((int)d.N, (int)d.D, Q) || ssdc::fused2_supported((int)d.N, (int)d.D, Q));
 }
 
+// The fused head mixer's counters: one per (batch row, row tile of min(Q, 64) tokens).
+int64_t mix_counters(const ssdc_dims& d, int Q) { return d.B * ssdc::ceil_div64(d.T, Q < 64 ? Q : 64); }
+size_t mix_ws_bytes(const ssdc_dims& d, int Q) {
+    return 256 + (((size_t)mix_counters(d, Q) * sizeof(int) + 255) & ~size_t(255));
+}
+
 size_t ws_bytes_for(const ssdc_dims& d, int Q) {
     if (use_fused(d, Q)) return 256;  // status word only
     const int64_t nc = ssdc::ceil_div64(d.T, Q);
@@ -132,7 +138,7 @@ int setup_device_attrs() {
 // initial state; in_bf16: x, B_t and C_t point to bfloat16 planes.
 int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt, ssdc_cin s0, ssdc_dims dims,
              int chunk_size, ssdc_cout y, ssdc_cout final_state, void* workspace, size_t ws_bytes,
-             cudaStream_t stream, bool in_bf16 = false);
+             cudaStream_t stream, bool in_bf16 = false, const float* mix = nullptr);
 
 }  // namespace
 
@@ -169,22 +175,43 @@ int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_ci
                     workspace, ws_bytes, stream, true);
 }
 
+size_t ssd_complex_fwd_mimo_workspace_bytes(ssdc_dims dims, int chunk_size) {
+    if (check_sizes(dims, chunk_size) != SSDC_OK || dims.precision != SSDC_PREC_TF32 || chunk_size > 64 ||
+        dims.H > 16 || !ssdc::fused2_supported((int)dims.N, (int)dims.D, chunk_size))
+        return 0;
+    return mix_ws_bytes(dims, chunk_size);
+}
+
+int ssd_complex_fwd_mimo(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt, const float* mix,
+                         ssdc_cin initial_state, ssdc_dims dims, int chunk_size, float* out,
+                         ssdc_cout final_state, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (mix == nullptr) return SSDC_ERR_INVALID;
+    return fwd_impl(x, A, B_t, C_t, dt, initial_state, dims, chunk_size, ssdc_cout{out, nullptr}, final_state,
+                    workspace, ws_bytes, stream, false, mix);
+}
+
 }  // extern "C"
 
 namespace {
 
 int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt, ssdc_cin s0, ssdc_dims dims,
              int chunk_size, ssdc_cout y, ssdc_cout final_state, void* workspace, size_t ws_bytes,
-             cudaStream_t stream, bool in_bf16) {
+             cudaStream_t stream, bool in_bf16, const float* mix) {
     int rc = check_sizes(dims, chunk_size);
     if (rc != SSDC_OK) return rc;
+    // the fused head mixer runs on the tensor-memory kernel, chunks of up to 64 tokens, H <= 16
+    if (mix != nullptr && (dims.precision != SSDC_PREC_TF32 || chunk_size > 64 || dims.H > 16 ||
+                           !ssdc::fused2_supported((int)dims.N, (int)dims.D, chunk_size)))
+        return SSDC_ERR_UNSUPPORTED;
     // bfloat16 inputs run on the tensor-memory kernel only
     if (in_bf16 && (dims.precision != SSDC_PREC_TF32 ||
                     !ssdc::fused2_supported((int)dims.N, (int)dims.D, chunk_size)))
         return SSDC_ERR_UNSUPPORTED;
-    // x.im may be null: a real x (its imaginary plane is zero and is not read)
+    // x.im may be null: a real x (its imaginary plane is zero and is not read); with the fused head
+    // mixer y.im is null (only the mixed Re(y) is written) and the matrix is required
+    if (mix != nullptr ? y.im != nullptr : y.im == nullptr) return SSDC_ERR_INVALID;
     const void* ptrs[] = {x.re, A.re, A.im, B_t.re, B_t.im, C_t.re, C_t.im, dt,
-                          y.re, y.im, final_state.re, final_state.im};
+                          y.re, mix != nullptr ? static_cast<const void*>(mix) : y.im, final_state.re, final_state.im};
     for (const void* q : ptrs)
         if (q == nullptr) return SSDC_ERR_INVALID;
     for (const void* q : ptrs)
@@ -196,7 +223,8 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     if (has_s0 && (!aligned16(s0.re) || !aligned16(s0.im))) return SSDC_ERR_ALIGN;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return SSDC_ERR_WORKSPACE;
-    if (ws_bytes < ws_bytes_for(dims, chunk_size)) return SSDC_ERR_WORKSPACE;
+    if (ws_bytes < (mix != nullptr ? mix_ws_bytes(dims, chunk_size) : ws_bytes_for(dims, chunk_size)))
+        return SSDC_ERR_WORKSPACE;
 
     // outputs must not overlap inputs, the workspace or each other
     const int64_t BTH = dims.B * dims.T * dims.H;
@@ -209,7 +237,8 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
                         rng(A.im, dims.H), rng(B_t.re, BTH * dims.N, ie), rng(B_t.im, BTH * dims.N, ie),
                         rng(C_t.re, BTH * dims.N, ie), rng(C_t.im, BTH * dims.N, ie), rng(dt, BTH),
                         Range{reinterpret_cast<uintptr_t>(workspace),
-                              reinterpret_cast<uintptr_t>(workspace) + ws_bytes}};
+                              reinterpret_cast<uintptr_t>(workspace) + ws_bytes},
+                        rng(mix, dims.H * dims.H)};
     const int64_t fsn = dims.B * dims.H * dims.N * dims.D;
     const Range out[] = {rng(y.re, BTH * dims.D), rng(y.im, BTH * dims.D), rng(final_state.re, fsn),
                          rng(final_state.im, fsn)};
@@ -245,12 +274,19 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     p.drop_send_chunk = g_opt_drop_state_chunk.load(std::memory_order_relaxed);
     p.in_bf16 = in_bf16 ? 1 : 0;
     ssdc::Workspace w = carve(workspace, dims, chunk_size);
+    if (mix != nullptr) {
+        p.mix_w = mix;
+        p.mix_count = reinterpret_cast<int*>(static_cast<char*>(workspace) + 256);
+    }
 
     (void)cudaGetLastError();  // clear a stale error from unrelated work
     int launches = 0;
     if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
-    // the status word starts at SSDC_OK; a kernel's failed wait records the first error
-    if (cudaMemsetAsync(w.status, 0, sizeof(int), stream) != cudaSuccess) return SSDC_ERR_CUDA;
+    // the status word starts at SSDC_OK; a kernel's failed wait records the first error (and the
+    // fused head mixer's counters start at zero)
+    if (cudaMemsetAsync(w.status, 0, mix != nullptr ? mix_ws_bytes(dims, chunk_size) : sizeof(int), stream) !=
+        cudaSuccess)
+        return SSDC_ERR_CUDA;
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
                          (unsigned)(p.B * p.H));
     int path = SSDC_PATH_STAGED_FP32;
@@ -270,8 +306,8 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
         // ceil(sequences / SMs) x chunks at about 3.7 us a chunk; the cluster kernel, its chosen
         // cost at about 4.1 us a chunk with one CTA per sequence and 5.2 us with the state
         // handed between CTAs.
-        int kernel = in_bf16 ? 2 : g_opt_kernel.load(std::memory_order_relaxed);
-        const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q) && !in_bf16;
+        int kernel = (in_bf16 || mix != nullptr) ? 2 : g_opt_kernel.load(std::memory_order_relaxed);
+        const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q) && !in_bf16 && mix == nullptr;
         if (kernel == 0) {
             if (!cluster_ok) {
                 kernel = 2;
@@ -292,7 +328,7 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
             }
         }
         if (kernel == 1 && !cluster_ok) return SSDC_ERR_UNSUPPORTED;
-        const int n = kernel == 2 ? ssdc::fused2_launch(p, w, stream, plane_maps)
+        const int n = kernel == 2 ? ssdc::fused2_launch(p, w, stream, plane_maps && mix == nullptr)
                                   : ssdc::fused_launch(p, w, stream, force, plane_maps);
         if (n < 0) return n;
         path = kernel == 2 ? SSDC_PATH_FUSED_TMEM : SSDC_PATH_FUSED_CLUSTER;

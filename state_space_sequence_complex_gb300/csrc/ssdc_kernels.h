@@ -20,6 +20,11 @@ struct Problem {
     // x, B_t and C_t hold bfloat16 planes (the pointers above are their
     // addresses, read only through tensor maps); 0: fp32
     int in_bf16 = 0;
+    // The MIMO head mixer fused into the epilogue (the tensor-memory kernel): mix_w
+    // (H x H, H <= 16) or null; y_re then receives the mixed Re(y) and y_im is null;
+    // mix_count: B * ceil(T / min(Q, 64)) counters, zero at launch.
+    const float* mix_w = nullptr;
+    int* mix_count = nullptr;
     // Test hook of the fused kernel: the CTA of this chunk index does not send
     // the state it computes (-1 = off), so that its successor's bounded wait
     // gives up and reports SSDC_ERR_TIMEOUT.

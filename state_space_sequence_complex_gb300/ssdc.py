@@ -32,7 +32,8 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
            "ssd_complex_fwd_noalloc", "ssd_complex_fwd_host_scratch_bytes", "ssd_complex_fwd_host",
            "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd",
            "ssd_complex_set_option", "ssd_complex_noalloc_status", "ssd_complex_last_path",
-           "ssd_complex_segment_decay", "ssd_complex_state_combine", "ssd_complex_fwd_bf16")
+           "ssd_complex_segment_decay", "ssd_complex_state_combine", "ssd_complex_fwd_bf16",
+           "ssd_complex_fwd_mimo", "ssd_complex_fwd_mimo_workspace_bytes")
 
 PATHS = {0: "staged_fp32", 1: "staged_tf32", 2: "fused_cluster", 3: "fused_tmem"}
 
@@ -85,6 +86,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_fwd_init.restype = ctypes.c_int
     lib.ssd_complex_fwd_bf16.argtypes = common[:5] + [ssdc_cin] + common[5:] + [vp, sz, vp]
     lib.ssd_complex_fwd_bf16.restype = ctypes.c_int
+    lib.ssd_complex_fwd_mimo.argtypes = common[:5] + [vp, ssdc_cin, ssdc_dims, ctypes.c_int, vp, ssdc_cout,
+                                                      vp, sz, vp]
+    lib.ssd_complex_fwd_mimo.restype = ctypes.c_int
+    lib.ssd_complex_fwd_mimo_workspace_bytes.argtypes = [ssdc_dims, ctypes.c_int]
+    lib.ssd_complex_fwd_mimo_workspace_bytes.restype = sz
     lib.ssd_complex_fwd.argtypes = common + [vp]
     lib.ssd_complex_fwd.restype = ctypes.c_int
     lib.ssd_complex_status.argtypes = [vp, vp]
@@ -227,6 +233,46 @@ def ssd_complex_fwd_bf16(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chu
     if check and rc != SSDC_OK:
         raise SSDCError(rc, "ssd_complex_fwd_bf16")
     return rc
+
+
+class MimoForward:
+    """The forward pass with the MIMO head mixer fused (``ssd_complex_fwd_mimo``):
+    holds the output (the mixed Re(y), (B,T,H,D)), the final state and the
+    workspace of one problem size. ``__call__`` takes the planar inputs and the
+    (H,H) mixing matrix as CUDA tensors and returns ``(out, fs_re, fs_im)``."""
+
+    def __init__(self, Bn, T, H, N, D, chunk_size, device="cuda"):
+        import torch
+
+        self.shape = (Bn, T, H, N, D)
+        self.chunk_size = int(chunk_size)
+        d = dims(Bn, T, H, N, D, "tf32")
+        nbytes = load().ssd_complex_fwd_mimo_workspace_bytes(d, int(chunk_size))
+        if nbytes == 0:
+            raise SSDCError(SSDC_ERR_UNSUPPORTED, "ssd_complex_fwd_mimo_workspace_bytes")
+        f32 = dict(dtype=torch.float32, device=device)
+        self.out = torch.empty((Bn, T, H, D), **f32)
+        self.fs_re = torch.empty((Bn, H, N, D), **f32)
+        self.fs_im = torch.empty((Bn, H, N, D), **f32)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, mix, stream=None, s0_re=None,
+                 s0_im=None):
+        import torch
+
+        Bn, T, H, N, D = self.shape
+        s = torch.cuda.current_stream() if stream is None else stream
+        rc = load().ssd_complex_fwd_mimo(
+            _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _cin(C_re, C_im), _ptr(dt), _ptr(mix),
+            _opt_in(s0_re, s0_im), dims(Bn, T, H, N, D, "tf32"), self.chunk_size, _ptr(self.out),
+            _cout(self.fs_re, self.fs_im), _ptr(self.workspace), int(self.workspace.numel()),
+            ctypes.c_void_p(s.cuda_stream))
+        if rc != SSDC_OK:
+            raise SSDCError(rc, "ssd_complex_fwd_mimo")
+        return self.out, self.fs_re, self.fs_im
+
+    def status(self, stream=None) -> int:
+        return ssd_complex_status(self.workspace, stream)
 
 
 def ssd_complex_fwd_noalloc(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chunk_size, *,
