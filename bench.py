@@ -59,6 +59,9 @@ def parse():
                          "previous segment's final state (the initial-state entry point)")
     ap.add_argument("--bf16", action="store_true",
                     help="measurement mode: x, B_t and C_t in bfloat16 (ssd_complex_fwd_bf16), the rest fp32")
+    ap.add_argument("--mimo", action="store_true",
+                    help="measurement mode: the MIMO head mixer fused into the forward (ssd_complex_fwd_mimo; "
+                         "only the mixed Re(y) is written), timed against the plain forward plus a separate mixer")
     ap.add_argument("--real-x", action="store_true",
                     help="measurement mode: x real (x.im = NULL, only x.re is read), as in the model")
     ap.add_argument("--backward", action="store_true",
@@ -192,10 +195,13 @@ def algorithmic_bytes_per_unit(w) -> float:
     return 16 * w.D + 16 * w.N + 4 + 8 * w.N * w.D / w.T
 
 
-def input_bytes_per_unit(w, bf16=False, real_x=False) -> float:
+def input_bytes_per_unit(w, bf16=False, real_x=False, mimo=False) -> float:
     """algorithmic_bytes_per_unit with x, B_t, C_t in bfloat16 (2 bytes a plane element
-    instead of 4: 4 D + 8 N fewer) and / or a real x (no imaginary plane)."""
+    instead of 4: 4 D + 8 N fewer), a real x (no imaginary plane) and / or the fused head
+    mixer (only the mixed Re(y) written: 4 D fewer)."""
     b = algorithmic_bytes_per_unit(w)
+    if mimo:
+        b -= 4.0 * w.D
     if bf16:
         b -= 4.0 * w.D + 8.0 * w.N
     if real_x:
@@ -526,11 +532,20 @@ def other_workload(args, w):
         precision = "tf32" if ssdc.ssd_complex_fwd_supported(ssdc.dims(w.B, Ts, w.H, w.N, w.D, "tf32"), Q) == 0 else "fp32"
     if args.bf16 and precision != "tf32":
         raise SystemExit("--bf16 runs on the TF32 path only")
-    f = ssdc.Forward(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev, bf16_inputs=args.bf16)
+    if args.mimo and (precision != "tf32" or args.bf16 or K > 1):
+        raise SystemExit("--mimo runs on the TF32 path, fp32 inputs, unsegmented")
+    if args.mimo:
+        # identity plus a cross-head part, as a trained mixer would have
+        W = (torch.eye(w.H, device=dev) + 0.3 * torch.randn(w.H, w.H, device=dev, generator=g)).contiguous()
+        f = ssdc.MimoForward(w.B, Ts, w.H, w.N, w.D, Q, device=dev)
+    else:
+        f = ssdc.Forward(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev, bf16_inputs=args.bf16)
 
     def run_layer(L, timed=False):
         for k, seg in enumerate(L):
-            if k == 0:
+            if args.mimo:
+                f(*seg, W)
+            elif k == 0:
                 f(*seg)
             else:
                 f(*seg, s0_re=f.fs_re, s0_im=f.fs_im)
@@ -580,7 +595,7 @@ def other_workload(args, w):
     peak, peak_kind = peaks()
     wq = w.with_(Q=Q, T=Ts)
     # per launch; a segment after the first also reads its initial state (8 N D bytes per sequence)
-    bytes_per_launch = (input_bytes_per_unit(wq, bf16=args.bf16, real_x=args.real_x) * wq.token_heads
+    bytes_per_launch = (input_bytes_per_unit(wq, bf16=args.bf16, real_x=args.real_x, mimo=args.mimo) * wq.token_heads
                         + 8.0 * w.N * w.D * w.B * w.H * (K - 1) / K)
     launch_ms = sum(kmeans)
     units = w.token_heads * w.layers
@@ -593,7 +608,8 @@ def other_workload(args, w):
         "config": {"workload": f"{w.name} Q{Q}" + (f" in {K} segments of T={Ts}, state carried" if K > 1 else "")
                    + (f", {w.layers} layer(s) run" if args.layers > 0 else "")
                    + (f", batch {w.B}" if args.batch > 0 else "")
-                   + (", real x" if args.real_x else "") + (", bf16 x/B/C" if args.bf16 else ""),
+                   + (", real x" if args.real_x else "") + (", bf16 x/B/C" if args.bf16 else "")
+                   + (", fused head mixer (mixed Re(y) only)" if args.mimo else ""),
                    "real_x": bool(args.real_x), "bf16_inputs": bool(args.bf16),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
                    "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
@@ -609,6 +625,41 @@ def other_workload(args, w):
         "gpu_launches": nk * w.layers * K * args.steps,
         "clocks": clocks,
     }
+    if args.mimo:
+        # the unfused counterpart: the plain forward (y written), then the same mixer as a separate
+        # op on Re(y) (torch einsum), each timed with CUDA events, L2 flushed before each step
+        fp = ssdc.Forward(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev)
+        mixed = [None]
+
+        def plain(L):
+            for seg in L:
+                fp(*seg)
+
+        def mixer(L):
+            mixed[0] = torch.einsum("gh,bthd->btgd", W, fp.y_re)
+
+        def timed(fn, n):
+            for i in range(3):
+                flush.fill_(float(i))
+                for L in layers:
+                    fn(L)
+            tot = 0.0
+            for k in range(n):
+                flush.fill_(float(k))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for L in layers:
+                    fn(L)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+            return tot / n
+        n = max(3, min(args.steps, 50))
+        scan_ms = timed(plain, n)
+        mixer_ms = timed(mixer, n)
+        line["unfused"] = {"scan_ms": scan_ms, "mixer_ms": mixer_ms, "total_ms": scan_ms + mixer_ms,
+                           "what": "the plain forward (path chosen as usual, y written) plus the mixer as a "
+                                   "separate torch einsum over Re(y); the fused figure is ms_per_step"}
     print(json.dumps(line), flush=True)
 
 
@@ -619,7 +670,7 @@ def main():
             raise SystemExit("the backward measurement runs with --impl ours, unsegmented")
         backward_workload(args, inputs.ALL[args.workload])
         return
-    if args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0 or args.bf16:
+    if args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0 or args.bf16 or args.mimo:
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
         w = inputs.ALL[args.workload]

@@ -98,7 +98,8 @@ struct Tail {
     uint64_t xt_ready, bt_ready, c_ready, p_ready, sin_ready;  // worker hand-offs (one arrival per warp)
     uint64_t mma_g, mma_s, mma_yo, mma_y;      // MMA completions
     uint32_t tmem;
-    int mix_task;            // fused head mixer: the tile this CTA mixes now, or -1
+    int mix_task;            // fused head mixer: the tile whose share this CTA mixes now, or -1
+    int mix_pend;            // fused head mixer: the next tile of the current sequence to mix a share of
     float wmix[16 * 16];     // fused head mixer: W, zero past H
 };
 
@@ -296,6 +297,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     const int nseq = p.B * H;
     const int nseq_cta = (int)blockIdx.x < nseq ? (nseq - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nitems = nseq_cta * nc * (R * (R + 1) / 2);
+    const int mix_ntiles = (int)((p.T + rows - 1) / rows);  // fused head mixer: row tiles per sequence
 
     // the swizzled tiles need a 1024-byte aligned base (uniform across the grid)
     if (ptx::smem_addr(smem_raw) & 1023u) {
@@ -324,6 +326,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         ptx::tmem_alloc(&sm.tmem, kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (kMix && tid == 0) sm.mix_pend = 0;
     if (kMix)
         for (int i = tid; i < 16 * 16; i += kThreads)
             sm.wmix[i] = ((i >> 4) < H && (i & 15) < H) ? p.mix_w[(i >> 4) * H + (i & 15)] : 0.0f;
@@ -510,8 +513,20 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     }
             ptx::fence_proxy_async_smem();
             ptx::named_sync(kWorkerBar, kWorkers);
-            if (tid == 0) {
-                const int t0 = row.c * Q + kQ * row.r, yb = row.q / H, yh = row.q - yb * H;
+            const int t0 = row.c * Q + kQ * row.r, yb = row.q / H, yh = row.q - yb * H;
+            if constexpr (kMix) {
+                // Re(y) only, by every worker with 16-byte stores (rows past T or the chunk skipped),
+                // so that a fence of each thread publishes it before the tile is counted
+                const int nrow = (int)(p.T - t0 < (int64_t)rows ? p.T - t0 : (int64_t)rows);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int u = tid + kWorkers * k, l = u >> 4, dq = u & 15;
+                    if (l < nrow && 4 * dq < D) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(buf + stk_row(dq >> 3, 0, l) + chunk16(dq & 7, l));
+                        *reinterpret_cast<float4*>(p.y_re + (((int64_t)yb * p.T + t0 + l) * H + yh) * D + 4 * dq) = v4;
+                    }
+                }
+            } else if (tid == 0) {
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, yh, t0, yb);
@@ -521,32 +536,20 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             }
         };
 
-        // Fused head mixer (p.mix_w): a row tile's Re(y) of every head of batch row b goes to
-        // y_re by the staged stores; the CTA whose store completes the count of its (b, tile)
-        // (one per head) then mixes the tile in place, out[t, g, :] = sum_h W[g, h] Re(y)[t, h, :].
-        // Nothing waits for another CTA: the last to arrive does the work.
-        const int ntiles = (int)((p.T + rows - 1) / rows);
-        auto tile_slot = [&](const Item& row) {
-            const int yb = row.q / H;
-            return yb * ntiles + (row.c * Q + kQ * row.r) / rows;
-        };
-        auto mix_after_store = [&](int slot) {
-            if (tid == 0) {
-                ptx::bulk_wait_all();  // the tile's Re(y) is in global memory
-                ptx::fence_proxy_async_global();
-                __threadfence();
-                const int old = atomicAdd(p.mix_count + slot, 1);
-                __threadfence();
-                sm.mix_task = old == H - 1 ? slot : -1;
-            }
-            ptx::named_sync(kWorkerBar, kWorkers);
-            const int task = sm.mix_task;
-            if (task < 0) return;
-            const int mb = task / ntiles;
-            const int64_t mt0 = (int64_t)(task - mb * ntiles) * rows;
+        // Fused head mixer (kMix): each CTA stores its sequence's Re(y) tile by tile and counts
+        // every stored tile per (batch row, tile). The mixing of a tile, out[t, g, :] =
+        // sum_h W[g, h] Re(y)[t, h, :], is shared out by head: the CTA of head h mixes the h-th
+        // 1 / H of the tile's tokens, in place, once all H heads have stored the tile. A CTA
+        // mixes its ready shares after each tile it stores without waiting, and waits (bounded)
+        // only for the shares still open after its sequence's last tile. (Such a wait is for heads
+        // whose CTAs are in the same round of sequences, or in the next round after their own;
+        // with at least H CTAs no two waits form a cycle.)
+        auto mix_share = [&](int mb, int mh, int tile) {
+            const int64_t mt0 = (int64_t)tile * rows;
             const int nt = (int)(p.T - mt0 < (int64_t)rows ? p.T - mt0 : (int64_t)rows);
-            for (int e = tid; e < nt * D; e += kWorkers) {
-                const int tt = e / D, d = e - tt * D;
+            const int lo = (mh * nt) / H, hi = ((mh + 1) * nt) / H;
+            for (int e = tid; e < (hi - lo) * D; e += kWorkers) {
+                const int tt = lo + e / D, d = e - (e / D) * D;
                 float* col = p.y_re + (((int64_t)mb * p.T + mt0 + tt) * H) * D + d;
                 float v[16];
 #pragma unroll
@@ -562,6 +565,52 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 }
             }
         };
+        auto mix_after_store = [&](const Item& row) {
+            const int mb = row.q / H, mh = row.q - mb * H;
+            const int tile = (row.c * Q + kQ * row.r) / rows;
+            const bool last_tile = tile == mix_ntiles - 1;
+            int* cnt = p.mix_count + (int64_t)mb * mix_ntiles;
+            // every worker's Re(y) stores precede the barrier; the release fence of the counting
+            // thread is cumulative over them
+            ptx::named_sync(kWorkerBar, kWorkers);
+            if (tid == 0) {
+                __threadfence();
+                atomicAdd(cnt + tile, 1);
+            }
+            for (;;) {
+                if (tid == 0) {
+                    int task = -1;
+                    const int pend = sm.mix_pend;
+                    if (pend <= tile) {
+                        volatile int* c = cnt + pend;
+                        bool ready = *c >= H;
+                        if (!ready && last_tile) {
+                            const uint64_t t_start = ptx::globaltimer_ns();
+                            while (*c < H) {
+                                if (ptx::globaltimer_ns() - t_start > kWaitIters) {
+                                    fail(ws.status);
+                                    break;
+                                }
+                                __nanosleep(256);
+                            }
+                            ready = true;
+                        }
+                        if (ready) {
+                            __threadfence();
+                            task = pend;
+                            sm.mix_pend = pend + 1;
+                        }
+                    }
+                    sm.mix_task = task;
+                }
+                ptx::named_sync(kWorkerBar, kWorkers);
+                const int task = sm.mix_task;
+                ptx::named_sync(kWorkerBar, kWorkers);  // every worker has read the task
+                if (task < 0) break;
+                mix_share(mb, mh, task);
+            }
+            if (tid == 0 && last_tile) sm.mix_pend = 0;  // the next sequence starts at its tile 0
+        };
 
         Item cur = item_at((int)blockIdx.x, 0, 0, 0);
         // the S window of the first chunk: its initial state, if any
@@ -575,7 +624,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 
         int ndiag = 0, nchunk = 0;  // diagonal blocks and chunks begun
         for (int it = 0; it < nitems; ++it) {
-            int mix_slot = -1;  // the row tile staged in this item (fused head mixer)
+            Item mix_row = cur;  // the row tile staged in this item (fused head mixer)
             const int s = it & 1;
             const uint32_t ph = (uint32_t)it & 1u, pd = (uint32_t)ndiag & 1u;
             const bool diag = cur.j == cur.r;
@@ -718,7 +767,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     if (cur.c == 0) row.q = cur.q - (int)gridDim.x;
                 }
                 stage_y(ystage, row);
-                mix_slot = tile_slot(row);
+                mix_row = row;
             }
 
             // ---- C: C'_r = C_r o exp(Acs[l]) in place, plane 0 real. Unit: physical 16-byte chunk
@@ -859,12 +908,9 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 if (lane == 0) ptx::mbar_arrive(&sm.sin_ready);
             }
             if (kMix && staged) {
-                // the stores have completed (and read the staging tile): release x, count, mix
-                if (tid == 0) {
-                    ptx::bulk_wait_all();
-                    if (!kBf16) ptx::mbar_arrive(&sm.free_x[s]);
-                }
-                mix_after_store(mix_slot);
+                // the Re(y) stores read the staging tile before mix_after_store's barrier
+                mix_after_store(mix_row);
+                if (tid == 0 && !kBf16) ptx::mbar_arrive(&sm.free_x[s]);
             } else if (tid == 0 && staged) {  // the y stores have read the staging tile
                 ptx::bulk_wait_read_all();
                 if (!kBf16) ptx::mbar_arrive(&sm.free_x[s]);
@@ -882,7 +928,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             char* buf = reinterpret_cast<char*>(sm.x[(nitems - 1) & 1]);
             if constexpr (kBf16) buf = reinterpret_cast<char*>(sm.yw);
             stage_y(buf, item_at(qlast, nc - 1, R - 1, R - 1));
-            if (kMix) mix_after_store(tile_slot(item_at(qlast, nc - 1, R - 1, R - 1)));
+            if (kMix) mix_after_store(item_at(qlast, nc - 1, R - 1, R - 1));
             else if (tid == 0) ptx::bulk_wait_all();
         }
     }
