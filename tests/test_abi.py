@@ -303,3 +303,32 @@ def test_bf16_entry_checks_before_launch(lib):
     inside = list(ptrs)
     inside[9] = ptrs[0] + BTH * d.D * 2 - 16
     assert _call_bf16(lib, inside, d, ws=end) == ssdc.SSDC_ERR_INVALID
+
+
+def _call_mimo(lib, ptrs, mix, d, Q=64, ws=None, ws_bytes=1 << 30):
+    p = ptrs
+    cin = lambda a, b: ssdc.ssdc_cin(a, b)
+    cout = lambda a, b: ssdc.ssdc_cout(a, b)
+    return lib.ssd_complex_fwd_mimo(cin(p[0], p[1]), cin(p[2], p[3]), cin(p[4], p[5]), cin(p[6], p[7]),
+                                    p[8], mix, cin(None, None), d, Q, p[9], cout(p[11], p[12]),
+                                    ws, ws_bytes, None)
+
+
+def test_mimo_entry_checks_before_launch(lib):
+    """The fused head mixer takes the TF32 precision, Q <= 64 and H <= 16; the matrix is required,
+    must be aligned and must not overlap an output; its workspace holds the tile counters."""
+    d = ssdc.dims(2, 128, 16, 64, 64, "tf32")
+    ptrs, end = fake_ptrs(d)
+    mix = end + (1 << 20)
+    need = lib.ssd_complex_fwd_mimo_workspace_bytes(d, 64)
+    assert need >= 256 + 4 * 2 * 2
+    assert _call_mimo(lib, ptrs, None, d, ws=end) == ssdc.SSDC_ERR_INVALID
+    assert _call_mimo(lib, ptrs, mix + 4, d, ws=end) == ssdc.SSDC_ERR_ALIGN
+    assert _call_mimo(lib, ptrs, ptrs[9], d, ws=end) == ssdc.SSDC_ERR_INVALID       # on top of out
+    assert _call_mimo(lib, ptrs, mix, d, ws=end, ws_bytes=need - 1) == ssdc.SSDC_ERR_WORKSPACE
+    for prec, H, Q in (("fp32", 16, 64), ("tf32", 16, 128), ("tf32", 32, 64)):
+        dd = ssdc.dims(2, 128, H, 64, 64, prec)
+        p2, e2 = fake_ptrs(dd)
+        assert _call_mimo(lib, p2, e2 + (1 << 20), dd, Q=Q, ws=e2) == ssdc.SSDC_ERR_UNSUPPORTED
+    assert _call_mimo(lib, ptrs, mix, d, ws=end, ws_bytes=need) not in (
+        ssdc.SSDC_ERR_INVALID, ssdc.SSDC_ERR_ALIGN, ssdc.SSDC_ERR_WORKSPACE, ssdc.SSDC_OK)
