@@ -513,8 +513,8 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     }
             ptx::fence_proxy_async_smem();
             ptx::named_sync(kWorkerBar, kWorkers);
-            const int t0 = row.c * Q + kQ * row.r, yb = row.q / H, yh = row.q - yb * H;
             if constexpr (kMix) {
+                const int t0 = row.c * Q + kQ * row.r, yb = row.q / H, yh = row.q - yb * H;
                 // Re(y) only, by every worker with 16-byte stores (rows past T or the chunk skipped),
                 // so that a fence of each thread publishes it before the tile is counted
                 const int nrow = (int)(p.T - t0 < (int64_t)rows ? p.T - t0 : (int64_t)rows);
@@ -527,10 +527,13 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                     }
                 }
             } else if (tid == 0) {
+                const int t0 = row.c * Q + kQ * row.r, yb = row.q / H, yh = row.q - yb * H;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, yh, t0, yb);
-                    if (fm.y_im_out) ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
+                    // (y_im is absent only with the fused head mixer, which stores above; the fp32
+                    // instances keep the test, which leaves them without register spills)
+                    if (kBf16 || fm.y_im_out) ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
                 }
                 ptx::bulk_commit();
             }
