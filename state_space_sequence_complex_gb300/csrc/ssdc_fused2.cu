@@ -298,6 +298,13 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     const int nseq_cta = (int)blockIdx.x < nseq ? (nseq - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nitems = nseq_cta * nc * (R * (R + 1) / 2);
     const int mix_ntiles = (int)((p.T + rows - 1) / rows);  // fused head mixer: row tiles per sequence
+    // The four TMA stores of a staged y tile (two 32-column halves of each plane) leave from lane
+    // 0 of worker warps 0-3, one each, in the bfloat16 and the block instances, so that no warp
+    // carries all four on its way to the next phase (each then waits for its store to read the
+    // tile and releases the x tile); in the fp32 single-block instance thread 0 issues all four,
+    // which measured faster there. (tid & kYMask) == 0 selects the issuing threads.
+    constexpr int kYWarps = (kBf16 || kBlocks) && !kMix ? 4 : 1;
+    constexpr int kYMask = ~((kYWarps - 1) << 5);
 
     // the swizzled tiles need a 1024-byte aligned base (uniform across the grid)
     if (ptx::smem_addr(smem_raw) & 1023u) {
@@ -307,7 +314,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&sm.full[s], 1);
-            ptx::mbar_init(&sm.free_x[s], 1);
+            ptx::mbar_init(&sm.free_x[s], kYWarps);
             ptx::mbar_init(&sm.free_b[s], 1);
             ptx::mbar_init(&sm.free_c[s], 1);
         }
@@ -458,10 +465,18 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         const int i4 = lane >> 2, lq = lane & 3;
         const int rr = 16 * qd + 8 * blk + i4;
         const uint32_t tl = lane_base(tmem, warp) + ((uint32_t)(16 * blk) << 16);
-        const int swx = fm.swap & 1, swb = (fm.swap >> 1) & 1;
+        // Offsets that follow the planes' order in the tiles (fm.swap): held in registers by the
+        // fp32 single-block instance and read where they are used by the others, whichever keeps
+        // each instance off register spills.
+        constexpr bool kSwapAtUse = kBf16 || kBlocks || kMix;
+        const int swx0 = fm.swap & 1, swb0 = (fm.swap >> 1) & 1;
+        const uint32_t gbr0 = kAccG + 64 * swb0, gbi0 = kAccG + 64 * (1 - swb0);
+        auto swx = [&] { return kSwapAtUse ? (fm.swap & 1) : swx0; };
+        auto swb = [&] { return kSwapAtUse ? ((fm.swap >> 1) & 1) : swb0; };
+        auto gbr = [&] { return kSwapAtUse ? kAccG + 64 * ((fm.swap >> 1) & 1) : gbr0; };  // B_r products
+        auto gbi = [&] { return kSwapAtUse ? kAccG + 64 * (1 - ((fm.swap >> 1) & 1)) : gbi0; };  // B_i
         constexpr int kCr = kSwapC ? 1 : 0;              // C plane in TMEM lane plane 0 / 1
         constexpr int kRr = 2 * kCr, kRi = 2 - 2 * kCr;  // register offset of the C_r / C_i lanes
-        const uint32_t gbr = kAccG + 64 * swb, gbi = kAccG + 64 * (1 - swb);  // B_r / B_i products
         bool ok = true;
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             if (ok && !ptx::mbar_wait(bar, parity, kWaitIters)) {
@@ -488,8 +503,8 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
         // 16g + 8p + i = plane p of token 8g + i of P and of C') into the staging tile `buf`
         // (two stacked planes, rows l, the 128-byte swizzle of the TMA boxes; the four rows and
         // eight columns of a warp's store fall on distinct 16-byte positions), then, once every
-        // worker has written its part, one thread stores the tile with four TMA copies (rows
-        // past T are not written) and commits them as one bulk group.
+        // worker has written its part, the tile leaves in four TMA copies (rows past T are not
+        // written) from the threads that kYWarps names, each committing its own bulk group.
         auto stage_y = [&](char* buf, const Item& row) {
             float v[32];
             ptx::tmem_ld_16x256b_x4(tl + kAccY + 64 * kh, v);
@@ -526,14 +541,20 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                         *reinterpret_cast<float4*>(p.y_re + (((int64_t)yb * p.T + t0 + l) * H + yh) * D + 4 * dq) = v4;
                     }
                 }
-            } else if (tid == 0) {
+            } else if ((tid & kYMask) == 0) {
                 const int t0 = row.c * Q + kQ * row.r, yb = row.q / H, yh = row.q - yb * H;
+                // (y_im is absent only with the fused head mixer, which stores above; the fp32
+                // instances keep the test, which leaves them without register spills)
+                if constexpr (kYWarps == 1) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, yh, t0, yb);
-                    // (y_im is absent only with the fused head mixer, which stores above; the fp32
-                    // instances keep the test, which leaves them without register spills)
-                    if (kBf16 || fm.y_im_out) ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
+                    for (int half = 0; half < 2; ++half) {
+                        ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, yh, t0, yb);
+                        if (kBf16 || fm.y_im_out) ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
+                    }
+                } else {
+                    const int half = warp & 1, plane = warp >> 1;
+                    if (plane == 0) ptx::tma_store_4d(&fm.y_re, buf + stk_row(half, 0, 0), 32 * half, yh, t0, yb);
+                    else if (kBf16 || fm.y_im_out) ptx::tma_store_4d(&fm.y_im, buf + stk_row(half, 1, 0), 32 * half, yh, t0, yb);
                 }
                 ptx::bulk_commit();
             }
@@ -691,7 +712,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
 #pragma unroll
                     for (int k = 0; k < 16; ++k) v[k] = xp ? r[k ^ 4] : r[k];
                 } else {
-                    const char* rowbase = xbase + stk_row(xd >> 5, xp ^ swx, 0) + 4 * (xd & 3);
+                    const char* rowbase = xbase + stk_row(xd >> 5, xp ^ swx(), 0) + 4 * (xd & 3);
                     const int cq = (xd & 31) >> 2;
                     float r[16];
 #pragma unroll
@@ -720,7 +741,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                                 bbase + pp * kPlane16 + off16(sr, 4 * bnb + 2 * bjh));
                             bv[pp][i] = make_float2(ptx::bf16_lo(two), ptx::bf16_hi(two));
                         } else {
-                            bv[pp][i] = *reinterpret_cast<const float2*>(bbase + stk_row(bnb >> 3, pp ^ swb, sr) +
+                            bv[pp][i] = *reinterpret_cast<const float2*>(bbase + stk_row(bnb >> 3, pp ^ swb(), sr) +
                                                                          chunk16(bnb & 7, sr) + 8 * bjh);
                         }
                     }
@@ -730,7 +751,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             ptx::named_sync(kWorkerBar, kWorkers);
             // every worker has read x; the tile is free at once, unless the previous row's y is
             // staged in it below (then once its TMA stores have read it)
-            if (tid == 0 && (kBf16 || !staged)) ptx::mbar_arrive(&sm.free_x[s]);
+            if ((kBf16 || !staged) && (tid & kYMask) == 0) ptx::mbar_arrive(&sm.free_x[s]);
             if (lane == 0) ptx::mbar_arrive(&sm.xt_ready);
 
             // ---- B: (dec o B_j)^T in place of B (after C B^T has read it)
@@ -819,8 +840,8 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             // plane 0 / 1 of the row holds the products of C's plane 0 / 1 (C_r first unless kSwapC).
             {
                 float ga[16], gb[16];
-                ptx::tmem_ld_16x256b_x4(tl + gbr + 32 * kh, ga);
-                ptx::tmem_ld_16x256b_x4(tl + gbi + 32 * kh, gb);
+                ptx::tmem_ld_16x256b_x4(tl + gbr() + 32 * kh, ga);
+                ptx::tmem_ld_16x256b_x4(tl + gbi() + 32 * kh, gb);
                 ptx::tmem_wait_ld();
                 const float2 acs_l = sm.acs[cp][orow + rr];
                 float2 pv[4][2];
@@ -914,7 +935,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 // the Re(y) stores read the staging tile before mix_after_store's barrier
                 mix_after_store(mix_row);
                 if (tid == 0 && !kBf16) ptx::mbar_arrive(&sm.free_x[s]);
-            } else if (tid == 0 && staged) {  // the y stores have read the staging tile
+            } else if (staged && (tid & kYMask) == 0) {  // its y stores have read the staging tile
                 ptx::bulk_wait_read_all();
                 if (!kBf16) ptx::mbar_arrive(&sm.free_x[s]);
             }
@@ -932,7 +953,7 @@ fused2_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
             if constexpr (kBf16) buf = reinterpret_cast<char*>(sm.yw);
             stage_y(buf, item_at(qlast, nc - 1, R - 1, R - 1));
             if (kMix) mix_after_store(item_at(qlast, nc - 1, R - 1, R - 1));
-            else if (tid == 0) ptx::bulk_wait_all();
+            else if ((tid & kYMask) == 0) ptx::bulk_wait_all();
         }
     }
     ptx::tc_fence_before();
