@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--mimo", action="store_true",
                     help="measurement mode: the MIMO head mixer fused into the forward (ssd_complex_fwd_mimo; "
                          "only the mixed Re(y) is written), timed against the plain forward plus a separate mixer")
+    ap.add_argument("--state-only", action="store_true",
+                    help="measurement mode: the final state alone (ssd_complex_final_state: reads x, B_t, dt; "
+                         "no y), as the joining of time segments uses it")
     ap.add_argument("--real-x", action="store_true",
                     help="measurement mode: x real (x.im = NULL, only x.re is read), as in the model")
     ap.add_argument("--backward", action="store_true",
@@ -195,11 +198,14 @@ def algorithmic_bytes_per_unit(w) -> float:
     return 16 * w.D + 16 * w.N + 4 + 8 * w.N * w.D / w.T
 
 
-def input_bytes_per_unit(w, bf16=False, real_x=False, mimo=False) -> float:
+def input_bytes_per_unit(w, bf16=False, real_x=False, mimo=False, state_only=False) -> float:
     """algorithmic_bytes_per_unit with x, B_t, C_t in bfloat16 (2 bytes a plane element
-    instead of 4: 4 D + 8 N fewer), a real x (no imaginary plane) and / or the fused head
-    mixer (only the mixed Re(y) written: 4 D fewer)."""
+    instead of 4: 4 D + 8 N fewer), a real x (no imaginary plane), the fused head
+    mixer (only the mixed Re(y) written: 4 D fewer) and / or the final state alone
+    (ssd_complex_final_state: no C_t read and no y written, 8 N + 8 D fewer)."""
     b = algorithmic_bytes_per_unit(w)
+    if state_only:
+        b -= 8.0 * w.N + 8.0 * w.D
     if mimo:
         b -= 4.0 * w.D
     if bf16:
@@ -534,7 +540,11 @@ def other_workload(args, w):
         raise SystemExit("--bf16 runs on the TF32 path only")
     if args.mimo and (precision != "tf32" or args.bf16 or K > 1):
         raise SystemExit("--mimo runs on the TF32 path, fp32 inputs, unsegmented")
-    if args.mimo:
+    if args.state_only and (args.bf16 or args.mimo):
+        raise SystemExit("--state-only takes fp32 inputs and no mixer")
+    if args.state_only:
+        f = ssdc.FinalState(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev)
+    elif args.mimo:
         # identity plus a cross-head part, as a trained mixer would have
         W = (torch.eye(w.H, device=dev) + 0.3 * torch.randn(w.H, w.H, device=dev, generator=g)).contiguous()
         f = ssdc.MimoForward(w.B, Ts, w.H, w.N, w.D, Q, device=dev)
@@ -543,7 +553,13 @@ def other_workload(args, w):
 
     def run_layer(L, timed=False):
         for k, seg in enumerate(L):
-            if args.mimo:
+            if args.state_only:  # x, A, B_t, dt
+                sel = [seg[i] for i in (0, 1, 2, 3, 4, 5, 8)]
+                if k == 0:
+                    f(*sel)
+                else:
+                    f(*sel, s0_re=f.fs_re, s0_im=f.fs_im)
+            elif args.mimo:
                 f(*seg, W)
             elif k == 0:
                 f(*seg)
@@ -588,14 +604,16 @@ def other_workload(args, w):
     nk = min(len(p) for p in per_kernel)
     kmeans = [sum(p[i] for p in per_kernel) / len(per_kernel) for i in range(nk)]
     path = ssdc.last_path()
-    names = {1: ["fused_tmem_kernel" if path == "fused_tmem" else "fused_kernel"],
+    names = {1: [{"fused_tmem": "fused_tmem_kernel", "state_tmem": "state_tmem_kernel"}.get(path, "fused_kernel")],
+             2: ["chunk_state", "state_pass"],
              3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
         nk, [f"launch{i}" for i in range(nk)])
     top = int(np.argmax(kmeans))
     peak, peak_kind = peaks()
     wq = w.with_(Q=Q, T=Ts)
     # per launch; a segment after the first also reads its initial state (8 N D bytes per sequence)
-    bytes_per_launch = (input_bytes_per_unit(wq, bf16=args.bf16, real_x=args.real_x, mimo=args.mimo) * wq.token_heads
+    bytes_per_launch = (input_bytes_per_unit(wq, bf16=args.bf16, real_x=args.real_x, mimo=args.mimo,
+                                             state_only=args.state_only) * wq.token_heads
                         + 8.0 * w.N * w.D * w.B * w.H * (K - 1) / K)
     launch_ms = sum(kmeans)
     units = w.token_heads * w.layers
@@ -609,7 +627,8 @@ def other_workload(args, w):
                    + (f", {w.layers} layer(s) run" if args.layers > 0 else "")
                    + (f", batch {w.B}" if args.batch > 0 else "")
                    + (", real x" if args.real_x else "") + (", bf16 x/B/C" if args.bf16 else "")
-                   + (", fused head mixer (mixed Re(y) only)" if args.mimo else ""),
+                   + (", fused head mixer (mixed Re(y) only)" if args.mimo else "")
+                   + (", final state alone (no y)" if args.state_only else ""),
                    "real_x": bool(args.real_x), "bf16_inputs": bool(args.bf16),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
                    "chunk_size": Q, "layers": w.layers, "segments": K, "precision": precision,
@@ -670,7 +689,8 @@ def main():
             raise SystemExit("the backward measurement runs with --impl ours, unsegmented")
         backward_workload(args, inputs.ALL[args.workload])
         return
-    if args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0 or args.bf16 or args.mimo:
+    if (args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0 or args.bf16 or args.mimo
+            or args.state_only):
         if args.impl == "reference" or args.gpus != 1:
             raise SystemExit("the measurement workloads run on one GPU with --impl ours")
         w = inputs.ALL[args.workload]

@@ -212,10 +212,11 @@ int ssd_complex_fwd_mimo(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, con
  * end state S_seg (scanned from a zero state) takes the incoming state S_in to
  * a_seg S_in + S_seg, and consecutive segments compose as
  *   (a2, S2) o (a1, S1) = (a2 a1, a2 S1 + S2).
- * A rank that holds segment r of T therefore scans it from zero, gathers the
- * (a_seg, S_seg) of the segments before it, combines them in order into its
- * incoming state, and scans its segment again from that state
- * (ssd_complex_fwd_init) for its rows of y and its final state.
+ * A rank that holds segment r of T therefore computes the state its segment
+ * leaves from zero (ssd_complex_final_state), gathers the (a_seg, S_seg) of
+ * the segments before it, combines them in order into its incoming state, and
+ * scans its segment from that state (ssd_complex_fwd_init) for its rows of y
+ * and its final state.
  *
  * ssd_complex_segment_decay: a_seg[b,h] = exp(sum_t softplus(dt[b,t,h]) A[h])
  * over the T tokens of dt (B,T,H); the sum and the exponential in fp64.
@@ -233,6 +234,35 @@ int ssd_complex_segment_decay(ssdc_cin A, const float *dt, ssdc_dims dims,
                               ssdc_cout a_seg, cudaStream_t stream);
 int ssd_complex_state_combine(ssdc_cin a, ssdc_cin s_in, ssdc_cin s_add, ssdc_dims dims,
                               ssdc_cout s_out, cudaStream_t stream);
+
+/*
+ * The state a scan leaves behind, without its rows of y: the chunked
+ * decomposition's state side alone (landing page "03 Chunkwise SSD": the
+ * per-chunk states B^T (decay o X), decay[s] = exp(Acs[Q-1] - Acs[s]), and the
+ * pass between chunks, the STATE line), from the given initial state. It gives
+ * the final state of ssd_complex_fwd_init on the same arguments, reading only
+ * x, B_t and dt (1028 instead of 2068 bytes per token-head at N = D = 64):
+ * the end state S_seg of a segment scanned from zero, for the joining above,
+ * before the incoming states are known.
+ *   x, A, B_t, dt, dims, chunk_size   as for ssd_complex_fwd_ws (x.im may be
+ *                   NULL: a real x); the sizes each precision takes are the
+ *                   same as for the forward pass
+ *   initial_state   as for ssd_complex_fwd_init (both planes NULL: zero); it
+ *                   may be final_state itself (updated in place)
+ *   final_state     output (B,H,N,D) complex
+ *   workspace       ssd_complex_final_state_workspace_bytes(dims, chunk_size)
+ *                   bytes, 256-byte aligned; a device-side error is read with
+ *                   ssd_complex_status(workspace, stream)
+ * SSDC_PREC_TF32 runs one launch with the tensor-memory forward kernel's tiles
+ * and products (its final state bit for bit); SSDC_PREC_FP32 and
+ * SSDC_PREC_TF32_STAGED run the staged path's chunk-state and state-pass
+ * launches. Asynchronous on `stream`; errors as for ssd_complex_fwd_ws.
+ */
+size_t ssd_complex_final_state_workspace_bytes(ssdc_dims dims, int chunk_size);
+int ssd_complex_final_state(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, const float *dt,
+                            ssdc_cin initial_state, ssdc_dims dims, int chunk_size,
+                            ssdc_cout final_state, void *workspace, size_t ws_bytes,
+                            cudaStream_t stream);
 
 /*
  * Forward pass that allocates its workspace on `stream` (cudaMallocAsync /
@@ -255,23 +285,27 @@ const char *ssd_complex_strerror(int status);
  * stream (from the calling thread). */
 int ssd_complex_last_launch_count(void);
 
-/* The path the last successful forward call took (from the calling thread),
- * or -1 before the first:
+/* The path the last successful forward call (or ssd_complex_final_state)
+ * took, from the calling thread, or -1 before the first:
  *   SSDC_PATH_STAGED_FP32    exact fp32: chunk states, state pass, chunk outputs
- *   SSDC_PATH_STAGED_TF32    the same three launches on the tensor cores
+ *                            (the first two for ssd_complex_final_state)
+ *   SSDC_PATH_STAGED_TF32    the same launches on the tensor cores
  *   SSDC_PATH_FUSED_CLUSTER  one launch; each sequence's chunks dealt over the
  *                            CTAs of a thread-block cluster, chunk states passed
  *                            through distributed shared memory (Q = N = D = 64)
  *   SSDC_PATH_FUSED_TMEM     one launch; one CTA per SM walks whole sequences,
- *                            the chunk state held in tensor memory (Q = 16, 32,
- *                            64; N, D multiples of 8 up to 64)
+ *                            the chunk state held in tensor memory (Q = 16 to
+ *                            256; N, D multiples of 8 up to 64)
+ *   SSDC_PATH_STATE_TMEM     ssd_complex_final_state at SSDC_PREC_TF32: one
+ *                            launch, the state side of SSDC_PATH_FUSED_TMEM
  * SSDC_PREC_TF32 takes SSDC_PATH_FUSED_TMEM wherever the sequences fill the GPU
- * one CTA each, SSDC_PATH_FUSED_CLUSTER for fewer sequences at Q = N = D = 64,
- * and the staged path for Q = 128 and 256. */
+ * one CTA each and SSDC_PATH_FUSED_CLUSTER for fewer sequences at
+ * Q = N = D = 64. */
 #define SSDC_PATH_STAGED_FP32 0
 #define SSDC_PATH_STAGED_TF32 1
 #define SSDC_PATH_FUSED_CLUSTER 2
 #define SSDC_PATH_FUSED_TMEM 3
+#define SSDC_PATH_STATE_TMEM 4
 int ssd_complex_last_path(void);
 
 /*

@@ -239,47 +239,6 @@ __device__ __forceinline__ uint32_t off16(int r, int f) {
     return (uint32_t)(r * 128) + chunk16(f >> 3, r) + (uint32_t)((f & 7) << 1);
 }
 
-// Producer: the cumulative log-decay of a chunk of Q = 128 or 256 tokens (Q / 32
-// consecutive tokens per lane, a warp scan of the lane sums), tokens past T with
-// zero log-decay. The sum is fp32: its rounding (about 1e-7 of |Acs|, so about
-// 1e-5 relative on a decay factor) is far below TF32's. (Chunks of up to 64
-// tokens take the cluster kernel's loader, two tokens a lane, which also gives
-// the rows of a tile past Q zero log-decay.)
-__device__ __forceinline__ void chunk_acs(const Problem& p, int b, int h, int64_t t0, int Q, int lane, float2* acs) {
-    const int per = Q / 32;
-    const float Ar = p.A_re[h], Ai = p.A_im[h];
-    float lr[kMaxQc / 32], li[kMaxQc / 32];
-    float sr = 0.0f, si = 0.0f;
-#pragma unroll
-    for (int k = 0; k < kMaxQc / 32; ++k) {
-        const int64_t tok = t0 + lane * per + k;
-        float ar = 0.0f, ai = 0.0f;
-        if (k < per && tok < p.T) {
-            const float sp = softplus_f(p.dt[((int64_t)b * p.T + tok) * p.H + h]);
-            ar = sp * Ar;
-            ai = sp * Ai;
-        }
-        sr += ar;
-        si += ai;
-        lr[k] = sr;
-        li[k] = si;
-    }
-    float cr = sr, ci = si;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float ur = __shfl_up_sync(0xffffffffu, cr, off);
-        const float ui = __shfl_up_sync(0xffffffffu, ci, off);
-        if (lane >= off) {
-            cr += ur;
-            ci += ui;
-        }
-    }
-    const float er = cr - sr, ei = ci - si;  // exclusive prefix of this lane's tokens
-#pragma unroll
-    for (int k = 0; k < kMaxQc / 32; ++k)
-        if (k < per) acs[lane * per + k] = make_float2(er + lr[k], ei + li[k]);
-}
-
 // kBlocks: chunks of Q = 128 or 256 tokens, several 64 x 64 blocks each.
 // kBf16: x, B_t and C_t in bfloat16. C B^T then multiplies them as they are
 // (kind::f16, exact products); x enters the X^T window and B and C the

@@ -354,7 +354,120 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     return SSDC_OK;
 }
 
+
+// The final state alone (ssd_complex_final_state): the forward's chunk states and
+// state pass, with no chunk outputs; C_t and y are not used.
+int final_state_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, const float* dt, ssdc_cin s0, ssdc_dims dims,
+                     int chunk_size, ssdc_cout final_state, void* workspace, size_t ws_bytes,
+                     cudaStream_t stream) {
+    int rc = check_sizes(dims, chunk_size);
+    if (rc != SSDC_OK) return rc;
+    const void* ptrs[] = {x.re, A.re, A.im, B_t.re, B_t.im, dt, final_state.re, final_state.im};
+    for (const void* q : ptrs)
+        if (q == nullptr) return SSDC_ERR_INVALID;
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return SSDC_ERR_ALIGN;
+    if (!aligned16(x.im)) return SSDC_ERR_ALIGN;
+    if (x.im == x.re) return SSDC_ERR_INVALID;
+    const bool has_s0 = s0.re != nullptr;
+    if ((s0.re == nullptr) != (s0.im == nullptr) || (has_s0 && s0.re == s0.im)) return SSDC_ERR_INVALID;
+    if (has_s0 && (!aligned16(s0.re) || !aligned16(s0.im))) return SSDC_ERR_ALIGN;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return SSDC_ERR_WORKSPACE;
+    if (ws_bytes < ws_bytes_for(dims, chunk_size)) return SSDC_ERR_WORKSPACE;
+
+    // the final state must not overlap an input, the workspace or its other plane; the
+    // initial state may be the final state itself (in place, plane for plane)
+    const int64_t BTH = dims.B * dims.T * dims.H;
+    auto rng = [](const void* p, int64_t n) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return Range{lo, p == nullptr ? lo : lo + (uintptr_t)n * sizeof(float)};  // null: empty
+    };
+    const int64_t fsn = dims.B * dims.H * dims.N * dims.D;
+    const Range in[] = {rng(x.re, BTH * dims.D), rng(x.im, BTH * dims.D), rng(A.re, dims.H), rng(A.im, dims.H),
+                        rng(B_t.re, BTH * dims.N), rng(B_t.im, BTH * dims.N), rng(dt, BTH),
+                        Range{reinterpret_cast<uintptr_t>(workspace),
+                              reinterpret_cast<uintptr_t>(workspace) + ws_bytes}};
+    const Range out[] = {rng(final_state.re, fsn), rng(final_state.im, fsn)};
+    for (const Range& o : out)
+        for (const Range& i : in)
+            if (overlaps(o, i)) return SSDC_ERR_INVALID;
+    if (overlaps(out[0], out[1])) return SSDC_ERR_INVALID;
+    if (has_s0) {
+        const bool in_place = s0.re == final_state.re && s0.im == final_state.im;
+        const Range st[] = {rng(s0.re, fsn), rng(s0.im, fsn)};
+        if (overlaps(st[0], st[1])) return SSDC_ERR_INVALID;
+        for (const Range& r : st) {
+            if (overlaps(r, in[7])) return SSDC_ERR_INVALID;
+            if (!in_place && (overlaps(r, out[0]) || overlaps(r, out[1]))) return SSDC_ERR_INVALID;
+        }
+    }
+
+    rc = setup_device_attrs();
+    if (rc != SSDC_OK) return rc;
+
+    ssdc::Problem p;
+    p.x_re = x.re; p.x_im = x.im; p.A_re = A.re; p.A_im = A.im;
+    p.B_re = B_t.re; p.B_im = B_t.im; p.C_re = nullptr; p.C_im = nullptr; p.dt = dt;
+    p.s0_re = s0.re; p.s0_im = s0.im;
+    p.y_re = nullptr; p.y_im = nullptr; p.fs_re = final_state.re; p.fs_im = final_state.im;
+    p.T = dims.T; p.B = (int)dims.B; p.H = (int)dims.H; p.N = (int)dims.N; p.D = (int)dims.D;
+    p.Q = chunk_size;
+    p.nc = ssdc::ceil_div64(dims.T, chunk_size);
+    p.drop_send_chunk = -1;
+    ssdc::Workspace w = carve(workspace, dims, chunk_size);
+
+    (void)cudaGetLastError();  // clear a stale error from unrelated work
+    int launches = 0;
+    if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
+    if (cudaMemsetAsync(w.status, 0, sizeof(int), stream) != cudaSuccess) return SSDC_ERR_CUDA;
+    const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
+                         (unsigned)(p.B * p.H));
+    int path = SSDC_PATH_STAGED_FP32;
+    if (dims.precision == SSDC_PREC_TF32) {
+        if (!ssdc::state_supported(p.N, p.D, p.Q)) return SSDC_ERR_UNSUPPORTED;
+        const int n = ssdc::state_launch(p, w, stream, g_opt_plane_maps.load(std::memory_order_relaxed) != 0);
+        if (n < 0) return n;
+        launches += n;
+        path = SSDC_PATH_STATE_TMEM;
+    } else {
+        if (dims.precision == SSDC_PREC_FP32) {
+            ssdc::simt_launch_chunk_state(p, w, stream);
+            ++launches;
+        } else {
+            const int n = ssdc::tc_launch_chunk_state(p, w, stream);
+            if (n < 0) return n;
+            launches += n;
+            path = SSDC_PATH_STAGED_TF32;
+        }
+        record_event(launches, stream);
+        ssdc::ssdc_state_pass<<<pass_grid, ssdc::kPassThreads, 0, stream>>>(p, w);
+        ++launches;
+    }
+    record_event(launches, stream);
+    if (cudaGetLastError() != cudaSuccess) return SSDC_ERR_CUDA;
+    g_last_launches = launches;
+    g_last_path = path;
+    if (g_timing) g_timed_launches = launches;
+    return SSDC_OK;
+}
+
 }  // namespace
+
+extern "C" {
+
+size_t ssd_complex_final_state_workspace_bytes(ssdc_dims dims, int chunk_size) {
+    return check_sizes(dims, chunk_size) == SSDC_OK ? ws_bytes_for(dims, chunk_size) : 0;
+}
+
+int ssd_complex_final_state(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, const float* dt, ssdc_cin initial_state,
+                            ssdc_dims dims, int chunk_size, ssdc_cout final_state, void* workspace, size_t ws_bytes,
+                            cudaStream_t stream) {
+    return final_state_impl(x, A, B_t, dt, initial_state, dims, chunk_size, final_state, workspace, ws_bytes,
+                            stream);
+}
+
+}  // extern "C"
 
 extern "C" {
 

@@ -108,9 +108,15 @@ int fused_cluster_choice(const Problem& p, int* cl, double* cost);
 int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int force_cluster, bool plane_maps);
 
 // Fused TF32 kernel with the chunk state in tensor memory: one CTA per SM walks
-// whole sequences. Q in {16, 32, 64}; N, D multiples of 8 up to 64.
+// whole sequences. Q in {16, 32, 64, 128, 256}; N, D multiples of 8 up to 64.
 bool fused2_supported(int N, int D, int Q);
 int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bool plane_maps);
+
+// The state side of the same kernel alone (ssdc_state.cu): the final state of
+// each sequence from x, B_t and dt, without y (p.C_*, p.y_* unused). The same
+// sizes as fused2; returns launches or an error.
+bool state_supported(int N, int D, int Q);
+int state_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bool plane_maps);
 
 // Launch count reported by ssd_complex_last_launch_count() for the calling thread.
 void set_last_launch_count(int n);

@@ -447,8 +447,9 @@ int make_maps(const Problem& p, const float* ws_S, TcMaps* m) {
               (p.x_im == nullptr || make_feature_map(&m->x_im, p.x_im, 64, p.H, p.T, p.B)) &&
               make_feature_map(&m->B_re, p.B_re, 64, p.H, p.T, p.B) &&
               make_feature_map(&m->B_im, p.B_im, 64, p.H, p.T, p.B) &&
-              make_feature_map(&m->C_re, p.C_re, 64, p.H, p.T, p.B) &&
-              make_feature_map(&m->C_im, p.C_im, 64, p.H, p.T, p.B) &&
+              // (no C for the chunk states alone: ssd_complex_final_state)
+              (p.C_re == nullptr || (make_feature_map(&m->C_re, p.C_re, 64, p.H, p.T, p.B) &&
+                                     make_feature_map(&m->C_im, p.C_im, 64, p.H, p.T, p.B))) &&
               (ws_S == nullptr || make_state_map(&m->S, ws_S, (int64_t)p.B * p.H * p.nc * 2 * 64));
     return ok ? SSDC_OK : SSDC_ERR_CUDA;
 }

@@ -33,9 +33,10 @@ EXPORTS = ("ssd_complex_fwd_supported", "ssd_complex_fwd_workspace_bytes", "ssd_
            "ssd_complex_fwd_init", "ssd_complex_bwd_workspace_bytes", "ssd_complex_bwd",
            "ssd_complex_set_option", "ssd_complex_noalloc_status", "ssd_complex_last_path",
            "ssd_complex_segment_decay", "ssd_complex_state_combine", "ssd_complex_fwd_bf16",
-           "ssd_complex_fwd_mimo", "ssd_complex_fwd_mimo_workspace_bytes")
+           "ssd_complex_fwd_mimo", "ssd_complex_fwd_mimo_workspace_bytes", "ssd_complex_final_state",
+           "ssd_complex_final_state_workspace_bytes")
 
-PATHS = {0: "staged_fp32", 1: "staged_tf32", 2: "fused_cluster", 3: "fused_tmem"}
+PATHS = {0: "staged_fp32", 1: "staged_tf32", 2: "fused_cluster", 3: "fused_tmem", 4: "state_tmem"}
 
 # ssd_complex_set_option keys
 OPT_FUSED_CLUSTER = 1
@@ -117,6 +118,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_complex_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
     lib.ssd_complex_set_option.restype = ctypes.c_int
     lib.ssd_complex_segment_decay.argtypes = [ssdc_cin, vp, ssdc_dims, ssdc_cout, vp]
+    lib.ssd_complex_final_state.argtypes = [ssdc_cin, ssdc_cin, ssdc_cin, vp, ssdc_cin, ssdc_dims, ctypes.c_int,
+                                            ssdc_cout, vp, sz, vp]
+    lib.ssd_complex_final_state.restype = ctypes.c_int
+    lib.ssd_complex_final_state_workspace_bytes.argtypes = [ssdc_dims, ctypes.c_int]
+    lib.ssd_complex_final_state_workspace_bytes.restype = sz
     lib.ssd_complex_segment_decay.restype = ctypes.c_int
     lib.ssd_complex_state_combine.argtypes = [ssdc_cin, ssdc_cin, ssdc_cin, ssdc_dims, ssdc_cout, vp]
     lib.ssd_complex_state_combine.restype = ctypes.c_int
@@ -479,6 +485,53 @@ def ssd_complex_segment_decay(A_re, A_im, dt, *, a_re, a_im, stream=None) -> Non
                                           _cout(a_re, a_im), ctypes.c_void_p(s.cuda_stream))
     if rc != SSDC_OK:
         raise SSDCError(rc, "ssd_complex_segment_decay")
+
+
+def ssd_complex_final_state(x_re, x_im, A_re, A_im, B_re, B_im, dt, chunk_size, *, precision="tf32",
+                            s0_re=None, s0_im=None, fs_re, fs_im, workspace, stream=None, check=True) -> int:
+    """Call ``ssd_complex_final_state`` on torch CUDA tensors: the state the scan of
+    (x, A, B_t, dt) leaves, from the initial state (s0_re, s0_im) (None, None: zero),
+    into (fs_re, fs_im) (B,H,N,D), without y. ``workspace``: a uint8 CUDA tensor of
+    ``ssd_complex_final_state_workspace_bytes`` bytes. Returns the status."""
+    import torch
+    Bn, T, H, D = x_re.shape
+    N = B_re.shape[-1]
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = load().ssd_complex_final_state(
+        _cin(x_re, x_im), _cin(A_re, A_im), _cin(B_re, B_im), _ptr(dt), _opt_in(s0_re, s0_im),
+        dims(Bn, T, H, N, D, precision), int(chunk_size), _cout(fs_re, fs_im), _ptr(workspace),
+        int(workspace.numel()), ctypes.c_void_p(s.cuda_stream))
+    if check and rc != SSDC_OK:
+        raise SSDCError(rc, "ssd_complex_final_state")
+    return rc
+
+
+class FinalState:
+    """The state a scan leaves (ssd_complex_final_state) with its output and workspace
+    held: no allocation per call."""
+
+    def __init__(self, Bn, T, H, N, D, chunk_size, precision="tf32", device="cuda"):
+        import torch
+        self.shape = (Bn, T, H, N, D)
+        self.chunk_size = int(chunk_size)
+        self.precision = precision
+        d = dims(Bn, T, H, N, D, precision)
+        rc = ssd_complex_fwd_supported(d, chunk_size)
+        if rc != SSDC_OK:
+            raise SSDCError(rc, "ssd_complex_fwd_supported")
+        nbytes = load().ssd_complex_final_state_workspace_bytes(d, int(chunk_size))
+        self.fs_re = torch.empty((Bn, H, N, D), dtype=torch.float32, device=device)
+        self.fs_im = torch.empty((Bn, H, N, D), dtype=torch.float32, device=device)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, x_re, x_im, A_re, A_im, B_re, B_im, dt, stream=None, s0_re=None, s0_im=None):
+        ssd_complex_final_state(x_re, x_im, A_re, A_im, B_re, B_im, dt, self.chunk_size, precision=self.precision,
+                                s0_re=s0_re, s0_im=s0_im, fs_re=self.fs_re, fs_im=self.fs_im,
+                                workspace=self.workspace, stream=stream)
+        return self.fs_re, self.fs_im
+
+    def status(self, stream=None) -> int:
+        return ssd_complex_status(self.workspace, stream)
 
 
 def ssd_complex_state_combine(a_re, a_im, s_in_re, s_in_im, s_add_re, s_add_im, *, out_re, out_im,

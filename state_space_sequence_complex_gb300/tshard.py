@@ -9,20 +9,22 @@ decay a_seg = prod_t A_bar_t, so it maps S_in to a_seg S_in + S_seg, and
 consecutive segments compose as (a2, S2) o (a1, S1) = (a2 a1, a2 S1 + S2).
 Each rank therefore
 
-1. scans its segment from zero (y rows discarded) and forms (a_seg, S_seg);
+1. forms its segment's (a_seg, S_seg): S_seg is the state its segment leaves
+   from zero, without rows of y (ssd_complex_final_state); rank 0, whose
+   segment starts from the zero state, scans it in full instead, and its rows
+   are final;
 2. all-gathers the (a_seg, S_seg) of every rank (one collective);
 3. folds the aggregates of ranks 0 .. r-1, in order, into its incoming state;
-4. scans its segment again from that state (ranks r > 0; rank 0 keeps its
-   first scan) for its rows of y and the state after the segment; the last
-   rank's is the sequences' final state.
+4. scans its segment from that state (ranks r > 0) for its rows of y and the
+   state after the segment; the last rank's is the sequences' final state.
 
 Every computation runs in the backend: ``LibraryBackend`` calls libssdc
-(ssd_complex_fwd / _init, ssd_complex_segment_decay, ssd_complex_state_combine)
-on the rank's GPU; this module only orders the calls and moves one flat tensor
-per rank through the collective. Step 4 repeats step 1's scan from another
-state; a segment boundary on a chunk boundary keeps the chunking of the whole
-sequence. ``forward_segments`` runs the same steps for segments held by one
-process (no collective).
+(ssd_complex_fwd / _init, ssd_complex_final_state, ssd_complex_segment_decay,
+ssd_complex_state_combine) on the rank's GPU; this module only orders the calls
+and moves one flat tensor per rank through the collective. A segment boundary
+on a chunk boundary keeps the chunking of the whole sequence.
+``forward_segments`` runs the same steps for segments held by one process (no
+collective).
 """
 from __future__ import annotations
 
@@ -59,14 +61,25 @@ class LibraryBackend:
         m = Bn * H * N * D
         return k, m
 
-    def local(self, seg):
-        """The segment scanned from zero: its outputs (y_re, y_im, fs_re, fs_im) and
-        its aggregate (a_seg, S_seg) as one flat tensor [a_re (B H), a_im (B H),
-        S_re (B H N D), S_im (B H N D)], each plane padded to 16 bytes."""
+    def local(self, seg, rows=True):
+        """The segment from zero: its outputs (y_re, y_im, fs_re, fs_im) if ``rows``
+        (a full scan), else None (the state alone, ssd_complex_final_state), and its
+        aggregate (a_seg, S_seg) as one flat tensor [a_re (B H), a_im (B H), S_re
+        (B H N D), S_im (B H N D)], each plane padded to 16 bytes."""
         import torch
         from . import ssdc
-        out = self._forward(seg)
-        fs_re, fs_im = out[2], out[3]
+        if rows:
+            out = self._forward(seg)
+            fs_re, fs_im = out[2], out[3]
+        else:
+            out = None
+            Bn, T, H, N = seg["B_re"].shape
+            D = seg["x_re"].shape[-1]
+            f = ssdc.FinalState(Bn, T, H, N, D, self.Q, self.precision, device=seg["x_re"].device)
+            fs_re, fs_im = f(*[seg[k] for k in ("x_re", "x_im", "A_re", "A_im", "B_re", "B_im", "dt")])
+            st = f.status()
+            if st != ssdc.SSDC_OK:
+                raise ssdc.SSDCError(st, "segment state")
         shape = self.state_shape(seg)
         Bn, H = shape[0], shape[1]
         k, m = self._offsets(shape)
@@ -124,7 +137,7 @@ def forward(seg, backend, group=None):
     import torch.distributed as dist
     rank, world = dist.get_rank(group), dist.get_world_size(group)
     shape = backend.state_shape(seg)
-    out, flat = backend.local(seg)
+    out, flat = backend.local(seg, rows=rank == 0)
     flats = [torch.empty_like(flat) for _ in range(world)]
     dist.all_gather(flats, flat, group=group)
     if rank == 0:  # the first segment starts from the zero state: its local scan is final
@@ -136,7 +149,7 @@ def forward_segments(segs, backend):
     """The same steps for consecutive segments held by one process: returns the
     list of per-segment (y_re, y_im, fs_re, fs_im)."""
     shape = backend.state_shape(segs[0])
-    local = [backend.local(s) for s in segs]
+    local = [backend.local(s, rows=r == 0) for r, s in enumerate(segs)]
     flats = [f for _, f in local]
     return [local[0][0]] + [backend.rescan(s, incoming_state(backend, flats, r, shape))
                             for r, s in enumerate(segs) if r > 0]

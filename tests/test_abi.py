@@ -332,3 +332,54 @@ def test_mimo_entry_checks_before_launch(lib):
         assert _call_mimo(lib, p2, e2 + (1 << 20), dd, Q=Q, ws=e2) == ssdc.SSDC_ERR_UNSUPPORTED
     assert _call_mimo(lib, ptrs, mix, d, ws=end, ws_bytes=need) not in (
         ssdc.SSDC_ERR_INVALID, ssdc.SSDC_ERR_ALIGN, ssdc.SSDC_ERR_WORKSPACE, ssdc.SSDC_OK)
+
+
+def _call_state(lib, ptrs, d, s0=(None, None), Q=64, ws=None, ws_bytes=1 << 30):
+    # ptrs in fake_ptrs order: x (0, 1), A (2, 3), B (4, 5), C (6, 7), dt (8), y (9, 10), final state (11, 12)
+    p = ptrs
+    cin = lambda a, b: ssdc.ssdc_cin(a, b)
+    return lib.ssd_complex_final_state(cin(p[0], p[1]), cin(p[2], p[3]), cin(p[4], p[5]), p[8], cin(*s0), d, Q,
+                                       ssdc.ssdc_cout(p[11], p[12]), ws, ws_bytes, None)
+
+
+def test_final_state_entry_checks_before_launch(lib):
+    """ssd_complex_final_state: the forward's size sets, its workspace (the status word on the
+    TF32 path, the chunk states on the staged ones), every required pointer, 16-byte alignment,
+    no output overlapping an input or the workspace, and an initial state that is either apart
+    from the final state or the final state itself."""
+    d = ssdc.dims(2, 128, 4, 64, 64, "tf32")
+    ptrs, end = fake_ptrs(d)
+    need = lib.ssd_complex_final_state_workspace_bytes(d, 64)
+    assert need == 256
+    assert lib.ssd_complex_final_state_workspace_bytes(ssdc.dims(2, 128, 4, 64, 64, "fp32"), 64) == \
+        lib.ssd_complex_fwd_workspace_bytes(ssdc.dims(2, 128, 4, 64, 64, "fp32"), 64)
+    assert lib.ssd_complex_final_state_workspace_bytes(ssdc.dims(2, 128, 4, 64, 64, "tf32"), 48) == 0
+    call = lambda p=ptrs, **kw: _call_state(lib, p, d, ws=kw.pop("ws", end), **kw)
+    for i in (0, 2, 3, 4, 5, 8, 11, 12):  # x.re, A, B, dt, the final state
+        bad = list(ptrs)
+        bad[i] = None
+        assert call(bad) == ssdc.SSDC_ERR_INVALID, i
+    bad = list(ptrs)
+    bad[4] += 4
+    assert call(bad) == ssdc.SSDC_ERR_ALIGN
+    assert call(ws=None) == ssdc.SSDC_ERR_WORKSPACE
+    assert call(ws_bytes=need - 1) == ssdc.SSDC_ERR_WORKSPACE
+    bad = list(ptrs)
+    bad[11] = ptrs[4]  # the final state on top of B
+    assert call(bad) == ssdc.SSDC_ERR_INVALID
+    bad = list(ptrs)
+    bad[12] = ptrs[11] + 16  # its planes overlapping
+    assert call(bad) == ssdc.SSDC_ERR_INVALID
+    s0 = (end + (4 << 20), end + (8 << 20))
+    assert call(s0=(s0[0], None)) == ssdc.SSDC_ERR_INVALID
+    assert call(s0=(ptrs[11] + 16, s0[1])) == ssdc.SSDC_ERR_INVALID  # part of the final state
+    assert call(s0=(end, s0[1])) == ssdc.SSDC_ERR_INVALID            # inside the workspace
+    assert _call_state(lib, ptrs, d, Q=48, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
+    # C and y are not arguments: their fake addresses may hold anything; a real x, the final
+    # state as its own initial state and a separate one pass the argument checks (without a GPU
+    # the call then fails on the device)
+    real = list(ptrs)
+    real[1] = None
+    for p, s in ((real, (None, None)), (ptrs, (ptrs[11], ptrs[12])), (ptrs, s0)):
+        assert _call_state(lib, p, d, s0=s, ws=end, ws_bytes=need) not in (
+            ssdc.SSDC_ERR_INVALID, ssdc.SSDC_ERR_ALIGN, ssdc.SSDC_ERR_WORKSPACE, ssdc.SSDC_OK)

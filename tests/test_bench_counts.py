@@ -19,6 +19,9 @@ def test_forward_bytes_bf16_and_real_x():
     assert bench.input_bytes_per_unit(w, real_x=True) == 2068 - 256
     assert bench.input_bytes_per_unit(w, bf16=True, real_x=True) == 1300 - 128
     assert bench.input_bytes_per_unit(w) == 2068
+    # the final state alone reads x (512), B_t (512) and dt (4) and writes the state once per sequence
+    assert bench.input_bytes_per_unit(w, state_only=True) == 512 + 512 + 4 + 8 * 64 * 64 / 2048 == 1044
+    assert bench.input_bytes_per_unit(w, state_only=True, real_x=True) == 1044 - 256
 
 
 def test_forward_flops_per_token_head():

@@ -11,7 +11,8 @@ launches of varying size in between (which shift the timing of the CTAs
 against each other), and every output must equal the first run's bit for
 bit. Cases: the cluster kernel at 1, 2, 4 and 8 CTAs per sequence (with and
 without an initial state), the tensor-memory kernel at every chunk size, its
-bfloat16-input and fused head-mixer instances, and the staged TF32 path.
+bfloat16-input and fused head-mixer instances, the final state alone
+(ssd_complex_final_state), and the staged TF32 path.
 """
 import numpy as np
 import pytest
@@ -114,3 +115,12 @@ def test_staged_tf32_repeats_bit_for_bit():
     inp = inputs.custom(4, 1000, 16, 64, 64, seed=70)
     call, status = forward_call(inp, 128, "tf32_staged")
     repeat_identical(call, status, "staged_tf32")
+
+
+@pytest.mark.parametrize("Q", [64, 256])
+def test_final_state_alone_repeats_bit_for_bit(Q):
+    inp = inputs.custom(20, 1000, 16, 64, 64, seed=80 + Q)
+    t = to_device(inp)
+    f = ssdc.FinalState(*inp.dims, Q, "tf32")
+    repeat_identical(lambda: f(*[t[k] for k in ("x_re", "x_im", "A_re", "A_im", "B_re", "B_im", "dt")]), f.status,
+                     "state_tmem")

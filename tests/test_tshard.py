@@ -40,12 +40,12 @@ class OracleBackend:
         return self.scan(seg["x_re"], seg["x_im"], seg["A_re"], seg["A_im"], seg["B_re"], seg["B_im"],
                          seg["C_re"], seg["C_im"], seg["dt"], s0=s0, threads=1)
 
-    def local(self, seg):
+    def local(self, seg, rows=True):
         y, s = self._run(seg)
         sp = np.logaddexp(0.0, seg["dt"].astype(np.float64)).sum(axis=1)  # (B, H)
         a = np.exp(sp * (seg["A_re"].astype(np.float64) + 1j * seg["A_im"].astype(np.float64)))
         flat = torch.from_numpy(np.concatenate([a.real.ravel(), a.imag.ravel(), s.real.ravel(), s.imag.ravel()]))
-        return (y, s), flat
+        return ((y, s) if rows else None), flat
 
     @staticmethod
     def unpack(flat, shape):
