@@ -46,14 +46,16 @@
  * workspace and reported by ssd_complex_status().
  *
  * Precision. SSDC_PREC_TF32 runs the chunk contractions on the tcgen05 tensor
- * cores with TF32 operands and fp32 accumulation; for Q = 64, N = D = 64 it
- * is one fused kernel that passes the chunk states between the CTAs of a
- * thread-block cluster through distributed shared memory, otherwise the
- * staged path below. SSDC_PREC_TF32_STAGED is the same arithmetic as three
- * kernels (chunk states, state pass, chunk outputs) with the per-chunk states
- * staged in the workspace. SSDC_PREC_FP32 runs every step in exact fp32 on
- * the SIMT cores (the checking variant), staged the same way. The state pass
- * between chunks is fp32 in all three.
+ * cores with TF32 operands and fp32 accumulation, in one fused launch: a
+ * kernel whose CTAs each walk whole sequences with the chunk state held in
+ * tensor memory (every supported size), or, for fewer sequences than SMs at
+ * Q = N = D = 64, one that deals each sequence's chunks over the CTAs of a
+ * thread-block cluster and passes the states through distributed shared
+ * memory (ssd_complex_last_path() reports which ran). SSDC_PREC_TF32_STAGED
+ * is the same arithmetic as three kernels (chunk states, state pass, chunk
+ * outputs) with the per-chunk states staged in the workspace. SSDC_PREC_FP32
+ * runs every step in exact fp32 on the SIMT cores (the checking variant),
+ * staged the same way. The state pass between chunks is fp32 in all three.
  */
 #ifndef SSDC_H
 #define SSDC_H
@@ -184,8 +186,10 @@ int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_ci
  * the same matrix for every feature d. Only the mixed Re(y) is written (no
  * y.im, no separate Re(y)), so y does not make a round trip through memory
  * before the mixer. The tiles of Re(y) of one batch row and 64-token tile from
- * all H heads meet in `out`; the CTA that stores the last of them mixes them
- * in place (no CTA waits for another).
+ * all H heads meet in `out` and are counted there; once all H are stored, the
+ * CTA of head h mixes the h-th 1/H of the tile's tokens in place. A CTA mixes
+ * its ready shares after each tile it stores, and waits (bounded) only for the
+ * shares still open after its sequence's last tile.
  *
  *   mix             (H, H) fp32 device array, row g = output head g; required
  *   out             (B, T, H, D) fp32 device array, 16-byte aligned
