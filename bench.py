@@ -687,7 +687,12 @@ def main():
     if args.backward:
         if args.impl == "reference" or args.segments > 1:
             raise SystemExit("the backward measurement runs with --impl ours, unsegmented")
-        backward_workload(args, inputs.ALL[args.workload])
+        w = inputs.ALL[args.workload]
+        if args.layers > 0:
+            w = w.with_(layers=args.layers)
+        if args.batch > 0:
+            w = w.with_(B=args.batch)
+        backward_workload(args, w)
         return
     if (args.workload != "layer" or args.segments > 1 or args.real_x or args.batch > 0 or args.bf16 or args.mimo
             or args.state_only):

@@ -144,53 +144,10 @@ ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw) {
 // becomes S_in[c] (the forward's state pass, from the initial state) and the
 // final state is written; backwards, U_c in its slot becomes R_c (the
 // gradient of the state leaving chunk c) and conj(a_0) R_0 + U_0 is the
-// initial-state gradient. The loads do not depend on the chain, so they are
-// issued a group of chunks ahead.
+// initial-state gradient. Both are chain_walk (ssdc_kernels.h): forwards with
+// a_c, backwards with conj(a_c).
 
-constexpr int kPassAhead = 8;
-
-// backwards: R_{c-1} = conj(a_c) R_c + U_c, lane j of sequence bh
-__device__ __forceinline__ void adjoint_chain(const GradProblem& g, const GradWorkspace& gw,
-                                              const float* a, int64_t bh, int64_t nc, int ND, int j,
-                                              int64_t o) {
-    float* R = gw.R + bh * nc * 2 * ND + j;
-    float rr = 0.0f, ri = 0.0f;
-    if (g.dfs_re != nullptr) {
-        rr = g.dfs_re[o];
-        ri = g.dfs_im[o];
-    }
-    for (int64_t c1 = nc - 1; c1 >= 0; c1 -= kPassAhead) {
-        float ur[kPassAhead], ui[kPassAhead], ar[kPassAhead], ai[kPassAhead];
-#pragma unroll
-        for (int k = 0; k < kPassAhead; ++k) {
-            const int64_t c = c1 - k;
-            if (c >= 0) {
-                ur[k] = __ldcg(R + c * 2 * ND);
-                ui[k] = __ldcg(R + c * 2 * ND + ND);
-                ar[k] = __ldg(a + 2 * c);
-                ai[k] = __ldg(a + 2 * c + 1);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kPassAhead; ++k) {
-            const int64_t c = c1 - k;
-            if (c >= 0) {
-                __stcg(R + c * 2 * ND, rr);
-                __stcg(R + c * 2 * ND + ND, ri);
-                const float nr = fmaf(ar[k], rr, fmaf(ai[k], ri, ur[k]));
-                const float ni = fmaf(ar[k], ri, fmaf(-ai[k], rr, ui[k]));
-                rr = nr;
-                ri = ni;
-            }
-        }
-    }
-    if (g.ds0_re != nullptr) {
-        g.ds0_re[o] = rr;
-        g.ds0_im[o] = ri;
-    }
-}
-
-__global__ void __launch_bounds__(kPassThreads)
+__global__ void __launch_bounds__(kPassThreads, 4)
 ssdc_bwd_passes(GradProblem g, Workspace ws, GradWorkspace gw) {
     const Problem& p = g.f;
     const int64_t bh = blockIdx.y;
@@ -203,41 +160,24 @@ ssdc_bwd_passes(GradProblem g, Workspace ws, GradWorkspace gw) {
     const float* a = ws.a + bh * nc * 2;
     const int d = j / p.N, n = j % p.N;
     const int64_t o = (bh * p.N + n) * p.D + d;  // (b, h, n, d) of the state arrays
-    if (backwards) {
-        adjoint_chain(g, gw, a, bh, nc, ND, j, o);
-        return;
+    float* X = (backwards ? gw.R : ws.S) + bh * nc * 2 * ND + j;
+    const float* x0r = backwards ? g.dfs_re : p.s0_re;
+    const float* x0i = backwards ? g.dfs_im : p.s0_im;
+    float xr = 0.0f, xi = 0.0f;
+    if (x0r != nullptr) {
+        xr = x0r[o];
+        xi = x0i[o];
     }
-
-    // forwards: S_in[c+1] = a_c S_in[c] + S_loc[c]
-    float* S = ws.S + bh * nc * 2 * ND + j;
-    float sr = 0.0f, si = 0.0f;
-    if (p.s0_re != nullptr) {
-        sr = p.s0_re[o];
-        si = p.s0_im[o];
+    const float2 xo = chain_walk(X, a, nc, ND, backwards, make_float2(xr, xi));
+    xr = xo.x;
+    xi = xo.y;
+    // the final state, or the initial-state gradient conj(a_0) R_0 + U_0
+    float* outr = backwards ? g.ds0_re : p.fs_re;
+    float* outi = backwards ? g.ds0_im : p.fs_im;
+    if (outr != nullptr) {
+        outr[o] = xr;
+        outi[o] = xi;
     }
-    for (int64_t c0 = 0; c0 < nc; c0 += kPassAhead) {
-        float lr[kPassAhead], li[kPassAhead], ar[kPassAhead], ai[kPassAhead];
-#pragma unroll
-        for (int k = 0; k < kPassAhead; ++k)
-            if (c0 + k < nc) {
-                lr[k] = __ldcg(S + (c0 + k) * 2 * ND);
-                li[k] = __ldcg(S + (c0 + k) * 2 * ND + ND);
-                ar[k] = __ldg(a + 2 * (c0 + k));
-                ai[k] = __ldg(a + 2 * (c0 + k) + 1);
-            }
-#pragma unroll
-        for (int k = 0; k < kPassAhead; ++k)
-            if (c0 + k < nc) {
-                __stcg(S + (c0 + k) * 2 * ND, sr);
-                __stcg(S + (c0 + k) * 2 * ND + ND, si);
-                const float nr = fmaf(ar[k], sr, fmaf(-ai[k], si, lr[k]));
-                const float ni = fmaf(ar[k], si, fmaf(ai[k], sr, li[k]));
-                sr = nr;
-                si = ni;
-            }
-    }
-    p.fs_re[o] = sr;
-    p.fs_im[o] = si;
 }
 
 // ---------------------------------------------------------------------------

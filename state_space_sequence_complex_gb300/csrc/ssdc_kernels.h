@@ -90,6 +90,61 @@ void simt_launch_chunk_scan(const Problem& p, const Workspace& ws, cudaStream_t 
 __global__ void ssdc_state_pass(Problem p, Workspace ws);
 constexpr int kPassThreads = 256;
 
+// One lane of a chunk recurrence: x <- a_c x + l_c over the nc chunks of one
+// sequence, l_c at X + c * 2 ND (real plane) and + ND (imaginary plane), each
+// replaced in its slot by the x entering the step; a_c at a + 2 c. Step k is
+// chunk k, or chunk nc - 1 - k with `backwards`, whose coefficient is conj(a_c).
+// The loads do not depend on the chain, so kPassAhead chunks' loads stay in
+// flight: a slot is refilled, with the chunk kPassAhead steps on (a slot not yet
+// written), as soon as its chunk is consumed. x is the incoming value; the
+// last is returned.
+constexpr int kPassAhead = 8;
+__device__ __forceinline__ float2 chain_walk(float* X, const float* a, int64_t nc, int ND, bool backwards,
+                                             float2 x) {
+    float xr = x.x, xi = x.y;
+    const float sg = backwards ? -1.0f : 1.0f;
+    auto chunk_of = [&](int64_t k) { return backwards ? nc - 1 - k : k; };
+    float lr[kPassAhead], li[kPassAhead], ar[kPassAhead], ai[kPassAhead];
+#pragma unroll
+    for (int k = 0; k < kPassAhead; ++k)
+        if (k < nc) {
+            const int64_t c = chunk_of(k);
+            lr[k] = __ldcg(X + c * 2 * ND);
+            li[k] = __ldcg(X + c * 2 * ND + ND);
+            ar[k] = __ldg(a + 2 * c);
+            ai[k] = sg * __ldg(a + 2 * c + 1);
+        }
+#pragma unroll 1
+    for (int64_t k0 = 0; k0 < nc; k0 += kPassAhead) {
+#pragma unroll
+        for (int k = 0; k < kPassAhead; ++k) {
+            if (k0 + k < nc) {
+                const int64_t c = chunk_of(k0 + k);
+                __stcg(X + c * 2 * ND, xr);
+                __stcg(X + c * 2 * ND + ND, xi);
+                const float nr = fmaf(ar[k], xr, fmaf(-ai[k], xi, lr[k]));
+                const float ni = fmaf(ar[k], xi, fmaf(ai[k], xr, li[k]));
+                xr = nr;
+                xi = ni;
+            }
+            if (k0 + k + kPassAhead < nc) {
+                const int64_t c = chunk_of(k0 + k + kPassAhead);
+                lr[k] = __ldcg(X + c * 2 * ND);
+                li[k] = __ldcg(X + c * 2 * ND + ND);
+                ar[k] = __ldg(a + 2 * c);
+                ai[k] = sg * __ldg(a + 2 * c + 1);
+            }
+        }
+    }
+    return make_float2(xr, xi);
+}
+// The same, not inlined, for a caller whose direction is fixed: a direction known
+// at compile time let the compiler hold more addresses than registers.
+static __device__ __noinline__ float2 chain_walk_call(float* X, const float* a, int64_t nc, int ND, bool backwards,
+                                                      float2 x) {
+    return chain_walk(X, a, nc, ND, backwards, x);
+}
+
 // tcgen05 / TMA kernels (TF32 tensor cores). Returns the number of launches
 // enqueued, or a negative SSDC_ERR_* code.
 int tc_launch_chunk_state(const Problem& p, const Workspace& ws, cudaStream_t stream);

@@ -7,18 +7,16 @@
 //
 // This is the sequential form of the pages' "decay_chunk matrix" recurrence.
 // One thread owns one complex (d, n) lane of one (b, h) sequence and walks its
-// chunks in order, replacing S_loc[c] in the workspace by S_in[c]. The loads
-// of S_loc do not depend on the chain, so they are issued a group of chunks
-// ahead; only the complex multiply-add is serial. fp32 throughout.
+// chunks in order, replacing S_loc[c] in the workspace by S_in[c] (chain_walk:
+// the loads of S_loc do not depend on the chain and stay a window of chunks
+// ahead; only the complex multiply-add is serial). fp32 throughout.
 #include <cuda_runtime.h>
 
 #include "ssdc_kernels.h"
 
 namespace ssdc {
 
-constexpr int kPassAhead = 8;
-
-__global__ void __launch_bounds__(kPassThreads)
+__global__ void __launch_bounds__(kPassThreads, 4)
 ssdc_state_pass(Problem p, Workspace ws) {
     const int64_t bh = blockIdx.y;
     const int ND = p.N * p.D;
@@ -34,31 +32,9 @@ ssdc_state_pass(Problem p, Workspace ws) {
         sr = p.s0_re[o];
         si = p.s0_im[o];
     }
-    for (int64_t c0 = 0; c0 < nc; c0 += kPassAhead) {
-        float lr[kPassAhead], li[kPassAhead], ar[kPassAhead], ai[kPassAhead];
-#pragma unroll
-        for (int k = 0; k < kPassAhead; ++k) {
-            if (c0 + k < nc) {
-                const float* s = S + (c0 + k) * 2 * ND;
-                lr[k] = __ldcg(s);
-                li[k] = __ldcg(s + ND);
-                ar[k] = __ldg(a + 2 * (c0 + k));
-                ai[k] = __ldg(a + 2 * (c0 + k) + 1);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kPassAhead; ++k) {
-            if (c0 + k < nc) {
-                float* s = S + (c0 + k) * 2 * ND;
-                __stcg(s, sr);
-                __stcg(s + ND, si);
-                const float nr = fmaf(ar[k], sr, fmaf(-ai[k], si, lr[k]));
-                const float ni = fmaf(ar[k], si, fmaf(ai[k], sr, li[k]));
-                sr = nr;
-                si = ni;
-            }
-        }
-    }
+    const float2 so = chain_walk_call(S, a, nc, ND, false, make_float2(sr, si));
+    sr = so.x;
+    si = so.y;
     p.fs_re[o] = sr;
     p.fs_im[o] = si;
 }
