@@ -660,14 +660,23 @@ int make_maps(const GradProblem& g, BwdMaps* m) {
 // A operands are TMEM windows (x^T, dY^T) read from the stacked tiles by
 // column; B operands are the B and C tiles transposed in place (rows n, K =
 // the token), the decay and the conjugation applied as they are written.
+//
+// One CTA per SM walks chunks blockIdx.x, blockIdx.x + grid, ...: x and dY are
+// free once the windows are built (early in a chunk), so the next chunk's x and
+// dY load during this chunk's transposes, products and output; B and C, which
+// the products read, have two stages, so the next chunk's B and C load during
+// this whole chunk. Every wait is on a barrier's parity for the chunk (or the
+// stage's use), bounded.
 
 struct StatesSmem {
     float x[64 * 128];  // x, stacked (rows s)
-    float b[64 * 128];  // B, stacked; then (dec o B)^T in place (rows n, K = s)
-    float y[64 * 128];  // dY, stacked (rows l)
-    float c[64 * 128];  // C, stacked; then conj(C')^T in place (rows n, K = l)
-    float2 acs[64], dec[64], eacs[64];
-    uint64_t full, ready, done;
+    float y[64 * 128];     // dY, stacked (rows l)
+    float b[2][64 * 128];  // [stage] B, stacked; then (dec o B)^T in place (rows n, K = s)
+    float c[2][64 * 128];  // [stage] C, stacked; then conj(C')^T in place (rows n, K = l)
+    float2 acs[2][64];     // [chunk parity]
+    float2 dec[64], eacs[64];
+    uint64_t full_xy, xy_free, ready, done, acc_free;
+    uint64_t full_bc[2], bc_free[2];  // [stage]
     uint32_t tmem;
 };
 
@@ -687,11 +696,8 @@ bwd_states_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H, N = p.N, D = p.D, Q = p.Q;
     const int64_t nc = p.nc;
-    const int64_t chunk = blockIdx.x;  // (b H + h) nc + c
-    const int c = (int)(chunk % nc);
-    const int64_t bh = chunk / nc;
-    const int b = (int)(bh / H), h = (int)(bh % H);
-    const int64_t t0 = (int64_t)c * Q;
+    const int64_t nchunks = (int64_t)p.B * H * nc;
+    const int64_t mine = (int64_t)blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int rows = Q < kQ ? Q : kQ;
     constexpr uint32_t kS = 0, kU = 128, kWx = 256, kWy = 320;
 
@@ -700,18 +706,26 @@ bwd_states_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_consta
         return;
     }
     if (tid == 0) {
-        ptx::mbar_init(&sm.full, 1);
+        ptx::mbar_init(&sm.full_xy, 1);
+        ptx::mbar_init(&sm.xy_free, kWorkerWarps);
+        for (int st = 0; st < 2; ++st) {
+            ptx::mbar_init(&sm.full_bc[st], 1);
+            ptx::mbar_init(&sm.bc_free[st], 1);
+        }
         ptx::mbar_init(&sm.ready, kWorkerWarps);
         ptx::mbar_init(&sm.done, 1);
+        ptx::mbar_init(&sm.acc_free, kWorkerWarps);
         ptx::fence_mbar_init();
     }
     if (warp == 0) {
         ptx::tmem_alloc(&sm.tmem, kTmemCols);
         ptx::tmem_relinquish();
     }
-    if (Q < kQ || mp.real_x || mp.real_dy) {
+    {
+        // rows past Q and the planes of a real x or dY are never loaded: zero (x and dY are only
+        // read, so they stay zero; the rows past Q of B and C meet zero window columns)
         float4* z = reinterpret_cast<float4*>(sm.x);
-        constexpr int kVecs = 4 * 64 * 128 / 4;  // the four tiles
+        constexpr int kVecs = 6 * 64 * 128 / 4;  // the six tiles
         for (int i = tid; i < kVecs; i += kThreads) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         ptx::fence_proxy_async_smem();
     }
@@ -719,39 +733,75 @@ bwd_states_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_consta
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem;
+    auto chunk_at = [&](int64_t k) { return (int64_t)blockIdx.x + k * gridDim.x; };
 
     if (warp == kProducer) {
-        const Alog al = load_alog(p, b, h, t0, lane, rows);
-        if (lane == 0) {
-            const uint32_t planes = 8u - (mp.real_x ? 1u : 0u) - (mp.real_dy ? 1u : 0u);
-            ptx::mbar_expect_tx(&sm.full, (uint32_t)rows * 256u * planes);
-        }
-        __syncwarp();
-        if (lane < 16) {  // tensor (x, B, dY, C), 32-column half, plane
-            const int which = lane >> 2, half = (lane >> 1) & 1, pl = lane & 1;
-            const bool skip = pl == 1 && ((which == 0 && mp.real_x) || (which == 2 && mp.real_dy));
-            if (!skip) {
-                float* tiles[4] = {sm.x, sm.b, sm.y, sm.c};
-                const CUtensorMap* maps[4][2] = {{&mp.x_re, &mp.x_im}, {&mp.b_re, &mp.b_im},
-                                                 {&mp.y_re, &mp.y_im}, {&mp.c_re, &mp.c_im}};
-                char* dst = reinterpret_cast<char*>(tiles[which]) + half * kIntHalf + pl * kHalfBytes;
-                ptx::tma_load_4d(dst, maps[which][pl], &sm.full, 32 * half, h, (int)t0, b);
-            }
-        }
-        store_acs(sm.acs, &sm.full, al, lane);
-    } else if (warp == kIssuer) {
-        if (lane == 0) {
-            bool ok = true;
-            if (!ptx::mbar_wait(&sm.ready, 0u, kWaitIters)) {
+        bool ok = true;
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (lane == 0 && ok && !ptx::mbar_wait(bar, parity, kWaitIters)) {
                 fail(ws.status);
                 ok = false;
             }
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_ts128(tmem + kS, tmem + kWx, desc128(ptx::smem_addr(sm.b)), false);  // x^T (dec o B)
-                issue_ts128(tmem + kU, tmem + kWy, desc128(ptx::smem_addr(sm.c)), false);  // dY^T conj(C')
+            __syncwarp();
+        };
+        // tensor `which` (x, B, dY, C) of chunk (b, h, t0) into its tile (B and C: stage st):
+        // lanes (32-column half, plane)
+        auto load = [&](int which, int st, int b, int h, int64_t t0) {
+            if (lane < 4) {
+                const int half = lane >> 1, pl = lane & 1;
+                const bool skip = pl == 1 && ((which == 0 && mp.real_x) || (which == 2 && mp.real_dy));
+                if (!skip) {
+                    float* tiles[4] = {sm.x, sm.b[st], sm.y, sm.c[st]};
+                    const CUtensorMap* maps[4][2] = {{&mp.x_re, &mp.x_im}, {&mp.b_re, &mp.b_im},
+                                                     {&mp.y_re, &mp.y_im}, {&mp.c_re, &mp.c_im}};
+                    char* dst = reinterpret_cast<char*>(tiles[which]) + half * kIntHalf + pl * kHalfBytes;
+                    ptx::tma_load_4d(dst, maps[which][pl], which == 0 || which == 2 ? &sm.full_xy : &sm.full_bc[st],
+                                     32 * half, h, (int)t0, b);
+                }
             }
+        };
+        for (int64_t k = 0; k < mine; ++k) {
+            const int64_t chunk = chunk_at(k);
+            const int64_t bh = chunk / nc;
+            const int b = (int)(bh / H), h = (int)(bh % H);
+            const int64_t t0 = (chunk % nc) * Q;
+            const uint32_t pp = (uint32_t)(k - 1) & 1u;  // the previous chunk's parity (x and dY)
+            // x and dY: after the previous chunk's windows are built
+            if (k > 0) wait(&sm.xy_free, pp);
+            const Alog al = load_alog(p, b, h, t0, lane, rows);
+            if (lane == 0) {
+                const uint32_t planes = 4u - (mp.real_x ? 1u : 0u) - (mp.real_dy ? 1u : 0u);
+                ptx::mbar_expect_tx(&sm.full_xy, (uint32_t)rows * 256u * planes);
+            }
+            __syncwarp();
+            load(0, 0, b, h, t0);
+            load(2, 0, b, h, t0);
+            store_acs(sm.acs[k & 1], &sm.full_xy, al, lane);
+            // B and C into stage k & 1: after the products of chunk k - 2, its previous use
+            const int st = (int)(k & 1);
+            if (k >= 2) wait(&sm.bc_free[st], (uint32_t)((k >> 1) - 1) & 1u);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full_bc[st], (uint32_t)rows * 256u * 4u);
+            __syncwarp();
+            load(1, st, b, h, t0);
+            load(3, st, b, h, t0);
+        }
+    } else if (warp == kIssuer) {
+        bool ok = true;
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (ok && !ptx::mbar_wait(bar, parity, kWaitIters)) {
+                fail(ws.status);
+                ok = false;
+            }
+        };
+        for (int64_t k = 0; k < mine && lane == 0; ++k) {
+            wait(&sm.ready, (uint32_t)k & 1u);
+            if (k > 0) wait(&sm.acc_free, (uint32_t)(k - 1) & 1u);  // the accumulators were read out
+            ptx::tc_fence_after();
+            const int st = (int)(k & 1);
+            issue_ts128(tmem + kS, tmem + kWx, desc128(ptx::smem_addr(sm.b[st])), false);  // x^T (dec o B)
+            issue_ts128(tmem + kU, tmem + kWy, desc128(ptx::smem_addr(sm.c[st])), false);  // dY^T conj(C')
             ptx::mma_commit(&sm.done);
+            ptx::mma_commit(&sm.bc_free[st]);
         }
         __syncwarp();
     } else {
@@ -762,19 +812,14 @@ bwd_states_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_consta
         const int wr = 16 * qd + 8 * (lane >> 4) + (lane & 7), wp = (lane >> 3) & 1, wc = warp >> 2;
         const uint32_t wl = lane_base(tmem, warp);
         char* xb = reinterpret_cast<char*>(sm.x);
-        char* bb = reinterpret_cast<char*>(sm.b);
         char* yb = reinterpret_cast<char*>(sm.y);
-        char* cb = reinterpret_cast<char*>(sm.c);
         bool ok = true;
-        if (!ptx::mbar_wait(&sm.full, 0u, kWaitIters)) {
-            fail(ws.status);
-            ok = false;
-        }
-        if (tid < 2 * kQ) {
-            const int t = tid % kQ;
-            if (tid < kQ) sm.dec[t] = t < Q ? cexp_fast(cdiff(sm.acs[Q - 1], sm.acs[t])) : make_float2(0.0f, 0.0f);
-            else sm.eacs[t] = cexp_fast(sm.acs[t]);
-        }
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (ok && !ptx::mbar_wait(bar, parity, kWaitIters)) {
+                fail(ws.status);
+                ok = false;
+            }
+        };
         // windows x^T and dY^T: row wr (d), column k (token) = plane wp of T[k][wr] from a stacked
         // tile; plane-1 lanes read row k ^ 4 (the planes' rows share banks)
         auto window = [&](const char* src, uint32_t col0) {
@@ -785,74 +830,98 @@ bwd_states_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_consta
             for (int k = 0; k < 16; ++k) v[k] = ptx::to_tf32(wp ? r[k ^ 4] : r[k]);
             ptx::tmem_st16(wl + col0 + 16 * wc, v);
         };
-        window(xb, kWx);
-        window(yb, kWy);
-        // B and C blocks: rows s = 4 bsb + i, columns n = 4 bnb + 2 bjh + {0, 1}, both planes
         const int L0 = lane & 1, L1 = (lane >> 1) & 1, L2 = (lane >> 2) & 1, L3 = (lane >> 3) & 1, L4 = lane >> 4;
         const int bjh = L1, bsb = L2 + 2 * (warp >> 1), bnb = L0 + 2 * L3 + 4 * L4 + 8 * (warp & 1);
-        float2 bv[2][4], cv[2][4];
-#pragma unroll
-        for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int sr = 4 * bsb + i, n = 4 * bnb + 2 * bjh;
-                bv[pp][i] = make_float2(ld(bb, stk(pp, sr, n)), ld(bb, stk(pp, sr, n + 1)));
-                cv[pp][i] = make_float2(ld(cb, stk(pp, sr, n)), ld(cb, stk(pp, sr, n + 1)));
+        for (int64_t k = 0; k < mine; ++k) {
+            const int64_t chunk = chunk_at(k);
+            const uint32_t ph = (uint32_t)k & 1u;
+            // ---- the chunk's decay tables and windows (the previous chunk's products, which read
+            // the windows, are done: this warp waited for them before its output stage)
+            wait(&sm.full_xy, ph);
+            if (tid < 2 * kQ) {
+                const float2* acs = sm.acs[k & 1];
+                const int t = tid % kQ;
+                if (tid < kQ) sm.dec[t] = t < Q ? cexp_fast(cdiff(acs[Q - 1], acs[t])) : make_float2(0.0f, 0.0f);
+                else sm.eacs[t] = cexp_fast(acs[t]);
             }
-        ptx::named_sync(kWorkerBar, kWorkers);  // every B and C read is done; the tables are written
+            window(xb, kWx);
+            window(yb, kWy);
+            ptx::tmem_wait_st();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.xy_free);  // this warp is done with x and dY
+            // ---- B and C blocks (stage k & 1): rows s = 4 bsb + i, columns n = 4 bnb + 2 bjh + {0, 1}
+            const int st = (int)(k & 1);
+            char* bb = reinterpret_cast<char*>(sm.b[st]);
+            char* cb = reinterpret_cast<char*>(sm.c[st]);
+            wait(&sm.full_bc[st], (uint32_t)(k >> 1) & 1u);
+            float2 bv[2][4], cv[2][4];
 #pragma unroll
-        for (int jn = 0; jn < 2; ++jn) {  // column n -> row n of the transposed tiles
-            const int nr = 4 * bnb + 2 * bjh + jn;
-            float br[4], bi[4], cr[4], ci[4];
+            for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int sr = 4 * bsb + i;
-                const float2 bvv = jn ? make_float2(bv[0][i].y, bv[1][i].y) : make_float2(bv[0][i].x, bv[1][i].x);
-                const float2 cvv = jn ? make_float2(cv[0][i].y, cv[1][i].y) : make_float2(cv[0][i].x, cv[1][i].x);
-                const float2 db = cmul(sm.dec[sr], bvv);   // dec o B
-                const float2 ce = cmul(sm.eacs[sr], cvv);  // C' = exp(Acs) o C, conjugated below
-                br[i] = ptx::to_tf32(db.x);
-                bi[i] = ptx::to_tf32(db.y);
-                cr[i] = ptx::to_tf32(ce.x);
-                ci[i] = ptx::to_tf32(-ce.y);
+                for (int i = 0; i < 4; ++i) {
+                    const int sr = 4 * bsb + i, n = 4 * bnb + 2 * bjh;
+                    bv[pp][i] = make_float2(ld(bb, stk(pp, sr, n)), ld(bb, stk(pp, sr, n + 1)));
+                    cv[pp][i] = make_float2(ld(cb, stk(pp, sr, n)), ld(cb, stk(pp, sr, n + 1)));
+                }
+            ptx::named_sync(kWorkerBar, kWorkers);  // every B and C read is done; the tables are written
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn) {  // column n -> row n of the transposed tiles
+                const int nr = 4 * bnb + 2 * bjh + jn;
+                float br[4], bi[4], cr[4], ci[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int sr = 4 * bsb + i;
+                    const float2 bvv = jn ? make_float2(bv[0][i].y, bv[1][i].y) : make_float2(bv[0][i].x, bv[1][i].x);
+                    const float2 cvv = jn ? make_float2(cv[0][i].y, cv[1][i].y) : make_float2(cv[0][i].x, cv[1][i].x);
+                    const float2 db = cmul(sm.dec[sr], bvv);   // dec o B
+                    const float2 ce = cmul(sm.eacs[sr], cvv);  // C' = exp(Acs) o C, conjugated below
+                    br[i] = ptx::to_tf32(db.x);
+                    bi[i] = ptx::to_tf32(db.y);
+                    cr[i] = ptx::to_tf32(ce.x);
+                    ci[i] = ptx::to_tf32(-ce.y);
+                }
+                *reinterpret_cast<float4*>(bb + stk(0, nr, 4 * bsb)) = make_float4(br[0], br[1], br[2], br[3]);
+                *reinterpret_cast<float4*>(bb + stk(1, nr, 4 * bsb)) = make_float4(bi[0], bi[1], bi[2], bi[3]);
+                *reinterpret_cast<float4*>(cb + stk(0, nr, 4 * bsb)) = make_float4(cr[0], cr[1], cr[2], cr[3]);
+                *reinterpret_cast<float4*>(cb + stk(1, nr, 4 * bsb)) = make_float4(ci[0], ci[1], ci[2], ci[3]);
             }
-            *reinterpret_cast<float4*>(bb + stk(0, nr, 4 * bsb)) = make_float4(br[0], br[1], br[2], br[3]);
-            *reinterpret_cast<float4*>(bb + stk(1, nr, 4 * bsb)) = make_float4(bi[0], bi[1], bi[2], bi[3]);
-            *reinterpret_cast<float4*>(cb + stk(0, nr, 4 * bsb)) = make_float4(cr[0], cr[1], cr[2], cr[3]);
-            *reinterpret_cast<float4*>(cb + stk(1, nr, 4 * bsb)) = make_float4(ci[0], ci[1], ci[2], ci[3]);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.ready);
-        if (ok && !ptx::mbar_wait(&sm.done, 0u, kWaitIters)) fail(ws.status);
-        ptx::tc_fence_after();
-        // S_loc^T and U^T rows d = rr: Re = A0 B0 - A1 B1, Im = A0 B1 + A1 B0
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.ready);
+            // ---- output: S_loc^T and U^T rows d = rr: Re = A0 B0 - A1 B1, Im = A0 B1 + A1 B0
+            wait(&sm.done, ph);
+            ptx::tc_fence_after();
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            float ga[16], gb[16];
-            ptx::tmem_ld_16x256b_x4(tl + (which ? kU : kS) + 32 * kh, ga);
-            ptx::tmem_ld_16x256b_x4(tl + (which ? kU : kS) + 64 + 32 * kh, gb);
-            ptx::tmem_wait_ld();
-            float* out = (which ? gw.R : ws.S) + chunk * 2 * (int64_t)D * N;
-            if (rr < D) {
+            for (int which = 0; which < 2; ++which) {
+                float ga[16], gb[16];
+                ptx::tmem_ld_16x256b_x4(tl + (which ? kU : kS) + 32 * kh, ga);
+                ptx::tmem_ld_16x256b_x4(tl + (which ? kU : kS) + 64 + 32 * kh, gb);
+                ptx::tmem_wait_ld();
+                float* out = (which ? gw.R : ws.S) + chunk * 2 * (int64_t)D * N;
+                if (rr < D) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int n = 32 * kh + 8 * j + 2 * lq;
-                    if (n < N) {  // N is a multiple of 8: n + 1 < N too
-                        *reinterpret_cast<float2*>(out + rr * N + n) =
-                            make_float2(ga[4 * j] - gb[4 * j + 2], ga[4 * j + 1] - gb[4 * j + 3]);
-                        *reinterpret_cast<float2*>(out + (int64_t)D * N + rr * N + n) =
-                            make_float2(gb[4 * j] + ga[4 * j + 2], gb[4 * j + 1] + ga[4 * j + 3]);
+                    for (int j = 0; j < 4; ++j) {
+                        const int n = 32 * kh + 8 * j + 2 * lq;
+                        if (n < N) {  // N is a multiple of 8: n + 1 < N too
+                            *reinterpret_cast<float2*>(out + rr * N + n) =
+                                make_float2(ga[4 * j] - gb[4 * j + 2], ga[4 * j + 1] - gb[4 * j + 3]);
+                            *reinterpret_cast<float2*>(out + (int64_t)D * N + rr * N + n) =
+                                make_float2(gb[4 * j] + ga[4 * j + 2], gb[4 * j + 1] + ga[4 * j + 3]);
+                        }
                     }
                 }
             }
-        }
-        if (tid == 0) {
-            const float2 a = sm.eacs[Q - 1];
-            ws.a[2 * chunk] = a.x;
-            ws.a[2 * chunk + 1] = a.y;
+            if (tid == 0) {
+                const float2 a = sm.eacs[Q - 1];
+                ws.a[2 * chunk] = a.x;
+                ws.a[2 * chunk + 1] = a.y;
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.acc_free);  // this warp has read the accumulators
+            // the next chunk's tables overwrite dec and eacs: every warp's transposes and a_c are done
+            ptx::named_sync(kWorkerBar, kWorkers);
         }
     }
     ptx::tc_fence_before();
@@ -919,8 +988,12 @@ int bwd_tc_launch_chunk_states(const GradProblem& g, const Workspace& ws, const 
     const int rc = bwdtc::make_states_maps(g, &m);
     if (rc != SSDC_OK) return rc;
     const Problem& p = g.f;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return SSDC_ERR_CUDA;
     const int64_t chunks = (int64_t)p.B * p.H * p.nc;
-    bwdtc::bwd_states_tc<<<(unsigned)chunks, bwdtc::kThreads, bwdtc::kStatesSmemBytes, stream>>>(g, ws, gw, m);
+    const unsigned grid = (unsigned)(chunks < sms ? chunks : sms);  // one CTA per SM walks the chunks
+    bwdtc::bwd_states_tc<<<grid, bwdtc::kThreads, bwdtc::kStatesSmemBytes, stream>>>(g, ws, gw, m);
     return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
 }
 
