@@ -153,36 +153,8 @@ __device__ __forceinline__ Item item_next(const Item& p, int R, int nc) {
     return item_at(p.q + (int)gridDim.x, 0, 0, 0);
 }
 
-// Producer: TMA of one block's x (stacked; only the real plane for a real x),
-// C (interleaved) or B (stacked) into stage buffers, counted on `bar`. A box
-// of `rows` rows of one 32-column half of one plane is rows x 128 bytes.
-__device__ __forceinline__ void load_x(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int rows,
-                                       int lane) {
-    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * (fm.real_x ? 2 : 4)));
-    __syncwarp();
-    if (fm.fast & 1) {
-        if (lane < 2) ptx::tma_load_5d(dst + stk_row(lane, 0, 0), &fm.x2, bar, 32 * lane, h, t0, 0, b);
-    } else {
-        const int n = fm.real_x ? 2 : 4;
-        if (lane < n) {
-            const int half = fm.real_x ? lane : lane >> 1, pl = fm.real_x ? 0 : lane & 1;
-            ptx::tma_load_4d(dst + stk_row(half, pl, 0), pl ? &fm.x_im : &fm.x_re, bar, 32 * half, h, t0, b);
-        }
-    }
-}
-
-__device__ __forceinline__ void load_b(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int rows,
-                                       int lane) {
-    if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * 4));
-    __syncwarp();
-    if ((fm.fast >> 1) & 1) {
-        if (lane < 2) ptx::tma_load_5d(dst + stk_row(lane, 0, 0), &fm.B2, bar, 32 * lane, h, t0, 0, b);
-    } else if (lane < 4) {
-        const int half = lane >> 1, pl = lane & 1;
-        ptx::tma_load_4d(dst + stk_row(half, pl, 0), pl ? &fm.B_im : &fm.B_re, bar, 32 * half, h, t0, b);
-    }
-}
-
+// Producer: TMA of one block's C (interleaved) into a stage buffer, counted on
+// `bar` (x and B: load_x, load_b of the shared header).
 __device__ __forceinline__ void load_c(char* dst, const FusedMaps& fm, uint64_t* bar, int h, int t0, int b, int64_t T,
                                        int rows, int lane) {
     if (lane == 0) ptx::mbar_expect_tx(bar, (uint32_t)(rows * 128 * 4));
