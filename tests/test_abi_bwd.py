@@ -88,7 +88,9 @@ def test_precisions_the_backward_takes(lib):
     p, end = fake_ptrs(d)
     assert call(lib, p, d, Q=128, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
     for Q in (16, 32, 64):
-        assert call(lib, p, d, Q=Q, ws=end) in PASSED_HOST_CHECKS
+        assert ssdc.ssd_complex_bwd_workspace_bytes(d, Q) > 0
+        if no_gpu():  # passes the host checks (with a GPU it would launch on the fake addresses)
+            assert call(lib, p, d, Q=Q, ws=end) in PASSED_HOST_CHECKS
 
 
 def test_rejects_null_required_pointer(lib):

@@ -60,6 +60,8 @@ CASES = [
     (2, 333, 3, 40, 16, 64),
     (1, 1, 2, 64, 64, 64),
     (3, 100, 2, 24, 56, 32),
+    (4, 1000, 16, 64, 64, 32),  # many chunks a CTA: the unloaded rows past Q zeroed again each chunk
+    (3, 700, 16, 40, 24, 16),
 ]
 
 
@@ -80,9 +82,11 @@ def test_tf32_backward_initial_state_no_final_gradient():
     check_tf32(got, oracle_grads(inp, og, s0=s0, with_dfs=False), inp, "tf32 backward, initial state")
 
 
-def test_tf32_backward_real_x_and_real_loss():
-    inp = inputs.custom(2, 256, 4, 64, 64, seed=8300)
-    og = inputs.output_grads(2, 256, 4, 64, 64, seed=8301)
+@pytest.mark.parametrize("Bn,T,H", [(2, 256, 4), (4, 1000, 16)])
+def test_tf32_backward_real_x_and_real_loss(Bn, T, H):
+    # (4, 1000, 16): 1024 chunks, several a CTA, so the imaginary planes are zeroed again each chunk
+    inp = inputs.custom(Bn, T, H, 64, 64, seed=8300 + T)
+    og = inputs.output_grads(Bn, T, H, 64, 64, seed=8301 + T)
     got = run_tf32(inp, og, 64, real_x=True, dy_imag=False, with_dfs=False)
     ref = oracle_grads(inp, og, real_x=True, dy_imag=False, with_dfs=False)
     check_tf32(got, ref, inp, "tf32 backward, real x, Re(y) loss")
