@@ -471,8 +471,10 @@ int ssd_complex_fwd_host(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t,
  * Precision: SSDC_PREC_FP32 is exact fp32 on the SIMT cores (every decay with
  * the accurate expf / sincosf), for the sizes of SSDC_PREC_FP32 in the forward
  * pass. SSDC_PREC_TF32 computes the per-chunk gradient products (dx, dB_t,
- * dC_t) on the TF32 tensor cores, with chunk_size 16, 32 or 64 and N, D
- * multiples of 8 up to 64; the chunk recurrences and the step-size gradients
+ * dC_t) on the TF32 tensor cores, with chunk_size 16, 32, 64, 128 or 256 and
+ * N, D multiples of 8 up to 64; at 128 and 256 it works on chunks of 64
+ * tokens (the gradients of the scan do not depend on how it is chunked; the
+ * workspace size follows). The chunk recurrences and the step-size gradients
  * stay exact fp32. SSDC_PREC_TF32_STAGED returns SSDC_ERR_UNSUPPORTED.
  * Errors, streams and ownership as for ssd_complex_fwd_ws.
  */

@@ -570,8 +570,14 @@ struct BwdLayout {
 
 size_t pad256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// The chunk size the backward's kernels run at: the TF32 chunk kernels take
+// chunks of up to 64 tokens, so a longer chunk (128, 256) is worked as 64-token
+// chunks. The gradients of the scan do not depend on its chunking (only their
+// rounding does), so this changes no result beyond that.
+int bwd_chunk(const ssdc_dims& d, int Q) { return d.precision == SSDC_PREC_TF32 && Q > 64 ? 64 : Q; }
+
 BwdLayout bwd_layout(const ssdc_dims& d, int Q) {
-    const int64_t nc = ssdc::ceil_div64(d.T, Q);
+    const int64_t nc = ssdc::ceil_div64(d.T, bwd_chunk(d, Q));
     const size_t chunks = (size_t)(d.B * d.H * nc);
     const size_t states = pad256(chunks * 2 * d.N * d.D * sizeof(float));
     BwdLayout l;
@@ -587,13 +593,14 @@ BwdLayout bwd_layout(const ssdc_dims& d, int Q) {
 }
 
 // The exact fp32 backward takes every size the forward does; the TF32 one
-// (chunk gradients on the tensor cores) Q = 16, 32, 64 with N, D multiples of
-// 8 up to 64.
+// (chunk gradients on the tensor cores) every Q the forward takes (64-token
+// chunks for Q = 128, 256) with N, D multiples of 8 up to 64.
 int check_bwd_sizes(const ssdc_dims& d, int Q) {
     const int rc = check_sizes(d, Q);
     if (rc != SSDC_OK) return rc;
     if (d.precision == SSDC_PREC_FP32) return SSDC_OK;
-    if (d.precision == SSDC_PREC_TF32 && ssdc::bwd_tc_supported((int)d.N, (int)d.D, Q)) return SSDC_OK;
+    if (d.precision == SSDC_PREC_TF32 && ssdc::bwd_tc_supported((int)d.N, (int)d.D, bwd_chunk(d, Q)))
+        return SSDC_OK;
     return SSDC_ERR_UNSUPPORTED;
 }
 
@@ -684,8 +691,8 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     p.y_re = nullptr; p.y_im = nullptr;  // the forward rows are not needed
     p.fs_re = fs; p.fs_im = fs + fsn;
     p.T = dims.T; p.B = (int)dims.B; p.H = (int)dims.H; p.N = (int)dims.N; p.D = (int)dims.D;
-    p.Q = chunk_size;
-    p.nc = ssdc::ceil_div64(dims.T, chunk_size);
+    p.Q = bwd_chunk(dims, chunk_size);
+    p.nc = ssdc::ceil_div64(dims.T, p.Q);
     p.drop_send_chunk = -1;
     g.dy_re = dy.re; g.dy_im = dy.im;
     g.dfs_re = d_final_state.re; g.dfs_im = d_final_state.im;

@@ -71,7 +71,12 @@ def test_workspace_bytes(lib):
     assert nb >= 2 * chunks * 2 * 64 * 64 * 4 + chunks * 8 + 2 * 16 * 64 * 64 * 8 + 2 * 2048 * 16 * 8
     # the TF32 backward (Q <= 64) has the same workspace as the exact one
     assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 64) == nb
-    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 128) == 0
+    # at Q = 128 and 256 it works on 64-token chunks: the workspace of Q = 64
+    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 128) == nb
+    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 256) == nb
+    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "fp32"), 128) < nb
+    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32"), 48) == 0
+    assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 12, 64, "tf32"), 64) == 0
     assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "tf32_staged"), 64) == 0
     assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(2, 2048, 16, 64, 64, "fp32"), 48) == 0
     assert ssdc.ssd_complex_bwd_workspace_bytes(ssdc.dims(1, 65, 1, 64, 64, "fp32"), 64) > \
@@ -79,15 +84,15 @@ def test_workspace_bytes(lib):
 
 
 def test_precisions_the_backward_takes(lib):
-    """exact fp32 at every size; TF32 at Q <= 64 (the tensor-core chunk gradients); never
-    the staged TF32 precision."""
+    """exact fp32 at every size; TF32 at every Q the forward takes (the tensor-core chunk
+    gradients, on 64-token chunks above 64); never the staged TF32 precision."""
     d = ssdc.dims(1, 128, 2, 64, 64, "tf32_staged")
     p, end = fake_ptrs(d)
     assert call(lib, p, d, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
     d = ssdc.dims(1, 128, 2, 64, 64, "tf32")
     p, end = fake_ptrs(d)
-    assert call(lib, p, d, Q=128, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
-    for Q in (16, 32, 64):
+    assert call(lib, p, d, Q=48, ws=end) == ssdc.SSDC_ERR_UNSUPPORTED
+    for Q in (16, 32, 64, 128, 256):
         assert ssdc.ssd_complex_bwd_workspace_bytes(d, Q) > 0
         if no_gpu():  # passes the host checks (with a GPU it would launch on the fake addresses)
             assert call(lib, p, d, Q=Q, ws=end) in PASSED_HOST_CHECKS
@@ -160,7 +165,7 @@ def test_binding_rejects_unsupported_backward_before_allocating(lib):
     with pytest.raises(ssdc.SSDCError):
         ssdc.Backward(1, 128, 2, 64, 64, 64, precision="tf32_staged", device="cpu")
     with pytest.raises(ssdc.SSDCError):
-        ssdc.Backward(1, 128, 2, 64, 64, 128, precision="tf32", device="cpu")
+        ssdc.Backward(1, 128, 2, 64, 64, 48, precision="tf32", device="cpu")
     with pytest.raises(ssdc.SSDCError):
         ssdc.Backward(1, 128, 2, 64, 64, 48, device="cpu")
     with pytest.raises(ssdc.SSDCError):

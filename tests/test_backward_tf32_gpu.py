@@ -3,9 +3,11 @@ per-chunk gradient products on the tensor cores) with the gradient oracle.
 The bar is the TF32 forward's, 2e-3: relative Frobenius error for dx, dB_t,
 dC_t and d_initial_state, and, for ddt and dA, error relative to the size of
 the per-token terms their sums cancel (the scales of the exact backward's
-tests). Cases: the single-layer size, every chunk size the kernel takes, N
-and D below 64, ragged tails, T = 1, an initial state, no final-state
-gradient, a real x with a loss of Re(y) alone."""
+tests). Cases: the single-layer size, every chunk size (128 and 256 worked
+as 64-token chunks), N and D below 64, ragged tails, T = 1, an initial
+state, no final-state gradient, a real x with a loss of Re(y) alone; and,
+for the chunk kernel, which walks several chunks a CTA, Q below 64 and the
+real x and loss with more chunks than SMs."""
 import numpy as np
 import pytest
 
@@ -62,6 +64,8 @@ CASES = [
     (3, 100, 2, 24, 56, 32),
     (4, 1000, 16, 64, 64, 32),  # many chunks a CTA: the unloaded rows past Q zeroed again each chunk
     (3, 700, 16, 40, 24, 16),
+    (2, 300, 3, 64, 64, 128),   # Q = 128 and 256: worked as 64-token chunks
+    (1, 600, 2, 32, 48, 256),
 ]
 
 
