@@ -64,6 +64,7 @@ CASES = [
     (3, 100, 2, 24, 56, 32),
     (4, 1000, 16, 64, 64, 32),  # many chunks a CTA: the unloaded rows past Q zeroed again each chunk
     (3, 700, 16, 40, 24, 16),
+    (1, 640, 16, 64, 64, 64),   # 160 chunks: 8 CTAs take two, the rest one
     (2, 300, 3, 64, 64, 128),   # Q = 128 and 256: worked as 64-token chunks
     (1, 600, 2, 32, 48, 256),
 ]
@@ -86,12 +87,13 @@ def test_tf32_backward_initial_state_no_final_gradient():
     check_tf32(got, oracle_grads(inp, og, s0=s0, with_dfs=False), inp, "tf32 backward, initial state")
 
 
-@pytest.mark.parametrize("Bn,T,H", [(2, 256, 4), (4, 1000, 16)])
-def test_tf32_backward_real_x_and_real_loss(Bn, T, H):
-    # (4, 1000, 16): 1024 chunks, several a CTA, so the imaginary planes are zeroed again each chunk
-    inp = inputs.custom(Bn, T, H, 64, 64, seed=8300 + T)
-    og = inputs.output_grads(Bn, T, H, 64, 64, seed=8301 + T)
-    got = run_tf32(inp, og, 64, real_x=True, dy_imag=False, with_dfs=False)
+@pytest.mark.parametrize("Bn,T,H,Q", [(2, 256, 4, 64), (4, 1000, 16, 64), (4, 1000, 16, 32)])
+def test_tf32_backward_real_x_and_real_loss(Bn, T, H, Q):
+    # (4, 1000, 16): 1024 and 2048 chunks, several a CTA, so the imaginary planes (and at Q = 32 the
+    # rows past Q) are zeroed again each chunk
+    inp = inputs.custom(Bn, T, H, 64, 64, seed=8300 + T + Q)
+    og = inputs.output_grads(Bn, T, H, 64, 64, seed=8301 + T + Q)
+    got = run_tf32(inp, og, Q, real_x=True, dy_imag=False, with_dfs=False)
     ref = oracle_grads(inp, og, real_x=True, dy_imag=False, with_dfs=False)
     check_tf32(got, ref, inp, "tf32 backward, real x, Re(y) loss")
 
