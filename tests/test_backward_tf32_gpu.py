@@ -132,3 +132,17 @@ def test_scan_autograd_with_tf32_backward():
            "dB": n(leaves["B_re"]) + 1j * n(leaves["B_im"]), "dC": n(leaves["C_re"]) + 1j * n(leaves["C_im"]),
            "ddt": n(leaves["dt"]), "ds0": n(s0_re) + 1j * n(s0_im)}
     check_tf32(got, oracle_grads(inp, og, s0=s0), inp, "tf32 backward through autograd")
+
+
+@pytest.mark.parametrize("Q", [64, 128])
+def test_tf32_backward_long_sequence(Q):
+    """The long-memory workload's length (T = 65536: 1024 chunks of 64 tokens in one sequence,
+    all walked by one CTA after another) with its slow decays, at N = D = 8 so that the oracle's
+    stored states stay small, from an initial state."""
+    from tests.test_backward_gpu import state
+    Bn, T, H, D, N = 1, 65536, 2, 8, 8
+    inp = inputs.custom(Bn, T, H, D, N, seed=8700 + Q, dt_mean=-2.0, dt_std=0.5, re_lo=-0.1, re_hi=-0.01)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=8701)
+    s0 = state(inp, 8702)
+    got = run_tf32(inp, og, Q, s0=s0)
+    check_tf32(got, oracle_grads(inp, og, s0=s0), inp, f"tf32 backward, long sequence Q{Q}")
