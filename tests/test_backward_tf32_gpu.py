@@ -146,3 +146,16 @@ def test_tf32_backward_long_sequence(Q):
     s0 = state(inp, 8702)
     got = run_tf32(inp, og, Q, s0=s0)
     check_tf32(got, oracle_grads(inp, og, s0=s0), inp, f"tf32 backward, long sequence Q{Q}")
+
+
+def test_tf32_backward_dt_zero_and_growing_states():
+    """dt = 0 everywhere (A_bar = 2^A at every token; the TF32 kernels' decay tables then
+    hold exact powers) and Re(A) > 0 on a short sequence, where the states grow."""
+    Bn, T, H, D, N, Q = 2, 200, 2, 16, 16, 32
+    inp = inputs.custom(Bn, T, H, D, N, seed=8800, dt_mode="zero")
+    og = inputs.output_grads(Bn, T, H, D, N, seed=8801)
+    check_tf32(run_tf32(inp, og, Q), oracle_grads(inp, og), inp, "tf32 backward, dt = 0")
+    Bn, T = 1, 48
+    inp = inputs.custom(Bn, T, H, D, N, seed=8802, re_lo=0.01, re_hi=0.1)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=8803)
+    check_tf32(run_tf32(inp, og, 16), oracle_grads(inp, og), inp, "tf32 backward, Re(A) > 0")
