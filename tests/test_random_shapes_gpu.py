@@ -8,7 +8,8 @@ initial state or none, and sometimes fewer sequences than SMs at Q = N = D =
 fused kernel the library picks), the final state alone, and every fourth the
 exact fp32 forward and the bfloat16-input forward, each against the oracle's
 scan at the path's tolerance (relative Frobenius error on y and the final
-state; the bfloat16 path against the oracle on the same bfloat16 values)."""
+state; the bfloat16 path against the oracle on the same bfloat16 values).
+Then 24 random problems for the TF32 backward against the gradient oracle."""
 import dataclasses
 
 import numpy as np
@@ -103,3 +104,30 @@ def test_random_problem(i):
         torch.cuda.synchronize()
         assert h.status() == ssdc.SSDC_OK
         assert_close(cplx(hy_re, hy_im), cplx(hs_re, hs_im), yb_ref, sb_ref, "tf32", what + ", bf16 inputs")
+
+
+NBWD = 24
+
+
+@pytest.mark.parametrize("i", range(NBWD))
+def test_random_backward_problem(i):
+    """The TF32 backward on seeded random problems: B in [1, 4], T in [1, 900], H in [1, 19],
+    N and D multiples of 8 in [8, 64], Q in {16, 32, 64, 128, 256}, a real x or a complex one,
+    a complex loss or one of Re(y) alone, a final-state gradient or none; against the gradient
+    oracle at the TF32 bar."""
+    from tests.test_backward_gpu import oracle_grads, run_bwd
+    from tests.test_backward_tf32_gpu import check_tf32
+    rng = np.random.default_rng(40_000 + i)
+    Bn, H = int(rng.integers(1, 5)), int(rng.integers(1, 20))
+    N, D = 8 * int(rng.integers(1, 9)), 8 * int(rng.integers(1, 9))
+    Q = int(rng.choice([16, 32, 64, 128, 256]))
+    T = int(rng.integers(1, 901))
+    real_x, dy_imag, with_dfs = bool(rng.random() < 0.25), bool(rng.random() < 0.8), bool(rng.random() < 0.7)
+    what = f"random backward #{i}: B{Bn} T{T} H{H} D{D} N{N} Q{Q}" + (" real x" if real_x else "") + \
+        ("" if dy_imag else ", Re(y) loss") + ("" if with_dfs else ", no final-state gradient")
+    inp = inputs.custom(Bn, T, H, D, N, seed=41_000 + i)
+    og = inputs.output_grads(Bn, T, H, D, N, seed=42_000 + i)
+    b = ssdc.Backward(Bn, T, H, N, D, Q, precision="tf32")
+    got = run_bwd(inp, og, Q, backward=b, real_x=real_x, dy_imag=dy_imag, with_dfs=with_dfs)
+    ref = oracle_grads(inp, og, real_x=real_x, dy_imag=dy_imag, with_dfs=with_dfs)
+    check_tf32(got, ref, inp, what)
