@@ -60,8 +60,9 @@ def parse():
     ap.add_argument("--bf16", action="store_true",
                     help="measurement mode: x, B_t and C_t in bfloat16 (ssd_complex_fwd_bf16), the rest fp32")
     ap.add_argument("--mimo", action="store_true",
-                    help="measurement mode: the MIMO head mixer fused into the forward (ssd_complex_fwd_mimo; "
-                         "only the mixed Re(y) is written), timed against the plain forward plus a separate mixer")
+                    help="measurement mode: the forward with the MIMO head mixer (ssd_complex_fwd_mimo: the scan "
+                         "writes Re(y), a second kernel mixes it in place), timed against the mixer fused into "
+                         "the scan's epilogue and against the plain forward plus a torch einsum")
     ap.add_argument("--state-only", action="store_true",
                     help="measurement mode: the final state alone (ssd_complex_final_state: reads x, B_t, dt; "
                          "no y), as the joining of time segments uses it")
@@ -200,8 +201,9 @@ def algorithmic_bytes_per_unit(w) -> float:
 
 def input_bytes_per_unit(w, bf16=False, real_x=False, mimo=False, state_only=False) -> float:
     """algorithmic_bytes_per_unit with x, B_t, C_t in bfloat16 (2 bytes a plane element
-    instead of 4: 4 D + 8 N fewer), a real x (no imaginary plane), the fused head
-    mixer (only the mixed Re(y) written: 4 D fewer) and / or the final state alone
+    instead of 4: 4 D + 8 N fewer), a real x (no imaginary plane), the head mixer
+    (only the mixed Re(y) leaves the call: 4 D fewer; the separate mixer's round trip
+    of Re(y), 8 D more, is not counted as algorithmic) and / or the final state alone
     (ssd_complex_final_state: no C_t read and no y written, 8 N + 8 D fewer)."""
     b = algorithmic_bytes_per_unit(w)
     if state_only:
@@ -608,6 +610,8 @@ def other_workload(args, w):
              2: ["chunk_state", "state_pass"],
              3: ["chunk_state", "state_pass", "chunk_scan"]}.get(
         nk, [f"launch{i}" for i in range(nk)])
+    if args.mimo and nk == 2:  # the scan (either fused kernel), then the in-place head mixer
+        names = [{"fused_tmem": "fused_tmem_kernel"}.get(path, "fused_kernel"), "head_mix"]
     top = int(np.argmax(kmeans))
     peak, peak_kind = peaks()
     wq = w.with_(Q=Q, T=Ts)
@@ -627,7 +631,7 @@ def other_workload(args, w):
                    + (f", {w.layers} layer(s) run" if args.layers > 0 else "")
                    + (f", batch {w.B}" if args.batch > 0 else "")
                    + (", real x" if args.real_x else "") + (", bf16 x/B/C" if args.bf16 else "")
-                   + (", fused head mixer (mixed Re(y) only)" if args.mimo else "")
+                   + (", head mixer on Re(y) (scan, then the in-place mixer kernel)" if args.mimo else "")
                    + (", final state alone (no y)" if args.state_only else ""),
                    "real_x": bool(args.real_x), "bf16_inputs": bool(args.bf16),
                    "B": w.B, "T": w.T, "H": w.H, "D": w.D, "N": w.N,
@@ -645,8 +649,9 @@ def other_workload(args, w):
         "clocks": clocks,
     }
     if args.mimo:
-        # the unfused counterpart: the plain forward (y written), then the same mixer as a separate
-        # op on Re(y) (torch einsum), each timed with CUDA events, L2 flushed before each step
+        # the alternatives: the mixer fused into the scan's epilogue (one launch), and the plain
+        # forward (y written) followed by the same mixer as a torch einsum on Re(y); each timed with
+        # CUDA events, L2 flushed before each step
         fp = ssdc.Forward(w.B, Ts, w.H, w.N, w.D, Q, precision, device=dev)
         mixed = [None]
 
@@ -673,12 +678,22 @@ def other_workload(args, w):
                 torch.cuda.synchronize()
                 tot += e0.elapsed_time(e1)
             return tot / n
+        def fused(L):
+            for seg in L:
+                f(*seg, W)
+
         n = max(3, min(args.steps, 50))
+        with ssdc.option(ssdc.OPT_MIMO_FUSED, 1):
+            fused_ms = timed(fused, n)
         scan_ms = timed(plain, n)
         mixer_ms = timed(mixer, n)
-        line["unfused"] = {"scan_ms": scan_ms, "mixer_ms": mixer_ms, "total_ms": scan_ms + mixer_ms,
-                           "what": "the plain forward (path chosen as usual, y written) plus the mixer as a "
-                                   "separate torch einsum over Re(y); the fused figure is ms_per_step"}
+        line["alternatives"] = {"fused_epilogue_ms": fused_ms,
+                                "torch_einsum": {"scan_ms": scan_ms, "mixer_ms": mixer_ms,
+                                                 "total_ms": scan_ms + mixer_ms},
+                                "what": "ms_per_step is the default call (the scan writes Re(y), then the "
+                                        "mixer kernel); fused_epilogue_ms the same call with the mixer in "
+                                        "the scan's epilogue (SSDC_OPT_MIMO_FUSED = 1); torch_einsum the plain "
+                                        "forward (path chosen as usual, y written) plus a torch einsum over Re(y)"}
     print(json.dumps(line), flush=True)
 
 

@@ -179,17 +179,24 @@ int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_ci
                          void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
- * Forward pass with the MIMO head mixer fused into its epilogue (landing page,
- * "02 MIMO Mixer": a fully connected mixer across the H SSM heads, H x H,
- * identity-initialised, applied to the Re(y) the block consumes):
+ * Forward pass followed by the MIMO head mixer (landing page, "02 MIMO Mixer":
+ * a fully connected mixer across the H SSM heads, H x H, identity-initialised,
+ * applied to the Re(y) the block consumes):
  *   out[b, t, g, d] = sum_h mix[g * H + h] Re(y)[b, t, h, d],
- * the same matrix for every feature d. Only the mixed Re(y) is written (no
- * y.im, no separate Re(y)), so y does not make a round trip through memory
- * before the mixer. The tiles of Re(y) of one batch row and 64-token tile from
- * all H heads meet in `out` and are counted there; once all H are stored, the
- * CTA of head h mixes the h-th 1/H of the tile's tokens in place. A CTA mixes
- * its ready shares after each tile it stores, and waits (bounded) only for the
- * shares still open after its sequence's last tile.
+ * the same matrix for every feature d. No y.im is written. Two ways, chosen by
+ * SSDC_OPT_MIMO_FUSED:
+ *   0 (default)  the scan (the fused kernel the library picks, as for
+ *                ssd_complex_fwd_ws) writes Re(y) into `out`, then a second
+ *                kernel mixes each token's H x D block in place (it reads and
+ *                writes `out` once: 8 H D bytes a token). Two launches.
+ *   1            the mixer in the epilogue of the kernel with the state in
+ *                tensor memory: the tiles of Re(y) of one batch row and 64-token
+ *                tile from all H heads meet in `out` and are counted there;
+ *                once all H are stored, the CTA of head h mixes the h-th 1/H of
+ *                the tile's tokens in place. A CTA mixes its ready shares after
+ *                each tile it stores, and waits (bounded) only for the shares
+ *                still open after its sequence's last tile. One launch; slower
+ *                on a GB300 (the exchange lands on the chunk loop's critical path).
  *
  *   mix             (H, H) fp32 device array, row g = output head g; required
  *   out             (B, T, H, D) fp32 device array, 16-byte aligned
@@ -197,10 +204,10 @@ int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_ci
  *   dims.precision  SSDC_PREC_TF32; H <= 16; N, D multiples of 8 in [8, 64];
  *                   chunk_size 16, 32 or 64 (else SSDC_ERR_UNSUPPORTED)
  *   workspace       ssd_complex_fwd_mimo_workspace_bytes() bytes (a status word
- *                   and one counter per batch row and 64-token tile)
+ *                   and one counter per batch row and 64-token tile, which the
+ *                   fused epilogue uses), either way
  * The other arguments, the overlap rules and the errors are those of
- * ssd_complex_fwd_ws. One launch, the fused kernel with the state in tensor
- * memory.
+ * ssd_complex_fwd_ws.
  */
 size_t ssd_complex_fwd_mimo_workspace_bytes(ssdc_dims dims, int chunk_size);
 int ssd_complex_fwd_mimo(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float *dt,
@@ -336,6 +343,10 @@ int ssd_complex_timing_read(float *ms, int n);
  *   SSDC_OPT_FUSED_KERNEL         fused TF32 kernel: 0 = chosen per call
  *                                 (default), 1 = the cluster kernel, 2 = the
  *                                 kernel with the state in tensor memory
+ *   SSDC_OPT_MIMO_FUSED           ssd_complex_fwd_mimo: 0 (default) = the scan writes
+ *                                 Re(y) into the output, then a separate kernel mixes
+ *                                 it in place; 1 = the mixer fused into the scan's
+ *                                 epilogue (one launch)
  *   SSDC_OPT_TEST_DROP_STATE_CHUNK  test hook, -1 = off (default): the fused
  *                                 kernel does not send the state of this chunk
  *                                 index to the next CTA, whose bounded wait then
@@ -345,6 +356,7 @@ int ssd_complex_timing_read(float *ms, int n);
 #define SSDC_OPT_FUSED_PLANE_MAPS 2
 #define SSDC_OPT_TEST_DROP_STATE_CHUNK 3
 #define SSDC_OPT_FUSED_KERNEL 4
+#define SSDC_OPT_MIMO_FUSED 5
 int ssd_complex_set_option(int option, int64_t value);
 
 /*

@@ -405,8 +405,9 @@ fused_kernel(Problem p, Workspace ws, const __grid_constant__ FusedMaps fm) {
                 if (t < p.T) {
                     *reinterpret_cast<float4*>(p.y_re + row + d) =
                         odd ? make_float4(rre.x, rre.y, re[1].x, re[1].y) : make_float4(re[0].x, re[0].y, rre.x, rre.y);
-                    *reinterpret_cast<float4*>(p.y_im + row + d) =
-                        odd ? make_float4(rim.x, rim.y, im[1].x, im[1].y) : make_float4(im[0].x, im[0].y, rim.x, rim.y);
+                    if (p.y_im != nullptr)  // absent when only Re(y) is asked for (the head mixer's input)
+                        *reinterpret_cast<float4*>(p.y_im + row + d) =
+                            odd ? make_float4(rim.x, rim.y, im[1].x, im[1].y) : make_float4(im[0].x, im[0].y, rim.x, rim.y);
                 }
             }
         };

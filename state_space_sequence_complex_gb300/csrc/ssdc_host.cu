@@ -26,6 +26,7 @@ std::atomic<int> g_opt_cluster{0};           // SSDC_OPT_FUSED_CLUSTER: 0 = chos
 std::atomic<int> g_opt_plane_maps{1};        // SSDC_OPT_FUSED_PLANE_MAPS
 std::atomic<int64_t> g_opt_drop_state_chunk{-1};  // SSDC_OPT_TEST_DROP_STATE_CHUNK: -1 = off
 std::atomic<int> g_opt_kernel{0};            // SSDC_OPT_FUSED_KERNEL: 0 = chosen per call
+std::atomic<int> g_opt_mimo_fused{0};        // SSDC_OPT_MIMO_FUSED: 0 = scan, then the mixer kernel
 
 // Instrumentation events (see ssd_complex_timing_enable).
 constexpr int kMaxTimed = 8;
@@ -274,7 +275,10 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     p.drop_send_chunk = g_opt_drop_state_chunk.load(std::memory_order_relaxed);
     p.in_bf16 = in_bf16 ? 1 : 0;
     ssdc::Workspace w = carve(workspace, dims, chunk_size);
-    if (mix != nullptr) {
+    // the head mixer: fused into the scan's epilogue (SSDC_OPT_MIMO_FUSED), or by default a
+    // separate in-place kernel over the Re(y) the scan writes into the output
+    const bool mix_fused = mix != nullptr && g_opt_mimo_fused.load(std::memory_order_relaxed) != 0;
+    if (mix_fused) {
         p.mix_w = mix;
         p.mix_count = reinterpret_cast<int*>(static_cast<char*>(workspace) + 256);
     }
@@ -284,7 +288,7 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
     if (record_event(0, stream) != SSDC_OK) return SSDC_ERR_CUDA;
     // the status word starts at SSDC_OK; a kernel's failed wait records the first error (and the
     // fused head mixer's counters start at zero)
-    if (cudaMemsetAsync(w.status, 0, mix != nullptr ? mix_ws_bytes(dims, chunk_size) : sizeof(int), stream) !=
+    if (cudaMemsetAsync(w.status, 0, mix_fused ? mix_ws_bytes(dims, chunk_size) : sizeof(int), stream) !=
         cudaSuccess)
         return SSDC_ERR_CUDA;
     const dim3 pass_grid((unsigned)ssdc::ceil_div64((int64_t)p.N * p.D, ssdc::kPassThreads),
@@ -306,8 +310,8 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
         // ceil(sequences / SMs) x chunks at about 3.7 us a chunk; the cluster kernel, its chosen
         // cost at about 4.1 us a chunk with one CTA per sequence and 5.2 us with the state
         // handed between CTAs.
-        int kernel = (in_bf16 || mix != nullptr) ? 2 : g_opt_kernel.load(std::memory_order_relaxed);
-        const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q) && !in_bf16 && mix == nullptr;
+        int kernel = (in_bf16 || mix_fused) ? 2 : g_opt_kernel.load(std::memory_order_relaxed);
+        const bool cluster_ok = ssdc::fused_supported(p.N, p.D, p.Q) && !in_bf16 && !mix_fused;
         if (kernel == 0) {
             if (!cluster_ok) {
                 kernel = 2;
@@ -328,12 +332,18 @@ int fwd_impl(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const float* dt
             }
         }
         if (kernel == 1 && !cluster_ok) return SSDC_ERR_UNSUPPORTED;
-        const int n = kernel == 2 ? ssdc::fused2_launch(p, w, stream, plane_maps && mix == nullptr)
+        const int n = kernel == 2 ? ssdc::fused2_launch(p, w, stream, plane_maps && !mix_fused)
                                   : ssdc::fused_launch(p, w, stream, force, plane_maps);
         if (n < 0) return n;
         path = kernel == 2 ? SSDC_PATH_FUSED_TMEM : SSDC_PATH_FUSED_CLUSTER;
         launches += n;
         record_event(launches, stream);
+        if (mix != nullptr && !mix_fused) {
+            const int m = ssdc::head_mix_launch(p.y_re, mix, dims.B * dims.T, p.H, p.D, stream);
+            if (m < 0) return m;
+            launches += m;
+            record_event(launches, stream);
+        }
     } else {
         path = SSDC_PATH_STAGED_TF32;
         int n = ssdc::tc_launch_chunk_state(p, w, stream);
@@ -525,6 +535,10 @@ int ssd_complex_set_option(int option, int64_t value) {
         case SSDC_OPT_FUSED_KERNEL:
             if (value < 0 || value > 2) return SSDC_ERR_INVALID;
             g_opt_kernel.store((int)value);
+            return SSDC_OK;
+        case SSDC_OPT_MIMO_FUSED:
+            if (value != 0 && value != 1) return SSDC_ERR_INVALID;
+            g_opt_mimo_fused.store((int)value);
             return SSDC_OK;
         case SSDC_OPT_TEST_DROP_STATE_CHUNK:
             if (value < -1) return SSDC_ERR_INVALID;

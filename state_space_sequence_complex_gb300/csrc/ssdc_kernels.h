@@ -167,6 +167,11 @@ int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int
 bool fused2_supported(int N, int D, int Q);
 int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bool plane_maps);
 
+// MIMO head mixer in place over y (ssdc_mix.cu): y[n, g, :] = sum_h w[g * H + h] y[n, h, :]
+// for ntok tokens of H x D fp32 (16-byte aligned, D a multiple of 4, H <= 16). Returns the
+// launches (0 or 1) or an error.
+int head_mix_launch(float* y, const float* w, int64_t ntok, int H, int D, cudaStream_t stream);
+
 // The state side of the same kernel alone (ssdc_state.cu): the final state of
 // each sequence from x, B_t and dt, without y (p.C_*, p.y_* unused). The same
 // sizes as fused2; returns launches or an error.

@@ -43,6 +43,7 @@ OPT_FUSED_CLUSTER = 1
 OPT_FUSED_PLANE_MAPS = 2
 OPT_TEST_DROP_STATE_CHUNK = 3
 OPT_FUSED_KERNEL = 4
+OPT_MIMO_FUSED = 5
 
 
 class ssdc_dims(ctypes.Structure):
@@ -242,8 +243,9 @@ def ssd_complex_fwd_bf16(x_re, x_im, A_re, A_im, B_re, B_im, C_re, C_im, dt, chu
 
 
 class MimoForward:
-    """The forward pass with the MIMO head mixer fused (``ssd_complex_fwd_mimo``):
-    holds the output (the mixed Re(y), (B,T,H,D)), the final state and the
+    """The forward pass followed by the MIMO head mixer (``ssd_complex_fwd_mimo``:
+    the scan writes Re(y) into the output and a second kernel mixes it in place,
+    or with ``OPT_MIMO_FUSED`` = 1 the mixer runs in the scan's epilogue): holds the output (the mixed Re(y), (B,T,H,D)), the final state and the
     workspace of one problem size. ``__call__`` takes the planar inputs and the
     (H,H) mixing matrix as CUDA tensors and returns ``(out, fs_re, fs_im)``."""
 
@@ -566,7 +568,8 @@ class option:
     """Context manager: set an option for the duration of a block, then restore
     `restore` (the option's default)."""
 
-    DEFAULTS = {OPT_FUSED_CLUSTER: 0, OPT_FUSED_PLANE_MAPS: 1, OPT_TEST_DROP_STATE_CHUNK: -1, OPT_FUSED_KERNEL: 0}
+    DEFAULTS = {OPT_FUSED_CLUSTER: 0, OPT_FUSED_PLANE_MAPS: 1, OPT_TEST_DROP_STATE_CHUNK: -1, OPT_FUSED_KERNEL: 0,
+                OPT_MIMO_FUSED: 0}
 
     def __init__(self, key: int, value: int):
         self.key, self.value = key, value

@@ -279,6 +279,7 @@ def test_set_option_rejects_bad_values(lib):
     assert lib.ssd_complex_set_option(ssdc.OPT_FUSED_CLUSTER, 3) == ssdc.SSDC_ERR_INVALID
     assert lib.ssd_complex_set_option(ssdc.OPT_FUSED_PLANE_MAPS, 2) == ssdc.SSDC_ERR_INVALID
     assert lib.ssd_complex_set_option(ssdc.OPT_TEST_DROP_STATE_CHUNK, -2) == ssdc.SSDC_ERR_INVALID
+    assert lib.ssd_complex_set_option(ssdc.OPT_MIMO_FUSED, 2) == ssdc.SSDC_ERR_INVALID
     assert lib.ssd_complex_set_option(99, 0) == ssdc.SSDC_ERR_INVALID
     for key, default in ssdc.option.DEFAULTS.items():  # defaults are accepted (and left set)
         assert lib.ssd_complex_set_option(key, default) == ssdc.SSDC_OK

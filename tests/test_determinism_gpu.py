@@ -11,7 +11,8 @@ launches of varying size in between (which shift the timing of the CTAs
 against each other), and every output must equal the first run's bit for
 bit. Cases: the cluster kernel at 1, 2, 4 and 8 CTAs per sequence (with and
 without an initial state), the tensor-memory kernel at every chunk size, its
-bfloat16-input and fused head-mixer instances, the final state alone
+bfloat16-input and fused head-mixer instances, the scan followed by the
+separate head mixer, the final state alone
 (ssd_complex_final_state), the staged TF32 path, and the TF32 backward
 (whose chunk kernels walk several chunks a CTA, loading the next chunk's
 tiles as the current one frees them).
@@ -105,7 +106,9 @@ def test_bf16_inputs_repeat_bit_for_bit(Q):
     repeat_identical(call, status, "fused_tmem")
 
 
-def test_fused_mixer_repeats_bit_for_bit():
+@pytest.mark.parametrize("fused", [0, 1], ids=["separate_mixer", "fused_mixer"])
+def test_mixer_repeats_bit_for_bit(fused, lib_option):
+    lib_option(ssdc.OPT_MIMO_FUSED, fused)
     inp = inputs.custom(20, 1000, 16, 64, 64, seed=60)
     t = to_device(inp)
     W = torch.from_numpy((np.eye(16) + 0.3 * np.random.default_rng(61).standard_normal((16, 16)))
