@@ -188,7 +188,8 @@ int ssd_complex_fwd_bf16(ssdc_cin_bf16 x, ssdc_cin A, ssdc_cin_bf16 B_t, ssdc_ci
  *   0 (default)  the scan (the fused kernel the library picks, as for
  *                ssd_complex_fwd_ws) writes Re(y) into `out`, then a second
  *                kernel mixes each token's H x D block in place (it reads and
- *                writes `out` once: 8 H D bytes a token). Two launches.
+ *                writes `out` once: 8 H D bytes a token), launched as a
+ *                programmatic dependent of the scan. Two launches.
  *   1            the mixer in the epilogue of the kernel with the state in
  *                tensor memory: the tiles of Re(y) of one batch row and 64-token
  *                tile from all H heads meet in `out` and are counted there;
