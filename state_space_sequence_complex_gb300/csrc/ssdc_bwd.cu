@@ -149,6 +149,7 @@ ssdc_bwd_chunk_states(GradProblem g, Workspace ws, GradWorkspace gw) {
 
 __global__ void __launch_bounds__(kPassThreads, 4)
 ssdc_bwd_passes(GradProblem g, Workspace ws, GradWorkspace gw) {
+    grid_dependency_wait();  // launched as a dependent of the kernel before it
     const Problem& p = g.f;
     const int64_t bh = blockIdx.y;
     const int ND = p.N * p.D;
@@ -625,6 +626,7 @@ constexpr int kDtWarps = kDtThreads / 32;
 
 __global__ void __launch_bounds__(kDtThreads)
 ssdc_bwd_dt(GradProblem g, Workspace ws, GradWorkspace gw) {
+    grid_dependency_wait();  // launched as a dependent of the kernel before it
     const Problem& p = g.f;
     const int lane = threadIdx.x & 31;
     const int64_t nc = p.nc;
@@ -687,6 +689,7 @@ ssdc_bwd_dt(GradProblem g, Workspace ws, GradWorkspace gw) {
 // sums a strided set of chunks, then a fixed-order reduction.
 __global__ void __launch_bounds__(kDtThreads)
 ssdc_bwd_dA(GradProblem g, Workspace ws, GradWorkspace gw) {
+    grid_dependency_wait();  // launched as a dependent of the kernel before it
     __shared__ double red[kDtWarps][2];
     const Problem& p = g.f;
     const int h = blockIdx.x, tid = threadIdx.x;

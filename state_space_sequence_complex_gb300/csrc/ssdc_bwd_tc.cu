@@ -137,6 +137,7 @@ __device__ __forceinline__ void zero_unloaded(char* tile, int i, bool interleave
 
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_chunk_tc(GradProblem g, Workspace ws, GradWorkspace gw, const __grid_constant__ BwdMaps bm) {
+    grid_dependency_wait();  // launched as a dependent of the state passes
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const Problem& p = g.f;
@@ -1132,7 +1133,9 @@ int bwd_tc_launch_chunk(const GradProblem& g, const Workspace& ws, const GradWor
         return SSDC_ERR_CUDA;
     const int64_t chunks = (int64_t)p.B * p.H * p.nc;
     const unsigned grid = (unsigned)(chunks < sms ? chunks : sms);  // one CTA per SM walks the chunks
-    bwdtc::bwd_chunk_tc<<<grid, bwdtc::kThreads, bwdtc::kSmemBytes, stream>>>(g, ws, gw, m);
+    if (launch_dependent(bwdtc::bwd_chunk_tc, dim3(grid), dim3(bwdtc::kThreads), bwdtc::kSmemBytes, stream, g, ws,
+                         gw, m) != cudaSuccess)
+        return SSDC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
 }
 

@@ -729,7 +729,11 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     }
     record_event(++launches, stream);
     const dim3 passes_grid(2 * pass_grid.x, pass_grid.y);  // forward and backward chains side by side
-    ssdc::ssdc_bwd_passes<<<passes_grid, ssdc::kPassThreads, 0, stream>>>(g, w, gw);
+    // the passes, the TF32 chunk kernel, dt and dA are launched as programmatic dependents of the
+    // kernel before each (their CTAs wait for it in griddepcontrol.wait before touching memory)
+    if (ssdc::launch_dependent(ssdc::ssdc_bwd_passes, passes_grid, dim3(ssdc::kPassThreads), 0, stream, g, w, gw) !=
+        cudaSuccess)
+        return SSDC_ERR_CUDA;
     record_event(++launches, stream);
     if (dims.precision == SSDC_PREC_TF32) {
         const int n = ssdc::bwd_tc_launch_chunk(g, w, gw, stream);
@@ -739,9 +743,13 @@ int ssd_complex_bwd(ssdc_cin x, ssdc_cin A, ssdc_cin B_t, ssdc_cin C_t, const fl
     }
     record_event(++launches, stream);
     const int64_t dt_blocks = ssdc::ceil_div64((int64_t)p.B * p.H * p.nc, ssdc::kBwdDtThreads / 32);
-    ssdc::ssdc_bwd_dt<<<(unsigned)dt_blocks, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);
+    if (ssdc::launch_dependent(ssdc::ssdc_bwd_dt, dim3((unsigned)dt_blocks), dim3(ssdc::kBwdDtThreads), 0, stream, g,
+                               w, gw) != cudaSuccess)
+        return SSDC_ERR_CUDA;
     record_event(++launches, stream);
-    ssdc::ssdc_bwd_dA<<<(unsigned)p.H, ssdc::kBwdDtThreads, 0, stream>>>(g, w, gw);
+    if (ssdc::launch_dependent(ssdc::ssdc_bwd_dA, dim3((unsigned)p.H), dim3(ssdc::kBwdDtThreads), 0, stream, g, w,
+                               gw) != cudaSuccess)
+        return SSDC_ERR_CUDA;
     record_event(++launches, stream);
     if (cudaGetLastError() != cudaSuccess) return SSDC_ERR_CUDA;
     g_last_launches = launches;

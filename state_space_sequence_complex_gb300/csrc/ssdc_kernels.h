@@ -167,6 +167,29 @@ int fused_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, int
 bool fused2_supported(int N, int D, int Q);
 int fused2_launch(const Problem& p, const Workspace& ws, cudaStream_t stream, bool plane_maps);
 
+// Programmatic dependent launch. A kernel launched with launch_dependent may have its CTAs
+// scheduled while the previous kernel on the stream finishes its last CTAs; it must call
+// grid_dependency_wait() before it reads anything that kernel writes (or writes anything that
+// kernel reads), which holds it until that kernel has completed and its writes are visible.
+// Launched the ordinary way, the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // MIMO head mixer in place over y (ssdc_mix.cu): y[n, g, :] = sum_h w[g * H + h] y[n, h, :]
 // for ntok tokens of H x D fp32 (16-byte aligned, D a multiple of 4, H <= 16). Returns the
 // launches (0 or 1) or an error.

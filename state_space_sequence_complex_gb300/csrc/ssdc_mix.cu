@@ -32,7 +32,7 @@ ssdc_head_mix(float* y, const float* __restrict__ w, int64_t ntok, int H, int D2
     }
     // launched as a programmatic dependent of the scan that writes y: W (written, if at all,
     // before the scan started) is fetched above while the scan finishes; y only after it has
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    grid_dependency_wait();
     __syncthreads();
     // one column a thread (a grid-stride loop would let the compiler hold all of W in registers)
     const int64_t i = (int64_t)blockIdx.x * kMixThreads + threadIdx.x;
@@ -69,19 +69,9 @@ int head_mix_launch(float* y, const float* w, int64_t ntok, int H, int D, cudaSt
     if (ntok == 0) return 0;
     const int64_t grid = (ntok * (D / 2) + kMixThreads - 1) / kMixThreads;
     if (grid > 0x7fffffff) return SSDC_ERR_UNSUPPORTED;
-    // programmatic stream serialisation: the CTAs may be scheduled as the previous kernel's
-    // CTAs exit; griddepcontrol.wait holds each one until that kernel has completed
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kMixThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, ssdc_head_mix, y, w, ntok, H, D / 2) != cudaSuccess) return SSDC_ERR_CUDA;
+    if (launch_dependent(ssdc_head_mix, dim3((unsigned)grid), dim3(kMixThreads), 0, stream, y, w, ntok, H, D / 2) !=
+        cudaSuccess)
+        return SSDC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? 1 : SSDC_ERR_CUDA;
 }
 
