@@ -83,18 +83,19 @@ def test_mixer_matches_oracle(case, mimo_path):
 
 @pytest.mark.parametrize("kernel", [1, 2], ids=["cluster", "tmem"])
 def test_identity_mixer_is_the_plain_forward_re_y(lib_option, mimo_path, kernel):
-    # the same kernel without the mixer (forced, per-plane tensor maps like the mixer's); the
-    # fused epilogue exists on the tensor-memory kernel only
-    if mimo_path == "fused" and kernel == 1:
-        pytest.skip("the fused epilogue runs on the tensor-memory kernel")
-    lib_option(ssdc.OPT_FUSED_KERNEL, kernel)
+    # the same kernel without the mixer (forced, per-plane tensor maps like the mixer's). The fused
+    # epilogue exists on the tensor-memory kernel only: forcing the cluster kernel leaves it there
+    on = 2 if mimo_path == "fused" else kernel
+    lib_option(ssdc.OPT_FUSED_KERNEL, on)
     lib_option(ssdc.OPT_FUSED_PLANE_MAPS, 0)
     inp = inputs.custom(2, 640, 16, 64, 64, seed=9200)
     t = to_device(inp)
     f = ssdc.Forward(*inp.dims, 64, "tf32")
     y_re, _, fs_re, fs_im = f(*[t[k] for k in ORDER])
+    assert ssdc.last_path() == ("fused_cluster" if on == 1 else "fused_tmem")
+    lib_option(ssdc.OPT_FUSED_KERNEL, kernel)
     out, s = run_mimo(inp, 64, np.eye(16, dtype=np.float32))
-    assert ssdc.last_path() == ("fused_cluster" if kernel == 1 else "fused_tmem")
+    assert ssdc.last_path() == ("fused_cluster" if on == 1 else "fused_tmem")
     assert np.array_equal(out, y_re.double().cpu().numpy())
     assert np.array_equal(s, fs_re.double().cpu().numpy() + 1j * fs_im.double().cpu().numpy())
 
